@@ -1,0 +1,362 @@
+"""Pins for the fp64 oracle, against facts that do not come from the oracle itself.
+
+Each pin is a closed form, an invariant of the mathematics, an independent
+library routine (PyTorch's scaled_dot_product_attention and autograd, in fp64
+on the CPU) or brute force (central finite differences).  The last test plants
+plausible mistakes in copies of the oracle and checks that some pin fails for
+each, so the pins are known to bite.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle.attn_ref as ref
+
+RNG = np.random.default_rng(1234)
+
+
+def rand(*shape):
+    return RNG.standard_normal(shape)
+
+
+# ---------------------------------------------------------------- pins as functions
+def pin_rows_sum_to_one(m=ref):
+    q, k = rand(1, 2, 9, 8), rand(1, 1, 11, 8)
+    for causal in (False, True):
+        s = m.scores_head(q, k, rand(1, 1, 1, 11), 0, 1, 0, 0.3, causal)
+        p, _ = m.probs_head(s)
+        assert np.allclose(p.sum(axis=1), 1.0, atol=1e-12)
+        assert np.all(p >= 0)
+
+
+def pin_constant_v(m=ref):
+    q, k = rand(2, 2, 7, 16), rand(2, 2, 13, 16)
+    v = np.full((2, 2, 13, 16), 0.0) + np.arange(16)[None, None, None, :] * 0.5 - 1.0
+    for causal in (False, True):
+        o, _ = m.attn_fwd(q, k, v, bias=rand(1, 1, 1, 13), causal=causal)
+        assert np.allclose(o, v[:, :, :1, :].repeat(7, axis=2), atol=1e-12)
+
+
+def pin_zero_q(m=ref):
+    # Q = 0: every visible key gets weight exp(bias_j) / sum; without bias the mean.
+    n, nkv, d = 6, 10, 8
+    q, k, v = np.zeros((1, 1, n, d)), rand(1, 1, nkv, d), rand(1, 1, nkv, d)
+    o, lse = m.attn_fwd(q, k, v, causal=False)
+    assert np.allclose(o[0, 0], v[0, 0].mean(axis=0)[None, :], atol=1e-12)
+    assert np.allclose(lse, math.log(nkv), atol=1e-12)
+    o, lse = m.attn_fwd(q, k, v, causal=True)
+    for i in range(n):
+        assert np.allclose(o[0, 0, i], v[0, 0, : i + 1].mean(axis=0), atol=1e-12)
+        assert abs(lse[0, 0, i] - math.log(i + 1)) < 1e-12
+    bias = rand(1, 1, 1, nkv)
+    o, lse = m.attn_fwd(q, k, v, bias=bias)
+    w = np.exp(bias[0, 0, 0])
+    assert np.allclose(o[0, 0], (w @ v[0, 0] / w.sum())[None, :], atol=1e-12)
+    assert np.allclose(lse, math.log(nkv) + math.log(np.mean(w)), atol=1e-12)
+
+
+def pin_causal_row0(m=ref):
+    q, k, v = rand(1, 1, 5, 8), rand(1, 1, 5, 8), rand(1, 1, 5, 8)
+    bias = rand(1, 1, 1, 5)
+    scale = 0.37
+    o, lse = m.attn_fwd(q, k, v, bias=bias, causal=True, scale=scale)
+    assert np.allclose(o[0, 0, 0], v[0, 0, 0], atol=1e-12)
+    assert abs(lse[0, 0, 0] - (scale * q[0, 0, 0] @ k[0, 0, 0] + bias[0, 0, 0, 0])) < 1e-12
+
+
+def pin_single_key(m=ref):
+    q, k, v = rand(1, 2, 4, 8), rand(1, 2, 1, 8), rand(1, 2, 1, 8)
+    o, lse = m.attn_fwd(q, k, v)
+    assert np.allclose(o, np.broadcast_to(v, o.shape), atol=1e-12)
+    assert np.allclose(lse[0, 1], q[0, 1] @ k[0, 1, 0] / math.sqrt(8), atol=1e-12)
+
+
+def pin_bias_shift(m=ref):
+    q, k, v = rand(1, 1, 6, 8), rand(1, 1, 9, 8), rand(1, 1, 9, 8)
+    bias = rand(1, 1, 1, 9)
+    o1, l1 = m.attn_fwd(q, k, v, bias=bias)
+    o2, l2 = m.attn_fwd(q, k, v, bias=bias + 2.5)
+    assert np.allclose(o1, o2, atol=1e-12) and np.allclose(l1 + 2.5, l2, atol=1e-12)
+
+
+def pin_permutation(m=ref):
+    q, k, v = rand(1, 1, 6, 8), rand(1, 1, 9, 8), rand(1, 1, 9, 8)
+    perm = RNG.permutation(9)
+    o1, l1 = m.attn_fwd(q, k, v)
+    o2, l2 = m.attn_fwd(q, k[:, :, perm], v[:, :, perm])
+    assert np.allclose(o1, o2, atol=1e-12) and np.allclose(l1, l2, atol=1e-12)
+
+
+def pin_gqa_repeat_interleave(m=ref):
+    q, k, v = rand(2, 6, 7, 8), rand(2, 2, 9, 8), rand(2, 2, 9, 8)
+    do = rand(2, 6, 7, 8)
+    ke = torch.from_numpy(k).repeat_interleave(3, dim=1).numpy()
+    ve = torch.from_numpy(v).repeat_interleave(3, dim=1).numpy()
+    for causal in (False, True):
+        o1, l1 = m.attn_fwd(q, k, v, causal=causal)
+        o2, l2 = m.attn_fwd(q, ke, ve, causal=causal)
+        assert np.allclose(o1, o2, atol=1e-12) and np.allclose(l1, l2, atol=1e-12)
+        g1 = m.attn_bwd(q, k, v, do, causal=causal)
+        g2 = m.attn_bwd(q, ke, ve, do, causal=causal)
+        assert np.allclose(g1[0], g2[0], atol=1e-12)
+        # the group's gradient is the sum over its expanded heads
+        assert np.allclose(g1[1], g2[1].reshape(2, 2, 3, 9, 8).sum(axis=2), atol=1e-12)
+        assert np.allclose(g1[2], g2[2].reshape(2, 2, 3, 9, 8).sum(axis=2), atol=1e-12)
+
+
+def _torch_sdpa(q, k, v, bias, causal, scale, gqa):
+    t = lambda x: torch.from_numpy(np.ascontiguousarray(x))
+    mask = None if bias is None else t(np.broadcast_to(bias, (q.shape[0], q.shape[1], q.shape[2], k.shape[2])))
+    if causal:
+        tri = torch.ones(q.shape[2], k.shape[2], dtype=torch.bool).tril()
+        cm = torch.zeros(q.shape[2], k.shape[2], dtype=torch.float64).masked_fill(~tri, float("-inf"))
+        mask = cm if mask is None else mask + cm
+    return torch.nn.functional.scaled_dot_product_attention(
+        t(q), t(k), t(v), attn_mask=mask, scale=scale, enable_gqa=gqa)
+
+
+def pin_torch_sdpa(m=ref):
+    # torch's is_causal is top-left; the explicit lower-triangular mask says the same.
+    for (b, hq, hkv, nq, nkv, d, causal, use_bias) in [
+        (1, 1, 1, 5, 5, 4, False, False), (2, 4, 2, 7, 11, 8, False, True),
+        (1, 2, 2, 9, 9, 16, True, False), (1, 4, 1, 6, 10, 8, True, True),
+        (1, 1, 1, 1, 13, 8, False, True),
+    ]:
+        q, k, v = rand(b, hq, nq, d), rand(b, hkv, nkv, d), rand(b, hkv, nkv, d)
+        bias = rand(1, 1, 1, nkv) if use_bias else None
+        scale = 1.0 / math.sqrt(d)
+        o, lse = m.attn_fwd(q, k, v, bias=bias, causal=causal)
+        ot = _torch_sdpa(q, k, v, bias, causal, scale, hq != hkv).numpy()
+        assert np.allclose(o, ot, atol=1e-12, rtol=1e-12)
+        # lse against torch.logsumexp of independently formed scores
+        kt = torch.from_numpy(k).repeat_interleave(hq // hkv, dim=1)
+        st = torch.from_numpy(q) @ kt.transpose(-1, -2) * scale
+        if bias is not None:
+            st = st + torch.from_numpy(bias)
+        if causal:
+            st = st.masked_fill(~torch.ones(nq, nkv, dtype=torch.bool).tril(), float("-inf"))
+        assert np.allclose(lse, torch.logsumexp(st, dim=-1).numpy(), atol=1e-12)
+
+
+def pin_torch_autograd(m=ref):
+    for (hq, hkv, nq, nkv, d, causal, use_bias) in [
+        (2, 1, 5, 7, 4, False, True), (2, 2, 6, 6, 8, True, False), (4, 2, 3, 9, 8, True, True)]:
+        q, k, v, do = rand(1, hq, nq, d), rand(1, hkv, nkv, d), rand(1, hkv, nkv, d), rand(1, hq, nq, d)
+        bias = rand(1, 1, 1, nkv) if use_bias else None
+        tq, tk, tv = (torch.from_numpy(x).requires_grad_(True) for x in (q, k, v))
+        mask = None if bias is None else torch.from_numpy(bias)
+        if causal:
+            cm = torch.zeros(nq, nkv, dtype=torch.float64).masked_fill(
+                ~torch.ones(nq, nkv, dtype=torch.bool).tril(), float("-inf"))
+            mask = cm if mask is None else mask + cm
+        out = torch.nn.functional.scaled_dot_product_attention(tq, tk, tv, attn_mask=mask, enable_gqa=hq != hkv)
+        out.backward(torch.from_numpy(do))
+        dq, dk, dv = m.attn_bwd(q, k, v, do, bias=bias, causal=causal)
+        assert np.allclose(dq, tq.grad.numpy(), atol=1e-11)
+        assert np.allclose(dk, tk.grad.numpy(), atol=1e-11)
+        assert np.allclose(dv, tv.grad.numpy(), atol=1e-11)
+
+
+def pin_finite_differences(m=ref):
+    # B=1, Hq=2, Hkv=1, N=5, D=4: central differences of L = sum(O * dO)
+    q, k, v, do = rand(1, 2, 5, 4), rand(1, 1, 5, 4), rand(1, 1, 5, 4), rand(1, 2, 5, 4)
+    bias = rand(1, 1, 1, 5)
+    for causal in (False, True):
+        loss = lambda q_, k_, v_: float(np.sum(m.attn_fwd(q_, k_, v_, bias=bias, causal=causal)[0] * do))
+        grads = m.attn_bwd(q, k, v, do, bias=bias, causal=causal)
+        h = 1e-6
+        for which, x in enumerate((q, k, v)):
+            num = np.zeros_like(x)
+            it = np.nditer(x, flags=["multi_index"])
+            for _ in it:
+                idx = it.multi_index
+                args_p = [q.copy(), k.copy(), v.copy()]
+                args_m = [q.copy(), k.copy(), v.copy()]
+                args_p[which][idx] += h
+                args_m[which][idx] -= h
+                num[idx] = (loss(*args_p) - loss(*args_m)) / (2 * h)
+            err = np.linalg.norm(grads[which] - num) / np.linalg.norm(num)
+            assert err < 1e-6, (which, causal, err)
+
+
+def pin_bwd_sums(m=ref):
+    q, k, v, do = rand(2, 4, 7, 8), rand(2, 2, 9, 8), rand(2, 2, 9, 8), rand(2, 4, 7, 8)
+    for causal in (False, True):
+        dq, dk, dv = m.attn_bwd(q, k, v, do, bias=rand(1, 1, 1, 9), causal=causal)
+        assert np.allclose(dk.sum(axis=2), 0.0, atol=1e-12)
+        assert np.allclose(dv.sum(axis=2), do.reshape(2, 2, 2, 7, 8).sum(axis=(2, 3)), atol=1e-12)
+
+
+def pin_sampled_bwd(m=ref):
+    q, k, v, do = rand(1, 4, 37, 8), rand(1, 2, 41, 8), rand(1, 2, 41, 8), rand(1, 4, 37, 8)
+    bias = rand(1, 1, 1, 41)
+    for causal in (False, True):
+        dq, dk, dv = m.attn_bwd(q, k, v, do, bias=bias, causal=causal)
+        qr, kr = m.sample_rows(37, 6, 3), m.sample_rows(41, 5, 4)
+        for g in range(2):
+            sdq, sdk, sdv = m.attn_bwd_sampled(q, k, v, do, 0, g, qr, kr, bias=bias, causal=causal, block=8)
+            for h, val in sdq.items():
+                assert np.allclose(val, dq[0, h, qr], atol=1e-12)
+            assert np.allclose(sdk, dk[0, g, kr], atol=1e-12)
+            assert np.allclose(sdv, dv[0, g, kr], atol=1e-12)
+        o, lse = m.attn_fwd(q, k, v, bias=bias, causal=causal)
+        orow, lrow = m.attn_fwd_rows(q, k, v, 0, 3, qr, bias=bias, causal=causal)
+        assert np.allclose(orow, o[0, 3, qr], atol=1e-12) and np.allclose(lrow, lse[0, 3, qr], atol=1e-12)
+
+
+def pin_query_bias(m=ref):
+    # a [1,1,Nq,Nkv] bias whose rows are equal is the [1,1,1,Nkv] bias
+    q, k, v = rand(1, 2, 5, 8), rand(1, 2, 7, 8), rand(1, 2, 7, 8)
+    row = rand(1, 1, 1, 7)
+    o1, l1 = m.attn_fwd(q, k, v, bias=row)
+    o2, l2 = m.attn_fwd(q, k, v, bias=np.repeat(row, 5, axis=2))
+    assert np.allclose(o1, o2, atol=1e-12) and np.allclose(l1, l2, atol=1e-12)
+
+
+PINS = [pin_rows_sum_to_one, pin_constant_v, pin_zero_q, pin_causal_row0, pin_single_key, pin_bias_shift,
+        pin_permutation, pin_gqa_repeat_interleave, pin_torch_sdpa, pin_torch_autograd, pin_finite_differences,
+        pin_bwd_sums, pin_sampled_bwd, pin_query_bias]
+
+
+@pytest.mark.parametrize("pin", PINS, ids=[p.__name__ for p in PINS])
+def test_pin(pin):
+    pin()
+
+
+def test_dead_row_convention():
+    # reading: a row with every score at -inf gives P = 0 and lse = -inf
+    s = np.array([[-np.inf, -np.inf], [0.0, 1.0]])
+    p, lse = ref.probs_head(s)
+    assert np.all(p[0] == 0) and lse[0] == -np.inf
+    assert np.allclose(p[1].sum(), 1.0)
+
+
+def test_sample_rows():
+    r = ref.sample_rows(8192, 64, 1000)
+    assert len(r) == 64 and len(set(r.tolist())) == 64 and r[0] == 0 and r[-1] == 8191
+    assert np.array_equal(r, ref.sample_rows(8192, 64, 1000))
+    assert np.array_equal(ref.sample_rows(10, 64, 0), np.arange(10))
+
+
+def test_lse_magnitude():
+    # N(0,1) inputs with scale 1/sqrt(D): scores ~ N(0,1), lse ~ ln N + 1/2 (loose sanity range)
+    q, k, v = rand(1, 1, 64, 512), rand(1, 1, 256, 512), rand(1, 1, 256, 512)
+    _, lse = ref.attn_fwd(q, k, v)
+    assert abs(lse.mean() - (math.log(256) + 0.5)) < 0.3
+
+
+# ---------------------------------------------------------------- the pins bite
+class _Mutant:
+    """A copy of the oracle's module namespace with one function replaced."""
+
+    def __init__(self, **over):
+        for name in dir(ref):
+            if not name.startswith("__"):
+                setattr(self, name, getattr(ref, name))
+        for name, fn in over.items():
+            setattr(self, name, fn)
+        # rebind the module-level helpers the public functions use
+        self._bound = over
+
+
+def _mutant_module(**over):
+    import importlib.util
+    spec = importlib.util.spec_from_file_location("attn_ref_mutant", ref.__file__)
+    mod = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(mod)
+    for name, fn in over.items():
+        setattr(mod, name, fn(mod))
+    return mod
+
+
+def _mut_no_scale(mod):
+    orig = mod.scores_head
+    return lambda q, k, bias, b, h, g, scale, causal, rows=None, cols=None: orig(q, k, bias, b, h, g, 1.0, causal, rows, cols)
+
+
+def _mut_causal_flipped(mod):
+    orig = mod.scores_head
+
+    def f(q, k, bias, b, h, g, scale, causal, rows=None, cols=None):
+        if not causal:
+            return orig(q, k, bias, b, h, g, scale, False, rows, cols)
+        s = orig(q, k, bias, b, h, g, scale, False, rows, cols)
+        r = np.arange(q.shape[2]) if rows is None else np.asarray(rows)
+        c = np.arange(k.shape[2]) if cols is None else np.asarray(cols)
+        return np.where(c[None, :] < r[:, None], -np.inf, s)
+    return f
+
+
+def _mut_gqa_modulo(mod):
+    return lambda h, hq, hkv: h % hkv
+
+
+def _mut_lse_log2(mod):
+    orig = mod.probs_head
+
+    def f(s):
+        p, lse = orig(s)
+        return p, lse / math.log(2)
+    return f
+
+
+def _mut_bias_sign(mod):
+    orig = mod._bias_rows
+    return lambda bias, b, h, rows, nkv: (lambda r: r if np.isscalar(r) else -r)(orig(bias, b, h, rows, nkv))
+
+
+def _mut_bwd_delta_dropped(mod):
+    def f(q, k, v, do, bias=None, causal=False, scale=None):
+        q, k, v, do = (np.asarray(x, dtype=np.float64) for x in (q, k, v, do))
+        scale = 1.0 / math.sqrt(q.shape[3]) if scale is None else scale
+        dq, dk, dv = np.zeros(q.shape), np.zeros(k.shape), np.zeros(v.shape)
+        for b in range(q.shape[0]):
+            for h in range(q.shape[1]):
+                g = mod.kv_head_of(h, q.shape[1], k.shape[1])
+                p, _ = mod.probs_head(mod.scores_head(q, k, bias, b, h, g, scale, causal))
+                dv[b, g] += p.T @ do[b, h]
+                ds = p * (do[b, h] @ v[b, g].T)          # Delta term dropped
+                dq[b, h] = scale * (ds @ k[b, g])
+                dk[b, g] += scale * (ds.T @ q[b, h])
+        return dq, dk, dv
+    return f
+
+
+def _mut_pv_transposed_v(mod):
+    orig = mod.attn_fwd
+
+    def f(q, k, v, bias=None, causal=False, scale=None):
+        v = np.asarray(v, dtype=np.float64)
+        if v.shape[2] == v.shape[3]:
+            v = np.swapaxes(v, 2, 3)
+        else:
+            v = v[:, :, ::-1]                             # wrong row order instead
+        return orig(q, k, v, bias, causal, scale)
+    return f
+
+
+MUTANTS = {
+    "no_scale": {"scores_head": _mut_no_scale},
+    "causal_flipped": {"scores_head": _mut_causal_flipped},
+    "gqa_modulo": {"kv_head_of": _mut_gqa_modulo},
+    "lse_log2": {"probs_head": _mut_lse_log2},
+    "bias_sign": {"_bias_rows": _mut_bias_sign},
+    "bwd_delta_dropped": {"attn_bwd": _mut_bwd_delta_dropped},
+    "pv_wrong_v": {"attn_fwd": _mut_pv_transposed_v},
+}
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_pins_catch_planted_mistake(name):
+    mod = _mutant_module(**MUTANTS[name])
+    caught = []
+    for pin in PINS:
+        try:
+            pin(mod)
+        except AssertionError:
+            caught.append(pin.__name__)
+        except Exception:
+            caught.append(pin.__name__ + "!")
+    assert caught, f"no pin catches mutant {name}"
