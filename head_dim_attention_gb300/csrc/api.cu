@@ -1,0 +1,319 @@
+// C ABI: argument validation, TMA descriptor encoding and dispatch.
+// Every check runs on the host before anything is enqueued; on failure the
+// call returns a status and launches nothing.
+#include <cmath>
+#include <cstring>
+#include <mutex>
+
+#include "ffpa.h"
+#include "internal.h"
+
+namespace ffpa {
+
+// Per-device status word, set by kernels whose bounded waits expire.
+__device__ uint32_t g_status_word;
+
+uint32_t* device_status_word() {
+  static std::mutex mu;
+  static uint32_t* cache[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!cache[dev]) {
+    void* ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_status_word) != cudaSuccess) return nullptr;
+    cache[dev] = static_cast<uint32_t*>(ptr);
+  }
+  return cache[dev];
+}
+
+bool dtype_is_bf16(int dtype) { return dtype == FFPA_BF16; }
+
+namespace {
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+struct Shape4 {
+  int64_t B, H, N, D;
+};
+
+bool is_half_dtype(int dt) { return dt == FFPA_F16 || dt == FFPA_BF16; }
+
+// Validate one [B, H, N, D] half-precision tensor.
+int check_bhnd(const ffpa_tensor_t* t, int dtype, const Shape4& want) {
+  if (!t || !t->data || t->reserved != 0) return FFPA_ERR_INVALID_ARG;
+  if (t->dtype != dtype) return is_half_dtype(t->dtype) ? FFPA_ERR_INVALID_ARG : FFPA_ERR_UNSUPPORTED;
+  if (t->shape[0] != want.B || t->shape[1] != want.H || t->shape[2] != want.N || t->shape[3] != want.D)
+    return FFPA_ERR_INVALID_ARG;
+  if (t->stride[3] != 1) return FFPA_ERR_UNSUPPORTED;
+  if (reinterpret_cast<uintptr_t>(t->data) % 16 != 0) return FFPA_ERR_ALIGNMENT;
+  for (int i = 0; i < 3; ++i) {
+    if (t->shape[i] > 1 && (t->stride[i] <= 0 || t->stride[i] % 8 != 0)) return FFPA_ERR_ALIGNMENT;
+  }
+  return FFPA_OK;
+}
+
+// Natural strides for size-1 dims so the TMA descriptor sees a well-formed map.
+void tma_strides(const ffpa_tensor_t* t, int64_t out[3]) {
+  // out[0] = row stride, out[1] = head stride, out[2] = batch stride (elements)
+  int64_t sn = t->shape[2] > 1 ? t->stride[2] : t->shape[3];
+  int64_t sh = t->shape[1] > 1 ? t->stride[1] : sn * t->shape[2];
+  int64_t sb = t->shape[0] > 1 ? t->stride[0] : sh * t->shape[1];
+  out[0] = sn;
+  out[1] = sh;
+  out[2] = sb;
+}
+
+int encode_map(CUtensorMap* m, const ffpa_tensor_t* t) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return FFPA_ERR_CUDA;
+  int64_t st[3];
+  tma_strides(t, st);
+  const cuuint64_t dims[4] = {(cuuint64_t)t->shape[3], (cuuint64_t)t->shape[2], (cuuint64_t)t->shape[1],
+                              (cuuint64_t)t->shape[0]};
+  const cuuint64_t strides[3] = {(cuuint64_t)st[0] * 2, (cuuint64_t)st[1] * 2, (cuuint64_t)st[2] * 2};
+  const cuuint32_t box[4] = {(cuuint32_t)kChunk, (cuuint32_t)kTileRows, 1, 1};
+  const cuuint32_t es[4] = {1, 1, 1, 1};
+  const CUtensorMapDataType dt =
+      t->dtype == FFPA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  CUresult r = enc(m, dt, 4, t->data, dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? FFPA_OK : FFPA_ERR_CUDA;
+}
+
+struct Common {
+  int64_t B, Hq, Hkv, Nq, Nkv, D;
+  int dtype;
+};
+
+int check_common(const ffpa_tensor_t* q, const ffpa_tensor_t* k, const ffpa_tensor_t* v,
+                 const ffpa_tensor_t* bias, float scale, Common* c) {
+  if (!q || !k || !v) return FFPA_ERR_INVALID_ARG;
+  if (!is_half_dtype(q->dtype)) return FFPA_ERR_UNSUPPORTED;
+  c->dtype = q->dtype;
+  c->B = q->shape[0];
+  c->Hq = q->shape[1];
+  c->Nq = q->shape[2];
+  c->D = q->shape[3];
+  c->Hkv = k->shape[1];
+  c->Nkv = k->shape[2];
+  if (c->B < 1 || c->Hq < 1 || c->Hkv < 1 || c->Nq < 1 || c->Nkv < 1 || c->D < 1) return FFPA_ERR_INVALID_ARG;
+  if (c->B > 65535 || c->Hq > 65535 || c->Nq > (1ll << 30) || c->Nkv > (1ll << 30)) return FFPA_ERR_UNSUPPORTED;
+  if (c->Hq % c->Hkv != 0) return FFPA_ERR_INVALID_ARG;
+  if (c->D % 64 != 0 || c->D < 64 || c->D > 1024) return FFPA_ERR_UNSUPPORTED;
+  if (!std::isfinite(scale) || !(scale > 0.f)) return FFPA_ERR_INVALID_ARG;
+  int rc = check_bhnd(q, c->dtype, {c->B, c->Hq, c->Nq, c->D});
+  if (rc) return rc;
+  rc = check_bhnd(k, c->dtype, {c->B, c->Hkv, c->Nkv, c->D});
+  if (rc) return rc;
+  rc = check_bhnd(v, c->dtype, {c->B, c->Hkv, c->Nkv, c->D});
+  if (rc) return rc;
+  if (bias) {
+    if (!bias->data || bias->reserved != 0) return FFPA_ERR_INVALID_ARG;
+    if (bias->dtype != FFPA_F32) return FFPA_ERR_UNSUPPORTED;
+    const int64_t* s = bias->shape;
+    if (!(s[0] == 1 || s[0] == c->B) || !(s[1] == 1 || s[1] == c->Hq) || !(s[2] == 1 || s[2] == c->Nq) ||
+        s[3] != c->Nkv)
+      return FFPA_ERR_INVALID_ARG;
+    if (reinterpret_cast<uintptr_t>(bias->data) % 4 != 0) return FFPA_ERR_ALIGNMENT;
+  }
+  return FFPA_OK;
+}
+
+int check_lse(const ffpa_tensor_t* lse, const Common& c) {
+  if (!lse->data || lse->reserved != 0) return FFPA_ERR_INVALID_ARG;
+  if (lse->dtype != FFPA_F32) return FFPA_ERR_UNSUPPORTED;
+  if (lse->shape[0] != c.B || lse->shape[1] != c.Hq || lse->shape[2] != c.Nq || lse->shape[3] != 1)
+    return FFPA_ERR_INVALID_ARG;
+  // contiguous [B, Hq, Nq]
+  if ((c.Nq > 1 && lse->stride[2] != 1) || (c.Hq > 1 && lse->stride[1] != c.Nq) ||
+      (c.B > 1 && lse->stride[0] != c.Hq * c.Nq))
+    return FFPA_ERR_UNSUPPORTED;
+  if (reinterpret_cast<uintptr_t>(lse->data) % 4 != 0) return FFPA_ERR_ALIGNMENT;
+  return FFPA_OK;
+}
+
+void bias_strides(const ffpa_tensor_t* bias, int64_t* sb, int64_t* sh, int64_t* sq, int64_t* sk) {
+  if (!bias) {
+    *sb = *sh = *sq = *sk = 0;
+    return;
+  }
+  *sb = bias->shape[0] > 1 ? bias->stride[0] : 0;
+  *sh = bias->shape[1] > 1 ? bias->stride[1] : 0;
+  *sq = bias->shape[2] > 1 ? bias->stride[2] : 0;
+  *sk = bias->stride[3];
+}
+
+int cuda_rc(cudaError_t e) { return e == cudaSuccess ? FFPA_OK : FFPA_ERR_CUDA; }
+
+constexpr int kDecodeMaxRows = 16;
+constexpr float kLog2e = 1.4426950408889634f;
+
+}  // namespace
+}  // namespace ffpa
+
+using namespace ffpa;
+
+extern "C" int ffpa_fwd(const ffpa_tensor_t* q, const ffpa_tensor_t* k, const ffpa_tensor_t* v,
+                        const ffpa_tensor_t* bias, int causal, float scale, const ffpa_tensor_t* out,
+                        const ffpa_tensor_t* lse, ffpa_stream_t stream) {
+  Common c;
+  int rc = check_common(q, k, v, bias, scale, &c);
+  if (rc) return rc;
+  if (causal != 0 && causal != 1) return FFPA_ERR_INVALID_ARG;
+  rc = check_bhnd(out, c.dtype, {c.B, c.Hq, c.Nq, c.D});
+  if (rc) return rc;
+  if (lse && (rc = check_lse(lse, c))) return rc;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  uint32_t* status = device_status_word();
+  if (!status) return FFPA_ERR_CUDA;
+  const bool bf16 = dtype_is_bf16(c.dtype);
+  int64_t bsb, bsh, bsq, bsk;
+  bias_strides(bias, &bsb, &bsh, &bsq, &bsk);
+
+  if (c.Nq <= kDecodeMaxRows) {
+    DecodeParams p = {};
+    p.q = q->data;
+    p.k = k->data;
+    p.v = v->data;
+    p.out = out->data;
+    p.lse = lse ? static_cast<float*>(lse->data) : nullptr;
+    p.bias = bias ? static_cast<const float*>(bias->data) : nullptr;
+    p.q_sb = q->stride[0]; p.q_sh = q->stride[1]; p.q_sn = q->stride[2];
+    p.k_sb = k->stride[0]; p.k_sh = k->stride[1]; p.k_sn = k->stride[2];
+    p.v_sb = v->stride[0]; p.v_sh = v->stride[1]; p.v_sn = v->stride[2];
+    p.o_sb = out->stride[0]; p.o_sh = out->stride[1]; p.o_sn = out->stride[2];
+    p.bias_sb = bsb; p.bias_sh = bsh; p.bias_sq = bsq; p.bias_sk = bsk;
+    p.B = (int)c.B; p.Hq = (int)c.Hq; p.Hkv = (int)c.Hkv; p.Nq = (int)c.Nq; p.Nkv = (int)c.Nkv; p.D = (int)c.D;
+    p.group = (int)(c.Hq / c.Hkv);
+    p.causal = causal;
+    p.scale_log2 = scale * kLog2e;
+    p.split_len = 128;
+    p.n_splits = (int)((c.Nkv + p.split_len - 1) / p.split_len);
+    const size_t n_rows = (size_t)c.B * c.Hq * c.Nq * p.n_splits;
+    void* scratch = nullptr;
+    const size_t o_bytes = n_rows * c.D * sizeof(float), ml_bytes = n_rows * 2 * sizeof(float);
+    if (cudaMallocAsync(&scratch, o_bytes + ml_bytes, st) != cudaSuccess) return FFPA_ERR_CUDA;
+    p.part_o = static_cast<float*>(scratch);
+    p.part_ml = reinterpret_cast<float*>(static_cast<char*>(scratch) + o_bytes);
+    cudaError_t e = launch_fwd_decode(p, bf16, st);
+    cudaError_t e2 = cudaFreeAsync(scratch, st);
+    return cuda_rc(e != cudaSuccess ? e : e2);
+  }
+
+  FwdParams p = {};
+  p.out = out->data;
+  p.lse = lse ? static_cast<float*>(lse->data) : nullptr;
+  p.bias = bias ? static_cast<const float*>(bias->data) : nullptr;
+  p.o_sb = out->stride[0]; p.o_sh = out->stride[1]; p.o_sn = out->stride[2];
+  p.bias_sb = bsb; p.bias_sh = bsh; p.bias_sq = bsq; p.bias_sk = bsk;
+  p.B = (int)c.B; p.Hq = (int)c.Hq; p.Hkv = (int)c.Hkv; p.Nq = (int)c.Nq; p.Nkv = (int)c.Nkv; p.D = (int)c.D;
+  p.group = (int)(c.Hq / c.Hkv);
+  p.causal = causal;
+  p.scale_log2 = scale * kLog2e;
+  p.n_chunks = (int)(c.D / kChunk);
+  p.q_tiles = (int)((c.Nq + kTileRows - 1) / kTileRows);
+  p.status = status;
+  FwdMaps m;
+  if ((rc = encode_map(&m.q, q)) || (rc = encode_map(&m.k, k)) || (rc = encode_map(&m.v, v))) return rc;
+  return cuda_rc(launch_fwd_main(p, m, bf16, st));
+}
+
+extern "C" int ffpa_bwd(const ffpa_tensor_t* q, const ffpa_tensor_t* k, const ffpa_tensor_t* v,
+                        const ffpa_tensor_t* bias, int causal, float scale, const ffpa_tensor_t* out,
+                        const ffpa_tensor_t* lse, const ffpa_tensor_t* dout, const ffpa_tensor_t* dq,
+                        const ffpa_tensor_t* dk, const ffpa_tensor_t* dv, ffpa_stream_t stream) {
+  Common c;
+  int rc = check_common(q, k, v, bias, scale, &c);
+  if (rc) return rc;
+  if (causal != 0 && causal != 1) return FFPA_ERR_INVALID_ARG;
+  if ((rc = check_bhnd(out, c.dtype, {c.B, c.Hq, c.Nq, c.D}))) return rc;
+  if ((rc = check_bhnd(dout, c.dtype, {c.B, c.Hq, c.Nq, c.D}))) return rc;
+  if ((rc = check_bhnd(dq, c.dtype, {c.B, c.Hq, c.Nq, c.D}))) return rc;
+  if ((rc = check_bhnd(dk, c.dtype, {c.B, c.Hkv, c.Nkv, c.D}))) return rc;
+  if ((rc = check_bhnd(dv, c.dtype, {c.B, c.Hkv, c.Nkv, c.D}))) return rc;
+  if (!lse) return FFPA_ERR_INVALID_ARG;
+  if ((rc = check_lse(lse, c))) return rc;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  uint32_t* status = device_status_word();
+  if (!status) return FFPA_ERR_CUDA;
+  int64_t bsb, bsh, bsq, bsk;
+  bias_strides(bias, &bsb, &bsh, &bsq, &bsk);
+  BwdParams p = {};
+  p.out = out->data;
+  p.dout = dout->data;
+  p.lse = static_cast<const float*>(lse->data);
+  p.bias = bias ? static_cast<const float*>(bias->data) : nullptr;
+  p.dq = dq->data;
+  p.dk = dk->data;
+  p.dv = dv->data;
+  p.o_sb = out->stride[0]; p.o_sh = out->stride[1]; p.o_sn = out->stride[2];
+  p.do_sb = dout->stride[0]; p.do_sh = dout->stride[1]; p.do_sn = dout->stride[2];
+  p.dq_sb = dq->stride[0]; p.dq_sh = dq->stride[1]; p.dq_sn = dq->stride[2];
+  p.dk_sb = dk->stride[0]; p.dk_sh = dk->stride[1]; p.dk_sn = dk->stride[2];
+  p.dv_sb = dv->stride[0]; p.dv_sh = dv->stride[1]; p.dv_sn = dv->stride[2];
+  p.bias_sb = bsb; p.bias_sh = bsh; p.bias_sq = bsq; p.bias_sk = bsk;
+  p.B = (int)c.B; p.Hq = (int)c.Hq; p.Hkv = (int)c.Hkv; p.Nq = (int)c.Nq; p.Nkv = (int)c.Nkv; p.D = (int)c.D;
+  p.group = (int)(c.Hq / c.Hkv);
+  p.causal = causal;
+  p.scale = scale;
+  p.scale_log2 = scale * kLog2e;
+  p.n_chunks = (int)(c.D / kChunk);
+  p.q_tiles = (int)((c.Nq + kTileRows - 1) / kTileRows);
+  p.kv_tiles = (int)((c.Nkv + kTileRows - 1) / kTileRows);
+  p.status = status;
+  BwdMaps m;
+  if ((rc = encode_map(&m.q, q)) || (rc = encode_map(&m.k, k)) || (rc = encode_map(&m.v, v)) ||
+      (rc = encode_map(&m.dout, dout)))
+    return rc;
+  const size_t rows = (size_t)c.B * c.Hq * c.Nq;
+  void* scratch = nullptr;
+  if (cudaMallocAsync(&scratch, rows * 2 * sizeof(float), st) != cudaSuccess) return FFPA_ERR_CUDA;
+  p.delta = static_cast<float*>(scratch);
+  p.lse2 = p.delta + rows;
+  cudaError_t e = launch_bwd(p, m, dtype_is_bf16(c.dtype), st);
+  cudaError_t e2 = cudaFreeAsync(scratch, st);
+  return cuda_rc(e != cudaSuccess ? e : e2);
+}
+
+extern "C" const char* ffpa_status_string(int status) {
+  switch (status) {
+    case FFPA_OK: return "ok";
+    case FFPA_ERR_INVALID_ARG: return "invalid argument";
+    case FFPA_ERR_UNSUPPORTED: return "unsupported dtype, head dimension or layout";
+    case FFPA_ERR_ALIGNMENT: return "pointer or stride not aligned for TMA (16 bytes)";
+    case FFPA_ERR_CUDA: return "CUDA runtime or launch error";
+    case FFPA_ERR_TIMEOUT: return "a kernel's bounded wait timed out";
+    default: return "unknown status";
+  }
+}
+
+extern "C" int ffpa_check_status(ffpa_stream_t stream) {
+  if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return FFPA_ERR_CUDA;
+  uint32_t v = 0;
+  if (cudaMemcpyFromSymbol(&v, g_status_word, sizeof(v)) != cudaSuccess) return FFPA_ERR_CUDA;
+  if (v != 0) {
+    const uint32_t zero = 0;
+    if (cudaMemcpyToSymbol(g_status_word, &zero, sizeof(zero)) != cudaSuccess) return FFPA_ERR_CUDA;
+    return FFPA_ERR_TIMEOUT;
+  }
+  return FFPA_OK;
+}
+
+extern "C" int ffpa_version(void) { return 100; }

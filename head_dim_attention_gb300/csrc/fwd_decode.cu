@@ -1,0 +1,262 @@
+// Decode-shaped attention forward (few query rows, many keys) on sm_103a.
+//
+// With Nq <= 16 a tensor-core tile of 128 query rows would be mostly
+// padding, and the work is bound by reading K and V from HBM once (the
+// "decode-attn" case of the FFPA Attention Benchmark page, Nq/Nkv = 1/8192).
+// So the keys are split into slices; each CTA takes one (batch, query head,
+// slice), computes its scores with CUDA-core dot products, a local softmax and
+// an unnormalised partial O, and a second kernel merges the slices with their
+// (max, sum) statistics:
+//     M = max_s m_s,  w_s = 2^(m_s - M),  O = sum_s w_s O_s / sum_s w_s l_s,
+//     lse = (M + log2 sum_s w_s l_s) ln 2.
+// The merge is exact (the same identity the online softmax uses).
+#include <type_traits>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace ffpa {
+namespace {
+
+constexpr int kDecThreads = 256;
+constexpr int kMaxRows = 16;  // Nq limit of this path
+constexpr int kKeysPerIter = 4;
+
+template <bool BF16>
+struct Vec8 {
+  // 8 consecutive elements (16 bytes) converted to fp32
+  __device__ __forceinline__ static void load(const void* ptr, float (&f)[8]) {
+    const uint4 u = __ldg(reinterpret_cast<const uint4*>(ptr));
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      if constexpr (BF16) {
+        const __nv_bfloat162 h = *reinterpret_cast<const __nv_bfloat162*>(&w[i]);
+        const float2 x = __bfloat1622float2(h);
+        f[2 * i] = x.x;
+        f[2 * i + 1] = x.y;
+      } else {
+        const __half2 h = *reinterpret_cast<const __half2*>(&w[i]);
+        const float2 x = __half22float2(h);
+        f[2 * i] = x.x;
+        f[2 * i + 1] = x.y;
+      }
+    }
+  }
+};
+
+// One CTA per (split, query head, batch).  Shared memory: q rows as fp32
+// [Nq][D] and the slice's scores [Nq][split_len].
+template <bool BF16>
+__global__ void __launch_bounds__(kDecThreads) decode_split_kernel(const __grid_constant__ DecodeParams p) {
+  extern __shared__ __align__(16) float dsm[];
+  const int split = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+  const int g = h / p.group;
+  const int D = p.D, Nq = p.Nq, L = p.split_len;
+  float* q_s = dsm;           // [Nq][D]
+  float* sc = dsm + Nq * D;   // [Nq][L]
+  float* stat = sc + Nq * L;  // [Nq][2]
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int kv_begin = split * L;
+  const int kv_len = min(L, p.Nkv - kv_begin);
+  typedef typename std::conditional<BF16, __nv_bfloat16, __half>::type T;
+
+  // q rows -> fp32 smem
+  for (int i = tid; i < Nq * (D / 8); i += kDecThreads) {
+    const int r = i / (D / 8), c = (i % (D / 8)) * 8;
+    float f[8];
+    Vec8<BF16>::load(reinterpret_cast<const T*>(p.q) + b * p.q_sb + h * p.q_sh + static_cast<int64_t>(r) * p.q_sn + c,
+                     f);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) q_s[r * D + c + e] = f[e];
+  }
+  __syncthreads();
+
+  // scores: warps stride over keys, lanes over D in 8-element groups
+  const T* kbase = reinterpret_cast<const T*>(p.k) + b * p.k_sb + g * p.k_sh;
+  const int groups = D / 8;  // 16-byte groups per row
+  constexpr float kLog2e = 1.4426950408889634f;
+  for (int j0 = warp * kKeysPerIter; j0 < kv_len; j0 += (kDecThreads / 32) * kKeysPerIter) {
+    float acc[kKeysPerIter][kMaxRows];
+#pragma unroll
+    for (int u = 0; u < kKeysPerIter; ++u)
+#pragma unroll
+      for (int r = 0; r < kMaxRows; ++r) acc[u][r] = 0.f;
+    for (int c = lane; c < groups; c += 32) {
+      float kf[kKeysPerIter][8];
+#pragma unroll
+      for (int u = 0; u < kKeysPerIter; ++u) {
+        const int j = min(j0 + u, kv_len - 1);
+        Vec8<BF16>::load(kbase + static_cast<int64_t>(kv_begin + j) * p.k_sn + c * 8, kf[u]);
+      }
+#pragma unroll
+      for (int r = 0; r < kMaxRows; ++r) {
+        if (r < Nq) {
+          const float4 qa = *reinterpret_cast<const float4*>(&q_s[r * D + c * 8]);
+          const float4 qb = *reinterpret_cast<const float4*>(&q_s[r * D + c * 8 + 4]);
+#pragma unroll
+          for (int u = 0; u < kKeysPerIter; ++u)
+            acc[u][r] += qa.x * kf[u][0] + qa.y * kf[u][1] + qa.z * kf[u][2] + qa.w * kf[u][3] + qb.x * kf[u][4] +
+                         qb.y * kf[u][5] + qb.z * kf[u][6] + qb.w * kf[u][7];
+        }
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kKeysPerIter; ++u) {
+#pragma unroll
+      for (int r = 0; r < kMaxRows; ++r) {
+        if (r < Nq) {
+          float v = acc[u][r];
+#pragma unroll
+          for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+          const int j = j0 + u;
+          if (lane == 0 && j < kv_len) {
+            const int kv = kv_begin + j;
+            float x = v * p.scale_log2;
+            if (p.bias)
+              x = fmaf(__ldg(p.bias + b * p.bias_sb + h * p.bias_sh + static_cast<int64_t>(r) * p.bias_sq +
+                             static_cast<int64_t>(kv) * p.bias_sk),
+                       kLog2e, x);
+            if (p.causal && kv > r) x = -INFINITY;
+            sc[r * L + j] = x;
+          }
+        }
+      }
+    }
+  }
+  __syncthreads();
+
+  // per-row max and sum over the slice (one warp per row)
+  for (int r = warp; r < Nq; r += kDecThreads / 32) {
+    float m = -INFINITY;
+    for (int j = lane; j < kv_len; j += 32) m = fmaxf(m, sc[r * L + j]);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    const float mref = (m == -INFINITY) ? 0.f : m;
+    float l = 0.f;
+    for (int j = lane; j < kv_len; j += 32) {
+      const float e = exp2f(sc[r * L + j] - mref);
+      sc[r * L + j] = e;
+      l += e;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) l += __shfl_xor_sync(0xffffffffu, l, o);
+    if (lane == 0) {
+      stat[2 * r] = m;
+      stat[2 * r + 1] = l;
+    }
+  }
+  __syncthreads();
+
+  // partial O: threads over D (8-element groups), loop over the slice's keys
+  const T* vbase = reinterpret_cast<const T*>(p.v) + b * p.v_sb + g * p.v_sh;
+  for (int c = tid; c < groups; c += kDecThreads) {
+    float o[kMaxRows][8];
+#pragma unroll
+    for (int r = 0; r < kMaxRows; ++r)
+#pragma unroll
+      for (int e = 0; e < 8; ++e) o[r][e] = 0.f;
+    int j = 0;
+    for (; j + 4 <= kv_len; j += 4) {
+      float vf[4][8];
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        Vec8<BF16>::load(vbase + static_cast<int64_t>(kv_begin + j + u) * p.v_sn + c * 8, vf[u]);
+#pragma unroll
+      for (int r = 0; r < kMaxRows; ++r) {
+        if (r < Nq) {
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const float w = sc[r * L + j + u];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) o[r][e] = fmaf(w, vf[u][e], o[r][e]);
+          }
+        }
+      }
+    }
+    for (; j < kv_len; ++j) {
+      float vf[8];
+      Vec8<BF16>::load(vbase + static_cast<int64_t>(kv_begin + j) * p.v_sn + c * 8, vf);
+#pragma unroll
+      for (int r = 0; r < kMaxRows; ++r)
+        if (r < Nq) {
+          const float w = sc[r * L + j];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) o[r][e] = fmaf(w, vf[e], o[r][e]);
+        }
+    }
+#pragma unroll
+    for (int r = 0; r < kMaxRows; ++r) {
+      if (r < Nq) {
+        float* dst = p.part_o + ((((static_cast<int64_t>(b) * p.Hq + h) * Nq + r) * p.n_splits + split) * D) + c * 8;
+        reinterpret_cast<float4*>(dst)[0] = make_float4(o[r][0], o[r][1], o[r][2], o[r][3]);
+        reinterpret_cast<float4*>(dst)[1] = make_float4(o[r][4], o[r][5], o[r][6], o[r][7]);
+      }
+    }
+  }
+  if (tid < Nq) {
+    float* ml = p.part_ml + (((static_cast<int64_t>(b) * p.Hq + h) * Nq + tid) * p.n_splits + split) * 2;
+    ml[0] = stat[2 * tid];
+    ml[1] = stat[2 * tid + 1];
+  }
+}
+
+// One CTA per (row, query head, batch): merge the slices.
+template <bool BF16>
+__global__ void __launch_bounds__(128) decode_combine_kernel(const __grid_constant__ DecodeParams p) {
+  const int r = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+  const int S = p.n_splits, D = p.D;
+  const int64_t base = ((static_cast<int64_t>(b) * p.Hq + h) * p.Nq + r) * S;
+  const float* ml = p.part_ml + base * 2;
+  float M = -INFINITY;
+  for (int s = 0; s < S; ++s) M = fmaxf(M, ml[2 * s]);
+  const float Mref = (M == -INFINITY) ? 0.f : M;
+  float Lsum = 0.f;
+  for (int s = 0; s < S; ++s) Lsum += exp2f(ml[2 * s] - Mref) * ml[2 * s + 1];
+  const float inv = Lsum > 0.f ? 1.f / Lsum : 0.f;
+  typedef typename std::conditional<BF16, __nv_bfloat16, __half>::type T;
+  T* orow = reinterpret_cast<T*>(p.out) + b * p.o_sb + h * p.o_sh + static_cast<int64_t>(r) * p.o_sn;
+  for (int d = threadIdx.x * 4; d < D; d += blockDim.x * 4) {
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int s = 0; s < S; ++s) {
+      const float w = exp2f(ml[2 * s] - Mref);
+      const float4 o = *reinterpret_cast<const float4*>(p.part_o + (base + s) * D + d);
+      acc.x = fmaf(w, o.x, acc.x);
+      acc.y = fmaf(w, o.y, acc.y);
+      acc.z = fmaf(w, o.z, acc.z);
+      acc.w = fmaf(w, o.w, acc.w);
+    }
+    if constexpr (BF16) {
+      reinterpret_cast<__nv_bfloat162*>(orow + d)[0] = __floats2bfloat162_rn(acc.x * inv, acc.y * inv);
+      reinterpret_cast<__nv_bfloat162*>(orow + d)[1] = __floats2bfloat162_rn(acc.z * inv, acc.w * inv);
+    } else {
+      reinterpret_cast<__half2*>(orow + d)[0] = __floats2half2_rn(acc.x * inv, acc.y * inv);
+      reinterpret_cast<__half2*>(orow + d)[1] = __floats2half2_rn(acc.z * inv, acc.w * inv);
+    }
+  }
+  if (threadIdx.x == 0 && p.lse) {
+    constexpr float kLn2 = 0.6931471805599453f;
+    p.lse[(static_cast<int64_t>(b) * p.Hq + h) * p.Nq + r] = Lsum > 0.f ? (M + __log2f(Lsum)) * kLn2 : -INFINITY;
+  }
+}
+
+template <bool BF16>
+cudaError_t launch_decode_impl(const DecodeParams& p, cudaStream_t st) {
+  const size_t smem = (static_cast<size_t>(p.Nq) * p.D + static_cast<size_t>(p.Nq) * p.split_len + 2 * p.Nq) * 4;
+  auto k1 = decode_split_kernel<BF16>;
+  cudaError_t e = cudaFuncSetAttribute(k1, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  k1<<<dim3(p.n_splits, p.Hq, p.B), kDecThreads, smem, st>>>(p);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  decode_combine_kernel<BF16><<<dim3(p.Nq, p.Hq, p.B), 128, 0, st>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_fwd_decode(const DecodeParams& p, bool bf16, cudaStream_t s) {
+  return bf16 ? launch_decode_impl<true>(p, s) : launch_decode_impl<false>(p, s);
+}
+
+}  // namespace ffpa

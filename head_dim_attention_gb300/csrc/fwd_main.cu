@@ -1,0 +1,461 @@
+// Fused attention forward for large head dimensions on sm_103a.
+//
+// O = softmax(scale * Q K^T + bias) V and lse (natural log), the plain
+// definition in the attention-kernel-profiler design notes (generate_docs.py,
+// DESIGN section 3, "naive_math"), computed without materialising S: the keys
+// stream in tiles of 128 with an online softmax (running max and sum, lazy
+// rescale of O).
+//
+// Splitting D.  The FFPA pages' idea is to tile finely along the head
+// dimension so on-chip storage per tile stays bounded as D grows (FFPA-Attn
+// Performance Benchmarks page, "Why the Trends Look Like This": shared-memory
+// footprint and register pressure at large D).  On GB300 the binding on-chip
+// store is TMEM (512 fp32 columns x 128 lanes per SM): a 128 x 512 fp32 O
+// accumulator alone fills it.  So a cluster of two CTAs owns one 128-row
+// query tile and splits D in 64-column chunks between them:
+//   * CTA r holds Q[:, own chunks] resident in SMEM and its half of O in TMEM
+//     (<= 256 columns per pass);
+//   * it computes the partial score tile S_r = Q[:, own] K[:, own]^T with
+//     tcgen05.mma into TMEM (double-buffered, 2 x 128 columns);
+//   * the pair swaps the 128 x 128 fp32 partials through distributed shared
+//     memory (st.async with mbarrier complete_tx) and both add them, so both
+//     hold the exact S tile and run the same softmax;
+//   * P (f16/bf16) is written back into the S buffer in TMEM and used as the
+//     A operand of O[:, own] += P V[:, own].
+// With D <= 256 a single CTA holds all of O and no exchange is needed.
+// When a CTA owns more than 4 chunks (D > 512) it sweeps the keys once per
+// 4-chunk slice of its O columns ("passes"), recomputing S each time.
+//
+// Warp roles (256 threads): warp 0 = TMA producer, warp 1 = TMEM owner and
+// MMA issuer, warps 4-7 = softmax / correction / epilogue (one query row per
+// thread; warp 4+w reads TMEM lanes 32w..32w+31).
+#include <type_traits>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace ffpa {
+namespace {
+
+constexpr int kThreads = 256;
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kS0 = 256, kS1 = 384;  // TMEM columns of the two S/P buffers
+constexpr int kMaxOChunksPerPass = 4;     // O columns per pass: 4 x 64 = 256
+constexpr float kRescaleLog2 = 8.0f;      // rescale O only when the max grows by > 2^8
+constexpr int kLandingBytes = kTileRows * kTileRows * 4;  // 64 KB partial-S landing buffer
+
+struct Bars {
+  // indices into the barrier array
+  int full, empty, q_full, s_full, p_ready, o_ready, o_free, xfull, xfree, drain, count;
+};
+__host__ __device__ inline Bars bar_layout(int stages) {
+  Bars b;
+  b.full = 0;
+  b.empty = stages;
+  b.q_full = 2 * stages;
+  b.s_full = b.q_full + 1;   // 2
+  b.p_ready = b.s_full + 2;  // 2
+  b.o_ready = b.p_ready + 2;
+  b.o_free = b.o_ready + 1;
+  b.xfull = b.o_free + 1;
+  b.xfree = b.xfull + 1;
+  b.drain = b.xfree + 1;
+  b.count = b.drain + 1;
+  return b;
+}
+
+struct SmemPlan {
+  int own_max;  // chunks of the larger half
+  int q_off, ring_off, land_off, bar_off, total;
+};
+__host__ __device__ inline SmemPlan smem_plan(int n_chunks, int cs, int stages) {
+  SmemPlan s;
+  s.own_max = (n_chunks + cs - 1) / cs;
+  s.q_off = 0;
+  s.ring_off = s.own_max * kChunkBytes;
+  s.land_off = s.ring_off + stages * kChunkBytes;
+  s.bar_off = s.land_off + (cs == 2 ? kLandingBytes : 0);
+  s.total = s.bar_off + 1024;  // barriers + TMEM slot
+  return s;
+}
+
+template <bool BF16>
+__device__ __forceinline__ uint32_t pack2(float a, float b) {
+  if constexpr (BF16) {
+    __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+    return *reinterpret_cast<uint32_t*>(&h);
+  } else {
+    __half2 h = __floats2half2_rn(a, b);
+    return *reinterpret_cast<uint32_t*>(&h);
+  }
+}
+
+template <int CS, bool BF16>
+__global__ void __launch_bounds__(kThreads, 1)
+    fwd_main_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
+                    const __grid_constant__ CUtensorMap map_v, const __grid_constant__ FwdParams p) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int stages = p.stages;
+  const SmemPlan plan = smem_plan(p.n_chunks, CS, stages);
+  const Bars bl = bar_layout(stages);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + plan.bar_off);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + bl.count);
+  auto bar = [&](int i) { return smem_u32(&bars[i]); };
+  const uint32_t s_base = smem_u32(smem);
+  const uint32_t q_sm = s_base + plan.q_off, ring_sm = s_base + plan.ring_off, land_sm = s_base + plan.land_off;
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const uint32_t rank = (CS == 2) ? cluster_ctarank() : 0;
+  const int qt = p.q_tiles - 1 - static_cast<int>(blockIdx.x) / CS;  // heavy causal tiles first
+  const int h = blockIdx.y, b = blockIdx.z;
+  const int kvh = h / p.group;
+  const int q0 = qt * kTileRows;
+  const int n = p.n_chunks;
+  const int half = (n + CS - 1) / CS;
+  const int own0 = static_cast<int>(rank) * half;
+  const int own_n = min(half, n - own0);
+  const int passes = (half + kMaxOChunksPerPass - 1) / kMaxOChunksPerPass;
+  const int kv_end = p.causal ? min(p.Nkv, q0 + kTileRows) : p.Nkv;
+  const int ntiles = (kv_end + kTileRows - 1) / kTileRows;
+  uint32_t* status = p.status;
+
+  if (tid == 0) {
+    for (int i = 0; i < stages; ++i) {
+      mbar_init(bar(bl.full + i), 1);
+      mbar_init(bar(bl.empty + i), 1);
+    }
+    mbar_init(bar(bl.q_full), 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(bar(bl.s_full + i), 1);
+      mbar_init(bar(bl.p_ready + i), 4);
+    }
+    mbar_init(bar(bl.o_ready), 1);
+    mbar_init(bar(bl.o_free), 4);
+    mbar_init(bar(bl.xfull), 1);
+    mbar_init(bar(bl.xfree), kTileRows);
+    mbar_init(bar(bl.drain), 1);
+    fence_mbar_init();
+    if (CS == 2) mbar_expect_tx(bar(bl.xfull), kLandingBytes);  // arm exchange 0
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (CS == 2) cluster_sync();
+  tc_fence_after();
+  const uint32_t tbase = *tmem_slot;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      tma_prefetch_desc(&map_q);
+      tma_prefetch_desc(&map_k);
+      tma_prefetch_desc(&map_v);
+      bool ok = true;
+      mbar_expect_tx(bar(bl.q_full), own_n * kChunkBytes);
+      for (int c = 0; c < own_n; ++c)
+        tma_load_4d(q_sm + c * kChunkBytes, &map_q, bar(bl.q_full), (own0 + c) * kChunk, q0, h, b);
+      uint32_t it = 0;
+      auto load = [&](const CUtensorMap* m, int dcol, int row) {
+        const uint32_t s = it % stages, r = it / stages;
+        if (ok) ok = mbar_wait(bar(bl.empty + s), (r & 1) ^ 1, status);
+        if (ok) {
+          mbar_expect_tx(bar(bl.full + s), kChunkBytes);
+          tma_load_4d(ring_sm + s * kChunkBytes, m, bar(bl.full + s), dcol, row, kvh, b);
+          ++it;
+        }
+      };
+      for (int pass = 0; pass < passes && ok; ++pass) {
+        const int oc0 = pass * kMaxOChunksPerPass;
+        const int oc_n = max(0, min(kMaxOChunksPerPass, own_n - oc0));
+        for (int j = 0; j <= ntiles && ok; ++j) {
+          if (j < ntiles)
+            for (int c = 0; c < own_n; ++c) load(&map_k, (own0 + c) * kChunk, j * kTileRows);
+          if (j >= 1)
+            for (int c = 0; c < oc_n; ++c) load(&map_v, (own0 + oc0 + c) * kChunk, (j - 1) * kTileRows);
+        }
+      }
+      // Drain: every load this CTA issued has landed before the CTA can exit.
+      for (uint32_t u = (it > (uint32_t)stages ? it - stages : 0); u < it; ++u)
+        mbar_wait(bar(bl.full + u % stages), (u / stages) & 1, status);
+      mbar_wait(bar(bl.q_full), 0, status);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      const uint32_t idesc_s = idesc_f16(BF16, 128, 128, false, false);
+      const uint32_t idesc_pv = idesc_f16(BF16, 128, 64, false, true);
+      bool ok = mbar_wait(bar(bl.q_full), 0, status);
+      tc_fence_after();
+      uint32_t it = 0;
+      int t0 = 0;  // global tile counter at the start of the pass
+      for (int pass = 0; pass < passes && ok; ++pass) {
+        const int oc0 = pass * kMaxOChunksPerPass;
+        const int oc_n = max(0, min(kMaxOChunksPerPass, own_n - oc0));
+        if (pass > 0) {
+          ok = mbar_wait(bar(bl.o_free), (pass - 1) & 1, status);  // epilogue done reading O
+          tc_fence_after();
+        }
+        for (int j = 0; j <= ntiles && ok; ++j) {
+          if (j < ntiles) {
+            const int t = t0 + j;
+            const uint32_t s_tm = tbase + ((t & 1) ? kS1 : kS0);
+            for (int c = 0; c < own_n && ok; ++c) {
+              const uint32_t s = it % stages;
+              ok = mbar_wait(bar(bl.full + s), (it / stages) & 1, status);
+              if (!ok) break;
+              tc_fence_after();
+              const uint32_t a0 = q_sm + c * kChunkBytes, b0 = ring_sm + s * kChunkBytes;
+#pragma unroll
+              for (int kk = 0; kk < 4; ++kk)
+                umma_ss(s_tm, sdesc_sw128(a0 + kk * 32, 16, 1024), sdesc_sw128(b0 + kk * 32, 16, 1024), idesc_s,
+                        (c | kk) != 0);
+              umma_commit(bar(bl.empty + s));
+              ++it;
+            }
+            umma_commit(bar(bl.s_full + (t & 1)));
+          }
+          if (j >= 1 && ok) {
+            const int t = t0 + j - 1;
+            ok = mbar_wait(bar(bl.p_ready + (t & 1)), (t >> 1) & 1, status);
+            if (!ok) break;
+            tc_fence_after();
+            const uint32_t p_tm = tbase + ((t & 1) ? kS1 : kS0);
+            for (int c = 0; c < oc_n && ok; ++c) {
+              const uint32_t s = it % stages;
+              ok = mbar_wait(bar(bl.full + s), (it / stages) & 1, status);
+              if (!ok) break;
+              tc_fence_after();
+              const uint32_t b0 = ring_sm + s * kChunkBytes;
+#pragma unroll
+              for (int kk = 0; kk < 8; ++kk)
+                umma_ts(tbase + c * kChunk, p_tm + kk * 8, sdesc_sw128(b0 + kk * 2048, 16384, 1024), idesc_pv,
+                        (j - 1 > 0 || kk > 0));
+              umma_commit(bar(bl.empty + s));
+              ++it;
+            }
+            umma_commit(bar(bl.o_ready));
+          }
+        }
+        t0 += ntiles;
+      }
+      umma_commit(bar(bl.drain));
+      mbar_wait(bar(bl.drain), 0, status);
+    }
+  } else if (warp >= 4) {
+    // ------------------------------------------------------------ softmax / correction / epilogue
+    const int r = tid - 128;  // query row within the tile == TMEM lane
+    const int row = q0 + r;
+    const uint32_t lane_off = static_cast<uint32_t>((warp - 4) * 32) << 16;
+    const uint32_t peer = rank ^ 1u;
+    const uint32_t peer_land = (CS == 2) ? mapa(land_sm, peer) : 0;
+    const uint32_t peer_xfull = (CS == 2) ? mapa(bar(bl.xfull), peer) : 0;
+    const uint32_t peer_xfree = (CS == 2) ? mapa(bar(bl.xfree), peer) : 0;
+    const uint32_t swz = static_cast<uint32_t>(r & 7);
+    const float* bias_row = nullptr;
+    if (p.bias)
+      bias_row = p.bias + b * p.bias_sb + h * p.bias_sh + static_cast<int64_t>(min(row, p.Nq - 1)) * p.bias_sq;
+    constexpr float kLog2e = 1.4426950408889634f;
+    bool ok = true;
+    int t0 = 0;
+    float m_used = -INFINITY, l_sum = 0.f;
+    for (int pass = 0; pass < passes && ok; ++pass) {
+      const int oc0 = pass * kMaxOChunksPerPass;
+      const int oc_n = max(0, min(kMaxOChunksPerPass, own_n - oc0));
+      m_used = -INFINITY;
+      l_sum = 0.f;
+      for (int j = 0; j < ntiles; ++j) {
+        const int t = t0 + j;
+        const uint32_t s_col = (t & 1) ? kS1 : kS0;
+        ok = __all_sync(0xffffffffu, mbar_wait(bar(bl.s_full + (t & 1)), (t >> 1) & 1, status));
+        if (!ok) break;
+        tc_fence_after();
+        float s[128];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint32_t v[32];
+          tmem_ld32(tbase + lane_off + s_col + c * 32, v);
+          tmem_ld_wait();
+#pragma unroll
+          for (int i = 0; i < 32; ++i) s[c * 32 + i] = __uint_as_float(v[i]);
+        }
+        if constexpr (CS == 2) {
+          // swap partial scores with the peer CTA (it holds the other half of D)
+          if (t >= 1) {
+            ok = __all_sync(0xffffffffu, mbar_wait(bar(bl.xfree), (t - 1) & 1, status));
+            if (!ok) break;
+          }
+          const uint32_t dst = peer_land + r * 512;
+#pragma unroll
+          for (int c = 0; c < 32; ++c)
+            st_async_v4(dst + ((c ^ swz) << 4), s[4 * c], s[4 * c + 1], s[4 * c + 2], s[4 * c + 3], peer_xfull);
+          ok = __all_sync(0xffffffffu, mbar_wait(bar(bl.xfull), t & 1, status));
+          if (!ok) break;
+          const float4* src = reinterpret_cast<const float4*>(smem + plan.land_off + r * 512);
+#pragma unroll
+          for (int c = 0; c < 32; ++c) {
+            const float4 v = src[c ^ swz];
+            s[4 * c] += v.x;
+            s[4 * c + 1] += v.y;
+            s[4 * c + 2] += v.z;
+            s[4 * c + 3] += v.w;
+          }
+          if (r == 0) mbar_expect_tx(bar(bl.xfull), kLandingBytes);  // arm the next exchange
+          mbar_arrive_remote(peer_xfree);                            // my landing buffer is free again
+        }
+        // scale (log2 domain), bias, masks
+        const int kv0 = j * kTileRows;
+        float m_tile = -INFINITY;
+        const bool masked = (kv0 + kTileRows > p.Nkv) || (p.causal && kv0 + kTileRows - 1 > row);
+#pragma unroll
+        for (int i = 0; i < 128; ++i) {
+          float x = s[i] * p.scale_log2;
+          if (bias_row)
+            x = fmaf(__ldg(bias_row + static_cast<int64_t>(kv0 + min(i, p.Nkv - 1 - kv0)) * p.bias_sk), kLog2e, x);
+          if (masked) {
+            const int kv = kv0 + i;
+            if (kv >= p.Nkv || (p.causal && kv > row)) x = -INFINITY;
+          }
+          s[i] = x;
+          m_tile = fmaxf(m_tile, x);
+        }
+        float alpha = 1.f;
+        bool rescale = false;
+        if (m_used == -INFINITY) {
+          m_used = m_tile;
+        } else if (m_tile > m_used + kRescaleLog2) {
+          alpha = exp2f(m_used - m_tile);
+          m_used = m_tile;
+          rescale = true;
+        }
+        const float m_ref = (m_used == -INFINITY) ? 0.f : m_used;
+        float lsum = 0.f;
+        uint32_t pk[64];
+#pragma unroll
+        for (int i = 0; i < 64; ++i) {
+          const float p0 = exp2f(s[2 * i] - m_ref), p1 = exp2f(s[2 * i + 1] - m_ref);
+          lsum += p0 + p1;
+          pk[i] = pack2<BF16>(p0, p1);
+        }
+        l_sum = l_sum * alpha + lsum;
+        {
+          uint32_t(&lo)[32] = *reinterpret_cast<uint32_t(*)[32]>(&pk[0]);
+          uint32_t(&hi)[32] = *reinterpret_cast<uint32_t(*)[32]>(&pk[32]);
+          tmem_st32(tbase + lane_off + s_col, lo);
+          tmem_st32(tbase + lane_off + s_col + 32, hi);
+        }
+        tmem_st_wait();
+        if (__any_sync(0xffffffffu, rescale) && j >= 1) {
+          // correction: O of this row *= alpha, once the previous P V has landed
+          ok = __all_sync(0xffffffffu, mbar_wait(bar(bl.o_ready), (t - 1) & 1, status));
+          if (!ok) break;
+          tc_fence_after();
+          for (int c = 0; c < oc_n; ++c) {
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+              uint32_t v[32];
+              const uint32_t a = tbase + lane_off + c * kChunk + hh * 32;
+              tmem_ld32(a, v);
+              tmem_ld_wait();
+#pragma unroll
+              for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * alpha);
+              tmem_st32(a, v);
+            }
+          }
+          tmem_st_wait();
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(bl.p_ready + (t & 1)));
+      }
+      if (!ok) break;
+      // ---------------------------------------------------------- epilogue
+      const int t_last = t0 + ntiles - 1;
+      ok = __all_sync(0xffffffffu, mbar_wait(bar(bl.o_ready), t_last & 1, status));
+      if (!ok) break;
+      tc_fence_after();
+      const float inv_l = l_sum > 0.f ? 1.f / l_sum : 0.f;
+      typedef typename std::conditional<BF16, __nv_bfloat16, __half>::type T;
+      T* orow = reinterpret_cast<T*>(p.out) + b * p.o_sb + h * p.o_sh + static_cast<int64_t>(row) * p.o_sn;
+      for (int c = 0; c < oc_n; ++c) {
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+          uint32_t v[32];
+          tmem_ld32(tbase + lane_off + c * kChunk + hh * 32, v);
+          tmem_ld_wait();
+          if (row < p.Nq) {
+            uint4* dst = reinterpret_cast<uint4*>(orow + (own0 + oc0 + c) * kChunk + hh * 32);
+#pragma unroll
+            for (int g = 0; g < 4; ++g) {
+              uint4 w;
+              w.x = pack2<BF16>(__uint_as_float(v[8 * g + 0]) * inv_l, __uint_as_float(v[8 * g + 1]) * inv_l);
+              w.y = pack2<BF16>(__uint_as_float(v[8 * g + 2]) * inv_l, __uint_as_float(v[8 * g + 3]) * inv_l);
+              w.z = pack2<BF16>(__uint_as_float(v[8 * g + 4]) * inv_l, __uint_as_float(v[8 * g + 5]) * inv_l);
+              w.w = pack2<BF16>(__uint_as_float(v[8 * g + 6]) * inv_l, __uint_as_float(v[8 * g + 7]) * inv_l);
+              dst[g] = w;
+            }
+          }
+        }
+      }
+      if (pass == 0 && rank == 0 && p.lse && row < p.Nq) {
+        constexpr float kLn2 = 0.6931471805599453f;
+        p.lse[(static_cast<int64_t>(b) * p.Hq + h) * p.Nq + row] =
+            l_sum > 0.f ? (m_used + __log2f(l_sum)) * kLn2 : -INFINITY;
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(bl.o_free));
+      t0 += ntiles;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (CS == 2) cluster_sync();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tbase, kTmemCols);
+  }
+}
+
+template <int CS, bool BF16>
+cudaError_t launch_impl(const FwdParams& p_in, const FwdMaps& m, cudaStream_t st) {
+  FwdParams p = p_in;
+  constexpr int kMaxSmem = 232448;  // 227 KB opt-in per block
+  const SmemPlan base = smem_plan(p.n_chunks, CS, 0);
+  int stages = (kMaxSmem - 1024 - base.total) / kChunkBytes;
+  stages = stages > 8 ? 8 : stages;
+  if (stages < 2) return cudaErrorInvalidConfiguration;
+  p.stages = stages;
+  const SmemPlan plan = smem_plan(p.n_chunks, CS, stages);
+  const int smem = plan.total + 1024;  // + alignment slack
+  auto kern = fwd_main_kernel<CS, BF16>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(CS * p.q_tiles, p.Hq, p.B);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = CS;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, m.q, m.k, m.v, p);
+}
+
+}  // namespace
+
+cudaError_t launch_fwd_main(const FwdParams& p, const FwdMaps& m, bool bf16, cudaStream_t s) {
+  const bool pair = p.n_chunks > 4;
+  if (pair) return bf16 ? launch_impl<2, true>(p, m, s) : launch_impl<2, false>(p, m, s);
+  return bf16 ? launch_impl<1, true>(p, m, s) : launch_impl<1, false>(p, m, s);
+}
+
+}  // namespace ffpa

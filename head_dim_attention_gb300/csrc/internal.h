@@ -1,0 +1,98 @@
+// Host/device parameter blocks and launcher declarations shared between the
+// C-ABI layer (api.cu) and the kernel translation units.
+#pragma once
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace ffpa {
+
+constexpr int kTileRows = 128;  // query/key rows per tile (the MMA M)
+constexpr int kChunk = 64;      // D columns per chunk (one 128-byte swizzled row)
+constexpr int kChunkBytes = kTileRows * kChunk * 2;  // 16 KB
+
+// Forward, fused tcgen05 path.
+struct FwdParams {
+  void* out;
+  float* lse;         // nullable, contiguous [B, Hq, Nq]
+  const float* bias;  // nullable
+  int64_t o_sb, o_sh, o_sn;
+  int64_t bias_sb, bias_sh, bias_sq, bias_sk;
+  int B, Hq, Hkv, Nq, Nkv, D;
+  int group;          // Hq / Hkv
+  int causal;
+  float scale_log2;   // scale * log2(e)
+  int n_chunks;       // D / 64
+  int stages;         // ring stages of 16 KB
+  int q_tiles;        // ceil(Nq / 128)
+  uint32_t* status;   // device status word
+};
+
+struct FwdMaps {
+  CUtensorMap q, k, v;  // 4-D {D, N, H, B}, box {64, 128, 1, 1}, 128-byte swizzle
+};
+
+// Decode (small Nq) path.
+struct DecodeParams {
+  const void* q;
+  const void* k;
+  const void* v;
+  void* out;
+  float* lse;
+  const float* bias;
+  int64_t q_sb, q_sh, q_sn;
+  int64_t k_sb, k_sh, k_sn;
+  int64_t v_sb, v_sh, v_sn;
+  int64_t o_sb, o_sh, o_sn;
+  int64_t bias_sb, bias_sh, bias_sq, bias_sk;
+  int B, Hq, Hkv, Nq, Nkv, D;
+  int group;
+  int causal;
+  float scale_log2;
+  int split_len;      // keys per split
+  int n_splits;
+  float* part_o;      // [B, Hq, Nq, n_splits, D] fp32 scratch
+  float* part_ml;     // [B, Hq, Nq, n_splits, 2] fp32 scratch (max, sum), log2 domain
+};
+
+// Backward.
+struct BwdParams {
+  const void* out;
+  const void* dout;
+  const float* lse;   // [B, Hq, Nq] natural log
+  float* delta;       // [B, Hq, Nq] scratch
+  float* lse2;        // [B, Hq, Nq] scratch: lse in log2 units
+  const float* bias;
+  void* dq;
+  void* dk;
+  void* dv;
+  int64_t o_sb, o_sh, o_sn;
+  int64_t do_sb, do_sh, do_sn;
+  int64_t dq_sb, dq_sh, dq_sn;
+  int64_t dk_sb, dk_sh, dk_sn;
+  int64_t dv_sb, dv_sh, dv_sn;
+  int64_t bias_sb, bias_sh, bias_sq, bias_sk;
+  int B, Hq, Hkv, Nq, Nkv, D;
+  int group;
+  int causal;
+  float scale;
+  float scale_log2;
+  int n_chunks;
+  int stages;
+  int q_tiles, kv_tiles;
+  uint32_t* status;
+};
+
+struct BwdMaps {
+  CUtensorMap q, k, v, dout;
+};
+
+bool dtype_is_bf16(int dtype);
+
+cudaError_t launch_fwd_main(const FwdParams& p, const FwdMaps& m, bool bf16, cudaStream_t s);
+cudaError_t launch_fwd_decode(const DecodeParams& p, bool bf16, cudaStream_t s);
+cudaError_t launch_bwd(const BwdParams& p, const BwdMaps& m, bool bf16, cudaStream_t s);
+
+uint32_t* device_status_word();  // per current device
+
+}  // namespace ffpa

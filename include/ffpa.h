@@ -1,0 +1,128 @@
+/*
+ * ffpa.h: C ABI of a GB300 (sm_103a) fused scaled-dot-product attention
+ * library for large head dimensions (D = 64 .. 1024 in steps of 64; the
+ * regime the pages study is D = 320 .. 1024, headline D = 512).
+ *
+ * What it computes (per batch b and query head h, kv head g = h / (Hq/Hkv)):
+ *
+ *   S   = scale * Q_h K_g^T + bias          scores, never materialised
+ *   S_ij = -inf where causal and j > i      top-left causal mask
+ *   P   = softmax(S)  (row-wise)
+ *   O_h = P V_g,   lse_i = ln sum_j exp(S_ij)
+ *
+ * This is the "naive_math" definition written out in the attention-kernel-
+ * profiler design notes (generate_docs.py, "naive_math"),
+ * with the grouped-query mapping of its "gqa_4kv" variant (K/V expanded by
+ * repeat_interleave) and the additive key-position bias of the FFPA Attention
+ * Benchmark page ("Quick Start": compact [1,1,1,Nkv] bias, or [1,1,Nq,Nkv]).
+ * The backward is the one the FFPA Attention Benchmark page describes for
+ * SM100 ("More Benchmark"): a preprocess (Delta = rowsum(dO * O)) and then dV,
+ * dK and dQ launches.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - Tensors are described by ffpa_tensor_t: a data pointer, a dtype, four
+ *    sizes and four strides counted in ELEMENTS.  Q/K/V/O/dO/dQ/dK/dV are
+ *    [B, H, N, D] with the innermost stride equal to 1.
+ *  - Device pointers only.  The caller owns every buffer; the library never
+ *    allocates or frees caller memory.  Work is enqueued on `stream` and the
+ *    call returns without synchronising (stream-ordered, asynchronous).
+ *  - Validation happens on the host before anything is enqueued.  On any
+ *    non-zero return from validation nothing was launched and no buffer was
+ *    written.
+ *  - Each call is independent; the library keeps no per-call state except a
+ *    per-device status word that kernels set when a bounded wait times out
+ *    (read and cleared by ffpa_check_status).  Calls are thread-safe.
+ */
+#ifndef FFPA_H_
+#define FFPA_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* A CUDA stream (layout-compatible with cudaStream_t); NULL = legacy default stream. */
+typedef struct CUstream_st* ffpa_stream_t;
+
+enum ffpa_dtype { FFPA_F16 = 0, FFPA_BF16 = 1, FFPA_F32 = 2 };
+
+enum ffpa_status {
+  FFPA_OK = 0,
+  FFPA_ERR_INVALID_ARG = 1, /* null pointer, shape mismatch, Hq % Hkv != 0, N < 1, bad scale */
+  FFPA_ERR_UNSUPPORTED = 2, /* D % 64 != 0 or D outside [64, 1024]; dtype not f16/bf16; bias not f32;
+                               innermost stride != 1 */
+  FFPA_ERR_ALIGNMENT = 3,   /* base pointer not 16-byte aligned or a row/head/batch stride not a
+                               multiple of 8 elements (TMA needs 16-byte strides) */
+  FFPA_ERR_CUDA = 4,        /* a CUDA runtime call or kernel launch failed */
+  FFPA_ERR_TIMEOUT = 5      /* a kernel's bounded wait expired (reported by ffpa_check_status) */
+};
+
+typedef struct ffpa_tensor {
+  void* data;        /* device pointer */
+  int32_t dtype;     /* enum ffpa_dtype */
+  int32_t reserved;  /* must be 0 */
+  int64_t shape[4];  /* [B, H, N, D] (lse: [B, H, N, 1]; bias: [B|1, H|1, Nq|1, Nkv]) */
+  int64_t stride[4]; /* in elements */
+} ffpa_tensor_t;
+
+/*
+ * ffpa_fwd: attention forward, O and the row logsumexp.
+ *
+ *   q    [B, Hq, Nq, D]   f16 or bf16
+ *   k, v [B, Hkv, Nkv, D] same dtype as q; Hkv divides Hq (GQA when Hkv < Hq)
+ *   bias nullable.  f32, shape [B|1, Hq|1, Nq|1, Nkv], added to the scaled
+ *        scores; a size-1 dimension is broadcast (its stride is ignored).
+ *   causal  0 or 1: query i sees keys j <= i (top-left, also when Nq != Nkv)
+ *   scale   > 0 and finite; the usual value is 1/sqrt(D)
+ *   out  [B, Hq, Nq, D]   same dtype as q, written
+ *   lse  nullable.  f32 [B, Hq, Nq, 1], contiguous: written with
+ *        ln sum_j exp(S_ij); -inf for a row whose scores are all -inf (whose
+ *        O row is then 0).
+ *
+ * Nq <= 16 takes a split-KV decode path (CUDA-core dot products over slices
+ * of the keys, then an lse-weighted merge); it uses stream-ordered scratch
+ * from cudaMallocAsync on `stream`.  Otherwise one fused tcgen05 kernel runs.
+ * Returns FFPA_OK or an ffpa_status code (see above).
+ */
+int ffpa_fwd(const ffpa_tensor_t* q, const ffpa_tensor_t* k, const ffpa_tensor_t* v,
+             const ffpa_tensor_t* bias, int causal, float scale, const ffpa_tensor_t* out,
+             const ffpa_tensor_t* lse, ffpa_stream_t stream);
+
+/*
+ * ffpa_bwd: attention backward (FFPA Attention Benchmark page, "More
+ * Benchmark": preprocess, then dV, dK, dQ).
+ *
+ *   q, k, v, bias, causal, scale   exactly as passed to ffpa_fwd
+ *   out   [B, Hq, Nq, D]  the forward's O
+ *   lse   f32 [B, Hq, Nq, 1] the forward's lse (required)
+ *   dout  [B, Hq, Nq, D]  gradient of the loss with respect to O
+ *   dq    [B, Hq, Nq, D]  written
+ *   dk, dv [B, Hkv, Nkv, D] written (summed over the query heads of a group)
+ *
+ * No gradient is produced for the bias.  Delta (f32 [B, Hq, Nq]) lives in
+ * stream-ordered scratch from cudaMallocAsync on `stream`.
+ */
+int ffpa_bwd(const ffpa_tensor_t* q, const ffpa_tensor_t* k, const ffpa_tensor_t* v,
+             const ffpa_tensor_t* bias, int causal, float scale, const ffpa_tensor_t* out,
+             const ffpa_tensor_t* lse, const ffpa_tensor_t* dout, const ffpa_tensor_t* dq,
+             const ffpa_tensor_t* dk, const ffpa_tensor_t* dv, ffpa_stream_t stream);
+
+/* Static text for a status code (never NULL). */
+const char* ffpa_status_string(int status);
+
+/*
+ * Synchronise `stream`, then read and clear the current device's status word.
+ * Returns FFPA_ERR_TIMEOUT if a kernel's bounded wait expired since the last
+ * check, FFPA_ERR_CUDA if the synchronisation failed, FFPA_OK otherwise.
+ */
+int ffpa_check_status(ffpa_stream_t stream);
+
+/* Library version: major * 10000 + minor * 100 + patch. */
+int ffpa_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* FFPA_H_ */

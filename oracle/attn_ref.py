@@ -180,7 +180,8 @@ def attn_bwd_sampled(q, k, v, do, b, h_kv, q_rows, kv_rows, bias=None, causal=Fa
     """Exact gradients at selected rows, for shapes too large for the full backward.
 
     For kv head ``h_kv`` of batch ``b``: returns
-      dq:  {h: dQ[b, h, q_rows]} for each query head h of the group,
+      dq:  {h: dQ[b, h, rows_h]} for each query head h of the group, where
+           rows_h = q_rows[h] if q_rows is a dict, else q_rows,
       dk, dv: dK[b, h_kv, kv_rows], dV[b, h_kv, kv_rows] (summed over the group).
     Every P_ij needed is normalised by the full-row statistics (lse, Delta) that
     the oracle computes itself over all keys, in row blocks of ``block``.
@@ -191,7 +192,6 @@ def attn_bwd_sampled(q, k, v, do, b, h_kv, q_rows, kv_rows, bias=None, causal=Fa
     hkv = k.shape[1]
     scale = _scale(scale, d)
     group = hq // hkv
-    q_rows = np.asarray(q_rows)
     kv_rows = np.asarray(kv_rows)
     dq_out = {}
     dk = np.zeros((len(kv_rows), d))
@@ -205,9 +205,10 @@ def attn_bwd_sampled(q, k, v, do, b, h_kv, q_rows, kv_rows, bias=None, causal=Fa
             p, lse[rows] = probs_head(scores_head(q, k, bias, b, h, h_kv, scale, causal, rows=rows))
             delta[rows] = np.sum(do[b, h][rows] * (p @ v[b, h_kv]), axis=1)
         # dQ at the sampled query rows (needs those rows of P and dP over all keys)
-        p, _ = probs_head(scores_head(q, k, bias, b, h, h_kv, scale, causal, rows=q_rows))
-        dp = do[b, h][q_rows] @ v[b, h_kv].T
-        ds = p * (dp - delta[q_rows][:, None])
+        rows_h = np.asarray(q_rows[h] if isinstance(q_rows, dict) else q_rows)
+        p, _ = probs_head(scores_head(q, k, bias, b, h, h_kv, scale, causal, rows=rows_h))
+        dp = do[b, h][rows_h] @ v[b, h_kv].T
+        ds = p * (dp - delta[rows_h][:, None])
         dq_out[h] = scale * (ds @ k[b, h_kv])
         # dK/dV at the sampled key rows (needs those columns of P over all queries)
         s_cols = scores_head(q, k, bias, b, h, h_kv, scale, causal, cols=kv_rows)

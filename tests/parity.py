@@ -1,0 +1,129 @@
+"""Helpers for the GPU parity tests: run the C-ABI path, run the oracle, compare.
+
+Tolerances are the ones the task fixes for this method:
+  O:    |gpu - ref| <= 2e-3 + 2e-2 |ref| (bf16),  1e-3 + 5e-3 |ref| (fp16)
+  lse:  |gpu - ref| <= 1e-3
+  dQ/dK/dV: relative Frobenius error ||gpu - ref||_F / ||ref||_F <= 2e-2
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import oracle.attn_ref as ref
+from head_dim_attention_gb300 import attention_bwd, attention_fwd, ffpa_check_status
+from head_dim_attention_gb300.synth import make_inputs
+
+TOL = {torch.bfloat16: (2e-3, 2e-2), torch.float16: (1e-3, 5e-3)}
+LSE_ATOL = 1e-3
+GRAD_RTOL = 2e-2
+
+
+def f64(t):
+    return None if t is None else t.double().numpy()
+
+
+def assert_close(gpu, want, atol, rtol, what):
+    gpu = np.asarray(gpu, dtype=np.float64)
+    want = np.asarray(want, dtype=np.float64)
+    assert gpu.shape == want.shape, (what, gpu.shape, want.shape)
+    same_inf = np.isinf(want) & (gpu == want)
+    err = np.where(same_inf, 0.0, np.abs(gpu - want))
+    bound = atol + rtol * np.where(np.isinf(want), 0.0, np.abs(want))
+    bad = ~(err <= bound)
+    if bad.any():
+        i = np.unravel_index(np.argmax(np.where(bad, err - bound, -np.inf)), err.shape)
+        raise AssertionError(f"{what}: {int(bad.sum())} of {bad.size} outside tolerance; worst at {i}: "
+                             f"gpu={gpu[i]!r} ref={want[i]!r}")
+
+
+def rel_fro(gpu, want):
+    gpu = np.asarray(gpu, dtype=np.float64)
+    want = np.asarray(want, dtype=np.float64)
+    return float(np.linalg.norm(gpu - want) / max(np.linalg.norm(want), 1e-300))
+
+
+def gpu_fwd(inp, causal, scale):
+    dev = torch.device("cuda")
+    q, k, v = inp.q.to(dev), inp.k.to(dev), inp.v.to(dev)
+    bias = None if inp.bias is None else inp.bias.to(dev)
+    out, lse = attention_fwd(q, k, v, bias=bias, causal=causal, scale=scale)
+    torch.cuda.synchronize()
+    assert ffpa_check_status() == 0
+    return out, lse
+
+
+def check_fwd_full(B, Hq, Hkv, Nq, Nkv, D, dtype, causal=False, bias=False, seed=0):
+    inp = make_inputs(B, Hq, Hkv, Nq, Nkv, D, dtype, bias=bias, seed=seed)
+    scale = D ** -0.5
+    out, lse = gpu_fwd(inp, causal, scale)
+    o_ref, lse_ref = ref.attn_fwd(f64(inp.q), f64(inp.k), f64(inp.v), bias=f64(inp.bias), causal=causal,
+                                  scale=scale)
+    atol, rtol = TOL[dtype]
+    assert_close(out.float().cpu().numpy(), o_ref, atol, rtol, "O")
+    assert_close(lse.cpu().numpy(), lse_ref, LSE_ATOL, 0.0, "lse")
+
+
+def check_fwd_sampled(B, Hq, Hkv, Nq, Nkv, D, dtype, causal=False, bias=False, rows=64, seed=0):
+    """Large shapes: the oracle computes `rows` seeded query rows per head, one by one."""
+    inp = make_inputs(B, Hq, Hkv, Nq, Nkv, D, dtype, bias=bias, seed=seed)
+    scale = D ** -0.5
+    out, lse = gpu_fwd(inp, causal, scale)
+    out = out.float().cpu().numpy()
+    lse = lse.cpu().numpy()
+    q, k, v, bb = f64(inp.q), f64(inp.k), f64(inp.v), f64(inp.bias)
+    atol, rtol = TOL[dtype]
+    for b in range(B):
+        for h in range(Hq):
+            r = ref.sample_rows(Nq, rows, 1000 + h)
+            o_ref, lse_ref = ref.attn_fwd_rows(q, k, v, b, h, r, bias=bb, causal=causal, scale=scale)
+            assert_close(out[b, h, r], o_ref, atol, rtol, f"O[b={b},h={h}]")
+            assert_close(lse[b, h, r], lse_ref, LSE_ATOL, 0.0, f"lse[b={b},h={h}]")
+    return out, lse
+
+
+def gpu_fwd_bwd(inp, causal, scale):
+    dev = torch.device("cuda")
+    q, k, v, do = inp.q.to(dev), inp.k.to(dev), inp.v.to(dev), inp.do.to(dev)
+    bias = None if inp.bias is None else inp.bias.to(dev)
+    out, lse = attention_fwd(q, k, v, bias=bias, causal=causal, scale=scale)
+    dq, dk, dv = attention_bwd(q, k, v, out, lse, do, bias=bias, causal=causal, scale=scale)
+    torch.cuda.synchronize()
+    assert ffpa_check_status() == 0
+    return out, lse, dq, dk, dv
+
+
+def check_bwd_full(B, Hq, Hkv, Nq, Nkv, D, dtype, causal=False, bias=False, seed=0):
+    inp = make_inputs(B, Hq, Hkv, Nq, Nkv, D, dtype, bias=bias, grad=True, seed=seed)
+    scale = D ** -0.5
+    _, _, dq, dk, dv = gpu_fwd_bwd(inp, causal, scale)
+    gq, gk, gv = ref.attn_bwd(f64(inp.q), f64(inp.k), f64(inp.v), f64(inp.do), bias=f64(inp.bias),
+                              causal=causal, scale=scale)
+    errs = {}
+    for name, gpu, want in (("dQ", dq, gq), ("dK", dk, gk), ("dV", dv, gv)):
+        errs[name] = rel_fro(gpu.float().cpu().numpy(), want)
+    worst = max(errs, key=errs.get)
+    assert errs[worst] <= GRAD_RTOL, f"{worst} relative Frobenius error {errs[worst]:.3e} ({errs})"
+    return errs
+
+
+def check_bwd_sampled(B, Hq, Hkv, Nq, Nkv, D, dtype, causal=False, bias=False, rows=64, seed=0):
+    inp = make_inputs(B, Hq, Hkv, Nq, Nkv, D, dtype, bias=bias, grad=True, seed=seed)
+    scale = D ** -0.5
+    _, _, dq, dk, dv = gpu_fwd_bwd(inp, causal, scale)
+    dq, dk, dv = (x.float().cpu().numpy() for x in (dq, dk, dv))
+    q, k, v, do, bb = f64(inp.q), f64(inp.k), f64(inp.v), f64(inp.do), f64(inp.bias)
+    errs = {}
+    for b in range(B):
+        for g in range(Hkv):
+            kr = ref.sample_rows(Nkv, rows, 2000 + g)
+            group = Hq // Hkv
+            qrows = {h: ref.sample_rows(Nq, rows, 1000 + h) for h in range(g * group, (g + 1) * group)}
+            sdq, sdk, sdv = ref.attn_bwd_sampled(q, k, v, do, b, g, qrows, kr, bias=bb, causal=causal, scale=scale)
+            for h in qrows:
+                errs[f"dQ[{b},{h}]"] = rel_fro(dq[b, h, qrows[h]], sdq[h])
+            errs[f"dK[{b},{g}]"] = rel_fro(dk[b, g, kr], sdk)
+            errs[f"dV[{b},{g}]"] = rel_fro(dv[b, g, kr], sdv)
+    worst = max(errs, key=errs.get)
+    assert errs[worst] <= GRAD_RTOL, f"{worst} relative Frobenius error {errs[worst]:.3e}"
+    return errs

@@ -1,0 +1,91 @@
+"""Forward parity: the C-ABI CUDA path against the fp64 oracle on seeded inputs.
+
+Small shapes are compared element by element over the whole output; they span
+several 128-row tiles, ragged tails, both dtypes, every head-dimension regime
+of the fused kernel (one CTA for D <= 256, a D-split CTA pair above, several
+passes above D = 512) and the decode path (Nq <= 16).  The workload-sized
+cases compare 64 seeded query rows per head, which the oracle computes one by
+one.
+"""
+import pytest
+import torch
+
+from parity import check_fwd_full, check_fwd_sampled
+
+pytestmark = pytest.mark.gpu
+BF, FP = torch.bfloat16, torch.float16
+
+
+def test_config_small_self_attention():
+    # B=1, H=1, N=256, D=512, fp16, scale 1/sqrt(512), seed 0: full output
+    check_fwd_full(1, 1, 1, 256, 256, 512, FP)
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,Nq,Nkv,D,dtype,causal,bias", [
+    (1, 2, 2, 129, 129, 512, BF, False, False),
+    (1, 2, 2, 200, 333, 512, BF, False, True),
+    (1, 4, 1, 300, 300, 512, FP, True, False),
+    (2, 2, 1, 255, 255, 320, BF, True, True),
+    (1, 1, 1, 128, 1000, 576, FP, False, False),
+    (1, 1, 1, 257, 384, 1024, BF, True, False),
+    (1, 2, 2, 130, 130, 256, BF, False, False),
+    (1, 1, 1, 64, 64, 64, FP, False, False),
+    (1, 2, 2, 17, 140, 768, BF, False, True),
+    (1, 1, 1, 300, 100, 512, BF, True, False),
+    (1, 1, 1, 100, 300, 512, FP, True, True),
+    (1, 2, 1, 384, 384, 640, FP, False, False),
+    (1, 1, 1, 127, 1, 448, BF, False, False),
+])
+def test_fused_small(B, Hq, Hkv, Nq, Nkv, D, dtype, causal, bias):
+    check_fwd_full(B, Hq, Hkv, Nq, Nkv, D, dtype, causal=causal, bias=bias)
+
+
+def test_fused_query_bias_small():
+    # [1, 1, Nq, Nkv] per-query bias
+    check_fwd_full(1, 2, 2, 150, 260, 512, torch.bfloat16, bias="query")
+
+
+@pytest.mark.parametrize("D", [320, 384, 448, 512, 576, 640, 768, 1024])
+def test_head_dim_sweep_small(D):
+    check_fwd_full(1, 2, 2, 200, 200, D, FP, causal=(D % 128 == 0))
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,Nq,Nkv,D,dtype,causal,bias", [
+    (1, 8, 8, 1, 1000, 512, BF, False, False),
+    (1, 4, 2, 3, 257, 512, FP, True, True),
+    (2, 2, 2, 16, 130, 1024, BF, False, False),
+    (1, 2, 1, 5, 1, 320, FP, False, True),
+    (1, 1, 1, 16, 16, 64, BF, True, False),
+])
+def test_decode_small(B, Hq, Hkv, Nq, Nkv, D, dtype, causal, bias):
+    check_fwd_full(B, Hq, Hkv, Nq, Nkv, D, dtype, causal=causal, bias=bias)
+
+
+# ---------------------------------------------------------------- workload-sized cases
+def test_self_attention_8k_bf16():
+    check_fwd_sampled(1, 8, 8, 8192, 8192, 512, BF)
+
+
+@pytest.mark.parametrize("D", [320, 384, 448, 512, 576, 640, 768, 1024])
+def test_head_dim_sweep_4k_fp16(D):
+    check_fwd_sampled(1, 8, 8, 4096, 4096, D, FP, rows=16)
+
+
+def test_causal_8k():
+    check_fwd_sampled(1, 8, 8, 8192, 8192, 512, BF, causal=True)
+
+
+def test_gqa_8k():
+    check_fwd_sampled(1, 8, 2, 8192, 8192, 512, BF)
+
+
+def test_non_aligned_8191():
+    check_fwd_sampled(1, 8, 8, 8191, 8191, 512, BF)
+
+
+def test_cross_attention_bias():
+    check_fwd_sampled(1, 8, 8, 1024, 8192, 512, BF, bias=True)
+
+
+def test_decode_8k():
+    check_fwd_full(1, 8, 8, 1, 8192, 512, BF)
