@@ -1,5 +1,620 @@
-// Attention backward: not yet implemented in this revision of the library.
+// Attention backward for large head dimensions on sm_103a.
+//
+// The FFPA Attention Benchmark page ("More Benchmark") describes the SM100
+// backward as four launches, preprocess, dV, dK and dQ, executing 8 GEMM
+// passes.  This file builds the same decomposition:
+//   preprocess:  Delta_i = sum_d dO_id O_id,  lse2_i = lse_i * log2(e)
+//   dV  (per key tile):   S^T = K Q^T;  P^T = 2^(S^T c + bias2 - lse2);  dV += P^T dO        (2 GEMMs)
+//   dK  (per key tile):   S^T, dP^T = V dO^T;  dS^T = P^T (dP^T - Delta);  dK += dS^T Q    (3 GEMMs)
+//   dQ  (per query tile): S = Q K^T, dP = dO V^T;  dS = P (dP - Delta);  dQ += dS K        (3 GEMMs)
+// with c = scale * log2(e), and dK, dQ scaled by `scale` in the epilogue.
+// P is rebuilt exactly from the forward's lse, so no online softmax is needed.
+//
+// Each kernel keeps one 128-row tile "stationary" (key rows for dV/dK, query
+// rows for dQ) and sweeps the other side in 128-row "column" tiles.  As in
+// the forward, a cluster of two CTAs splits D in 64-column chunks: each CTA
+// computes partial score tiles over its own chunks with tcgen05.mma into TMEM,
+// the pair swaps the fp32 partials through distributed shared memory and adds
+// them, and each CTA accumulates the gradient for its own chunks (<= 256 TMEM
+// columns per pass).  GQA: the dV/dK kernels sweep every query head of the
+// group, so the group's sum forms in TMEM without any atomics or workspace.
+//
+// TMEM (512 columns): gradient accumulator [0, 256), X1 [256, 384) (scores,
+// then P or dS as the bf16/f16 A operand), X2 [384, 512) (dP).
+// Warp roles: warp 0 TMA producer, warp 1 TMEM owner + MMA issuer, warps 4-7
+// elementwise + epilogue (thread = stationary row = TMEM lane).
+#include <type_traits>
+
 #include "internal.h"
+#include "ptx.cuh"
+
 namespace ffpa {
-cudaError_t launch_bwd(const BwdParams&, const BwdMaps&, bool, cudaStream_t) { return cudaErrorNotSupported; }
+namespace {
+
+enum Mode : int { kDV = 0, kDK = 1, kDQ = 2 };
+
+constexpr int kThreads = 256;
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kX1 = 256, kX2 = 384;
+constexpr int kMaxAccChunks = 4;
+constexpr int kLandingBytes = kTileRows * kTileRows * 4;
+constexpr float kLog2e = 1.4426950408889634f;
+
+struct Bars {
+  int full, empty, a_full, x_full, p_ready, acc_ready, acc_free, xfull, xfree, drain, count;
+};
+__host__ __device__ inline Bars bar_layout(int stages) {
+  Bars b;
+  b.full = 0;
+  b.empty = stages;
+  b.a_full = 2 * stages;
+  b.x_full = b.a_full + 1;
+  b.p_ready = b.x_full + 1;
+  b.acc_ready = b.p_ready + 1;
+  b.acc_free = b.acc_ready + 1;
+  b.xfull = b.acc_free + 1;
+  b.xfree = b.xfull + 1;
+  b.drain = b.xfree + 1;
+  b.count = b.drain + 1;
+  return b;
+}
+
+struct Plan {
+  int own_max, n_a;  // resident A operands (0 = stream them through the ring)
+  int a_off, ring_off, land_off, bar_off, total;
+};
+__host__ __device__ inline Plan make_plan(int n_chunks, int cs, int mode, int stages, bool resident) {
+  Plan s;
+  s.own_max = (n_chunks + cs - 1) / cs;
+  s.n_a = resident ? (mode == kDV ? 1 : 2) : 0;
+  s.a_off = 0;
+  s.ring_off = s.n_a * s.own_max * kChunkBytes;
+  s.land_off = s.ring_off + stages * kChunkBytes;
+  s.bar_off = s.land_off + (cs == 2 ? kLandingBytes : 0);
+  s.total = s.bar_off + 1024;
+  return s;
+}
+
+template <bool BF16>
+__device__ __forceinline__ uint32_t pack2(float a, float b) {
+  if constexpr (BF16) {
+    __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+    return *reinterpret_cast<uint32_t*>(&h);
+  } else {
+    __half2 h = __floats2half2_rn(a, b);
+    return *reinterpret_cast<uint32_t*>(&h);
+  }
+}
+
+// Preprocess: one warp per query row.
+template <bool BF16>
+__global__ void __launch_bounds__(256) bwd_preprocess_kernel(const __grid_constant__ BwdParams p) {
+  typedef typename std::conditional<BF16, __nv_bfloat16, __half>::type T;
+  const int64_t rows = static_cast<int64_t>(p.B) * p.Hq * p.Nq;
+  const int64_t row = static_cast<int64_t>(blockIdx.x) * 8 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (row >= rows) return;
+  const int i = static_cast<int>(row % p.Nq);
+  const int h = static_cast<int>((row / p.Nq) % p.Hq);
+  const int b = static_cast<int>(row / (static_cast<int64_t>(p.Nq) * p.Hq));
+  const T* o = reinterpret_cast<const T*>(p.out) + b * p.o_sb + h * p.o_sh + static_cast<int64_t>(i) * p.o_sn;
+  const T* d = reinterpret_cast<const T*>(p.dout) + b * p.do_sb + h * p.do_sh + static_cast<int64_t>(i) * p.do_sn;
+  float acc = 0.f;
+  for (int c = lane * 8; c < p.D; c += 256) {
+    const uint4 uo = __ldg(reinterpret_cast<const uint4*>(o + c));
+    const uint4 ud = __ldg(reinterpret_cast<const uint4*>(d + c));
+    const uint32_t wo[4] = {uo.x, uo.y, uo.z, uo.w}, wd[4] = {ud.x, ud.y, ud.z, ud.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      float2 fo, fd;
+      if constexpr (BF16) {
+        fo = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&wo[e]));
+        fd = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&wd[e]));
+      } else {
+        fo = __half22float2(*reinterpret_cast<const __half2*>(&wo[e]));
+        fd = __half22float2(*reinterpret_cast<const __half2*>(&wd[e]));
+      }
+      acc = fmaf(fo.x, fd.x, acc);
+      acc = fmaf(fo.y, fd.y, acc);
+    }
+  }
+#pragma unroll
+  for (int s = 16; s > 0; s >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, s);
+  if (lane == 0) {
+    p.delta[row] = acc;
+    p.lse2[row] = p.lse[row] * kLog2e;
+  }
+}
+
+// Stationary/column geometry of one CTA.
+struct Geo {
+  int b, h, kvh;      // batch, query head (dQ) and kv head
+  int s_head, s_row0; // stationary tile: head index in its tensor, first row
+  int s_limit;        // rows of the stationary tensor (Nkv for dV/dK, Nq for dQ)
+  int qt_begin, nq_h; // dV/dK: first query tile and query tiles per head
+  int ncols;          // column tiles
+};
+
+template <int MODE>
+__device__ __forceinline__ Geo make_geo(const BwdParams& p, int cs) {
+  Geo g;
+  g.b = blockIdx.z;
+  if (MODE == kDQ) {
+    const int qt = p.q_tiles - 1 - static_cast<int>(blockIdx.x) / cs;  // heavy causal tiles first
+    g.h = blockIdx.y;
+    g.kvh = g.h / p.group;
+    g.s_head = g.h;
+    g.s_row0 = qt * kTileRows;
+    g.s_limit = p.Nq;
+    const int kv_end = p.causal ? min(p.Nkv, g.s_row0 + kTileRows) : p.Nkv;
+    g.ncols = (kv_end + kTileRows - 1) / kTileRows;
+    g.qt_begin = 0;
+    g.nq_h = 0;
+  } else {
+    const int kvt = static_cast<int>(blockIdx.x) / cs;
+    g.kvh = blockIdx.y;
+    g.h = g.kvh * p.group;
+    g.s_head = g.kvh;
+    g.s_row0 = kvt * kTileRows;
+    g.s_limit = p.Nkv;
+    g.qt_begin = p.causal ? kvt : 0;  // top-left causal: query rows i >= key row j
+    g.nq_h = max(0, p.q_tiles - g.qt_begin);
+    g.ncols = p.group * g.nq_h;
+  }
+  return g;
+}
+
+// Column tile c -> (head, first row) in the column tensor.
+template <int MODE>
+__device__ __forceinline__ void column(const Geo& g, const BwdParams& p, int c, int* head, int* row0) {
+  if (MODE == kDQ) {
+    *head = g.kvh;
+    *row0 = c * kTileRows;
+  } else {
+    *head = g.kvh * p.group + c / g.nq_h;
+    *row0 = (g.qt_begin + c % g.nq_h) * kTileRows;
+  }
+}
+
+template <int MODE, int CS, bool BF16>
+__global__ void __launch_bounds__(kThreads, 1)
+    bwd_main_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
+                    const __grid_constant__ CUtensorMap map_v, const __grid_constant__ CUtensorMap map_do,
+                    const __grid_constant__ BwdParams p, const int resident) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int stages = p.stages;
+  const Plan plan = make_plan(p.n_chunks, CS, MODE, stages, resident != 0);
+  const Bars bl = bar_layout(stages);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + plan.bar_off);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + bl.count);
+  auto bar = [&](int i) { return smem_u32(&bars[i]); };
+  const uint32_t s_base = smem_u32(smem);
+  const uint32_t a_sm = s_base + plan.a_off, ring_sm = s_base + plan.ring_off, land_sm = s_base + plan.land_off;
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const uint32_t rank = (CS == 2) ? cluster_ctarank() : 0;
+  const Geo g = make_geo<MODE>(p, CS);
+  const int n = p.n_chunks;
+  const int half = (n + CS - 1) / CS;
+  const int own0 = static_cast<int>(rank) * half;
+  const int own_n = min(half, n - own0);
+  const int passes = (half + kMaxAccChunks - 1) / kMaxAccChunks;
+  const bool two = (MODE != kDV);  // a second score-like product (dP)
+  uint32_t* status = p.status;
+
+  const CUtensorMap* mA1 = (MODE == kDQ) ? &map_q : &map_k;
+  const CUtensorMap* mA2 = (MODE == kDQ) ? &map_do : &map_v;
+  const CUtensorMap* mB1 = (MODE == kDQ) ? &map_k : &map_q;
+  const CUtensorMap* mB2 = (MODE == kDQ) ? &map_v : &map_do;
+  const CUtensorMap* mB3 = (MODE == kDV) ? &map_do : ((MODE == kDK) ? &map_q : &map_k);
+
+  if (tid == 0) {
+    for (int i = 0; i < stages; ++i) {
+      mbar_init(bar(bl.full + i), 1);
+      mbar_init(bar(bl.empty + i), 1);
+    }
+    mbar_init(bar(bl.a_full), 1);
+    mbar_init(bar(bl.x_full), 1);
+    mbar_init(bar(bl.p_ready), 4);
+    mbar_init(bar(bl.acc_ready), 1);
+    mbar_init(bar(bl.acc_free), 4);
+    mbar_init(bar(bl.xfull), 1);
+    mbar_init(bar(bl.xfree), kTileRows);
+    mbar_init(bar(bl.drain), 1);
+    fence_mbar_init();
+    if (CS == 2) mbar_expect_tx(bar(bl.xfull), kLandingBytes);  // arm exchange 0
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (CS == 2) cluster_sync();
+  tc_fence_after();
+  const uint32_t tbase = *tmem_slot;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      tma_prefetch_desc(&map_q);
+      tma_prefetch_desc(&map_k);
+      tma_prefetch_desc(&map_v);
+      tma_prefetch_desc(&map_do);
+      bool ok = true;
+      if (resident) {
+        mbar_expect_tx(bar(bl.a_full), plan.n_a * own_n * kChunkBytes);
+        for (int c = 0; c < own_n; ++c) {
+          tma_load_4d(a_sm + c * kChunkBytes, mA1, bar(bl.a_full), (own0 + c) * kChunk, g.s_row0, g.s_head, g.b);
+          if (two)
+            tma_load_4d(a_sm + (plan.own_max + c) * kChunkBytes, mA2, bar(bl.a_full), (own0 + c) * kChunk,
+                        g.s_row0, g.s_head, g.b);
+        }
+      }
+      uint32_t it = 0;
+      auto load = [&](const CUtensorMap* m, int dcol, int row, int head) {
+        const uint32_t s = it % stages, r = it / stages;
+        if (ok) ok = mbar_wait(bar(bl.empty + s), (r & 1) ^ 1, status);
+        if (ok) {
+          mbar_expect_tx(bar(bl.full + s), kChunkBytes);
+          tma_load_4d(ring_sm + s * kChunkBytes, m, bar(bl.full + s), dcol, row, head, g.b);
+          ++it;
+        }
+      };
+      for (int pass = 0; pass < passes && ok; ++pass) {
+        const int oc0 = pass * kMaxAccChunks;
+        const int oc_n = max(0, min(kMaxAccChunks, own_n - oc0));
+        for (int c = 0; c < g.ncols && ok; ++c) {
+          int ch, cr0;
+          column<MODE>(g, p, c, &ch, &cr0);
+          for (int cc = 0; cc < own_n; ++cc) {
+            if (!resident) load(mA1, (own0 + cc) * kChunk, g.s_row0, g.s_head);
+            load(mB1, (own0 + cc) * kChunk, cr0, ch);
+          }
+          if (two)
+            for (int cc = 0; cc < own_n; ++cc) {
+              if (!resident) load(mA2, (own0 + cc) * kChunk, g.s_row0, g.s_head);
+              load(mB2, (own0 + cc) * kChunk, cr0, ch);
+            }
+          for (int oc = 0; oc < oc_n; ++oc) load(mB3, (own0 + oc0 + oc) * kChunk, cr0, ch);
+        }
+      }
+      for (uint32_t u = (it > (uint32_t)stages ? it - stages : 0); u < it; ++u)
+        mbar_wait(bar(bl.full + u % stages), (u / stages) & 1, status);
+      if (resident) mbar_wait(bar(bl.a_full), 0, status);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      const uint32_t idesc_x = idesc_f16(BF16, 128, 128, false, false);
+      const uint32_t idesc_acc = idesc_f16(BF16, 128, 64, false, true);
+      bool ok = resident ? mbar_wait(bar(bl.a_full), 0, status) : true;
+      tc_fence_after();
+      uint32_t it = 0;
+      int t0 = 0;
+      // one score-like product: X (+)= A B^T over the CTA's own chunks
+      auto product = [&](uint32_t x_tm, int a_slot) {
+        for (int cc = 0; cc < own_n && ok; ++cc) {
+          uint32_t a0;
+          uint32_t sa = 0;
+          if (resident) {
+            a0 = a_sm + (a_slot * plan.own_max + cc) * kChunkBytes;
+          } else {
+            sa = it % stages;
+            ok = mbar_wait(bar(bl.full + sa), (it / stages) & 1, status);
+            if (!ok) return;
+            ++it;
+            a0 = ring_sm + sa * kChunkBytes;
+          }
+          const uint32_t sb = it % stages;
+          ok = mbar_wait(bar(bl.full + sb), (it / stages) & 1, status);
+          if (!ok) return;
+          ++it;
+          tc_fence_after();
+          const uint32_t b0 = ring_sm + sb * kChunkBytes;
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            umma_ss(x_tm, sdesc_sw128(a0 + kk * 32, 16, 1024), sdesc_sw128(b0 + kk * 32, 16, 1024), idesc_x,
+                    (cc | kk) != 0);
+          if (!resident) umma_commit(bar(bl.empty + sa));
+          umma_commit(bar(bl.empty + sb));
+        }
+      };
+      for (int pass = 0; pass < passes && ok; ++pass) {
+        const int oc_n = max(0, min(kMaxAccChunks, own_n - pass * kMaxAccChunks));
+        if (pass > 0) {
+          ok = mbar_wait(bar(bl.acc_free), (pass - 1) & 1, status);
+          tc_fence_after();
+        }
+        for (int c = 0; c < g.ncols && ok; ++c) {
+          const int t = t0 + c;
+          product(tbase + kX1, 0);
+          if (two && ok) product(tbase + kX2, 1);
+          if (!ok) break;
+          umma_commit(bar(bl.x_full));
+          ok = mbar_wait(bar(bl.p_ready), t & 1, status);
+          if (!ok) break;
+          tc_fence_after();
+          for (int oc = 0; oc < oc_n && ok; ++oc) {
+            const uint32_t s = it % stages;
+            ok = mbar_wait(bar(bl.full + s), (it / stages) & 1, status);
+            if (!ok) break;
+            ++it;
+            tc_fence_after();
+            const uint32_t b0 = ring_sm + s * kChunkBytes;
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk)
+              umma_ts(tbase + oc * kChunk, tbase + kX1 + kk * 8, sdesc_sw128(b0 + kk * 2048, 16384, 1024), idesc_acc,
+                      (c > 0 || kk > 0));
+            umma_commit(bar(bl.empty + s));
+          }
+          umma_commit(bar(bl.acc_ready));
+        }
+        t0 += g.ncols;
+      }
+      umma_commit(bar(bl.drain));
+      mbar_wait(bar(bl.drain), 0, status);
+    }
+  } else if (warp >= 4) {
+    // ------------------------------------------------------------ elementwise + epilogue
+    typedef typename std::conditional<BF16, __nv_bfloat16, __half>::type T;
+    const int r = tid - 128;
+    const int srow = g.s_row0 + r;
+    const uint32_t lane_off = static_cast<uint32_t>((warp - 4) * 32) << 16;
+    const uint32_t peer = rank ^ 1u;
+    const uint32_t peer_land = (CS == 2) ? mapa(land_sm, peer) : 0;
+    const uint32_t peer_xfull = (CS == 2) ? mapa(bar(bl.xfull), peer) : 0;
+    const uint32_t peer_xfree = (CS == 2) ? mapa(bar(bl.xfree), peer) : 0;
+    const uint32_t swz = static_cast<uint32_t>(r & 7);
+    const float4* land = reinterpret_cast<const float4*>(smem + plan.land_off + r * 512);
+    float lse2_row = 0.f, delta_row = 0.f;
+    if (MODE == kDQ) {
+      const int64_t idx = (static_cast<int64_t>(g.b) * p.Hq + g.h) * p.Nq + min(srow, p.Nq - 1);
+      lse2_row = p.lse2[idx];
+      delta_row = p.delta[idx];
+    }
+    bool ok = true;
+    int t0 = 0;
+    uint32_t x = 0;  // exchanges done so far
+    // Send this CTA's partial tile at TMEM column `col` to the peer, then wait for the peer's.
+    auto send = [&](uint32_t col) {
+      if (x >= 1) {
+        ok = __all_sync(0xffffffffu, mbar_wait(bar(bl.xfree), (x - 1) & 1, status));
+        if (!ok) return;
+      }
+      const uint32_t dst = peer_land + r * 512;
+#pragma unroll
+      for (int c4 = 0; c4 < 4; ++c4) {
+        uint32_t v[32];
+        tmem_ld32(tbase + lane_off + col + c4 * 32, v);
+        tmem_ld_wait();
+#pragma unroll
+        for (int c8 = 0; c8 < 8; ++c8)
+          st_async_v4(dst + (((c4 * 8 + c8) ^ swz) << 4), __uint_as_float(v[4 * c8]), __uint_as_float(v[4 * c8 + 1]),
+                      __uint_as_float(v[4 * c8 + 2]), __uint_as_float(v[4 * c8 + 3]), peer_xfull);
+      }
+      ok = __all_sync(0xffffffffu, mbar_wait(bar(bl.xfull), x & 1, status));
+    };
+    auto release = [&]() {
+      if (r == 0) mbar_expect_tx(bar(bl.xfull), kLandingBytes);
+      mbar_arrive_remote(peer_xfree);
+      ++x;
+    };
+    // 32 columns of the full tile: own partial (TMEM) + the peer's (landing buffer)
+    auto chunk = [&](uint32_t col, int c4, float (&f)[32]) {
+      uint32_t v[32];
+      tmem_ld32(tbase + lane_off + col + c4 * 32, v);
+      tmem_ld_wait();
+#pragma unroll
+      for (int i = 0; i < 32; ++i) f[i] = __uint_as_float(v[i]);
+      if constexpr (CS == 2) {
+#pragma unroll
+        for (int c8 = 0; c8 < 8; ++c8) {
+          const float4 w = land[(c4 * 8 + c8) ^ swz];
+          f[4 * c8] += w.x;
+          f[4 * c8 + 1] += w.y;
+          f[4 * c8 + 2] += w.z;
+          f[4 * c8 + 3] += w.w;
+        }
+      }
+    };
+    for (int pass = 0; pass < passes && ok; ++pass) {
+      const int oc0 = pass * kMaxAccChunks;
+      const int oc_n = max(0, min(kMaxAccChunks, own_n - oc0));
+      for (int c = 0; c < g.ncols; ++c) {
+        const int t = t0 + c;
+        int ch, cr0;
+        column<MODE>(g, p, c, &ch, &cr0);
+        ok = __all_sync(0xffffffffu, mbar_wait(bar(bl.x_full), t & 1, status));
+        if (!ok) break;
+        tc_fence_after();
+        float pv[128];
+        if constexpr (CS == 2) {
+          send(kX1);
+          if (!ok) break;
+        }
+#pragma unroll
+        for (int c4 = 0; c4 < 4; ++c4) {
+          float f[32];
+          chunk(kX1, c4, f);
+#pragma unroll
+          for (int e = 0; e < 32; ++e) {
+            const int ci = c4 * 32 + e;
+            int i, j, ic;
+            float l2;
+            if (MODE == kDQ) {
+              i = srow;
+              j = cr0 + ci;
+              ic = min(i, p.Nq - 1);
+              l2 = lse2_row;
+            } else {
+              i = cr0 + ci;
+              j = srow;
+              ic = min(i, p.Nq - 1);
+              l2 = __ldg(p.lse2 + (static_cast<int64_t>(g.b) * p.Hq + ch) * p.Nq + ic);
+            }
+            const int hq = (MODE == kDQ) ? g.h : ch;
+            const bool valid = i < p.Nq && j < p.Nkv && !(p.causal && j > i) && l2 > -INFINITY;
+            float xv = fmaf(f[e], p.scale_log2, -l2);
+            if (p.bias)
+              xv = fmaf(__ldg(p.bias + g.b * p.bias_sb + hq * p.bias_sh + static_cast<int64_t>(ic) * p.bias_sq +
+                              static_cast<int64_t>(min(j, p.Nkv - 1)) * p.bias_sk),
+                        kLog2e, xv);
+            pv[ci] = valid ? exp2f(xv) : 0.f;
+          }
+        }
+        if constexpr (CS == 2) release();
+        if (two) {
+          if constexpr (CS == 2) {
+            send(kX2);
+            if (!ok) break;
+          }
+#pragma unroll
+          for (int c4 = 0; c4 < 4; ++c4) {
+            float f[32];
+            chunk(kX2, c4, f);
+#pragma unroll
+            for (int e = 0; e < 32; ++e) {
+              const int ci = c4 * 32 + e;
+              float dl;
+              if (MODE == kDQ) {
+                dl = delta_row;
+              } else {
+                const int ic = min(cr0 + ci, p.Nq - 1);
+                dl = __ldg(p.delta + (static_cast<int64_t>(g.b) * p.Hq + ch) * p.Nq + ic);
+              }
+              pv[ci] = pv[ci] * (f[e] - dl);
+            }
+          }
+          if constexpr (CS == 2) release();
+        }
+        {
+          uint32_t lo[32], hi[32];
+#pragma unroll
+          for (int e = 0; e < 32; ++e) {
+            lo[e] = pack2<BF16>(pv[2 * e], pv[2 * e + 1]);
+            hi[e] = pack2<BF16>(pv[64 + 2 * e], pv[64 + 2 * e + 1]);
+          }
+          tmem_st32(tbase + lane_off + kX1, lo);
+          tmem_st32(tbase + lane_off + kX1 + 32, hi);
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(bl.p_ready));
+      }
+      if (!ok) break;
+      // ---------------------------------------------------------- epilogue
+      if (g.ncols > 0) {
+        ok = __all_sync(0xffffffffu, mbar_wait(bar(bl.acc_ready), (t0 + g.ncols - 1) & 1, status));
+        if (!ok) break;
+        tc_fence_after();
+      }
+      T* dst_base;
+      int64_t sb, sh, sn;
+      if (MODE == kDV) {
+        dst_base = reinterpret_cast<T*>(p.dv); sb = p.dv_sb; sh = p.dv_sh; sn = p.dv_sn;
+      } else if (MODE == kDK) {
+        dst_base = reinterpret_cast<T*>(p.dk); sb = p.dk_sb; sh = p.dk_sh; sn = p.dk_sn;
+      } else {
+        dst_base = reinterpret_cast<T*>(p.dq); sb = p.dq_sb; sh = p.dq_sh; sn = p.dq_sn;
+      }
+      const float mul = (MODE == kDV) ? 1.f : p.scale;
+      T* orow = dst_base + g.b * sb + g.s_head * sh + static_cast<int64_t>(srow) * sn;
+      for (int oc = 0; oc < oc_n; ++oc) {
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+          uint32_t v[32];
+          if (g.ncols > 0) {
+            tmem_ld32(tbase + lane_off + oc * kChunk + hh * 32, v);
+            tmem_ld_wait();
+          } else {
+#pragma unroll
+            for (int e = 0; e < 32; ++e) v[e] = 0u;
+          }
+          if (srow < g.s_limit) {
+            uint4* dst = reinterpret_cast<uint4*>(orow + (own0 + oc0 + oc) * kChunk + hh * 32);
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4) {
+              uint4 w;
+              w.x = pack2<BF16>(__uint_as_float(v[8 * q4 + 0]) * mul, __uint_as_float(v[8 * q4 + 1]) * mul);
+              w.y = pack2<BF16>(__uint_as_float(v[8 * q4 + 2]) * mul, __uint_as_float(v[8 * q4 + 3]) * mul);
+              w.z = pack2<BF16>(__uint_as_float(v[8 * q4 + 4]) * mul, __uint_as_float(v[8 * q4 + 5]) * mul);
+              w.w = pack2<BF16>(__uint_as_float(v[8 * q4 + 6]) * mul, __uint_as_float(v[8 * q4 + 7]) * mul);
+              dst[q4] = w;
+            }
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(bl.acc_free));
+      t0 += g.ncols;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (CS == 2) cluster_sync();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tbase, kTmemCols);
+  }
+}
+
+template <int MODE, int CS, bool BF16>
+cudaError_t launch_mode(const BwdParams& p_in, const BwdMaps& m, cudaStream_t st) {
+  BwdParams p = p_in;
+  constexpr int kMaxSmem = 232448;
+  bool resident = true;
+  Plan base = make_plan(p.n_chunks, CS, MODE, 0, true);
+  int stages = (kMaxSmem - 1024 - base.total) / kChunkBytes;
+  if (stages < 3) {
+    resident = false;
+    base = make_plan(p.n_chunks, CS, MODE, 0, false);
+    stages = (kMaxSmem - 1024 - base.total) / kChunkBytes;
+  }
+  stages = stages > 8 ? 8 : stages;
+  if (stages < 2) return cudaErrorInvalidConfiguration;
+  p.stages = stages;
+  const Plan plan = make_plan(p.n_chunks, CS, MODE, stages, resident);
+  const int smem = plan.total + 1024;
+  auto kern = bwd_main_kernel<MODE, CS, BF16>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = (MODE == kDQ) ? dim3(CS * p.q_tiles, p.Hq, p.B) : dim3(CS * p.kv_tiles, p.Hkv, p.B);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = CS;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, m.q, m.k, m.v, m.dout, p, static_cast<int>(resident));
+}
+
+template <int CS, bool BF16>
+cudaError_t launch_all(const BwdParams& p, const BwdMaps& m, cudaStream_t st) {
+  const int64_t rows = static_cast<int64_t>(p.B) * p.Hq * p.Nq;
+  bwd_preprocess_kernel<BF16><<<static_cast<unsigned>((rows + 7) / 8), 256, 0, st>>>(p);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  if ((e = launch_mode<kDV, CS, BF16>(p, m, st)) != cudaSuccess) return e;
+  if ((e = launch_mode<kDK, CS, BF16>(p, m, st)) != cudaSuccess) return e;
+  return launch_mode<kDQ, CS, BF16>(p, m, st);
+}
+
+}  // namespace
+
+cudaError_t launch_bwd(const BwdParams& p, const BwdMaps& m, bool bf16, cudaStream_t s) {
+  const bool pair = p.n_chunks > 4;
+  if (pair) return bf16 ? launch_all<2, true>(p, m, s) : launch_all<2, false>(p, m, s);
+  return bf16 ? launch_all<1, true>(p, m, s) : launch_all<1, false>(p, m, s);
+}
+
 }  // namespace ffpa
