@@ -16,7 +16,8 @@ from . import build as _build
 FFPA_F16, FFPA_BF16, FFPA_F32 = 0, 1, 2
 STATUS = {0: "FFPA_OK", 1: "FFPA_ERR_INVALID_ARG", 2: "FFPA_ERR_UNSUPPORTED", 3: "FFPA_ERR_ALIGNMENT",
           4: "FFPA_ERR_CUDA", 5: "FFPA_ERR_TIMEOUT"}
-EXPORTS = ("ffpa_fwd", "ffpa_bwd", "ffpa_status_string", "ffpa_check_status", "ffpa_version")
+EXPORTS = ("ffpa_fwd", "ffpa_bwd", "ffpa_status_string", "ffpa_check_status", "ffpa_set_timing_events",
+           "ffpa_version")
 
 
 class FfpaTensor(ctypes.Structure):
@@ -51,6 +52,8 @@ def load(path: str | None = None) -> ctypes.CDLL:
     lib.ffpa_status_string.restype = ctypes.c_char_p
     lib.ffpa_check_status.argtypes = [ctypes.c_void_p]
     lib.ffpa_check_status.restype = ctypes.c_int
+    lib.ffpa_set_timing_events.argtypes = [ctypes.POINTER(ctypes.c_void_p), ctypes.c_int]
+    lib.ffpa_set_timing_events.restype = ctypes.c_int
     lib.ffpa_version.argtypes = []
     lib.ffpa_version.restype = ctypes.c_int
     if path is None:
@@ -123,6 +126,13 @@ def ffpa_check_status(stream=None) -> int:
 
 def ffpa_status_string(code: int) -> str:
     return load().ffpa_status_string(code).decode()
+
+
+def ffpa_set_timing_events(events) -> None:
+    """Register torch.cuda.Event objects (enable_timing=True) the library records between its launches."""
+    handles = [int(e.cuda_event) for e in (events or [])]
+    arr = (ctypes.c_void_p * max(1, len(handles)))(*handles)
+    _raise(load().ffpa_set_timing_events(arr if handles else None, len(handles)))
 
 
 def ffpa_version() -> int:

@@ -30,6 +30,20 @@ uint32_t* device_status_word() {
 bool dtype_is_bf16(int dtype) { return dtype == FFPA_BF16; }
 
 namespace {
+struct TimingHook {
+  cudaEvent_t ev[8];
+  int n = 0;
+  int next = 0;
+};
+thread_local TimingHook g_hook;
+void timing_begin() { g_hook.next = 0; }
+}  // namespace
+
+void timing_mark(cudaStream_t s) {
+  if (g_hook.next < g_hook.n) cudaEventRecord(g_hook.ev[g_hook.next++], s);
+}
+
+namespace {
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
@@ -186,6 +200,7 @@ extern "C" int ffpa_fwd(const ffpa_tensor_t* q, const ffpa_tensor_t* k, const ff
   const bool bf16 = dtype_is_bf16(c.dtype);
   int64_t bsb, bsh, bsq, bsk;
   bias_strides(bias, &bsb, &bsh, &bsq, &bsk);
+  timing_begin();
 
   if (c.Nq <= kDecodeMaxRows) {
     DecodeParams p = {};
@@ -283,6 +298,7 @@ extern "C" int ffpa_bwd(const ffpa_tensor_t* q, const ffpa_tensor_t* k, const ff
       (rc = encode_map(&m.dout, dout)))
     return rc;
   const size_t rows = (size_t)c.B * c.Hq * c.Nq;
+  timing_begin();
   void* scratch = nullptr;
   if (cudaMallocAsync(&scratch, rows * 2 * sizeof(float), st) != cudaSuccess) return FFPA_ERR_CUDA;
   p.delta = static_cast<float*>(scratch);
@@ -313,6 +329,14 @@ extern "C" int ffpa_check_status(ffpa_stream_t stream) {
     if (cudaMemcpyToSymbol(g_status_word, &zero, sizeof(zero)) != cudaSuccess) return FFPA_ERR_CUDA;
     return FFPA_ERR_TIMEOUT;
   }
+  return FFPA_OK;
+}
+
+extern "C" int ffpa_set_timing_events(void* const* events, int count) {
+  if (count < 0 || count > 8 || (count > 0 && !events)) return FFPA_ERR_INVALID_ARG;
+  for (int i = 0; i < count; ++i) g_hook.ev[i] = static_cast<cudaEvent_t>(events[i]);
+  g_hook.n = count;
+  g_hook.next = 0;
   return FFPA_OK;
 }
 

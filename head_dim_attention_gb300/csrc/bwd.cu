@@ -595,13 +595,17 @@ cudaError_t launch_mode(const BwdParams& p_in, const BwdMaps& m, cudaStream_t st
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kern, m.q, m.k, m.v, m.dout, p, static_cast<int>(resident));
+  e = cudaLaunchKernelEx(&cfg, kern, m.q, m.k, m.v, m.dout, p, static_cast<int>(resident));
+  timing_mark(st);
+  return e;
 }
 
 template <int CS, bool BF16>
 cudaError_t launch_all(const BwdParams& p, const BwdMaps& m, cudaStream_t st) {
   const int64_t rows = static_cast<int64_t>(p.B) * p.Hq * p.Nq;
+  timing_mark(st);
   bwd_preprocess_kernel<BF16><<<static_cast<unsigned>((rows + 7) / 8), 256, 0, st>>>(p);
+  timing_mark(st);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   if ((e = launch_mode<kDV, CS, BF16>(p, m, st)) != cudaSuccess) return e;

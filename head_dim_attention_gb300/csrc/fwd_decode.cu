@@ -246,10 +246,13 @@ cudaError_t launch_decode_impl(const DecodeParams& p, cudaStream_t st) {
   auto k1 = decode_split_kernel<BF16>;
   cudaError_t e = cudaFuncSetAttribute(k1, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return e;
+  timing_mark(st);
   k1<<<dim3(p.n_splits, p.Hq, p.B), kDecThreads, smem, st>>>(p);
+  timing_mark(st);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   decode_combine_kernel<BF16><<<dim3(p.Nq, p.Hq, p.B), 128, 0, st>>>(p);
+  timing_mark(st);
   return cudaGetLastError();
 }
 

@@ -447,7 +447,10 @@ cudaError_t launch_impl(const FwdParams& p_in, const FwdMaps& m, cudaStream_t st
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kern, m.q, m.k, m.v, p);
+  timing_mark(st);
+  e = cudaLaunchKernelEx(&cfg, kern, m.q, m.k, m.v, p);
+  timing_mark(st);
+  return e;
 }
 
 }  // namespace

@@ -95,4 +95,8 @@ cudaError_t launch_bwd(const BwdParams& p, const BwdMaps& m, bool bf16, cudaStre
 
 uint32_t* device_status_word();  // per current device
 
+// Measurement hook (ffpa_set_timing_events): record the caller's next event
+// on `s`; a no-op unless the calling thread registered events.
+void timing_mark(cudaStream_t s);
+
 }  // namespace ffpa

@@ -119,6 +119,23 @@ const char* ffpa_status_string(int status);
  */
 int ffpa_check_status(ffpa_stream_t stream);
 
+/*
+ * ffpa_set_timing_events: measurement hook (no counterpart on the pages; it
+ * exists so a benchmark can time each kernel of a call with CUDA events).
+ *
+ *   events  array of `count` cudaEvent_t handles created by the caller, or NULL
+ *   count   0 disables the hook
+ *
+ * While set (per calling host thread), every later ffpa_fwd / ffpa_bwd call on
+ * this thread records events[0] on its stream before its first kernel launch
+ * and events[i] right after its i-th launch, for as many events as given
+ * (ffpa_fwd launches 1 kernel on the fused path and 2 on the decode path;
+ * ffpa_bwd launches 4: preprocess, dV, dK, dQ).  The caller keeps ownership of
+ * the events.  Returns FFPA_ERR_INVALID_ARG if count < 0, count > 8 or
+ * events is NULL with count > 0.
+ */
+int ffpa_set_timing_events(void* const* events, int count);
+
 /* Library version: major * 10000 + minor * 100 + patch. */
 int ffpa_version(void);
 
