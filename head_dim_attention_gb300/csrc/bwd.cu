@@ -219,11 +219,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(bar(bl.p_ready), 4);
     mbar_init(bar(bl.acc_ready), 1);
     mbar_init(bar(bl.acc_free), 4);
-    mbar_init(bar(bl.xfull), 1);
-    mbar_init(bar(bl.xfree), kTileRows);
+    mbar_init(bar(bl.xfull), kTileRows);  // one arrive per peer row: "my partial is in your buffer"
+    mbar_init(bar(bl.xfree), kTileRows);  // one arrive per peer row: "your buffer is free again"
     mbar_init(bar(bl.drain), 1);
     fence_mbar_init();
-    if (CS == 2) mbar_expect_tx(bar(bl.xfull), kLandingBytes);  // arm exchange 0
   }
   if (warp == 1) {
     tmem_alloc(smem_u32(tmem_slot), kTmemCols);
@@ -268,15 +267,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int c = 0; c < g.ncols && ok; ++c) {
           int ch, cr0;
           column<MODE>(g, p, c, &ch, &cr0);
-          for (int cc = 0; cc < own_n; ++cc) {
-            if (!resident) load(mA1, (own0 + cc) * kChunk, g.s_row0, g.s_head);
-            load(mB1, (own0 + cc) * kChunk, cr0, ch);
-          }
           if (two)
             for (int cc = 0; cc < own_n; ++cc) {
               if (!resident) load(mA2, (own0 + cc) * kChunk, g.s_row0, g.s_head);
               load(mB2, (own0 + cc) * kChunk, cr0, ch);
             }
+          for (int cc = 0; cc < own_n; ++cc) {
+            if (!resident) load(mA1, (own0 + cc) * kChunk, g.s_row0, g.s_head);
+            load(mB1, (own0 + cc) * kChunk, cr0, ch);
+          }
           for (int oc = 0; oc < oc_n; ++oc) load(mB3, (own0 + oc0 + oc) * kChunk, cr0, ch);
         }
       }
@@ -329,8 +328,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int c = 0; c < g.ncols && ok; ++c) {
           const int t = t0 + c;
+          // X1 still holds the previous tile's P/dS, the A operand of its
+          // gradient MMA; tcgen05.mma does not order a later write of D after
+          // an earlier read of A in TMEM, so X1 is rewritten only after that
+          // MMA has completed.  X2 has no such reader and goes first.
+          if (two) product(tbase + kX2, 1);
+          if (!ok) break;
+          if (c >= 1) {
+            ok = mbar_wait(bar(bl.acc_ready), (t - 1) & 1, status);
+            if (!ok) break;
+            tc_fence_after();
+          }
           product(tbase + kX1, 0);
-          if (two && ok) product(tbase + kX2, 1);
           if (!ok) break;
           umma_commit(bar(bl.x_full));
           ok = mbar_wait(bar(bl.p_ready), t & 1, status);
@@ -391,13 +400,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_ld_wait();
 #pragma unroll
         for (int c8 = 0; c8 < 8; ++c8)
-          st_async_v4(dst + (((c4 * 8 + c8) ^ swz) << 4), __uint_as_float(v[4 * c8]), __uint_as_float(v[4 * c8 + 1]),
-                      __uint_as_float(v[4 * c8 + 2]), __uint_as_float(v[4 * c8 + 3]), peer_xfull);
+          st_cluster_v4(dst + (((c4 * 8 + c8) ^ swz) << 4), __uint_as_float(v[4 * c8]), __uint_as_float(v[4 * c8 + 1]),
+                        __uint_as_float(v[4 * c8 + 2]), __uint_as_float(v[4 * c8 + 3]));
       }
+      mbar_arrive_remote(peer_xfull);  // release.cluster: the stores above are visible first
       ok = __all_sync(0xffffffffu, mbar_wait(bar(bl.xfull), x & 1, status));
     };
     auto release = [&]() {
-      if (r == 0) mbar_expect_tx(bar(bl.xfull), kLandingBytes);
       mbar_arrive_remote(peer_xfree);
       ++x;
     };
@@ -461,7 +470,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               xv = fmaf(__ldg(p.bias + g.b * p.bias_sb + hq * p.bias_sh + static_cast<int64_t>(ic) * p.bias_sq +
                               static_cast<int64_t>(min(j, p.Nkv - 1)) * p.bias_sk),
                         kLog2e, xv);
-            pv[ci] = valid ? exp2f(xv) : 0.f;
+            pv[ci] = valid ? ex2(xv) : 0.f;
           }
         }
         if constexpr (CS == 2) release();

@@ -132,11 +132,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(bar(bl.o_ready), 1);
     mbar_init(bar(bl.o_free), 4);
-    mbar_init(bar(bl.xfull), 1);
-    mbar_init(bar(bl.xfree), kTileRows);
+    mbar_init(bar(bl.xfull), kTileRows);  // one arrive per peer row: "my partial is in your buffer"
+    mbar_init(bar(bl.xfree), kTileRows);  // one arrive per peer row: "your buffer is free again"
     mbar_init(bar(bl.drain), 1);
     fence_mbar_init();
-    if (CS == 2) mbar_expect_tx(bar(bl.xfull), kLandingBytes);  // arm exchange 0
   }
   if (warp == 1) {
     tmem_alloc(smem_u32(tmem_slot), kTmemCols);
@@ -186,7 +185,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      const uint32_t idesc_s = idesc_f16(BF16, 128, 128, false, false);
+      const uint32_t idesc_s = idesc_f16(BF16, 128, 64, false, false);     // half a key tile
+      const uint32_t idesc_s128 = idesc_f16(BF16, 128, 128, false, false);  // a whole key tile
       const uint32_t idesc_pv = idesc_f16(BF16, 128, 64, false, true);
       bool ok = mbar_wait(bar(bl.q_full), 0, status);
       tc_fence_after();
@@ -201,22 +201,67 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int j = 0; j <= ntiles && ok; ++j) {
           if (j < ntiles) {
+            // S_t lands in the buffer that held P_{t-2}.  tcgen05.mma does not
+            // order a later MMA's write of D after an earlier MMA's read of A
+            // from TMEM, so S_t is issued in two N=64 halves: keys 64..127
+            // (columns 64..127, disjoint from P) first, then, once P_{t-2} V
+            // has completed, keys 0..63 (the columns P_{t-2} occupied).
+            // When the ring is shallower than the tile's chunk count the halves
+            // cannot be held, so the wait comes first and S_t is issued whole.
             const int t = t0 + j;
             const uint32_t s_tm = tbase + ((t & 1) ? kS1 : kS0);
+            if (own_n > stages) {
+              if (j >= 2) {
+                ok = mbar_wait(bar(bl.o_ready), (t - 2) & 1, status);
+                if (!ok) break;
+                tc_fence_after();
+              }
+              for (int c = 0; c < own_n && ok; ++c) {
+                const uint32_t s = it % stages;
+                ok = mbar_wait(bar(bl.full + s), (it / stages) & 1, status);
+                if (!ok) break;
+                tc_fence_after();
+                const uint32_t a0 = q_sm + c * kChunkBytes, b0 = ring_sm + s * kChunkBytes;
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk)
+                  umma_ss(s_tm, sdesc_sw128(a0 + kk * 32, 16, 1024), sdesc_sw128(b0 + kk * 32, 16, 1024),
+                          idesc_s128, (c | kk) != 0);
+                umma_commit(bar(bl.empty + s));
+                ++it;
+              }
+              if (!ok) break;
+              umma_commit(bar(bl.s_full + (t & 1)));
+            } else {
+            const uint32_t it0 = it;
             for (int c = 0; c < own_n && ok; ++c) {
               const uint32_t s = it % stages;
               ok = mbar_wait(bar(bl.full + s), (it / stages) & 1, status);
               if (!ok) break;
               tc_fence_after();
+              const uint32_t a0 = q_sm + c * kChunkBytes, b0 = ring_sm + s * kChunkBytes + 64 * 128;
+#pragma unroll
+              for (int kk = 0; kk < 4; ++kk)
+                umma_ss(s_tm + 64, sdesc_sw128(a0 + kk * 32, 16, 1024), sdesc_sw128(b0 + kk * 32, 16, 1024), idesc_s,
+                        (c | kk) != 0);
+              ++it;
+            }
+            if (!ok) break;
+            if (j >= 2) {
+              ok = mbar_wait(bar(bl.o_ready), (t - 2) & 1, status);  // P_{t-2} V done
+              if (!ok) break;
+              tc_fence_after();
+            }
+            for (int c = 0; c < own_n; ++c) {
+              const uint32_t s = (it0 + c) % stages;
               const uint32_t a0 = q_sm + c * kChunkBytes, b0 = ring_sm + s * kChunkBytes;
 #pragma unroll
               for (int kk = 0; kk < 4; ++kk)
                 umma_ss(s_tm, sdesc_sw128(a0 + kk * 32, 16, 1024), sdesc_sw128(b0 + kk * 32, 16, 1024), idesc_s,
                         (c | kk) != 0);
               umma_commit(bar(bl.empty + s));
-              ++it;
             }
             umma_commit(bar(bl.s_full + (t & 1)));
+            }
           }
           if (j >= 1 && ok) {
             const int t = t0 + j - 1;
@@ -291,7 +336,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t dst = peer_land + r * 512;
 #pragma unroll
           for (int c = 0; c < 32; ++c)
-            st_async_v4(dst + ((c ^ swz) << 4), s[4 * c], s[4 * c + 1], s[4 * c + 2], s[4 * c + 3], peer_xfull);
+            st_cluster_v4(dst + ((c ^ swz) << 4), s[4 * c], s[4 * c + 1], s[4 * c + 2], s[4 * c + 3]);
+          mbar_arrive_remote(peer_xfull);  // release.cluster: the stores above are visible first
           ok = __all_sync(0xffffffffu, mbar_wait(bar(bl.xfull), t & 1, status));
           if (!ok) break;
           const float4* src = reinterpret_cast<const float4*>(smem + plan.land_off + r * 512);
@@ -303,56 +349,62 @@ __global__ void __launch_bounds__(kThreads, 1)
             s[4 * c + 2] += v.z;
             s[4 * c + 3] += v.w;
           }
-          if (r == 0) mbar_expect_tx(bar(bl.xfull), kLandingBytes);  // arm the next exchange
-          mbar_arrive_remote(peer_xfree);                            // my landing buffer is free again
+          mbar_arrive_remote(peer_xfree);  // my landing buffer is free again
         }
         // scale (log2 domain), bias, masks
         const int kv0 = j * kTileRows;
-        float m_tile = -INFINITY;
         const bool masked = (kv0 + kTileRows > p.Nkv) || (p.causal && kv0 + kTileRows - 1 > row);
+        const float c_scale = p.scale_log2;
+        if (bias_row) {
 #pragma unroll
-        for (int i = 0; i < 128; ++i) {
-          float x = s[i] * p.scale_log2;
-          if (bias_row)
-            x = fmaf(__ldg(bias_row + static_cast<int64_t>(kv0 + min(i, p.Nkv - 1 - kv0)) * p.bias_sk), kLog2e, x);
-          if (masked) {
-            const int kv = kv0 + i;
-            if (kv >= p.Nkv || (p.causal && kv > row)) x = -INFINITY;
-          }
-          s[i] = x;
-          m_tile = fmaxf(m_tile, x);
+          for (int i = 0; i < 128; ++i)
+            s[i] = fmaf(__ldg(bias_row + static_cast<int64_t>(kv0 + min(i, p.Nkv - 1 - kv0)) * p.bias_sk), kLog2e,
+                        s[i] * c_scale);
+        } else {
+#pragma unroll
+          for (int i = 0; i < 128; ++i) s[i] *= c_scale;
         }
+        if (masked) {
+#pragma unroll
+          for (int i = 0; i < 128; ++i) {
+            const int kv = kv0 + i;
+            if (kv >= p.Nkv || (p.causal && kv > row)) s[i] = -INFINITY;
+          }
+        }
+        float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+        for (int i = 0; i < 128; ++i) mx[i & 3] = fmaxf(mx[i & 3], s[i]);
+        const float m_tile = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
         float alpha = 1.f;
         bool rescale = false;
         if (m_used == -INFINITY) {
           m_used = m_tile;
         } else if (m_tile > m_used + kRescaleLog2) {
-          alpha = exp2f(m_used - m_tile);
+          alpha = ex2(m_used - m_tile);
           m_used = m_tile;
           rescale = true;
         }
         const float m_ref = (m_used == -INFINITY) ? 0.f : m_used;
-        float lsum = 0.f;
+        float ls[4] = {0.f, 0.f, 0.f, 0.f};
         uint32_t pk[64];
 #pragma unroll
         for (int i = 0; i < 64; ++i) {
-          const float p0 = exp2f(s[2 * i] - m_ref), p1 = exp2f(s[2 * i + 1] - m_ref);
-          lsum += p0 + p1;
+          const float p0 = ex2(s[2 * i] - m_ref), p1 = ex2(s[2 * i + 1] - m_ref);
+          ls[i & 3] += p0 + p1;
           pk[i] = pack2<BF16>(p0, p1);
         }
-        l_sum = l_sum * alpha + lsum;
-        {
-          uint32_t(&lo)[32] = *reinterpret_cast<uint32_t(*)[32]>(&pk[0]);
-          uint32_t(&hi)[32] = *reinterpret_cast<uint32_t(*)[32]>(&pk[32]);
-          tmem_st32(tbase + lane_off + s_col, lo);
-          tmem_st32(tbase + lane_off + s_col + 32, hi);
-        }
-        tmem_st_wait();
-        if (__any_sync(0xffffffffu, rescale) && j >= 1) {
-          // correction: O of this row *= alpha, once the previous P V has landed
+        l_sum = l_sum * alpha + ((ls[0] + ls[1]) + (ls[2] + ls[3]));
+        if (j >= 1) {
+          // Wait for the previous P V MMA before touching TMEM again: storing P
+          // while that MMA ran gave wrong O on GB300 (found by testing, single-
+          // CTA configuration), and the O correction below needs it anyway.
+          // The MMA is short, so this wait is normally already satisfied.
           ok = __all_sync(0xffffffffu, mbar_wait(bar(bl.o_ready), (t - 1) & 1, status));
           if (!ok) break;
           tc_fence_after();
+        }
+        if (__any_sync(0xffffffffu, rescale) && j >= 1) {
+          // correction: O of this row *= alpha
           for (int c = 0; c < oc_n; ++c) {
 #pragma unroll
             for (int hh = 0; hh < 2; ++hh) {
@@ -365,8 +417,14 @@ __global__ void __launch_bounds__(kThreads, 1)
               tmem_st32(a, v);
             }
           }
-          tmem_st_wait();
         }
+        {
+          uint32_t(&lo)[32] = *reinterpret_cast<uint32_t(*)[32]>(&pk[0]);
+          uint32_t(&hi)[32] = *reinterpret_cast<uint32_t(*)[32]>(&pk[32]);
+          tmem_st32(tbase + lane_off + s_col, lo);
+          tmem_st32(tbase + lane_off + s_col + 32, hi);
+        }
+        tmem_st_wait();
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(bl.p_ready + (t & 1)));
