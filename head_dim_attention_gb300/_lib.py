@@ -131,6 +131,8 @@ def ffpa_status_string(code: int) -> str:
 def ffpa_set_timing_events(events) -> None:
     """Register torch.cuda.Event objects (enable_timing=True) the library records between its launches."""
     handles = [int(e.cuda_event) for e in (events or [])]
+    if any(h == 0 for h in handles):
+        raise ValueError("record each torch.cuda.Event once before registering it (torch creates events lazily)")
     arr = (ctypes.c_void_p * max(1, len(handles)))(*handles)
     _raise(load().ffpa_set_timing_events(arr if handles else None, len(handles)))
 

@@ -334,6 +334,8 @@ extern "C" int ffpa_check_status(ffpa_stream_t stream) {
 
 extern "C" int ffpa_set_timing_events(void* const* events, int count) {
   if (count < 0 || count > 8 || (count > 0 && !events)) return FFPA_ERR_INVALID_ARG;
+  for (int i = 0; i < count; ++i)
+    if (!events[i]) return FFPA_ERR_INVALID_ARG;
   for (int i = 0; i < count; ++i) g_hook.ev[i] = static_cast<cudaEvent_t>(events[i]);
   g_hook.n = count;
   g_hook.next = 0;

@@ -131,8 +131,8 @@ int ffpa_check_status(ffpa_stream_t stream);
  * and events[i] right after its i-th launch, for as many events as given
  * (ffpa_fwd launches 1 kernel on the fused path and 2 on the decode path;
  * ffpa_bwd launches 4: preprocess, dV, dK, dQ).  The caller keeps ownership of
- * the events.  Returns FFPA_ERR_INVALID_ARG if count < 0, count > 8 or
- * events is NULL with count > 0.
+ * the events.  Returns FFPA_ERR_INVALID_ARG if count < 0, count > 8, or
+ * events (or one of its first `count` handles) is NULL with count > 0.
  */
 int ffpa_set_timing_events(void* const* events, int count);
 
