@@ -15,9 +15,9 @@ from . import build as _build
 
 FFPA_F16, FFPA_BF16, FFPA_F32 = 0, 1, 2
 STATUS = {0: "FFPA_OK", 1: "FFPA_ERR_INVALID_ARG", 2: "FFPA_ERR_UNSUPPORTED", 3: "FFPA_ERR_ALIGNMENT",
-          4: "FFPA_ERR_CUDA", 5: "FFPA_ERR_TIMEOUT"}
-EXPORTS = ("ffpa_fwd", "ffpa_bwd", "ffpa_status_string", "ffpa_check_status", "ffpa_set_timing_events",
-           "ffpa_version")
+          4: "FFPA_ERR_CUDA", 5: "FFPA_ERR_TIMEOUT", 6: "FFPA_ERR_SCRATCH_LIMIT"}
+EXPORTS = ("ffpa_fwd", "ffpa_bwd", "ffpa_fwd_decode_noalloc", "ffpa_status_string", "ffpa_check_status",
+           "ffpa_set_timing_events", "ffpa_version")
 
 
 class FfpaTensor(ctypes.Structure):
@@ -48,6 +48,8 @@ def load(path: str | None = None) -> ctypes.CDLL:
     lib.ffpa_fwd.restype = ctypes.c_int
     lib.ffpa_bwd.argtypes = [P, P, P, P, ctypes.c_int, ctypes.c_float, P, P, P, P, P, P, ctypes.c_void_p]
     lib.ffpa_bwd.restype = ctypes.c_int
+    lib.ffpa_fwd_decode_noalloc.argtypes = [P, P, P, P, ctypes.c_int, ctypes.c_float, P, P, ctypes.c_void_p]
+    lib.ffpa_fwd_decode_noalloc.restype = ctypes.c_int
     lib.ffpa_status_string.argtypes = [ctypes.c_int]
     lib.ffpa_status_string.restype = ctypes.c_char_p
     lib.ffpa_check_status.argtypes = [ctypes.c_void_p]
@@ -107,6 +109,15 @@ def ffpa_fwd(q, k, v, bias, causal, scale, out, lse, stream=None) -> None:
     ds = [describe(q), describe(k), describe(v), describe(bias), describe(out), describe(lse, as_lse=True)]
     rc = lib.ffpa_fwd(_ref(ds[0]), _ref(ds[1]), _ref(ds[2]), _ref(ds[3]), int(causal), float(scale),
                       _ref(ds[4]), _ref(ds[5]), _stream(stream))
+    _raise(rc)
+
+
+def ffpa_fwd_decode_noalloc(q, k, v, bias, causal, scale, out, lse, stream=None) -> None:
+    """Call ffpa_fwd_decode_noalloc (decode forward, Nq <= 16, no device allocation)."""
+    lib = load()
+    ds = [describe(q), describe(k), describe(v), describe(bias), describe(out), describe(lse, as_lse=True)]
+    rc = lib.ffpa_fwd_decode_noalloc(_ref(ds[0]), _ref(ds[1]), _ref(ds[2]), _ref(ds[3]), int(causal),
+                                     float(scale), _ref(ds[4]), _ref(ds[5]), _stream(stream))
     _raise(rc)
 
 

@@ -308,6 +308,44 @@ extern "C" int ffpa_bwd(const ffpa_tensor_t* q, const ffpa_tensor_t* k, const ff
   return cuda_rc(e != cudaSuccess ? e : e2);
 }
 
+// Decode without allocation: validation and parameters as ffpa_fwd's decode
+// path; the partials go to the library's fixed device array.
+extern "C" int ffpa_fwd_decode_noalloc(const ffpa_tensor_t* q, const ffpa_tensor_t* k, const ffpa_tensor_t* v,
+                                       const ffpa_tensor_t* bias, int causal, float scale,
+                                       const ffpa_tensor_t* out, const ffpa_tensor_t* lse, ffpa_stream_t stream) {
+  Common c;
+  int rc = check_common(q, k, v, bias, scale, &c);
+  if (rc) return rc;
+  if (causal != 0 && causal != 1) return FFPA_ERR_INVALID_ARG;
+  rc = check_bhnd(out, c.dtype, {c.B, c.Hq, c.Nq, c.D});
+  if (rc) return rc;
+  if (lse && (rc = check_lse(lse, c))) return rc;
+  if (c.Nq > kDecodeMaxRows) return FFPA_ERR_UNSUPPORTED;
+  int64_t bsb, bsh, bsq, bsk;
+  bias_strides(bias, &bsb, &bsh, &bsq, &bsk);
+  DecodeParams p = {};
+  p.q = q->data;
+  p.k = k->data;
+  p.v = v->data;
+  p.out = out->data;
+  p.lse = lse ? static_cast<float*>(lse->data) : nullptr;
+  p.bias = bias ? static_cast<const float*>(bias->data) : nullptr;
+  p.q_sb = q->stride[0]; p.q_sh = q->stride[1]; p.q_sn = q->stride[2];
+  p.k_sb = k->stride[0]; p.k_sh = k->stride[1]; p.k_sn = k->stride[2];
+  p.v_sb = v->stride[0]; p.v_sh = v->stride[1]; p.v_sn = v->stride[2];
+  p.o_sb = out->stride[0]; p.o_sh = out->stride[1]; p.o_sn = out->stride[2];
+  p.bias_sb = bsb; p.bias_sh = bsh; p.bias_sq = bsq; p.bias_sk = bsk;
+  p.B = (int)c.B; p.Hq = (int)c.Hq; p.Hkv = (int)c.Hkv; p.Nq = (int)c.Nq; p.Nkv = (int)c.Nkv; p.D = (int)c.D;
+  p.group = (int)(c.Hq / c.Hkv);
+  p.causal = causal;
+  p.scale_log2 = scale * kLog2e;
+  p.split_len = 128;
+  p.n_splits = (int)((c.Nkv + p.split_len - 1) / p.split_len);
+  if (decode_scratch_bytes(p) > decode_noalloc_capacity_bytes()) return FFPA_ERR_SCRATCH_LIMIT;
+  timing_begin();
+  return cuda_rc(launch_fwd_decode_noalloc(p, dtype_is_bf16(c.dtype), reinterpret_cast<cudaStream_t>(stream)));
+}
+
 extern "C" const char* ffpa_status_string(int status) {
   switch (status) {
     case FFPA_OK: return "ok";
@@ -316,6 +354,7 @@ extern "C" const char* ffpa_status_string(int status) {
     case FFPA_ERR_ALIGNMENT: return "pointer or stride not aligned for TMA (16 bytes)";
     case FFPA_ERR_CUDA: return "CUDA runtime or launch error";
     case FFPA_ERR_TIMEOUT: return "a kernel's bounded wait timed out";
+    case FFPA_ERR_SCRATCH_LIMIT: return "the call needs more than the fixed no-allocation scratch (8 MiB)";
     default: return "unknown status";
   }
 }

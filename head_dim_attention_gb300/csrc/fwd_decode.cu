@@ -263,3 +263,66 @@ cudaError_t launch_fwd_decode(const DecodeParams& p, bool bf16, cudaStream_t s) 
 }
 
 }  // namespace ffpa
+
+// ---------------------------------------------------------------------------
+// Decode without allocation (ffpa_fwd_decode_noalloc).
+//
+// Some callers cannot allocate device memory while they run attention: code
+// that runs inside another framework's memory pool, or a serving loop that
+// must not call into the CUDA allocator on its hot path.  For them the decode
+// partials live in this fixed, file-scope device array instead of
+// cudaMallocAsync memory.  Every GPU that loads the library holds the array
+// until the process exits.  All calls share it: the split kernel overwrites
+// every partial the merge kernel reads, so nothing has to start at zero, and
+// two such calls whose work overlaps on the GPU (other streams, other host
+// threads) race on the array.
+#include <mutex>
+
+namespace ffpa {
+
+constexpr size_t kNoAllocScratchBytes = size_t(8) << 20;  // 8 MiB per device
+static __device__ __align__(256) float g_noalloc_scratch[kNoAllocScratchBytes / sizeof(float)];
+
+size_t decode_noalloc_capacity_bytes() { return kNoAllocScratchBytes; }
+
+// Bytes of partials a decode call needs: (D + 2) floats per (b, h, row, slice).
+size_t decode_scratch_bytes(const DecodeParams& p) {
+  const size_t rows = static_cast<size_t>(p.B) * p.Hq * p.Nq * p.n_splits;
+  return rows * (static_cast<size_t>(p.D) + 2) * sizeof(float);
+}
+
+// The array's device address on the current device.  In host code the name
+// g_noalloc_scratch is only a host-side stand-in, so the address is fetched
+// with cudaGetSymbolAddress once per device (on that device's first call) and
+// cached.
+static cudaError_t noalloc_scratch_address(float** out) {
+  static std::mutex mu;
+  static float* cache[64] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!cache[dev]) {
+    void* ptr = nullptr;
+    e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
+    if (e != cudaSuccess) return e;
+    cache[dev] = static_cast<float*>(ptr);
+  }
+  *out = cache[dev];
+  return cudaSuccess;
+}
+
+cudaError_t launch_fwd_decode_noalloc(const DecodeParams& p_in, bool bf16, cudaStream_t s) {
+  if (decode_scratch_bytes(p_in) > kNoAllocScratchBytes) return cudaErrorInvalidValue;
+  float* base = nullptr;
+  cudaError_t e = noalloc_scratch_address(&base);
+  if (e != cudaSuccess) return e;
+  DecodeParams p = p_in;
+  const size_t rows = static_cast<size_t>(p.B) * p.Hq * p.Nq * p.n_splits;
+  p.part_o = base;
+  p.part_ml = base + rows * p.D;  // D is a multiple of 64: 256-byte aligned
+  return launch_fwd_decode(p, bf16, s);
+}
+
+}  // namespace ffpa

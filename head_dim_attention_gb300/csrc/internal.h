@@ -91,6 +91,10 @@ bool dtype_is_bf16(int dtype);
 
 cudaError_t launch_fwd_main(const FwdParams& p, const FwdMaps& m, bool bf16, cudaStream_t s);
 cudaError_t launch_fwd_decode(const DecodeParams& p, bool bf16, cudaStream_t s);
+// Same kernels, partials in the library's fixed device array (no allocation).
+cudaError_t launch_fwd_decode_noalloc(const DecodeParams& p, bool bf16, cudaStream_t s);
+size_t decode_scratch_bytes(const DecodeParams& p);
+size_t decode_noalloc_capacity_bytes();
 cudaError_t launch_bwd(const BwdParams& p, const BwdMaps& m, bool bf16, cudaStream_t s);
 
 uint32_t* device_status_word();  // per current device

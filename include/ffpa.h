@@ -56,7 +56,8 @@ enum ffpa_status {
   FFPA_ERR_ALIGNMENT = 3,   /* base pointer not 16-byte aligned or a row/head/batch stride not a
                                multiple of 8 elements (TMA needs 16-byte strides) */
   FFPA_ERR_CUDA = 4,        /* a CUDA runtime call or kernel launch failed */
-  FFPA_ERR_TIMEOUT = 5      /* a kernel's bounded wait expired (reported by ffpa_check_status) */
+  FFPA_ERR_TIMEOUT = 5,     /* a kernel's bounded wait expired (reported by ffpa_check_status) */
+  FFPA_ERR_SCRATCH_LIMIT = 6 /* ffpa_fwd_decode_noalloc: the call needs more than the fixed scratch */
 };
 
 typedef struct ffpa_tensor {
@@ -108,6 +109,34 @@ int ffpa_bwd(const ffpa_tensor_t* q, const ffpa_tensor_t* k, const ffpa_tensor_t
              const ffpa_tensor_t* bias, int causal, float scale, const ffpa_tensor_t* out,
              const ffpa_tensor_t* lse, const ffpa_tensor_t* dout, const ffpa_tensor_t* dq,
              const ffpa_tensor_t* dk, const ffpa_tensor_t* dv, ffpa_stream_t stream);
+
+/*
+ * ffpa_fwd_decode_noalloc: the decode forward (Nq <= 16) without allocating.
+ * The pages have no counterpart; it exists for callers that cannot allocate
+ * device memory during the call: code running under another framework's
+ * memory pool or a serving loop that must not enter the CUDA
+ * allocator on its hot path.  ffpa_fwd's decode path takes its slice
+ * partials from cudaMallocAsync; this entry point keeps them in a fixed
+ * 8 MiB device array inside the library (held by every GPU that loads the
+ * library until the process exits) and calls no allocating routine.
+ *
+ *   Arguments, layouts, results and validation exactly as ffpa_fwd, plus:
+ *   - Nq must be <= 16, else FFPA_ERR_UNSUPPORTED.
+ *   - The partials take (D + 2) * 4 bytes per (batch, query head, query row,
+ *     slice of 128 keys); a call that needs more than 8 MiB returns
+ *     FFPA_ERR_SCRATCH_LIMIT and launches nothing (e.g. B=1, Hq=8, Nq=1,
+ *     Nkv=8192, D=512 needs 1.05 MB).
+ *   - The first call on a device looks up the array's device address (one
+ *     cudaGetSymbolAddress for that device); make that first call before
+ *     any stream capture on the device.
+ *   - All calls share the array.  Each call overwrites every partial it
+ *     reads, so nothing carries over between calls, but calls whose work
+ *     overlaps on the GPU (different streams or host threads) race on it:
+ *     order them on one stream or synchronise between them.
+ */
+int ffpa_fwd_decode_noalloc(const ffpa_tensor_t* q, const ffpa_tensor_t* k, const ffpa_tensor_t* v,
+                            const ffpa_tensor_t* bias, int causal, float scale, const ffpa_tensor_t* out,
+                            const ffpa_tensor_t* lse, ffpa_stream_t stream);
 
 /* Static text for a status code (never NULL). */
 const char* ffpa_status_string(int status);
