@@ -19,6 +19,11 @@
 // columns per pass).  GQA: the dV/dK kernels sweep every query head of the
 // group, so the group's sum forms in TMEM without any atomics or workspace.
 //
+// For 320 <= D <= 512 the pair does not exchange: each CTA reduces the score
+// products over the whole of D itself (1.5x to 1.67x the MMA work) and owns
+// half of the gradient's columns.  The exchange's distributed-shared-memory
+// traffic (64 KB per product and tile) costs more time than the extra MMAs.
+//
 // TMEM (512 columns): gradient accumulator [0, 256), X1 [256, 384) (scores,
 // then P or dS as the bf16/f16 A operand), X2 [384, 512) (dP).
 // Warp roles: warp 0 TMA producer, warp 1 TMEM owner + MMA issuer, warps 4-7
@@ -59,18 +64,23 @@ __host__ __device__ inline Bars bar_layout(int stages) {
   return b;
 }
 
+// Kernel flavours: one CTA per stationary tile (D <= 256), a cluster pair that
+// exchanges partial score tiles, or an independent pair that recomputes them.
+enum Flavour : int { kSolo = 0, kExchange = 1, kRecompute = 2 };
+
 struct Plan {
-  int own_max, n_a;  // resident A operands (0 = stream them through the ring)
+  int a_chunks;  // chunks the score products reduce over (per resident operand)
+  int n_a;       // resident stationary operands (A1, then A2); the rest stream through the ring
   int a_off, ring_off, land_off, bar_off, total;
 };
-__host__ __device__ inline Plan make_plan(int n_chunks, int cs, int mode, int stages, bool resident) {
+__host__ __device__ inline Plan make_plan(int n_chunks, int fl, int stages, int n_res) {
   Plan s;
-  s.own_max = (n_chunks + cs - 1) / cs;
-  s.n_a = resident ? (mode == kDV ? 1 : 2) : 0;
+  s.a_chunks = (fl == kExchange) ? (n_chunks + 1) / 2 : n_chunks;
+  s.n_a = n_res;
   s.a_off = 0;
-  s.ring_off = s.n_a * s.own_max * kChunkBytes;
+  s.ring_off = s.n_a * s.a_chunks * kChunkBytes;
   s.land_off = s.ring_off + stages * kChunkBytes;
-  s.bar_off = s.land_off + (cs == 2 ? kLandingBytes : 0);
+  s.bar_off = s.land_off + (fl == kExchange ? kLandingBytes : 0);
   s.total = s.bar_off + 1024;
   return s;
 }
@@ -176,15 +186,17 @@ __device__ __forceinline__ void column(const Geo& g, const BwdParams& p, int c, 
   }
 }
 
-template <int MODE, int CS, bool BF16>
+template <int MODE, int FL, bool BF16>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_main_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
                     const __grid_constant__ CUtensorMap map_v, const __grid_constant__ CUtensorMap map_do,
-                    const __grid_constant__ BwdParams p, const int resident) {
+                    const __grid_constant__ BwdParams p, const int n_res) {
+  constexpr int CS = (FL == kSolo) ? 1 : 2;  // CTAs per stationary tile
+  constexpr bool XCH = (FL == kExchange);
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int stages = p.stages;
-  const Plan plan = make_plan(p.n_chunks, CS, MODE, stages, resident != 0);
+  const Plan plan = make_plan(p.n_chunks, FL, stages, n_res);
   const Bars bl = bar_layout(stages);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + plan.bar_off);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + bl.count);
@@ -193,12 +205,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t a_sm = s_base + plan.a_off, ring_sm = s_base + plan.ring_off, land_sm = s_base + plan.land_off;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const uint32_t rank = (CS == 2) ? cluster_ctarank() : 0;
+  const uint32_t rank = XCH ? cluster_ctarank() : static_cast<uint32_t>(blockIdx.x) % CS;  // which half of D
   const Geo g = make_geo<MODE>(p, CS);
   const int n = p.n_chunks;
   const int half = (n + CS - 1) / CS;
   const int own0 = static_cast<int>(rank) * half;
   const int own_n = min(half, n - own0);
+  const int s0 = XCH ? own0 : 0;  // chunks the score products reduce over
+  const int s_n = XCH ? own_n : n;
   const int passes = (half + kMaxAccChunks - 1) / kMaxAccChunks;
   const bool two = (MODE != kDV);  // a second score-like product (dP)
   uint32_t* status = p.status;
@@ -230,7 +244,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   tc_fence_before();
   __syncthreads();
-  if (CS == 2) cluster_sync();
+  if (XCH) cluster_sync();
   tc_fence_after();
   const uint32_t tbase = *tmem_slot;
 
@@ -242,12 +256,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_prefetch_desc(&map_v);
       tma_prefetch_desc(&map_do);
       bool ok = true;
-      if (resident) {
-        mbar_expect_tx(bar(bl.a_full), plan.n_a * own_n * kChunkBytes);
-        for (int c = 0; c < own_n; ++c) {
-          tma_load_4d(a_sm + c * kChunkBytes, mA1, bar(bl.a_full), (own0 + c) * kChunk, g.s_row0, g.s_head, g.b);
-          if (two)
-            tma_load_4d(a_sm + (plan.own_max + c) * kChunkBytes, mA2, bar(bl.a_full), (own0 + c) * kChunk,
+      if (n_res > 0) {
+        mbar_expect_tx(bar(bl.a_full), n_res * s_n * kChunkBytes);
+        for (int c = 0; c < s_n; ++c) {
+          tma_load_4d(a_sm + c * kChunkBytes, mA1, bar(bl.a_full), (s0 + c) * kChunk, g.s_row0, g.s_head, g.b);
+          if (n_res > 1)
+            tma_load_4d(a_sm + (plan.a_chunks + c) * kChunkBytes, mA2, bar(bl.a_full), (s0 + c) * kChunk,
                         g.s_row0, g.s_head, g.b);
         }
       }
@@ -268,37 +282,38 @@ __global__ void __launch_bounds__(kThreads, 1)
           int ch, cr0;
           column<MODE>(g, p, c, &ch, &cr0);
           if (two)
-            for (int cc = 0; cc < own_n; ++cc) {
-              if (!resident) load(mA2, (own0 + cc) * kChunk, g.s_row0, g.s_head);
-              load(mB2, (own0 + cc) * kChunk, cr0, ch);
+            for (int cc = 0; cc < s_n; ++cc) {
+              if (n_res < 2) load(mA2, (s0 + cc) * kChunk, g.s_row0, g.s_head);
+              load(mB2, (s0 + cc) * kChunk, cr0, ch);
             }
-          for (int cc = 0; cc < own_n; ++cc) {
-            if (!resident) load(mA1, (own0 + cc) * kChunk, g.s_row0, g.s_head);
-            load(mB1, (own0 + cc) * kChunk, cr0, ch);
+          for (int cc = 0; cc < s_n; ++cc) {
+            if (n_res < 1) load(mA1, (s0 + cc) * kChunk, g.s_row0, g.s_head);
+            load(mB1, (s0 + cc) * kChunk, cr0, ch);
           }
           for (int oc = 0; oc < oc_n; ++oc) load(mB3, (own0 + oc0 + oc) * kChunk, cr0, ch);
         }
       }
       for (uint32_t u = (it > (uint32_t)stages ? it - stages : 0); u < it; ++u)
         mbar_wait(bar(bl.full + u % stages), (u / stages) & 1, status);
-      if (resident) mbar_wait(bar(bl.a_full), 0, status);
+      if (n_res > 0) mbar_wait(bar(bl.a_full), 0, status);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       const uint32_t idesc_x = idesc_f16(BF16, 128, 128, false, false);
       const uint32_t idesc_acc = idesc_f16(BF16, 128, 64, false, true);
-      bool ok = resident ? mbar_wait(bar(bl.a_full), 0, status) : true;
+      bool ok = n_res > 0 ? mbar_wait(bar(bl.a_full), 0, status) : true;
       tc_fence_after();
       uint32_t it = 0;
       int t0 = 0;
       // one score-like product: X (+)= A B^T over the CTA's own chunks
       auto product = [&](uint32_t x_tm, int a_slot) {
-        for (int cc = 0; cc < own_n && ok; ++cc) {
+        const bool resident = a_slot < n_res;
+        for (int cc = 0; cc < s_n && ok; ++cc) {
           uint32_t a0;
           uint32_t sa = 0;
           if (resident) {
-            a0 = a_sm + (a_slot * plan.own_max + cc) * kChunkBytes;
+            a0 = a_sm + (a_slot * plan.a_chunks + cc) * kChunkBytes;
           } else {
             sa = it % stages;
             ok = mbar_wait(bar(bl.full + sa), (it / stages) & 1, status);
@@ -372,9 +387,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int srow = g.s_row0 + r;
     const uint32_t lane_off = static_cast<uint32_t>((warp - 4) * 32) << 16;
     const uint32_t peer = rank ^ 1u;
-    const uint32_t peer_land = (CS == 2) ? mapa(land_sm, peer) : 0;
-    const uint32_t peer_xfull = (CS == 2) ? mapa(bar(bl.xfull), peer) : 0;
-    const uint32_t peer_xfree = (CS == 2) ? mapa(bar(bl.xfree), peer) : 0;
+    const uint32_t peer_land = XCH ? mapa(land_sm, peer) : 0;
+    const uint32_t peer_xfull = XCH ? mapa(bar(bl.xfull), peer) : 0;
+    const uint32_t peer_xfree = XCH ? mapa(bar(bl.xfree), peer) : 0;
     const uint32_t swz = static_cast<uint32_t>(r & 7);
     const float4* land = reinterpret_cast<const float4*>(smem + plan.land_off + r * 512);
     float lse2_row = 0.f, delta_row = 0.f;
@@ -417,7 +432,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_ld_wait();
 #pragma unroll
       for (int i = 0; i < 32; ++i) f[i] = __uint_as_float(v[i]);
-      if constexpr (CS == 2) {
+      if constexpr (XCH) {
 #pragma unroll
         for (int c8 = 0; c8 < 8; ++c8) {
           const float4 w = land[(c4 * 8 + c8) ^ swz];
@@ -439,7 +454,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!ok) break;
         tc_fence_after();
         float pv[128];
-        if constexpr (CS == 2) {
+        if constexpr (XCH) {
           send(kX1);
           if (!ok) break;
         }
@@ -473,9 +488,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             pv[ci] = valid ? ex2(xv) : 0.f;
           }
         }
-        if constexpr (CS == 2) release();
+        if constexpr (XCH) release();
         if (two) {
-          if constexpr (CS == 2) {
+          if constexpr (XCH) {
             send(kX2);
             if (!ok) break;
           }
@@ -496,7 +511,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               pv[ci] = pv[ci] * (f[e] - dl);
             }
           }
-          if constexpr (CS == 2) release();
+          if constexpr (XCH) release();
         }
         {
           uint32_t lo[32], hi[32];
@@ -565,31 +580,34 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   tc_fence_before();
   __syncthreads();
-  if (CS == 2) cluster_sync();
+  if (XCH) cluster_sync();
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tbase, kTmemCols);
   }
 }
 
-template <int MODE, int CS, bool BF16>
+template <int MODE, int FL, bool BF16>
 cudaError_t launch_mode(const BwdParams& p_in, const BwdMaps& m, cudaStream_t st) {
   BwdParams p = p_in;
+  constexpr int CS = (FL == kSolo) ? 1 : 2;
   constexpr int kMaxSmem = 232448;
-  bool resident = true;
-  Plan base = make_plan(p.n_chunks, CS, MODE, 0, true);
-  int stages = (kMaxSmem - 1024 - base.total) / kChunkBytes;
-  if (stages < 3) {
-    resident = false;
-    base = make_plan(p.n_chunks, CS, MODE, 0, false);
+  // Keep as many stationary operands resident as leave a ring of >= 3 stages
+  // (>= 2 when nothing is resident).
+  int n_res = (MODE == kDV) ? 1 : 2;
+  int stages = 0;
+  for (; n_res >= 0; --n_res) {
+    const Plan base = make_plan(p.n_chunks, FL, 0, n_res);
     stages = (kMaxSmem - 1024 - base.total) / kChunkBytes;
+    if (stages >= 3) break;
   }
+  if (n_res < 0) n_res = 0;
   stages = stages > 8 ? 8 : stages;
   if (stages < 2) return cudaErrorInvalidConfiguration;
   p.stages = stages;
-  const Plan plan = make_plan(p.n_chunks, CS, MODE, stages, resident);
+  const Plan plan = make_plan(p.n_chunks, FL, stages, n_res);
   const int smem = plan.total + 1024;
-  auto kern = bwd_main_kernel<MODE, CS, BF16>;
+  auto kern = bwd_main_kernel<MODE, FL, BF16>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
@@ -603,13 +621,13 @@ cudaError_t launch_mode(const BwdParams& p_in, const BwdMaps& m, cudaStream_t st
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  e = cudaLaunchKernelEx(&cfg, kern, m.q, m.k, m.v, m.dout, p, static_cast<int>(resident));
+  cfg.numAttrs = (FL == kExchange) ? 1 : 0;  // only the exchanging pair is a cluster
+  e = cudaLaunchKernelEx(&cfg, kern, m.q, m.k, m.v, m.dout, p, n_res);
   timing_mark(st);
   return e;
 }
 
-template <int CS, bool BF16>
+template <int FL, bool BF16>
 cudaError_t launch_all(const BwdParams& p, const BwdMaps& m, cudaStream_t st) {
   const int64_t rows = static_cast<int64_t>(p.B) * p.Hq * p.Nq;
   timing_mark(st);
@@ -617,17 +635,17 @@ cudaError_t launch_all(const BwdParams& p, const BwdMaps& m, cudaStream_t st) {
   timing_mark(st);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  if ((e = launch_mode<kDV, CS, BF16>(p, m, st)) != cudaSuccess) return e;
-  if ((e = launch_mode<kDK, CS, BF16>(p, m, st)) != cudaSuccess) return e;
-  return launch_mode<kDQ, CS, BF16>(p, m, st);
+  if ((e = launch_mode<kDV, FL, BF16>(p, m, st)) != cudaSuccess) return e;
+  if ((e = launch_mode<kDK, FL, BF16>(p, m, st)) != cudaSuccess) return e;
+  return launch_mode<kDQ, FL, BF16>(p, m, st);
 }
 
 }  // namespace
 
 cudaError_t launch_bwd(const BwdParams& p, const BwdMaps& m, bool bf16, cudaStream_t s) {
-  const bool pair = p.n_chunks > 4;
-  if (pair) return bf16 ? launch_all<2, true>(p, m, s) : launch_all<2, false>(p, m, s);
-  return bf16 ? launch_all<1, true>(p, m, s) : launch_all<1, false>(p, m, s);
+  if (p.n_chunks <= 4) return bf16 ? launch_all<kSolo, true>(p, m, s) : launch_all<kSolo, false>(p, m, s);
+  if (p.n_chunks <= 8) return bf16 ? launch_all<kRecompute, true>(p, m, s) : launch_all<kRecompute, false>(p, m, s);
+  return bf16 ? launch_all<kExchange, true>(p, m, s) : launch_all<kExchange, false>(p, m, s);
 }
 
 }  // namespace ffpa

@@ -26,6 +26,13 @@
 // When a CTA owns more than 4 chunks (D > 512) it sweeps the keys once per
 // 4-chunk slice of its O columns ("passes"), recomputing S each time.
 //
+// Pair without exchange (320 <= D <= 512).  The exchange moves 64 KB per key
+// tile and CTA through distributed shared memory, whose bandwidth is far
+// below the tensor pipe's.  For D <= 512 the two CTAs of a query tile instead
+// each reduce S over the whole of D (Q fully resident, every K chunk
+// streamed) and own half of O: 1.5x the MMA work of the exchange, no cluster
+// and no DSMEM traffic, leaving shared-memory bandwidth as the bound.
+//
 // Warp roles (256 threads): warp 0 = TMA producer, warp 1 = TMEM owner and
 // MMA issuer, warps 4-7 = softmax / correction / epilogue (one query row per
 // thread; warp 4+w reads TMEM lanes 32w..32w+31).
@@ -64,17 +71,21 @@ __host__ __device__ inline Bars bar_layout(int stages) {
   return b;
 }
 
+// Kernel flavours: one CTA per query tile (D <= 256), a cluster pair that
+// exchanges partial scores, or an independent pair that recomputes them.
+enum Flavour : int { kSolo = 0, kExchange = 1, kRecompute = 2 };
+
 struct SmemPlan {
-  int own_max;  // chunks of the larger half
+  int q_chunks;  // resident Q chunks (the chunks this CTA reduces S over)
   int q_off, ring_off, land_off, bar_off, total;
 };
-__host__ __device__ inline SmemPlan smem_plan(int n_chunks, int cs, int stages) {
+__host__ __device__ inline SmemPlan smem_plan(int n_chunks, int fl, int stages) {
   SmemPlan s;
-  s.own_max = (n_chunks + cs - 1) / cs;
+  s.q_chunks = (fl == kExchange) ? (n_chunks + 1) / 2 : n_chunks;
   s.q_off = 0;
-  s.ring_off = s.own_max * kChunkBytes;
+  s.ring_off = s.q_chunks * kChunkBytes;
   s.land_off = s.ring_off + stages * kChunkBytes;
-  s.bar_off = s.land_off + (cs == 2 ? kLandingBytes : 0);
+  s.bar_off = s.land_off + (fl == kExchange ? kLandingBytes : 0);
   s.total = s.bar_off + 1024;  // barriers + TMEM slot
   return s;
 }
@@ -90,14 +101,16 @@ __device__ __forceinline__ uint32_t pack2(float a, float b) {
   }
 }
 
-template <int CS, bool BF16>
+template <int FL, bool BF16>
 __global__ void __launch_bounds__(kThreads, 1)
     fwd_main_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
                     const __grid_constant__ CUtensorMap map_v, const __grid_constant__ FwdParams p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int stages = p.stages;
-  const SmemPlan plan = smem_plan(p.n_chunks, CS, stages);
+  constexpr int CS = (FL == kSolo) ? 1 : 2;  // CTAs per query tile
+  constexpr bool XCH = (FL == kExchange);
+  const SmemPlan plan = smem_plan(p.n_chunks, FL, stages);
   const Bars bl = bar_layout(stages);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + plan.bar_off);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + bl.count);
@@ -106,7 +119,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t q_sm = s_base + plan.q_off, ring_sm = s_base + plan.ring_off, land_sm = s_base + plan.land_off;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const uint32_t rank = (CS == 2) ? cluster_ctarank() : 0;
+  const uint32_t rank = XCH ? cluster_ctarank() : static_cast<uint32_t>(blockIdx.x) % CS;  // which half of D
   const int qt = p.q_tiles - 1 - static_cast<int>(blockIdx.x) / CS;  // heavy causal tiles first
   const int h = blockIdx.y, b = blockIdx.z;
   const int kvh = h / p.group;
@@ -115,6 +128,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int half = (n + CS - 1) / CS;
   const int own0 = static_cast<int>(rank) * half;
   const int own_n = min(half, n - own0);
+  const int s0 = XCH ? own0 : 0;  // chunks S is reduced over (and Q chunks resident)
+  const int s_n = XCH ? own_n : n;
   const int passes = (half + kMaxOChunksPerPass - 1) / kMaxOChunksPerPass;
   const int kv_end = p.causal ? min(p.Nkv, q0 + kTileRows) : p.Nkv;
   const int ntiles = (kv_end + kTileRows - 1) / kTileRows;
@@ -143,7 +158,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   tc_fence_before();
   __syncthreads();
-  if (CS == 2) cluster_sync();
+  if (XCH) cluster_sync();
   tc_fence_after();
   const uint32_t tbase = *tmem_slot;
 
@@ -154,9 +169,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_prefetch_desc(&map_k);
       tma_prefetch_desc(&map_v);
       bool ok = true;
-      mbar_expect_tx(bar(bl.q_full), own_n * kChunkBytes);
-      for (int c = 0; c < own_n; ++c)
-        tma_load_4d(q_sm + c * kChunkBytes, &map_q, bar(bl.q_full), (own0 + c) * kChunk, q0, h, b);
+      mbar_expect_tx(bar(bl.q_full), s_n * kChunkBytes);
+      for (int c = 0; c < s_n; ++c)
+        tma_load_4d(q_sm + c * kChunkBytes, &map_q, bar(bl.q_full), (s0 + c) * kChunk, q0, h, b);
       uint32_t it = 0;
       auto load = [&](const CUtensorMap* m, int dcol, int row) {
         const uint32_t s = it % stages, r = it / stages;
@@ -172,7 +187,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int oc_n = max(0, min(kMaxOChunksPerPass, own_n - oc0));
         for (int j = 0; j <= ntiles && ok; ++j) {
           if (j < ntiles)
-            for (int c = 0; c < own_n; ++c) load(&map_k, (own0 + c) * kChunk, j * kTileRows);
+            for (int c = 0; c < s_n; ++c) load(&map_k, (s0 + c) * kChunk, j * kTileRows);
           if (j >= 1)
             for (int c = 0; c < oc_n; ++c) load(&map_v, (own0 + oc0 + c) * kChunk, (j - 1) * kTileRows);
         }
@@ -210,13 +225,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             // cannot be held, so the wait comes first and S_t is issued whole.
             const int t = t0 + j;
             const uint32_t s_tm = tbase + ((t & 1) ? kS1 : kS0);
-            if (own_n > stages) {
+            if (s_n > stages) {
               if (j >= 2) {
                 ok = mbar_wait(bar(bl.o_ready), (t - 2) & 1, status);
                 if (!ok) break;
                 tc_fence_after();
               }
-              for (int c = 0; c < own_n && ok; ++c) {
+              for (int c = 0; c < s_n && ok; ++c) {
                 const uint32_t s = it % stages;
                 ok = mbar_wait(bar(bl.full + s), (it / stages) & 1, status);
                 if (!ok) break;
@@ -233,7 +248,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               umma_commit(bar(bl.s_full + (t & 1)));
             } else {
             const uint32_t it0 = it;
-            for (int c = 0; c < own_n && ok; ++c) {
+            for (int c = 0; c < s_n && ok; ++c) {
               const uint32_t s = it % stages;
               ok = mbar_wait(bar(bl.full + s), (it / stages) & 1, status);
               if (!ok) break;
@@ -251,7 +266,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               if (!ok) break;
               tc_fence_after();
             }
-            for (int c = 0; c < own_n; ++c) {
+            for (int c = 0; c < s_n; ++c) {
               const uint32_t s = (it0 + c) % stages;
               const uint32_t a0 = q_sm + c * kChunkBytes, b0 = ring_sm + s * kChunkBytes;
 #pragma unroll
@@ -296,9 +311,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int row = q0 + r;
     const uint32_t lane_off = static_cast<uint32_t>((warp - 4) * 32) << 16;
     const uint32_t peer = rank ^ 1u;
-    const uint32_t peer_land = (CS == 2) ? mapa(land_sm, peer) : 0;
-    const uint32_t peer_xfull = (CS == 2) ? mapa(bar(bl.xfull), peer) : 0;
-    const uint32_t peer_xfree = (CS == 2) ? mapa(bar(bl.xfree), peer) : 0;
+    const uint32_t peer_land = XCH ? mapa(land_sm, peer) : 0;
+    const uint32_t peer_xfull = XCH ? mapa(bar(bl.xfull), peer) : 0;
+    const uint32_t peer_xfree = XCH ? mapa(bar(bl.xfree), peer) : 0;
     const uint32_t swz = static_cast<uint32_t>(r & 7);
     const float* bias_row = nullptr;
     if (p.bias)
@@ -327,7 +342,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int i = 0; i < 32; ++i) s[c * 32 + i] = __uint_as_float(v[i]);
         }
-        if constexpr (CS == 2) {
+        if constexpr (XCH) {
           // swap partial scores with the peer CTA (it holds the other half of D)
           if (t >= 1) {
             ok = __all_sync(0xffffffffu, mbar_wait(bar(bl.xfree), (t - 1) & 1, status));
@@ -472,25 +487,26 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   tc_fence_before();
   __syncthreads();
-  if (CS == 2) cluster_sync();
+  if (XCH) cluster_sync();
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tbase, kTmemCols);
   }
 }
 
-template <int CS, bool BF16>
+template <int FL, bool BF16>
 cudaError_t launch_impl(const FwdParams& p_in, const FwdMaps& m, cudaStream_t st) {
   FwdParams p = p_in;
+  constexpr int CS = (FL == kSolo) ? 1 : 2;
   constexpr int kMaxSmem = 232448;  // 227 KB opt-in per block
-  const SmemPlan base = smem_plan(p.n_chunks, CS, 0);
+  const SmemPlan base = smem_plan(p.n_chunks, FL, 0);
   int stages = (kMaxSmem - 1024 - base.total) / kChunkBytes;
   stages = stages > 8 ? 8 : stages;
   if (stages < 2) return cudaErrorInvalidConfiguration;
   p.stages = stages;
-  const SmemPlan plan = smem_plan(p.n_chunks, CS, stages);
+  const SmemPlan plan = smem_plan(p.n_chunks, FL, stages);
   const int smem = plan.total + 1024;  // + alignment slack
-  auto kern = fwd_main_kernel<CS, BF16>;
+  auto kern = fwd_main_kernel<FL, BF16>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
@@ -504,7 +520,7 @@ cudaError_t launch_impl(const FwdParams& p_in, const FwdMaps& m, cudaStream_t st
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = (FL == kExchange) ? 1 : 0;  // only the exchanging pair is a cluster
   timing_mark(st);
   e = cudaLaunchKernelEx(&cfg, kern, m.q, m.k, m.v, p);
   timing_mark(st);
@@ -514,9 +530,10 @@ cudaError_t launch_impl(const FwdParams& p_in, const FwdMaps& m, cudaStream_t st
 }  // namespace
 
 cudaError_t launch_fwd_main(const FwdParams& p, const FwdMaps& m, bool bf16, cudaStream_t s) {
-  const bool pair = p.n_chunks > 4;
-  if (pair) return bf16 ? launch_impl<2, true>(p, m, s) : launch_impl<2, false>(p, m, s);
-  return bf16 ? launch_impl<1, true>(p, m, s) : launch_impl<1, false>(p, m, s);
+  if (p.n_chunks <= 4) return bf16 ? launch_impl<kSolo, true>(p, m, s) : launch_impl<kSolo, false>(p, m, s);
+  if (p.n_chunks <= 8)
+    return bf16 ? launch_impl<kRecompute, true>(p, m, s) : launch_impl<kRecompute, false>(p, m, s);
+  return bf16 ? launch_impl<kExchange, true>(p, m, s) : launch_impl<kExchange, false>(p, m, s);
 }
 
 }  // namespace ffpa
