@@ -250,30 +250,52 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
-    if (lane == 0) {
-      tma_prefetch_desc(&map_q);
-      tma_prefetch_desc(&map_k);
-      tma_prefetch_desc(&map_v);
-      tma_prefetch_desc(&map_do);
-      bool ok = true;
-      if (n_res > 0) {
-        mbar_expect_tx(bar(bl.a_full), n_res * s_n * kChunkBytes);
-        for (int c = 0; c < s_n; ++c) {
-          tma_load_4d(a_sm + c * kChunkBytes, mA1, bar(bl.a_full), (s0 + c) * kChunk, g.s_row0, g.s_head, g.b);
-          if (n_res > 1)
-            tma_load_4d(a_sm + (plan.a_chunks + c) * kChunkBytes, mA2, bar(bl.a_full), (s0 + c) * kChunk,
-                        g.s_row0, g.s_head, g.b);
+    // G lanes issue consecutive loads together (arming a barrier and issuing a
+    // TMA load costs one thread ~500 cycles); lane g owns every G-th load.
+    const int G = stages >= 6 ? 4 : (stages >= 4 ? 2 : 1);
+    if (lane < G) {
+      const unsigned gmask = (1u << G) - 1u;
+      if (lane == 0) {
+        tma_prefetch_desc(&map_q);
+        tma_prefetch_desc(&map_k);
+        tma_prefetch_desc(&map_v);
+        tma_prefetch_desc(&map_do);
+        if (n_res > 0) {
+          mbar_expect_tx(bar(bl.a_full), n_res * s_n * kChunkBytes);
+          for (int c = 0; c < s_n; ++c) {
+            tma_load_4d(a_sm + c * kChunkBytes, mA1, bar(bl.a_full), (s0 + c) * kChunk, g.s_row0, g.s_head, g.b);
+            if (n_res > 1)
+              tma_load_4d(a_sm + (plan.a_chunks + c) * kChunkBytes, mA2, bar(bl.a_full), (s0 + c) * kChunk,
+                          g.s_row0, g.s_head, g.b);
+          }
         }
       }
+      bool ok = true;
       uint32_t it = 0;
-      auto load = [&](const CUtensorMap* m, int dcol, int row, int head) {
-        const uint32_t s = it % stages, r = it / stages;
-        if (ok) ok = mbar_wait(bar(bl.empty + s), (r & 1) ^ 1, status);
-        if (ok) {
-          mbar_expect_tx(bar(bl.full + s), kChunkBytes);
-          tma_load_4d(ring_sm + s * kChunkBytes, m, bar(bl.full + s), dcol, row, head, g.b);
-          ++it;
+      int my_it = -1, my_c0 = 0, my_c1 = 0, my_c2 = 0;
+      const CUtensorMap* my_m = nullptr;
+      auto flush = [&]() {
+        if (my_it >= 0 && ok) {
+          const uint32_t s = static_cast<uint32_t>(my_it) % stages, r = static_cast<uint32_t>(my_it) / stages;
+          ok = mbar_wait(bar(bl.empty + s), (r & 1) ^ 1, status);
+          if (ok) {
+            mbar_expect_tx(bar(bl.full + s), kChunkBytes);
+            tma_load_4d(ring_sm + s * kChunkBytes, my_m, bar(bl.full + s), my_c0, my_c1, my_c2, g.b);
+          }
         }
+        my_it = -1;
+        ok = __all_sync(gmask, ok);
+      };
+      auto load = [&](const CUtensorMap* m, int dcol, int row, int head) {
+        if (static_cast<int>(it % G) == lane) {
+          my_it = static_cast<int>(it);
+          my_m = m;
+          my_c0 = dcol;
+          my_c1 = row;
+          my_c2 = head;
+        }
+        ++it;
+        if (it % G == 0) flush();
       };
       for (int pass = 0; pass < passes && ok; ++pass) {
         const int oc0 = pass * kMaxAccChunks;
@@ -293,44 +315,53 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int oc = 0; oc < oc_n; ++oc) load(mB3, (own0 + oc0 + oc) * kChunk, cr0, ch);
         }
       }
-      for (uint32_t u = (it > (uint32_t)stages ? it - stages : 0); u < it; ++u)
-        mbar_wait(bar(bl.full + u % stages), (u / stages) & 1, status);
-      if (n_res > 0) mbar_wait(bar(bl.a_full), 0, status);
+      flush();
+      __syncwarp(gmask);
+      if (lane == 0) {
+        for (uint32_t u = (it > (uint32_t)stages ? it - stages : 0); u < it; ++u)
+          mbar_wait(bar(bl.full + u % stages), (u / stages) & 1, status);
+        if (n_res > 0) mbar_wait(bar(bl.a_full), 0, status);
+      }
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
+    // Descriptors are formed once and advanced by constants (building them per
+    // MMA made the issuing thread the bottleneck).
     if (lane == 0) {
       const uint32_t idesc_x = idesc_f16(BF16, 128, 128, false, false);
       const uint32_t idesc_acc = idesc_f16(BF16, 128, 64, false, true);
+      const uint32_t idesc_acc2 = idesc_f16(BF16, 128, 128, false, true);  // two chunks in adjacent slots
+      const uint64_t da = sdesc_sw128(a_sm, 16, 1024);                     // resident operands, K-major
+      const uint64_t dk = sdesc_sw128(ring_sm, 16, 1024);                  // ring slots, K-major
+      const uint64_t dm = sdesc_sw128(ring_sm, kChunkBytes, 1024);         // ring slots, MN-major
       bool ok = n_res > 0 ? mbar_wait(bar(bl.a_full), 0, status) : true;
       tc_fence_after();
       uint32_t it = 0;
       int t0 = 0;
-      // one score-like product: X (+)= A B^T over the CTA's own chunks
+      // one score-like product: X (+)= A B^T over the chunks s0 .. s0+s_n-1
       auto product = [&](uint32_t x_tm, int a_slot) {
         const bool resident = a_slot < n_res;
         for (int cc = 0; cc < s_n && ok; ++cc) {
-          uint32_t a0;
+          uint64_t a;
           uint32_t sa = 0;
           if (resident) {
-            a0 = a_sm + (a_slot * plan.a_chunks + cc) * kChunkBytes;
+            a = sdesc_advance(da, (a_slot * plan.a_chunks + cc) * kChunkBytes);
           } else {
             sa = it % stages;
             ok = mbar_wait(bar(bl.full + sa), (it / stages) & 1, status);
             if (!ok) return;
             ++it;
-            a0 = ring_sm + sa * kChunkBytes;
+            a = sdesc_advance(dk, sa * kChunkBytes);
           }
           const uint32_t sb = it % stages;
           ok = mbar_wait(bar(bl.full + sb), (it / stages) & 1, status);
           if (!ok) return;
           ++it;
           tc_fence_after();
-          const uint32_t b0 = ring_sm + sb * kChunkBytes;
+          const uint64_t bd = sdesc_advance(dk, sb * kChunkBytes);
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
-            umma_ss(x_tm, sdesc_sw128(a0 + kk * 32, 16, 1024), sdesc_sw128(b0 + kk * 32, 16, 1024), idesc_x,
-                    (cc | kk) != 0);
+            umma_ss(x_tm, sdesc_advance(a, kk * 32), sdesc_advance(bd, kk * 32), idesc_x, (cc | kk) != 0);
           if (!resident) umma_commit(bar(bl.empty + sa));
           umma_commit(bar(bl.empty + sb));
         }
@@ -360,18 +391,34 @@ __global__ void __launch_bounds__(kThreads, 1)
           ok = mbar_wait(bar(bl.p_ready), t & 1, status);
           if (!ok) break;
           tc_fence_after();
-          for (int oc = 0; oc < oc_n && ok; ++oc) {
+          // gradient += (P or dS) B3: two chunks per MMA (N=128) when they sit in adjacent ring slots
+          for (int oc = 0; oc < oc_n && ok;) {
             const uint32_t s = it % stages;
+            const bool pair = (oc + 1 < oc_n) && (s + 1 < static_cast<uint32_t>(stages));
             ok = mbar_wait(bar(bl.full + s), (it / stages) & 1, status);
+            if (ok && pair) ok = mbar_wait(bar(bl.full + s + 1), ((it + 1) / stages) & 1, status);
             if (!ok) break;
-            ++it;
             tc_fence_after();
-            const uint32_t b0 = ring_sm + s * kChunkBytes;
+            const uint64_t bd = sdesc_advance(dm, s * kChunkBytes);
+            const uint32_t acc0 = c > 0 ? 1u : 0u;
+            if (pair) {
 #pragma unroll
-            for (int kk = 0; kk < 8; ++kk)
-              umma_ts(tbase + oc * kChunk, tbase + kX1 + kk * 8, sdesc_sw128(b0 + kk * 2048, 16384, 1024), idesc_acc,
-                      (c > 0 || kk > 0));
-            umma_commit(bar(bl.empty + s));
+              for (int kk = 0; kk < 8; ++kk)
+                umma_ts(tbase + oc * kChunk, tbase + kX1 + kk * 8, sdesc_advance(bd, kk * 2048), idesc_acc2,
+                        acc0 | (kk > 0));
+              umma_commit(bar(bl.empty + s));
+              umma_commit(bar(bl.empty + s + 1));
+              it += 2;
+              oc += 2;
+            } else {
+#pragma unroll
+              for (int kk = 0; kk < 8; ++kk)
+                umma_ts(tbase + oc * kChunk, tbase + kX1 + kk * 8, sdesc_advance(bd, kk * 2048), idesc_acc,
+                        acc0 | (kk > 0));
+              umma_commit(bar(bl.empty + s));
+              it += 1;
+              oc += 1;
+            }
           }
           umma_commit(bar(bl.acc_ready));
         }

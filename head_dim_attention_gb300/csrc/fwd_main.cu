@@ -164,23 +164,45 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
-    if (lane == 0) {
-      tma_prefetch_desc(&map_q);
-      tma_prefetch_desc(&map_k);
-      tma_prefetch_desc(&map_v);
+    // Arming a barrier and issuing a TMA load costs one thread ~500 cycles, so
+    // G lanes issue consecutive loads of the sequence together (lane g owns
+    // every G-th load; each waits for its own ring slot).
+    const int G = stages >= 6 ? 4 : (stages >= 4 ? 2 : 1);
+    if (lane < G) {
+      const unsigned gmask = (1u << G) - 1u;
+      if (lane == 0) {
+        tma_prefetch_desc(&map_q);
+        tma_prefetch_desc(&map_k);
+        tma_prefetch_desc(&map_v);
+        mbar_expect_tx(bar(bl.q_full), s_n * kChunkBytes);
+        for (int c = 0; c < s_n; ++c)
+          tma_load_4d(q_sm + c * kChunkBytes, &map_q, bar(bl.q_full), (s0 + c) * kChunk, q0, h, b);
+      }
       bool ok = true;
-      mbar_expect_tx(bar(bl.q_full), s_n * kChunkBytes);
-      for (int c = 0; c < s_n; ++c)
-        tma_load_4d(q_sm + c * kChunkBytes, &map_q, bar(bl.q_full), (s0 + c) * kChunk, q0, h, b);
       uint32_t it = 0;
-      auto load = [&](const CUtensorMap* m, int dcol, int row) {
-        const uint32_t s = it % stages, r = it / stages;
-        if (ok) ok = mbar_wait(bar(bl.empty + s), (r & 1) ^ 1, status);
-        if (ok) {
-          mbar_expect_tx(bar(bl.full + s), kChunkBytes);
-          tma_load_4d(ring_sm + s * kChunkBytes, m, bar(bl.full + s), dcol, row, kvh, b);
-          ++it;
+      int my_it = -1, my_c0 = 0, my_c1 = 0;
+      const CUtensorMap* my_m = nullptr;
+      auto flush = [&]() {
+        if (my_it >= 0 && ok) {
+          const uint32_t s = static_cast<uint32_t>(my_it) % stages, r = static_cast<uint32_t>(my_it) / stages;
+          ok = mbar_wait(bar(bl.empty + s), (r & 1) ^ 1, status);
+          if (ok) {
+            mbar_expect_tx(bar(bl.full + s), kChunkBytes);
+            tma_load_4d(ring_sm + s * kChunkBytes, my_m, bar(bl.full + s), my_c0, my_c1, kvh, b);
+          }
         }
+        my_it = -1;
+        ok = __all_sync(gmask, ok);
+      };
+      auto load = [&](const CUtensorMap* m, int dcol, int row) {
+        if (static_cast<int>(it % G) == lane) {
+          my_it = static_cast<int>(it);
+          my_m = m;
+          my_c0 = dcol;
+          my_c1 = row;
+        }
+        ++it;
+        if (it % G == 0) flush();
       };
       for (int pass = 0; pass < passes && ok; ++pass) {
         const int oc0 = pass * kMaxOChunksPerPass;
@@ -192,17 +214,27 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int c = 0; c < oc_n; ++c) load(&map_v, (own0 + oc0 + c) * kChunk, (j - 1) * kTileRows);
         }
       }
+      flush();
+      __syncwarp(gmask);
       // Drain: every load this CTA issued has landed before the CTA can exit.
-      for (uint32_t u = (it > (uint32_t)stages ? it - stages : 0); u < it; ++u)
-        mbar_wait(bar(bl.full + u % stages), (u / stages) & 1, status);
-      mbar_wait(bar(bl.q_full), 0, status);
+      if (lane == 0) {
+        for (uint32_t u = (it > (uint32_t)stages ? it - stages : 0); u < it; ++u)
+          mbar_wait(bar(bl.full + u % stages), (u / stages) & 1, status);
+        mbar_wait(bar(bl.q_full), 0, status);
+      }
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
+    // Descriptors are formed once and advanced by constants: building them per
+    // MMA made the issuing thread, not the tensor pipe, the bottleneck.
     if (lane == 0) {
       const uint32_t idesc_s = idesc_f16(BF16, 128, 64, false, false);     // half a key tile
       const uint32_t idesc_s128 = idesc_f16(BF16, 128, 128, false, false);  // a whole key tile
-      const uint32_t idesc_pv = idesc_f16(BF16, 128, 64, false, true);
+      const uint32_t idesc_pv = idesc_f16(BF16, 128, 64, false, true);      // one V chunk
+      const uint32_t idesc_pv2 = idesc_f16(BF16, 128, 128, false, true);    // two V chunks in adjacent slots
+      const uint64_t dq = sdesc_sw128(q_sm, 16, 1024);                      // Q chunks, K-major
+      const uint64_t dk = sdesc_sw128(ring_sm, 16, 1024);                   // ring slots as K-major operands
+      const uint64_t dv = sdesc_sw128(ring_sm, kChunkBytes, 1024);          // ring slots as MN-major operands
       bool ok = mbar_wait(bar(bl.q_full), 0, status);
       tc_fence_after();
       uint32_t it = 0;
@@ -236,46 +268,44 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ok = mbar_wait(bar(bl.full + s), (it / stages) & 1, status);
                 if (!ok) break;
                 tc_fence_after();
-                const uint32_t a0 = q_sm + c * kChunkBytes, b0 = ring_sm + s * kChunkBytes;
+                const uint64_t a = sdesc_advance(dq, c * kChunkBytes), bd = sdesc_advance(dk, s * kChunkBytes);
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk)
-                  umma_ss(s_tm, sdesc_sw128(a0 + kk * 32, 16, 1024), sdesc_sw128(b0 + kk * 32, 16, 1024),
-                          idesc_s128, (c | kk) != 0);
+                  umma_ss(s_tm, sdesc_advance(a, kk * 32), sdesc_advance(bd, kk * 32), idesc_s128, (c | kk) != 0);
                 umma_commit(bar(bl.empty + s));
                 ++it;
               }
               if (!ok) break;
               umma_commit(bar(bl.s_full + (t & 1)));
             } else {
-            const uint32_t it0 = it;
-            for (int c = 0; c < s_n && ok; ++c) {
-              const uint32_t s = it % stages;
-              ok = mbar_wait(bar(bl.full + s), (it / stages) & 1, status);
-              if (!ok) break;
-              tc_fence_after();
-              const uint32_t a0 = q_sm + c * kChunkBytes, b0 = ring_sm + s * kChunkBytes + 64 * 128;
+              const uint32_t it0 = it;
+              for (int c = 0; c < s_n && ok; ++c) {
+                const uint32_t s = it % stages;
+                ok = mbar_wait(bar(bl.full + s), (it / stages) & 1, status);
+                if (!ok) break;
+                tc_fence_after();
+                const uint64_t a = sdesc_advance(dq, c * kChunkBytes);
+                const uint64_t bd = sdesc_advance(dk, s * kChunkBytes + 64 * 128);
 #pragma unroll
-              for (int kk = 0; kk < 4; ++kk)
-                umma_ss(s_tm + 64, sdesc_sw128(a0 + kk * 32, 16, 1024), sdesc_sw128(b0 + kk * 32, 16, 1024), idesc_s,
-                        (c | kk) != 0);
-              ++it;
-            }
-            if (!ok) break;
-            if (j >= 2) {
-              ok = mbar_wait(bar(bl.o_ready), (t - 2) & 1, status);  // P_{t-2} V done
+                for (int kk = 0; kk < 4; ++kk)
+                  umma_ss(s_tm + 64, sdesc_advance(a, kk * 32), sdesc_advance(bd, kk * 32), idesc_s, (c | kk) != 0);
+                ++it;
+              }
               if (!ok) break;
-              tc_fence_after();
-            }
-            for (int c = 0; c < s_n; ++c) {
-              const uint32_t s = (it0 + c) % stages;
-              const uint32_t a0 = q_sm + c * kChunkBytes, b0 = ring_sm + s * kChunkBytes;
+              if (j >= 2) {
+                ok = mbar_wait(bar(bl.o_ready), (t - 2) & 1, status);  // P_{t-2} V done
+                if (!ok) break;
+                tc_fence_after();
+              }
+              for (int c = 0; c < s_n; ++c) {
+                const uint32_t s = (it0 + c) % stages;
+                const uint64_t a = sdesc_advance(dq, c * kChunkBytes), bd = sdesc_advance(dk, s * kChunkBytes);
 #pragma unroll
-              for (int kk = 0; kk < 4; ++kk)
-                umma_ss(s_tm, sdesc_sw128(a0 + kk * 32, 16, 1024), sdesc_sw128(b0 + kk * 32, 16, 1024), idesc_s,
-                        (c | kk) != 0);
-              umma_commit(bar(bl.empty + s));
-            }
-            umma_commit(bar(bl.s_full + (t & 1)));
+                for (int kk = 0; kk < 4; ++kk)
+                  umma_ss(s_tm, sdesc_advance(a, kk * 32), sdesc_advance(bd, kk * 32), idesc_s, (c | kk) != 0);
+                umma_commit(bar(bl.empty + s));
+              }
+              umma_commit(bar(bl.s_full + (t & 1)));
             }
           }
           if (j >= 1 && ok) {
@@ -284,18 +314,32 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!ok) break;
             tc_fence_after();
             const uint32_t p_tm = tbase + ((t & 1) ? kS1 : kS0);
-            for (int c = 0; c < oc_n && ok; ++c) {
+            // O[:, c..] += P V[:, c..]: two chunks per MMA (N=128) when they sit in adjacent ring slots
+            for (int c = 0; c < oc_n && ok;) {
               const uint32_t s = it % stages;
+              const bool two = (c + 1 < oc_n) && (s + 1 < static_cast<uint32_t>(stages));
               ok = mbar_wait(bar(bl.full + s), (it / stages) & 1, status);
+              if (ok && two) ok = mbar_wait(bar(bl.full + s + 1), ((it + 1) / stages) & 1, status);
               if (!ok) break;
               tc_fence_after();
-              const uint32_t b0 = ring_sm + s * kChunkBytes;
+              const uint64_t bd = sdesc_advance(dv, s * kChunkBytes);
+              const uint32_t acc0 = (j - 1 > 0) ? 1u : 0u;
+              if (two) {
 #pragma unroll
-              for (int kk = 0; kk < 8; ++kk)
-                umma_ts(tbase + c * kChunk, p_tm + kk * 8, sdesc_sw128(b0 + kk * 2048, 16384, 1024), idesc_pv,
-                        (j - 1 > 0 || kk > 0));
-              umma_commit(bar(bl.empty + s));
-              ++it;
+                for (int kk = 0; kk < 8; ++kk)
+                  umma_ts(tbase + c * kChunk, p_tm + kk * 8, sdesc_advance(bd, kk * 2048), idesc_pv2, acc0 | (kk > 0));
+                umma_commit(bar(bl.empty + s));
+                umma_commit(bar(bl.empty + s + 1));
+                it += 2;
+                c += 2;
+              } else {
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk)
+                  umma_ts(tbase + c * kChunk, p_tm + kk * 8, sdesc_advance(bd, kk * 2048), idesc_pv, acc0 | (kk > 0));
+                umma_commit(bar(bl.empty + s));
+                it += 1;
+                c += 1;
+              }
             }
             umma_commit(bar(bl.o_ready));
           }

@@ -159,6 +159,10 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, ui
   return d;
 }
 
+// Descriptor of the operand `bytes` further on in shared memory (the start
+// address field is the low 14 bits; tiles stay below 256 KB, so no carry).
+__device__ __forceinline__ uint64_t sdesc_advance(uint64_t desc, uint32_t bytes) { return desc + (bytes >> 4); }
+
 // Instruction descriptor for kind::f16 with an fp32 accumulator:
 // D fmt [4,6)=1 (f32), A fmt [7,10), B fmt [10,13) (0 f16, 1 bf16),
 // A major bit 15, B major bit 16 (1 = MN-major), N>>3 at [17,23), M>>4 at [24,29).
