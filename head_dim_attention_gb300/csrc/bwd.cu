@@ -318,8 +318,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       flush();
       __syncwarp(gmask);
       if (lane == 0) {
-        for (uint32_t u = (it > (uint32_t)stages ? it - stages : 0); u < it; ++u)
-          mbar_wait(bar(bl.full + u % stages), (u / stages) & 1, status);
+        // Wait for the last release of every ring slot: the MMA warp's commit
+        // arrives on empty[s] only when the MMAs reading the slot are done, and
+        // commit arrivals are not ordered with respect to one another, so one
+        // still in flight at exit would land in the next CTA's shared memory.
+        for (uint32_t s = 0; s < static_cast<uint32_t>(stages) && s < it; ++s)
+          mbar_wait(bar(bl.empty + s), ((it - 1 - s) / stages) & 1, status);
         if (n_res > 0) mbar_wait(bar(bl.a_full), 0, status);
       }
     }
@@ -497,6 +501,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int t = t0 + c;
         int ch, cr0;
         column<MODE>(g, p, c, &ch, &cr0);
+        // Column statistics (dV, dK): lane l of every warp loads lse2 and Delta
+        // of column rows cr0 + l + 32 c4; each thread then takes the values it
+        // needs with warp shuffles instead of one dependent global load per
+        // score.  The loads are issued before the wait so their latency hides.
+        float l2v[4] = {0.f, 0.f, 0.f, 0.f}, dlv[4] = {0.f, 0.f, 0.f, 0.f};
+        if (MODE != kDQ) {
+          const int64_t sbase = (static_cast<int64_t>(g.b) * p.Hq + ch) * p.Nq;
+#pragma unroll
+          for (int c4 = 0; c4 < 4; ++c4) {
+            const int64_t i = sbase + min(cr0 + c4 * 32 + lane, p.Nq - 1);
+            l2v[c4] = p.lse2[i];
+            if (two) dlv[c4] = p.delta[i];
+          }
+        }
         ok = __all_sync(0xffffffffu, mbar_wait(bar(bl.x_full), t & 1, status));
         if (!ok) break;
         tc_fence_after();
@@ -523,7 +541,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               i = cr0 + ci;
               j = srow;
               ic = min(i, p.Nq - 1);
-              l2 = __ldg(p.lse2 + (static_cast<int64_t>(g.b) * p.Hq + ch) * p.Nq + ic);
+              l2 = __shfl_sync(0xffffffffu, l2v[c4], e);
             }
             const int hq = (MODE == kDQ) ? g.h : ch;
             const bool valid = i < p.Nq && j < p.Nkv && !(p.causal && j > i) && l2 > -INFINITY;
@@ -549,12 +567,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int e = 0; e < 32; ++e) {
               const int ci = c4 * 32 + e;
               float dl;
-              if (MODE == kDQ) {
+              if (MODE == kDQ)
                 dl = delta_row;
-              } else {
-                const int ic = min(cr0 + ci, p.Nq - 1);
-                dl = __ldg(p.delta + (static_cast<int64_t>(g.b) * p.Hq + ch) * p.Nq + ic);
-              }
+              else
+                dl = __shfl_sync(0xffffffffu, dlv[c4], e);
               pv[ci] = pv[ci] * (f[e] - dl);
             }
           }

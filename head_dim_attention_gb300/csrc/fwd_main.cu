@@ -218,8 +218,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp(gmask);
       // Drain: every load this CTA issued has landed before the CTA can exit.
       if (lane == 0) {
-        for (uint32_t u = (it > (uint32_t)stages ? it - stages : 0); u < it; ++u)
-          mbar_wait(bar(bl.full + u % stages), (u / stages) & 1, status);
+        // Wait for the last release of every ring slot: the MMA warp's commit
+        // arrives on empty[s] only when the MMAs reading the slot are done, and
+        // commit arrivals are not ordered with respect to one another, so one
+        // still in flight at exit would land in the next CTA's shared memory.
+        for (uint32_t s = 0; s < static_cast<uint32_t>(stages) && s < it; ++s)
+          mbar_wait(bar(bl.empty + s), ((it - 1 - s) / stages) & 1, status);
         mbar_wait(bar(bl.q_full), 0, status);
       }
     }
