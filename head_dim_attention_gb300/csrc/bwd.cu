@@ -523,6 +523,27 @@ __global__ void __launch_bounds__(kThreads, 1)
           send(kX1);
           if (!ok) break;
         }
+        // A tile with no masked score and no bias (every tile but the diagonal
+        // and the ragged edges) skips the per-score checks.
+        bool plain;
+        if (MODE == kDQ)
+          plain = srow < p.Nq && cr0 + kTileRows <= p.Nkv && (!p.causal || cr0 + kTileRows - 1 <= srow) &&
+                  lse2_row > -INFINITY;
+        else
+          plain = srow < p.Nkv && cr0 + kTileRows <= p.Nq && (!p.causal || srow <= cr0);
+        plain = __all_sync(0xffffffffu, plain) && p.bias == nullptr;
+        if (plain) {
+#pragma unroll
+          for (int c4 = 0; c4 < 4; ++c4) {
+            float f[32];
+            chunk(kX1, c4, f);
+#pragma unroll
+            for (int e = 0; e < 32; ++e) {
+              const float l2 = (MODE == kDQ) ? lse2_row : __shfl_sync(0xffffffffu, l2v[c4], e);
+              pv[c4 * 32 + e] = ex2(fmaf(f[e], p.scale_log2, -l2));
+            }
+          }
+        } else {
 #pragma unroll
         for (int c4 = 0; c4 < 4; ++c4) {
           float f[32];
@@ -552,6 +573,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         kLog2e, xv);
             pv[ci] = valid ? ex2(xv) : 0.f;
           }
+        }
         }
         if constexpr (XCH) release();
         if (two) {
