@@ -182,6 +182,7 @@ def run_ffpa(args, rank, world):
 
     from head_dim_attention_gb300 import ffpa_bwd, ffpa_check_status, ffpa_fwd, load
     from head_dim_attention_gb300._lib import ffpa_set_timing_events
+    from head_dim_attention_gb300.shard import max_over_ranks
     from head_dim_attention_gb300.synth import make_inputs
 
     local = int(os.environ.get("LOCAL_RANK", "0"))
@@ -236,10 +237,7 @@ def run_ffpa(args, rank, world):
     spans = [(0, 1), (2, 3), (3, 4), (4, 5), (5, 6)]
     kern_ms = {n: statistics.mean(evs[i][a].elapsed_time(evs[i][b]) for i in range(K))
                for n, (a, b) in zip(names, spans)}
-    if world > 1:
-        tm = torch.tensor([ms], device=dev, dtype=torch.float64)
-        dist.all_reduce(tm, op=dist.ReduceOp.MAX)
-        ms = float(tm.item())
+    ms = max_over_ranks(ms, dev)  # the slowest rank sets the job's time
     step_flop = FWD_FLOP + BWD_FLOP
     value = world * step_flop * K / (ms / 1e3) / 1e12
 
@@ -286,6 +284,8 @@ TRAFFIC: dict = {}
 
 
 def measure_e2e(step, inp, dev_in, dev_out, world, dev, steps=3):
+    from head_dim_attention_gb300.shard import max_over_ranks
+
     """The same step through the public API with pinned host buffers: H2D of the
     inputs and D2H of the gradients inside the timed region."""
     import torch
@@ -311,11 +311,7 @@ def measure_e2e(step, inp, dev_in, dev_out, world, dev, steps=3):
         one()
     e1.record()
     torch.cuda.synchronize()
-    ms = e0.elapsed_time(e1) / steps
-    if world > 1:
-        tm = torch.tensor([ms], device=dev, dtype=torch.float64)
-        dist.all_reduce(tm, op=dist.ReduceOp.MAX)
-        ms = float(tm.item())
+    ms = max_over_ranks(e0.elapsed_time(e1) / steps, dev)
     return {"value": world * (FWD_FLOP + BWD_FLOP) / (ms / 1e3) / 1e12, "unit": "TFLOPS",
             "h2d_bytes_per_step": sum(t.numel() * t.element_size() for t in hosts),
             "d2h_bytes_per_step": sum(t.numel() * t.element_size() for t in outs),
