@@ -143,6 +143,7 @@ struct Geo {
   int s_limit;        // rows of the stationary tensor (Nkv for dV/dK, Nq for dQ)
   int qt_begin, nq_h; // dV/dK: first query tile and query tiles per head
   int ncols;          // column tiles
+  int rot;            // column sweep starts here (stationary tiles start at different columns)
 };
 
 template <int MODE>
@@ -160,6 +161,7 @@ __device__ __forceinline__ Geo make_geo(const BwdParams& p, int cs) {
     g.ncols = (kv_end + kTileRows - 1) / kTileRows;
     g.qt_begin = 0;
     g.nq_h = 0;
+    g.rot = g.ncols > 0 ? qt % g.ncols : 0;
   } else {
     const int kvt = static_cast<int>(blockIdx.x) / cs;
     g.kvh = blockIdx.y;
@@ -170,6 +172,7 @@ __device__ __forceinline__ Geo make_geo(const BwdParams& p, int cs) {
     g.qt_begin = p.causal ? kvt : 0;  // top-left causal: query rows i >= key row j
     g.nq_h = max(0, p.q_tiles - g.qt_begin);
     g.ncols = p.group * g.nq_h;
+    g.rot = g.ncols > 0 ? kvt % g.ncols : 0;
   }
   return g;
 }
@@ -177,6 +180,11 @@ __device__ __forceinline__ Geo make_geo(const BwdParams& p, int cs) {
 // Column tile c -> (head, first row) in the column tensor.
 template <int MODE>
 __device__ __forceinline__ void column(const Geo& g, const BwdParams& p, int c, int* head, int* row0) {
+  // Concurrent CTAs of a head would otherwise stream the same column tiles at
+  // the same time; starting each sweep at a different tile spreads the reads.
+  // The gradient is a sum over columns, so the order does not change it.
+  c += g.rot;
+  if (c >= g.ncols) c -= g.ncols;
   if (MODE == kDQ) {
     *head = g.kvh;
     *row0 = c * kTileRows;
