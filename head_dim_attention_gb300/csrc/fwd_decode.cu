@@ -201,6 +201,199 @@ __global__ void __launch_bounds__(kDecThreads) decode_split_kernel(const __grid_
   }
 }
 
+// Streaming variant for Nq <= 2 (the decode case proper).  Each warp takes a
+// contiguous eighth of the slice's keys and streams K and V rows together,
+// U keys at a time (every lane holds G 16-byte groups of each row in flight),
+// keeping an online softmax (running max m, sum l and unnormalised O) in
+// registers; lane i owns elements 8(i + 32 k) .. +7 of D.  The eight warps
+// then merge their (m, l, O) through shared memory into the slice's partial,
+// which the combine kernel reads exactly as it reads the general kernel's.
+template <int R, int G, int U, bool BF16>
+__global__ void __launch_bounds__(kDecThreads) decode_stream_kernel(const __grid_constant__ DecodeParams p) {
+  extern __shared__ __align__(16) float wsm[];  // [8 warps][R][D] partial O, then [8][R] m and l
+  const int split = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+  const int g = h / p.group;
+  const int D = p.D, Nq = p.Nq, L = p.split_len;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int groups = D / 8;
+  const int kv_begin = split * L;
+  const int kv_len = min(L, p.Nkv - kv_begin);
+  const int per_warp = (L + 7) / 8;
+  const int j_begin = warp * per_warp;
+  const int j_end = min(kv_len, j_begin + per_warp);
+  typedef typename std::conditional<BF16, __nv_bfloat16, __half>::type T;
+  constexpr float kLog2e = 1.4426950408889634f;
+
+  float qf[R][G][8];
+#pragma unroll
+  for (int r = 0; r < R; ++r)
+#pragma unroll
+    for (int k = 0; k < G; ++k) {
+      const int c = lane + 32 * k;
+      if (r < Nq && c < groups)
+        Vec8<BF16>::load(reinterpret_cast<const T*>(p.q) + b * p.q_sb + h * p.q_sh + static_cast<int64_t>(r) * p.q_sn +
+                             c * 8,
+                         qf[r][k]);
+      else
+#pragma unroll
+        for (int e = 0; e < 8; ++e) qf[r][k][e] = 0.f;
+    }
+  float m[R], l[R], o[R][G][8];
+#pragma unroll
+  for (int r = 0; r < R; ++r) {
+    m[r] = -INFINITY;
+    l[r] = 0.f;
+#pragma unroll
+    for (int k = 0; k < G; ++k)
+#pragma unroll
+      for (int e = 0; e < 8; ++e) o[r][k][e] = 0.f;
+  }
+  const T* kbase = reinterpret_cast<const T*>(p.k) + b * p.k_sb + g * p.k_sh;
+  const T* vbase = reinterpret_cast<const T*>(p.v) + b * p.v_sb + g * p.v_sh;
+  for (int j0 = j_begin; j0 < j_end; j0 += U) {
+    // issue every load of the U keys (K and V rows) before using any of them
+    uint4 kr[U][G], vr[U][G];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int64_t row = kv_begin + min(j0 + u, j_end - 1);
+#pragma unroll
+      for (int k = 0; k < G; ++k) {
+        const int c = min(lane + 32 * k, groups - 1);
+        kr[u][k] = __ldg(reinterpret_cast<const uint4*>(kbase + row * p.k_sn + c * 8));
+        vr[u][k] = __ldg(reinterpret_cast<const uint4*>(vbase + row * p.v_sn + c * 8));
+      }
+    }
+    float s[U][R];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+#pragma unroll
+      for (int r = 0; r < R; ++r) s[u][r] = 0.f;
+#pragma unroll
+      for (int k = 0; k < G; ++k) {
+        if (lane + 32 * k < groups) {
+          float kf[8];
+          const uint32_t w[4] = {kr[u][k].x, kr[u][k].y, kr[u][k].z, kr[u][k].w};
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            float2 x;
+            if constexpr (BF16)
+              x = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[i]));
+            else
+              x = __half22float2(*reinterpret_cast<const __half2*>(&w[i]));
+            kf[2 * i] = x.x;
+            kf[2 * i + 1] = x.y;
+          }
+#pragma unroll
+          for (int r = 0; r < R; ++r)
+#pragma unroll
+            for (int e = 0; e < 8; ++e) s[u][r] = fmaf(qf[r][k][e], kf[e], s[u][r]);
+        }
+      }
+#pragma unroll
+      for (int r = 0; r < R; ++r) {
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) s[u][r] += __shfl_xor_sync(0xffffffffu, s[u][r], off);
+        const int kv = kv_begin + j0 + u;
+        float x = s[u][r] * p.scale_log2;
+        if (p.bias)
+          x = fmaf(__ldg(p.bias + b * p.bias_sb + h * p.bias_sh + static_cast<int64_t>(r) * p.bias_sq +
+                         static_cast<int64_t>(min(kv, p.Nkv - 1)) * p.bias_sk),
+                   kLog2e, x);
+        const bool valid = (j0 + u < j_end) && r < Nq && !(p.causal && kv > r);
+        s[u][r] = valid ? x : -INFINITY;
+      }
+    }
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+      float mx = m[r];
+#pragma unroll
+      for (int u = 0; u < U; ++u) mx = fmaxf(mx, s[u][r]);
+      if (mx == -INFINITY) continue;  // nothing visible yet for this row
+      const float alpha = ex2(m[r] - mx);  // m[r] = -inf gives 0
+      float pj[U];
+      float ps = 0.f;
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        pj[u] = ex2(s[u][r] - mx);
+        ps += pj[u];
+      }
+      l[r] = l[r] * alpha + ps;
+      m[r] = mx;
+#pragma unroll
+      for (int k = 0; k < G; ++k) {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) o[r][k][e] *= alpha;
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+          const uint32_t w[4] = {vr[u][k].x, vr[u][k].y, vr[u][k].z, vr[u][k].w};
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            float2 x;
+            if constexpr (BF16)
+              x = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[i]));
+            else
+              x = __half22float2(*reinterpret_cast<const __half2*>(&w[i]));
+            o[r][k][2 * i] = fmaf(pj[u], x.x, o[r][k][2 * i]);
+            o[r][k][2 * i + 1] = fmaf(pj[u], x.y, o[r][k][2 * i + 1]);
+          }
+        }
+      }
+    }
+  }
+  // merge the eight warps
+  float* so = wsm;                  // [8][R][D]
+  float* sm = wsm + 8 * R * D;      // [8][R]
+  float* sl = sm + 8 * R;           // [8][R]
+#pragma unroll
+  for (int r = 0; r < R; ++r) {
+#pragma unroll
+    for (int k = 0; k < G; ++k) {
+      const int c = lane + 32 * k;
+      if (c < groups) {
+        float4* dst = reinterpret_cast<float4*>(so + (warp * R + r) * D + c * 8);
+        dst[0] = make_float4(o[r][k][0], o[r][k][1], o[r][k][2], o[r][k][3]);
+        dst[1] = make_float4(o[r][k][4], o[r][k][5], o[r][k][6], o[r][k][7]);
+      }
+    }
+    if (lane == 0) {
+      sm[warp * R + r] = m[r];
+      sl[warp * R + r] = l[r];
+    }
+  }
+  __syncthreads();
+  for (int r = 0; r < Nq; ++r) {
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < 8; ++w) M = fmaxf(M, sm[w * R + r]);
+    const float Mref = (M == -INFINITY) ? 0.f : M;
+    float wgt[8];
+    float Ls = 0.f;
+#pragma unroll
+    for (int w = 0; w < 8; ++w) {
+      wgt[w] = ex2(sm[w * R + r] - Mref);  // -inf (empty warp) gives 0
+      Ls += wgt[w] * sl[w * R + r];
+    }
+    float* dst = p.part_o + ((((static_cast<int64_t>(b) * p.Hq + h) * Nq + r) * p.n_splits + split) * D);
+    for (int d = threadIdx.x * 4; d < D; d += kDecThreads * 4) {
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int w = 0; w < 8; ++w) {
+        const float4 v = *reinterpret_cast<const float4*>(so + (w * R + r) * D + d);
+        acc.x = fmaf(wgt[w], v.x, acc.x);
+        acc.y = fmaf(wgt[w], v.y, acc.y);
+        acc.z = fmaf(wgt[w], v.z, acc.z);
+        acc.w = fmaf(wgt[w], v.w, acc.w);
+      }
+      *reinterpret_cast<float4*>(dst + d) = acc;
+    }
+    if (threadIdx.x == 0) {
+      float* ml = p.part_ml + (((static_cast<int64_t>(b) * p.Hq + h) * Nq + r) * p.n_splits + split) * 2;
+      ml[0] = M;
+      ml[1] = Ls;
+    }
+  }
+}
+
 // One CTA per (row, query head, batch): merge the slices.
 template <bool BF16>
 __global__ void __launch_bounds__(128) decode_combine_kernel(const __grid_constant__ DecodeParams p) {
@@ -240,14 +433,32 @@ __global__ void __launch_bounds__(128) decode_combine_kernel(const __grid_consta
   }
 }
 
-template <bool BF16>
-cudaError_t launch_decode_impl(const DecodeParams& p, cudaStream_t st) {
-  const size_t smem = (static_cast<size_t>(p.Nq) * p.D + static_cast<size_t>(p.Nq) * p.split_len + 2 * p.Nq) * 4;
-  auto k1 = decode_split_kernel<BF16>;
+template <int R, int G, int U, bool BF16>
+cudaError_t launch_stream(const DecodeParams& p, cudaStream_t st) {
+  const size_t smem = (static_cast<size_t>(8) * R * p.D + 16 * R) * 4;
+  auto k1 = decode_stream_kernel<R, G, U, BF16>;
   cudaError_t e = cudaFuncSetAttribute(k1, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return e;
-  timing_mark(st);
   k1<<<dim3(p.n_splits, p.Hq, p.B), kDecThreads, smem, st>>>(p);
+  return cudaSuccess;
+}
+
+template <bool BF16>
+cudaError_t launch_decode_impl(const DecodeParams& p, cudaStream_t st) {
+  cudaError_t e = cudaSuccess;
+  timing_mark(st);
+  if (p.Nq <= 2 && p.D <= 512) {
+    e = p.Nq == 1 ? launch_stream<1, 2, 4, BF16>(p, st) : launch_stream<2, 2, 4, BF16>(p, st);
+  } else if (p.Nq <= 2) {
+    e = p.Nq == 1 ? launch_stream<1, 4, 2, BF16>(p, st) : launch_stream<2, 4, 2, BF16>(p, st);
+  } else {
+    const size_t smem = (static_cast<size_t>(p.Nq) * p.D + static_cast<size_t>(p.Nq) * p.split_len + 2 * p.Nq) * 4;
+    auto k1 = decode_split_kernel<BF16>;
+    e = cudaFuncSetAttribute(k1, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    k1<<<dim3(p.n_splits, p.Hq, p.B), kDecThreads, smem, st>>>(p);
+  }
+  if (e != cudaSuccess) return e;
   timing_mark(st);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
