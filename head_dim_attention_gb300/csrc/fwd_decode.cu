@@ -394,40 +394,82 @@ __global__ void __launch_bounds__(kDecThreads) decode_stream_kernel(const __grid
   }
 }
 
-// One CTA per (row, query head, batch): merge the slices.
+// Merge the slices.  One CTA per (row, 128-column chunk of D, query head,
+// batch): the block reduces the slices' (m, l) to M and L, then warp w sums
+// slices w, w+8, ... for its lane's four columns (all its loads in flight) and
+// the eight warps' sums are added through shared memory.
+constexpr int kCombThreads = 256;
+
+__device__ __forceinline__ float block_reduce(float v, bool is_max, float* red) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float w = __shfl_xor_sync(0xffffffffu, v, o);
+    v = is_max ? fmaxf(v, w) : v + w;
+  }
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  __syncthreads();  // red may still be read by a previous reduction
+  if (lane == 0) red[warp] = v;
+  __syncthreads();
+  v = red[0];
+#pragma unroll
+  for (int w = 1; w < kCombThreads / 32; ++w) v = is_max ? fmaxf(v, red[w]) : v + red[w];
+  return v;
+}
+
 template <bool BF16>
-__global__ void __launch_bounds__(128) decode_combine_kernel(const __grid_constant__ DecodeParams p) {
-  const int r = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+__global__ void __launch_bounds__(kCombThreads) decode_combine_kernel(const __grid_constant__ DecodeParams p) {
+  __shared__ float red[kCombThreads / 32];
+  __shared__ float4 part[kCombThreads / 32][32];
   const int S = p.n_splits, D = p.D;
+  const int nd = (D + 127) / 128;
+  const int chunk = blockIdx.x % nd, r = blockIdx.x / nd, h = blockIdx.y, b = blockIdx.z;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t base = ((static_cast<int64_t>(b) * p.Hq + h) * p.Nq + r) * S;
   const float* ml = p.part_ml + base * 2;
-  float M = -INFINITY;
-  for (int s = 0; s < S; ++s) M = fmaxf(M, ml[2 * s]);
+  float m = -INFINITY;
+  for (int s = threadIdx.x; s < S; s += kCombThreads) m = fmaxf(m, ml[2 * s]);
+  const float M = block_reduce(m, true, red);
   const float Mref = (M == -INFINITY) ? 0.f : M;
-  float Lsum = 0.f;
-  for (int s = 0; s < S; ++s) Lsum += exp2f(ml[2 * s] - Mref) * ml[2 * s + 1];
-  const float inv = Lsum > 0.f ? 1.f / Lsum : 0.f;
-  typedef typename std::conditional<BF16, __nv_bfloat16, __half>::type T;
-  T* orow = reinterpret_cast<T*>(p.out) + b * p.o_sb + h * p.o_sh + static_cast<int64_t>(r) * p.o_sn;
-  for (int d = threadIdx.x * 4; d < D; d += blockDim.x * 4) {
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int s = 0; s < S; ++s) {
+  float ls = 0.f;
+  for (int s = threadIdx.x; s < S; s += kCombThreads) ls += exp2f(ml[2 * s] - Mref) * ml[2 * s + 1];
+  const float Lsum = block_reduce(ls, false, red);
+  const int q4 = chunk * 32 + lane;  // this lane's float4 column
+  const bool col = q4 * 4 < D;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (col) {
+#pragma unroll 4
+    for (int s = warp; s < S; s += kCombThreads / 32) {
       const float w = exp2f(ml[2 * s] - Mref);
-      const float4 o = *reinterpret_cast<const float4*>(p.part_o + (base + s) * D + d);
+      const float4 o = *reinterpret_cast<const float4*>(p.part_o + (base + s) * D + q4 * 4);
       acc.x = fmaf(w, o.x, acc.x);
       acc.y = fmaf(w, o.y, acc.y);
       acc.z = fmaf(w, o.z, acc.z);
       acc.w = fmaf(w, o.w, acc.w);
     }
+  }
+  part[warp][lane] = acc;
+  __syncthreads();
+  if (warp == 0 && col) {
+    float4 t = part[0][lane];
+#pragma unroll
+    for (int w = 1; w < kCombThreads / 32; ++w) {
+      t.x += part[w][lane].x;
+      t.y += part[w][lane].y;
+      t.z += part[w][lane].z;
+      t.w += part[w][lane].w;
+    }
+    const float inv = Lsum > 0.f ? 1.f / Lsum : 0.f;
+    typedef typename std::conditional<BF16, __nv_bfloat16, __half>::type T;
+    T* orow = reinterpret_cast<T*>(p.out) + b * p.o_sb + h * p.o_sh + static_cast<int64_t>(r) * p.o_sn + q4 * 4;
     if constexpr (BF16) {
-      reinterpret_cast<__nv_bfloat162*>(orow + d)[0] = __floats2bfloat162_rn(acc.x * inv, acc.y * inv);
-      reinterpret_cast<__nv_bfloat162*>(orow + d)[1] = __floats2bfloat162_rn(acc.z * inv, acc.w * inv);
+      reinterpret_cast<__nv_bfloat162*>(orow)[0] = __floats2bfloat162_rn(t.x * inv, t.y * inv);
+      reinterpret_cast<__nv_bfloat162*>(orow)[1] = __floats2bfloat162_rn(t.z * inv, t.w * inv);
     } else {
-      reinterpret_cast<__half2*>(orow + d)[0] = __floats2half2_rn(acc.x * inv, acc.y * inv);
-      reinterpret_cast<__half2*>(orow + d)[1] = __floats2half2_rn(acc.z * inv, acc.w * inv);
+      reinterpret_cast<__half2*>(orow)[0] = __floats2half2_rn(t.x * inv, t.y * inv);
+      reinterpret_cast<__half2*>(orow)[1] = __floats2half2_rn(t.z * inv, t.w * inv);
     }
   }
-  if (threadIdx.x == 0 && p.lse) {
+  if (chunk == 0 && threadIdx.x == 0 && p.lse) {
     constexpr float kLn2 = 0.6931471805599453f;
     p.lse[(static_cast<int64_t>(b) * p.Hq + h) * p.Nq + r] = Lsum > 0.f ? (M + __log2f(Lsum)) * kLn2 : -INFINITY;
   }
@@ -462,7 +504,7 @@ cudaError_t launch_decode_impl(const DecodeParams& p, cudaStream_t st) {
   timing_mark(st);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  decode_combine_kernel<BF16><<<dim3(p.Nq, p.Hq, p.B), 128, 0, st>>>(p);
+  decode_combine_kernel<BF16><<<dim3(p.Nq * ((p.D + 127) / 128), p.Hq, p.B), kCombThreads, 0, st>>>(p);
   timing_mark(st);
   return cudaGetLastError();
 }
