@@ -31,9 +31,17 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
+def attention_flops(nq: int, nkv: int, d: int, bh: int, causal: bool = False, backward: bool = False) -> float:
+    """FLOP counted for one attention pass, the FFPA Attention Benchmark page's rule
+    ("More Benchmark"): forward 2 GEMMs = 4 Nq Nkv D per (batch, query head),
+    backward the standard 5 GEMMs = 10 Nq Nkv D; both halved when causal."""
+    f = (10 if backward else 4) * nq * nkv * d * bh
+    return f / 2 if causal else f
+
+
 B, H, N, D = 1, 8, 8192, 512
-FWD_FLOP = 4 * B * H * N * N * D
-BWD_FLOP = 10 * B * H * N * N * D
+FWD_FLOP = attention_flops(N, N, D, B * H)
+BWD_FLOP = attention_flops(N, N, D, B * H, backward=True)
 METRIC = "attention TFLOPS fwd/bwd at N=8192 D=512 bf16, % of GB300 dense peak"
 WORKLOAD = "self-attention forward+backward, B=1, Hq=Hkv=8, Nq=Nkv=8192, D=512, bf16, non-causal"
 CPU_ROWS = 1024      # cpu_baseline probe: query rows of one head against all keys
