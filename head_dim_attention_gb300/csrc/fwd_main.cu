@@ -26,12 +26,13 @@
 // When a CTA owns more than 4 chunks (D > 512) it sweeps the keys once per
 // 4-chunk slice of its O columns ("passes"), recomputing S each time.
 //
-// Pair without exchange (320 <= D <= 512).  The exchange moves 64 KB per key
+// Split without exchange (320 <= D <= 640).  The exchange moves 64 KB per key
 // tile and CTA through distributed shared memory, whose bandwidth is far
-// below the tensor pipe's.  For D <= 512 the two CTAs of a query tile instead
-// each reduce S over the whole of D (Q fully resident, every K chunk
-// streamed) and own half of O: 1.5x the MMA work of the exchange, no cluster
-// and no DSMEM traffic, leaving shared-memory bandwidth as the bound.
+// below the tensor pipe's.  So for D <= 512 two CTAs per query tile, and for
+// 576 <= D <= 640 three, each reduce S over the whole of D themselves (Q fully
+// resident, every K chunk streamed) and own at most four 64-column chunks of O:
+// more MMA work than the exchange (1.5x for two CTAs), but no cluster and no
+// DSMEM traffic.
 //
 // Warp roles (256 threads): warp 0 = TMA producer, warp 1 = TMEM owner and
 // MMA issuer, warps 4-7 = softmax / correction / epilogue (one query row per
@@ -73,7 +74,10 @@ __host__ __device__ inline Bars bar_layout(int stages) {
 
 // Kernel flavours: one CTA per query tile (D <= 256), a cluster pair that
 // exchanges partial scores, or an independent pair that recomputes them.
-enum Flavour : int { kSolo = 0, kExchange = 1, kRecompute = 2 };
+enum Flavour : int { kSolo = 0, kExchange = 1, kRecompute = 2, kRecompute3 = 3 };
+
+// CTAs that share one query tile (each owns a slice of O's columns).
+__host__ __device__ constexpr int ctas_per_tile(int fl) { return fl == kSolo ? 1 : (fl == kRecompute3 ? 3 : 2); }
 
 struct SmemPlan {
   int q_chunks;  // resident Q chunks (the chunks this CTA reduces S over)
@@ -88,6 +92,14 @@ __host__ __device__ inline SmemPlan smem_plan(int n_chunks, int fl, int stages) 
   s.bar_off = s.land_off + (fl == kExchange ? kLandingBytes : 0);
   s.total = s.bar_off + 1024;  // barriers + TMEM slot
   return s;
+}
+
+template <bool BF16>
+__device__ __forceinline__ float2 unpack2(uint32_t w) {
+  if constexpr (BF16)
+    return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w));
+  else
+    return __half22float2(*reinterpret_cast<const __half2*>(&w));
 }
 
 template <bool BF16>
@@ -108,7 +120,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int stages = p.stages;
-  constexpr int CS = (FL == kSolo) ? 1 : 2;  // CTAs per query tile
+  constexpr int CS = ctas_per_tile(FL);  // CTAs per query tile
   constexpr bool XCH = (FL == kExchange);
   const SmemPlan plan = smem_plan(p.n_chunks, FL, stages);
   const Bars bl = bar_layout(stages);
@@ -232,7 +244,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     // Descriptors are formed once and advanced by constants: building them per
     // MMA made the issuing thread, not the tensor pipe, the bottleneck.
     if (lane == 0) {
-      const uint32_t idesc_s = idesc_f16(BF16, 128, 64, false, false);     // half a key tile
       const uint32_t idesc_s128 = idesc_f16(BF16, 128, 128, false, false);  // a whole key tile
       const uint32_t idesc_pv = idesc_f16(BF16, 128, 64, false, true);      // one V chunk
       const uint32_t idesc_pv2 = idesc_f16(BF16, 128, 128, false, true);    // two V chunks in adjacent slots
@@ -252,65 +263,32 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int j = 0; j <= ntiles && ok; ++j) {
           if (j < ntiles) {
-            // S_t lands in the buffer that held P_{t-2}.  tcgen05.mma does not
-            // order a later MMA's write of D after an earlier MMA's read of A
-            // from TMEM, so S_t is issued in two N=64 halves: keys 64..127
-            // (columns 64..127, disjoint from P) first, then, once P_{t-2} V
-            // has completed, keys 0..63 (the columns P_{t-2} occupied).
-            // When the ring is shallower than the tile's chunk count the halves
-            // cannot be held, so the wait comes first and S_t is issued whole.
+            // S_t lands in the buffer that held P_{t-2}, the A operand of the
+            // P_{t-2} V MMA; tcgen05.mma does not order a later MMA's write of D
+            // after an earlier MMA's read of A from TMEM, so S_t is issued once
+            // that MMA has completed.  S is issued whole (N=128): splitting it
+            // into N=64 halves to start earlier measured slower.
             const int t = t0 + j;
             const uint32_t s_tm = tbase + ((t & 1) ? kS1 : kS0);
-            if (s_n > stages) {
-              if (j >= 2) {
-                ok = mbar_wait(bar(bl.o_ready), (t - 2) & 1, status);
-                if (!ok) break;
-                tc_fence_after();
-              }
-              for (int c = 0; c < s_n && ok; ++c) {
-                const uint32_t s = it % stages;
-                ok = mbar_wait(bar(bl.full + s), (it / stages) & 1, status);
-                if (!ok) break;
-                tc_fence_after();
-                const uint64_t a = sdesc_advance(dq, c * kChunkBytes), bd = sdesc_advance(dk, s * kChunkBytes);
-#pragma unroll
-                for (int kk = 0; kk < 4; ++kk)
-                  umma_ss(s_tm, sdesc_advance(a, kk * 32), sdesc_advance(bd, kk * 32), idesc_s128, (c | kk) != 0);
-                umma_commit(bar(bl.empty + s));
-                ++it;
-              }
+            if (j >= 2) {
+              ok = mbar_wait(bar(bl.o_ready), (t - 2) & 1, status);
               if (!ok) break;
-              umma_commit(bar(bl.s_full + (t & 1)));
-            } else {
-              const uint32_t it0 = it;
-              for (int c = 0; c < s_n && ok; ++c) {
-                const uint32_t s = it % stages;
-                ok = mbar_wait(bar(bl.full + s), (it / stages) & 1, status);
-                if (!ok) break;
-                tc_fence_after();
-                const uint64_t a = sdesc_advance(dq, c * kChunkBytes);
-                const uint64_t bd = sdesc_advance(dk, s * kChunkBytes + 64 * 128);
-#pragma unroll
-                for (int kk = 0; kk < 4; ++kk)
-                  umma_ss(s_tm + 64, sdesc_advance(a, kk * 32), sdesc_advance(bd, kk * 32), idesc_s, (c | kk) != 0);
-                ++it;
-              }
-              if (!ok) break;
-              if (j >= 2) {
-                ok = mbar_wait(bar(bl.o_ready), (t - 2) & 1, status);  // P_{t-2} V done
-                if (!ok) break;
-                tc_fence_after();
-              }
-              for (int c = 0; c < s_n; ++c) {
-                const uint32_t s = (it0 + c) % stages;
-                const uint64_t a = sdesc_advance(dq, c * kChunkBytes), bd = sdesc_advance(dk, s * kChunkBytes);
-#pragma unroll
-                for (int kk = 0; kk < 4; ++kk)
-                  umma_ss(s_tm, sdesc_advance(a, kk * 32), sdesc_advance(bd, kk * 32), idesc_s, (c | kk) != 0);
-                umma_commit(bar(bl.empty + s));
-              }
-              umma_commit(bar(bl.s_full + (t & 1)));
+              tc_fence_after();
             }
+            for (int c = 0; c < s_n && ok; ++c) {
+              const uint32_t s = it % stages;
+              ok = mbar_wait(bar(bl.full + s), (it / stages) & 1, status);
+              if (!ok) break;
+              tc_fence_after();
+              const uint64_t a = sdesc_advance(dq, c * kChunkBytes), bd = sdesc_advance(dk, s * kChunkBytes);
+#pragma unroll
+              for (int kk = 0; kk < 4; ++kk)
+                umma_ss(s_tm, sdesc_advance(a, kk * 32), sdesc_advance(bd, kk * 32), idesc_s128, (c | kk) != 0);
+              umma_commit(bar(bl.empty + s));
+              ++it;
+            }
+            if (!ok) break;
+            umma_commit(bar(bl.s_full + (t & 1)));
           }
           if (j >= 1 && ok) {
             const int t = t0 + j - 1;
@@ -332,6 +310,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk)
                   umma_ts(tbase + c * kChunk, p_tm + kk * 8, sdesc_advance(bd, kk * 2048), idesc_pv2, acc0 | (kk > 0));
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk)  // the P_lo term
+                  umma_ts(tbase + c * kChunk, p_tm + 64 + kk * 8, sdesc_advance(bd, kk * 2048), idesc_pv2, 1u);
                 umma_commit(bar(bl.empty + s));
                 umma_commit(bar(bl.empty + s + 1));
                 it += 2;
@@ -340,6 +321,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk)
                   umma_ts(tbase + c * kChunk, p_tm + kk * 8, sdesc_advance(bd, kk * 2048), idesc_pv, acc0 | (kk > 0));
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk)  // the P_lo term
+                  umma_ts(tbase + c * kChunk, p_tm + 64 + kk * 8, sdesc_advance(bd, kk * 2048), idesc_pv, 1u);
                 umma_commit(bar(bl.empty + s));
                 it += 1;
                 c += 1;
@@ -449,12 +433,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         const float m_ref = (m_used == -INFINITY) ? 0.f : m_used;
         float ls[4] = {0.f, 0.f, 0.f, 0.f};
-        uint32_t pk[64];
 #pragma unroll
-        for (int i = 0; i < 64; ++i) {
-          const float p0 = ex2(s[2 * i] - m_ref), p1 = ex2(s[2 * i + 1] - m_ref);
-          ls[i & 3] += p0 + p1;
-          pk[i] = pack2<BF16>(p0, p1);
+        for (int i = 0; i < 128; ++i) {
+          s[i] = ex2(s[i] - m_ref);  // P, in place
+          ls[i & 3] += s[i];
         }
         l_sum = l_sum * alpha + ((ls[0] + ls[1]) + (ls[2] + ls[3]));
         if (j >= 1) {
@@ -481,11 +463,23 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
         }
-        {
-          uint32_t(&lo)[32] = *reinterpret_cast<uint32_t(*)[32]>(&pk[0]);
-          uint32_t(&hi)[32] = *reinterpret_cast<uint32_t(*)[32]>(&pk[32]);
-          tmem_st32(tbase + lane_off + s_col, lo);
-          tmem_st32(tbase + lane_off + s_col + 32, hi);
+        // P goes to TMEM as two terms of the input type, P = P_hi + P_lo with
+        // P_lo the rounding residual of P_hi (columns 0..63 and 64..127 of the
+        // score buffer); the P V product sums both, so the 16-bit operand costs
+        // about 2^-17 of P instead of 2^-9 (bf16), which matters for outputs
+        // that are sums of nearly cancelling V rows.
+#pragma unroll
+        for (int g = 0; g < 4; ++g) {
+          uint32_t hi[16], lo[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            const float p0 = s[32 * g + 2 * e], p1 = s[32 * g + 2 * e + 1];
+            hi[e] = pack2<BF16>(p0, p1);
+            const float2 h = unpack2<BF16>(hi[e]);
+            lo[e] = pack2<BF16>(p0 - h.x, p1 - h.y);
+          }
+          tmem_st16(tbase + lane_off + s_col + 16 * g, hi);
+          tmem_st16(tbase + lane_off + s_col + 64 + 16 * g, lo);
         }
         tmem_st_wait();
         tc_fence_before();
@@ -545,7 +539,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 template <int FL, bool BF16>
 cudaError_t launch_impl(const FwdParams& p_in, const FwdMaps& m, cudaStream_t st) {
   FwdParams p = p_in;
-  constexpr int CS = (FL == kSolo) ? 1 : 2;
+  constexpr int CS = ctas_per_tile(FL);
   constexpr int kMaxSmem = 232448;  // 227 KB opt-in per block
   const SmemPlan base = smem_plan(p.n_chunks, FL, 0);
   int stages = (kMaxSmem - 1024 - base.total) / kChunkBytes;
@@ -581,6 +575,8 @@ cudaError_t launch_fwd_main(const FwdParams& p, const FwdMaps& m, bool bf16, cud
   if (p.n_chunks <= 4) return bf16 ? launch_impl<kSolo, true>(p, m, s) : launch_impl<kSolo, false>(p, m, s);
   if (p.n_chunks <= 8)
     return bf16 ? launch_impl<kRecompute, true>(p, m, s) : launch_impl<kRecompute, false>(p, m, s);
+  if (p.n_chunks <= 12)
+    return bf16 ? launch_impl<kRecompute3, true>(p, m, s) : launch_impl<kRecompute3, false>(p, m, s);
   return bf16 ? launch_impl<kExchange, true>(p, m, s) : launch_impl<kExchange, false>(p, m, s);
 }
 

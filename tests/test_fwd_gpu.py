@@ -2,8 +2,8 @@
 
 Small shapes are compared element by element over the whole output; they span
 several 128-row tiles, ragged tails, both dtypes, every head-dimension regime
-of the fused kernel (one CTA for D <= 256, a D-split CTA pair above, several
-passes above D = 512) and the decode path (Nq <= 16).  The workload-sized
+of the fused kernel (one CTA for D <= 256, two or three CTAs splitting D up to
+D = 768, an exchanging pair above) and the decode path (Nq <= 16).  The workload-sized
 cases compare 64 seeded query rows per head, which the oracle computes one by
 one.
 """
@@ -35,6 +35,11 @@ def test_config_small_self_attention():
     (1, 1, 1, 100, 300, 512, FP, True, True),
     (1, 2, 1, 384, 384, 640, FP, False, False),
     (1, 1, 1, 127, 1, 448, BF, False, False),
+    # GQA + key bias + causal + ragged at D=512 (early rows see few keys, so
+    # outputs can be sums of nearly cancelling V rows)
+    (1, 2, 1, 200, 200, 512, BF, True, True),
+    (1, 2, 2, 200, 200, 512, BF, True, True),
+    (1, 4, 2, 333, 333, 512, FP, True, True),
 ])
 def test_fused_small(B, Hq, Hkv, Nq, Nkv, D, dtype, causal, bias):
     check_fwd_full(B, Hq, Hkv, Nq, Nkv, D, dtype, causal=causal, bias=bias)
