@@ -291,7 +291,7 @@ def run_ffpa(args, rank, world):
 # DRAM bytes (read + write) per launch from the ncu capture summarised in
 # profiles/ncu_full_fwd_bwd_N8192_D512_bf16.md (same workload); only kernels
 # unchanged since that capture are listed.
-TRAFFIC: dict = {"bwd_dv": 250011392, "bwd_dk": 330317312, "bwd_dq": 344252928}
+TRAFFIC: dict = {"fwd_main": 253895936, "bwd_dv": 253783296, "bwd_dk": 334875392, "bwd_dq": 339085056}
 
 
 def measure_e2e(step, inp, dev_in, dev_out, world, dev, steps=3):
