@@ -24,10 +24,10 @@
 // half of the gradient's columns.  The exchange's distributed-shared-memory
 // traffic (64 KB per product and tile) costs more time than the extra MMAs.
 //
-// TMEM (512 columns): gradient accumulator [0, 256), X1 [256, 384) (scores,
-// then P or dS as the bf16/f16 A operand), X2 [384, 512) (dP).
-// Warp roles: warp 0 TMA producer, warp 1 TMEM owner + MMA issuer, warps 4-7
-// elementwise + epilogue (thread = stationary row = TMEM lane).
+// TMEM (512 columns): gradient accumulator [0, 256), X1 [256, 384) (scores),
+// X2 [384, 512) (dP, then P or dS as the bf16/f16 A operand of the gradient).
+// Warp roles: warps 0, 2, 3 TMA producers, warp 1 TMEM owner + MMA issuer,
+// warps 4-7 elementwise + epilogue (thread = stationary row = TMEM lane).
 #include <type_traits>
 
 #include "internal.h"
@@ -39,6 +39,7 @@ namespace {
 enum Mode : int { kDV = 0, kDK = 1, kDQ = 2 };
 
 constexpr int kThreads = 256;
+constexpr int kProducers = 3;  // warps 0, 2 and 3
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kX1 = 256, kX2 = 384;
 constexpr int kMaxAccChunks = 4;
@@ -46,7 +47,7 @@ constexpr int kLandingBytes = kTileRows * kTileRows * 4;
 constexpr float kLog2e = 1.4426950408889634f;
 
 struct Bars {
-  int full, empty, a_full, x_full, p_ready, acc_ready, acc_free, xfull, xfree, drain, count;
+  int full, empty, a_full, x_full, x1_free, p_ready, acc_ready, acc_free, xfull, xfree, drain, count;
 };
 __host__ __device__ inline Bars bar_layout(int stages) {
   Bars b;
@@ -54,7 +55,8 @@ __host__ __device__ inline Bars bar_layout(int stages) {
   b.empty = stages;
   b.a_full = 2 * stages;
   b.x_full = b.a_full + 1;
-  b.p_ready = b.x_full + 1;
+  b.x1_free = b.x_full + 1;
+  b.p_ready = b.x1_free + 1;
   b.acc_ready = b.p_ready + 1;
   b.acc_free = b.acc_ready + 1;
   b.xfull = b.acc_free + 1;
@@ -238,6 +240,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(bar(bl.a_full), 1);
     mbar_init(bar(bl.x_full), 1);
+    mbar_init(bar(bl.x1_free), 4);
     mbar_init(bar(bl.p_ready), 4);
     mbar_init(bar(bl.acc_ready), 1);
     mbar_init(bar(bl.acc_free), 4);
@@ -256,84 +259,89 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tbase = *tmem_slot;
 
-  if (warp == 0) {
-    // ------------------------------------------------------------ TMA producer
-    // G lanes issue consecutive loads together (arming a barrier and issuing a
-    // TMA load costs one thread ~500 cycles); lane g owns every G-th load.
-    const int G = stages >= 6 ? 4 : (stages >= 4 ? 2 : 1);
-    if (lane < G) {
-      const unsigned gmask = (1u << G) - 1u;
-      if (lane == 0) {
-        tma_prefetch_desc(&map_q);
-        tma_prefetch_desc(&map_k);
-        tma_prefetch_desc(&map_v);
-        tma_prefetch_desc(&map_do);
-        if (n_res > 0) {
-          mbar_expect_tx(bar(bl.a_full), n_res * s_n * kChunkBytes);
-          for (int c = 0; c < s_n; ++c) {
-            tma_load_4d(a_sm + c * kChunkBytes, mA1, bar(bl.a_full), (s0 + c) * kChunk, g.s_row0, g.s_head, g.b);
-            if (n_res > 1)
-              tma_load_4d(a_sm + (plan.a_chunks + c) * kChunkBytes, mA2, bar(bl.a_full), (s0 + c) * kChunk,
-                          g.s_row0, g.s_head, g.b);
-          }
+  if (warp == 0 || warp == 2 || warp == 3) {
+    // ------------------------------------------------------------ TMA producers
+    // Three warps (one lane each) issue the ring loads: producer pi owns every
+    // nprod-th load and waits only for its own slot to be released. Arming
+    // a barrier and issuing a TMA load blocks the issuing thread for ~500
+    // cycles, so one thread alone cannot keep the ring full, and lanes of one
+    // warp would have to wait for one another's slots.
+    // A parity wait tells apart only the current and the previous phase of a
+    // barrier, so no producer may run two rounds ahead of a slot's barrier:
+    // producer pi waits for load i - stages before issuing load i, having
+    // issued load i - nprod, which needs nprod <= stages.
+    const int nprod = min(kProducers, stages);
+    const int pi = (warp == 0) ? 0 : warp - 1;
+    if (lane == 0 && pi < nprod) {
+      tma_prefetch_desc(&map_q);
+      tma_prefetch_desc(&map_k);
+      tma_prefetch_desc(&map_v);
+      tma_prefetch_desc(&map_do);
+      if (pi == 0 && n_res > 0) {
+        mbar_expect_tx(bar(bl.a_full), n_res * s_n * kChunkBytes);
+        for (int c = 0; c < s_n; ++c) {
+          tma_load_4d(a_sm + c * kChunkBytes, mA1, bar(bl.a_full), (s0 + c) * kChunk, g.s_row0, g.s_head, g.b);
+          if (n_res > 1)
+            tma_load_4d(a_sm + (plan.a_chunks + c) * kChunkBytes, mA2, bar(bl.a_full), (s0 + c) * kChunk,
+                        g.s_row0, g.s_head, g.b);
         }
       }
       bool ok = true;
       uint32_t it = 0;
-      int my_it = -1, my_c0 = 0, my_c1 = 0, my_c2 = 0;
-      const CUtensorMap* my_m = nullptr;
-      auto flush = [&]() {
-        if (my_it >= 0 && ok) {
-          const uint32_t s = static_cast<uint32_t>(my_it) % stages, r = static_cast<uint32_t>(my_it) / stages;
+      auto load = [&](const CUtensorMap* m, int dcol, int row, int head) {
+        if (ok && static_cast<int>(it % nprod) == pi) {
+          const uint32_t s = it % stages, r = it / stages;
           ok = mbar_wait(bar(bl.empty + s), (r & 1) ^ 1, status);
           if (ok) {
             mbar_expect_tx(bar(bl.full + s), kChunkBytes);
-            tma_load_4d(ring_sm + s * kChunkBytes, my_m, bar(bl.full + s), my_c0, my_c1, my_c2, g.b);
+            tma_load_4d(ring_sm + s * kChunkBytes, m, bar(bl.full + s), dcol, row, head, g.b);
           }
         }
-        my_it = -1;
-        ok = __all_sync(gmask, ok);
-      };
-      auto load = [&](const CUtensorMap* m, int dcol, int row, int head) {
-        if (static_cast<int>(it % G) == lane) {
-          my_it = static_cast<int>(it);
-          my_m = m;
-          my_c0 = dcol;
-          my_c1 = row;
-          my_c2 = head;
-        }
         ++it;
-        if (it % G == 0) flush();
+      };
+      // Loads follow the MMA warp's order of use: X1 and X2 of column 0, then
+      // for each column c: X1 of c + 1, the gradient of c, X2 of c + 1.
+      auto x1_loads = [&](int c) {
+        int ch, cr0;
+        column<MODE>(g, p, c, &ch, &cr0);
+        for (int cc = 0; cc < s_n; ++cc) {
+          if (n_res < 1) load(mA1, (s0 + cc) * kChunk, g.s_row0, g.s_head);
+          load(mB1, (s0 + cc) * kChunk, cr0, ch);
+        }
+      };
+      auto x2_loads = [&](int c) {
+        int ch, cr0;
+        column<MODE>(g, p, c, &ch, &cr0);
+        for (int cc = 0; cc < s_n; ++cc) {
+          if (n_res < 2) load(mA2, (s0 + cc) * kChunk, g.s_row0, g.s_head);
+          load(mB2, (s0 + cc) * kChunk, cr0, ch);
+        }
       };
       for (int pass = 0; pass < passes && ok; ++pass) {
         const int oc0 = pass * kMaxAccChunks;
         const int oc_n = max(0, min(kMaxAccChunks, own_n - oc0));
+        if (g.ncols > 0) {
+          x1_loads(0);
+          if (two) x2_loads(0);
+        }
         for (int c = 0; c < g.ncols && ok; ++c) {
+          if (c + 1 < g.ncols) x1_loads(c + 1);
           int ch, cr0;
           column<MODE>(g, p, c, &ch, &cr0);
-          if (two)
-            for (int cc = 0; cc < s_n; ++cc) {
-              if (n_res < 2) load(mA2, (s0 + cc) * kChunk, g.s_row0, g.s_head);
-              load(mB2, (s0 + cc) * kChunk, cr0, ch);
-            }
-          for (int cc = 0; cc < s_n; ++cc) {
-            if (n_res < 1) load(mA1, (s0 + cc) * kChunk, g.s_row0, g.s_head);
-            load(mB1, (s0 + cc) * kChunk, cr0, ch);
-          }
           for (int oc = 0; oc < oc_n; ++oc) load(mB3, (own0 + oc0 + oc) * kChunk, cr0, ch);
+          if (two && c + 1 < g.ncols) x2_loads(c + 1);
         }
       }
-      flush();
-      __syncwarp(gmask);
-      if (lane == 0) {
-        // Wait for the last release of every ring slot: the MMA warp's commit
-        // arrives on empty[s] only when the MMAs reading the slot are done, and
-        // commit arrivals are not ordered with respect to one another, so one
-        // still in flight at exit would land in the next CTA's shared memory.
-        for (uint32_t s = 0; s < static_cast<uint32_t>(stages) && s < it; ++s)
-          mbar_wait(bar(bl.empty + s), ((it - 1 - s) / stages) & 1, status);
-        if (n_res > 0) mbar_wait(bar(bl.a_full), 0, status);
+      // Wait for the last release of each ring slot whose last load was ours:
+      // the MMA warp's commit arrives on empty[s] only when the MMAs reading the
+      // slot are done, and commit arrivals are not ordered with respect to one
+      // another, so one still in flight at exit would land in the next CTA's
+      // shared memory. (After a timeout `it` stops short; the waits stay bounded.)
+      for (uint32_t s = 0; s < static_cast<uint32_t>(stages) && s < it; ++s) {
+        const uint32_t last = s + ((it - 1 - s) / stages) * stages;
+        if (static_cast<int>(last % nprod) == pi) mbar_wait(bar(bl.empty + s), (last / stages) & 1, status);
       }
+      if (pi == 0 && n_res > 0) mbar_wait(bar(bl.a_full), 0, status);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
@@ -380,26 +388,35 @@ __global__ void __launch_bounds__(kThreads, 1)
       };
       for (int pass = 0; pass < passes && ok; ++pass) {
         const int oc_n = max(0, min(kMaxAccChunks, own_n - pass * kMaxAccChunks));
-        if (pass > 0) {
+        // With no columns the MMAs never touch the accumulator, and the epilogue
+        // may already have arrived for several passes (a parity wait would then
+        // alias), so there is nothing to wait for.
+        if (pass > 0 && g.ncols > 0) {
           ok = mbar_wait(bar(bl.acc_free), (pass - 1) & 1, status);
           tc_fence_after();
         }
+        // X1 (scores) is read only by the elementwise warps, which free it before
+        // computing P and dS; X2 ends up holding P or dS, the A operand of the
+        // gradient MMAs.  So the next column's X1 product overlaps this
+        // column's elementwise work, and X2 is rewritten only after the
+        // gradient MMAs reading it have completed (tcgen05.mma does not order a
+        // later write of D after an earlier read of A in TMEM).
+        if (g.ncols > 0) {
+          product(tbase + kX1, 0);
+          if (two && ok) product(tbase + kX2, 1);
+          if (ok) umma_commit(bar(bl.x_full));
+        }
         for (int c = 0; c < g.ncols && ok; ++c) {
           const int t = t0 + c;
-          // X1 still holds the previous tile's P/dS, the A operand of its
-          // gradient MMA; tcgen05.mma does not order a later write of D after
-          // an earlier read of A in TMEM, so X1 is rewritten only after that
-          // MMA has completed.  X2 has no such reader and goes first.
-          if (two) product(tbase + kX2, 1);
-          if (!ok) break;
-          if (c >= 1) {
-            ok = mbar_wait(bar(bl.acc_ready), (t - 1) & 1, status);
+          const bool more = c + 1 < g.ncols;
+          if (more) {
+            ok = mbar_wait(bar(bl.x1_free), t & 1, status);
             if (!ok) break;
             tc_fence_after();
+            product(tbase + kX1, 0);
+            if (!ok) break;
+            if (!two) umma_commit(bar(bl.x_full));
           }
-          product(tbase + kX1, 0);
-          if (!ok) break;
-          umma_commit(bar(bl.x_full));
           ok = mbar_wait(bar(bl.p_ready), t & 1, status);
           if (!ok) break;
           tc_fence_after();
@@ -416,7 +433,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (pair) {
 #pragma unroll
               for (int kk = 0; kk < 8; ++kk)
-                umma_ts(tbase + oc * kChunk, tbase + kX1 + kk * 8, sdesc_advance(bd, kk * 2048), idesc_acc2,
+                umma_ts(tbase + oc * kChunk, tbase + kX2 + kk * 8, sdesc_advance(bd, kk * 2048), idesc_acc2,
                         acc0 | (kk > 0));
               umma_commit(bar(bl.empty + s));
               umma_commit(bar(bl.empty + s + 1));
@@ -425,14 +442,23 @@ __global__ void __launch_bounds__(kThreads, 1)
             } else {
 #pragma unroll
               for (int kk = 0; kk < 8; ++kk)
-                umma_ts(tbase + oc * kChunk, tbase + kX1 + kk * 8, sdesc_advance(bd, kk * 2048), idesc_acc,
+                umma_ts(tbase + oc * kChunk, tbase + kX2 + kk * 8, sdesc_advance(bd, kk * 2048), idesc_acc,
                         acc0 | (kk > 0));
               umma_commit(bar(bl.empty + s));
               it += 1;
               oc += 1;
             }
           }
+          if (!ok) break;
           umma_commit(bar(bl.acc_ready));
+          if (more && two) {
+            ok = mbar_wait(bar(bl.acc_ready), t & 1, status);
+            if (!ok) break;
+            tc_fence_after();
+            product(tbase + kX2, 1);
+            if (!ok) break;
+            umma_commit(bar(bl.x_full));
+          }
         }
         t0 += g.ncols;
       }
@@ -584,6 +610,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         }
         if constexpr (XCH) release();
+        // The scores have been read: X1 may take the next column's.
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(bl.x1_free));
         if (two) {
           if constexpr (XCH) {
             send(kX2);
@@ -613,8 +643,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             lo[e] = pack2<BF16>(pv[2 * e], pv[2 * e + 1]);
             hi[e] = pack2<BF16>(pv[64 + 2 * e], pv[64 + 2 * e + 1]);
           }
-          tmem_st32(tbase + lane_off + kX1, lo);
-          tmem_st32(tbase + lane_off + kX1 + 32, hi);
+          if (!two && t > 0) {
+            // X2 held the previous column's P, read by its gradient MMAs (with
+            // dP, the X2 product of this column already waited for them).
+            ok = __all_sync(0xffffffffu, mbar_wait(bar(bl.acc_ready), (t - 1) & 1, status));
+            if (!ok) break;
+            tc_fence_after();
+          }
+          tmem_st32(tbase + lane_off + kX2, lo);
+          tmem_st32(tbase + lane_off + kX2 + 32, hi);
         }
         tmem_st_wait();
         tc_fence_before();

@@ -46,6 +46,7 @@ namespace ffpa {
 namespace {
 
 constexpr int kThreads = 256;
+constexpr int kProducers = 3;  // warps 0, 2 and 3
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kS0 = 256, kS1 = 384;  // TMEM columns of the two S/P buffers
 constexpr int kMaxOChunksPerPass = 4;     // O columns per pass: 4 x 64 = 256
@@ -174,47 +175,39 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tbase = *tmem_slot;
 
-  if (warp == 0) {
-    // ------------------------------------------------------------ TMA producer
-    // Arming a barrier and issuing a TMA load costs one thread ~500 cycles, so
-    // G lanes issue consecutive loads of the sequence together (lane g owns
-    // every G-th load; each waits for its own ring slot).
-    const int G = stages >= 6 ? 4 : (stages >= 4 ? 2 : 1);
-    if (lane < G) {
-      const unsigned gmask = (1u << G) - 1u;
-      if (lane == 0) {
-        tma_prefetch_desc(&map_q);
-        tma_prefetch_desc(&map_k);
-        tma_prefetch_desc(&map_v);
+  if (warp == 0 || warp == 2 || warp == 3) {
+    // ------------------------------------------------------------ TMA producers
+    // Three warps (one lane each) issue the ring loads: producer pi owns every
+    // nprod-th load of the sequence and waits only for its own slot to be
+    // released. Arming a barrier and issuing a TMA load blocks the issuing
+    // thread for ~500 cycles, so one thread alone cannot keep the ring full.
+    // A parity wait tells apart only the current and the previous phase of a
+    // barrier, so no producer may run two rounds ahead of a slot's barrier:
+    // producer pi waits for load i - stages before issuing load i, having
+    // issued load i - nprod, which needs nprod <= stages.
+    const int nprod = min(kProducers, stages);
+    const int pi = (warp == 0) ? 0 : warp - 1;
+    if (lane == 0 && pi < nprod) {
+      tma_prefetch_desc(&map_q);
+      tma_prefetch_desc(&map_k);
+      tma_prefetch_desc(&map_v);
+      if (pi == 0) {
         mbar_expect_tx(bar(bl.q_full), s_n * kChunkBytes);
         for (int c = 0; c < s_n; ++c)
           tma_load_4d(q_sm + c * kChunkBytes, &map_q, bar(bl.q_full), (s0 + c) * kChunk, q0, h, b);
       }
       bool ok = true;
       uint32_t it = 0;
-      int my_it = -1, my_c0 = 0, my_c1 = 0;
-      const CUtensorMap* my_m = nullptr;
-      auto flush = [&]() {
-        if (my_it >= 0 && ok) {
-          const uint32_t s = static_cast<uint32_t>(my_it) % stages, r = static_cast<uint32_t>(my_it) / stages;
+      auto load = [&](const CUtensorMap* m, int dcol, int row) {
+        if (ok && static_cast<int>(it % nprod) == pi) {
+          const uint32_t s = it % stages, r = it / stages;
           ok = mbar_wait(bar(bl.empty + s), (r & 1) ^ 1, status);
           if (ok) {
             mbar_expect_tx(bar(bl.full + s), kChunkBytes);
-            tma_load_4d(ring_sm + s * kChunkBytes, my_m, bar(bl.full + s), my_c0, my_c1, kvh, b);
+            tma_load_4d(ring_sm + s * kChunkBytes, m, bar(bl.full + s), dcol, row, kvh, b);
           }
         }
-        my_it = -1;
-        ok = __all_sync(gmask, ok);
-      };
-      auto load = [&](const CUtensorMap* m, int dcol, int row) {
-        if (static_cast<int>(it % G) == lane) {
-          my_it = static_cast<int>(it);
-          my_m = m;
-          my_c0 = dcol;
-          my_c1 = row;
-        }
         ++it;
-        if (it % G == 0) flush();
       };
       for (int pass = 0; pass < passes && ok; ++pass) {
         const int oc0 = pass * kMaxOChunksPerPass;
@@ -226,18 +219,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int c = 0; c < oc_n; ++c) load(&map_v, (own0 + oc0 + c) * kChunk, (j - 1) * kTileRows);
         }
       }
-      flush();
-      __syncwarp(gmask);
-      // Drain: every load this CTA issued has landed before the CTA can exit.
-      if (lane == 0) {
-        // Wait for the last release of every ring slot: the MMA warp's commit
-        // arrives on empty[s] only when the MMAs reading the slot are done, and
-        // commit arrivals are not ordered with respect to one another, so one
-        // still in flight at exit would land in the next CTA's shared memory.
-        for (uint32_t s = 0; s < static_cast<uint32_t>(stages) && s < it; ++s)
-          mbar_wait(bar(bl.empty + s), ((it - 1 - s) / stages) & 1, status);
-        mbar_wait(bar(bl.q_full), 0, status);
+      // Drain: wait for the last release of each ring slot whose last load was
+      // ours. The MMA warp's commit arrives on empty[s] only when the MMAs
+      // reading the slot are done, and commit arrivals are not ordered with
+      // respect to one another, so one still in flight at exit would land in
+      // the next CTA's shared memory.
+      for (uint32_t s = 0; s < static_cast<uint32_t>(stages) && s < it; ++s) {
+        const uint32_t last = s + ((it - 1 - s) / stages) * stages;
+        if (static_cast<int>(last % nprod) == pi) mbar_wait(bar(bl.empty + s), (last / stages) & 1, status);
       }
+      if (pi == 0) mbar_wait(bar(bl.q_full), 0, status);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
