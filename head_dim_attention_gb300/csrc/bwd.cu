@@ -75,13 +75,13 @@ struct Plan {
   int n_a;       // resident stationary operands (A1, then A2); the rest stream through the ring
   int a_off, ring_off, land_off, bar_off, total;
 };
-__host__ __device__ inline Plan make_plan(int n_chunks, int fl, int stages, int n_res) {
+__host__ __device__ inline Plan make_plan(int n_chunks, int fl, int stages, int n_res, int slot_chunks) {
   Plan s;
   s.a_chunks = (fl == kExchange) ? (n_chunks + 1) / 2 : n_chunks;
   s.n_a = n_res;
   s.a_off = 0;
   s.ring_off = s.n_a * s.a_chunks * kChunkBytes;
-  s.land_off = s.ring_off + stages * kChunkBytes;
+  s.land_off = s.ring_off + stages * slot_chunks * kChunkBytes;
   s.bar_off = s.land_off + (fl == kExchange ? kLandingBytes : 0);
   s.total = s.bar_off + 1024;
   return s;
@@ -206,7 +206,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int stages = p.stages;
-  const Plan plan = make_plan(p.n_chunks, FL, stages, n_res);
+  const int G = p.slot_chunks;  // 16 KB tiles per ring slot
+  const uint32_t slot_bytes = G * kChunkBytes;
+  const Plan plan = make_plan(p.n_chunks, FL, stages, n_res, G);
   const Bars bl = bar_layout(stages);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + plan.bar_off);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + bl.count);
@@ -288,35 +290,55 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       bool ok = true;
       uint32_t it = 0;
-      auto load = [&](const CUtensorMap* m, int dcol, int row, int head) {
+      // One ring slot holds up to G 16 KB tiles loaded under a single barrier
+      // phase: each phase of a slot (arm, land, wait, release) costs the SM a
+      // few hundred cycles whatever its size, so two tiles per phase move
+      // nearly twice the bytes of one.  Tile i of the slot is (m[i], chunk
+      // dc[i], rows from row[i], head hd[i]).
+      auto load = [&](int cn, const CUtensorMap* const* m, const int* dc, const int* row, const int* hd) {
         if (ok && static_cast<int>(it % nprod) == pi) {
           const uint32_t s = it % stages, r = it / stages;
           ok = mbar_wait(bar(bl.empty + s), (r & 1) ^ 1, status);
           if (ok) {
-            mbar_expect_tx(bar(bl.full + s), kChunkBytes);
-            tma_load_4d(ring_sm + s * kChunkBytes, m, bar(bl.full + s), dcol, row, head, g.b);
+            mbar_expect_tx(bar(bl.full + s), cn * kChunkBytes);
+            for (int i = 0; i < cn; ++i)
+              tma_load_4d(ring_sm + s * slot_bytes + i * kChunkBytes, m[i], bar(bl.full + s), dc[i] * kChunk, row[i],
+                          hd[i], g.b);
           }
         }
         ++it;
       };
+      // cn consecutive chunks of one operand
+      auto load_run = [&](const CUtensorMap* m, int c0, int cn, int row, int head) {
+        const CUtensorMap* ms[2] = {m, m};
+        const int dc[2] = {c0, c0 + 1}, rw[2] = {row, row}, hd[2] = {head, head};
+        load(cn, ms, dc, rw, hd);
+      };
+      // A score product over the chunks s0 .. s0+s_n-1: with A resident only B
+      // streams (G chunks per slot); otherwise chunk cc of A and of B share a
+      // slot (G = 2) or take one slot each (G = 1).
+      auto product_loads = [&](const CUtensorMap* mA, bool a_res, const CUtensorMap* mB, int c) {
+        int ch, cr0;
+        column<MODE>(g, p, c, &ch, &cr0);
+        if (a_res) {
+          for (int cc = 0; cc < s_n; cc += G) load_run(mB, s0 + cc, min(G, s_n - cc), cr0, ch);
+        } else if (G == 2) {
+          for (int cc = 0; cc < s_n; ++cc) {
+            const CUtensorMap* ms[2] = {mA, mB};
+            const int dc[2] = {s0 + cc, s0 + cc}, rw[2] = {g.s_row0, cr0}, hd[2] = {g.s_head, ch};
+            load(2, ms, dc, rw, hd);
+          }
+        } else {
+          for (int cc = 0; cc < s_n; ++cc) {
+            load_run(mA, s0 + cc, 1, g.s_row0, g.s_head);
+            load_run(mB, s0 + cc, 1, cr0, ch);
+          }
+        }
+      };
       // Loads follow the MMA warp's order of use: X1 and X2 of column 0, then
       // for each column c: X1 of c + 1, the gradient of c, X2 of c + 1.
-      auto x1_loads = [&](int c) {
-        int ch, cr0;
-        column<MODE>(g, p, c, &ch, &cr0);
-        for (int cc = 0; cc < s_n; ++cc) {
-          if (n_res < 1) load(mA1, (s0 + cc) * kChunk, g.s_row0, g.s_head);
-          load(mB1, (s0 + cc) * kChunk, cr0, ch);
-        }
-      };
-      auto x2_loads = [&](int c) {
-        int ch, cr0;
-        column<MODE>(g, p, c, &ch, &cr0);
-        for (int cc = 0; cc < s_n; ++cc) {
-          if (n_res < 2) load(mA2, (s0 + cc) * kChunk, g.s_row0, g.s_head);
-          load(mB2, (s0 + cc) * kChunk, cr0, ch);
-        }
-      };
+      auto x1_loads = [&](int c) { product_loads(mA1, n_res >= 1, mB1, c); };
+      auto x2_loads = [&](int c) { product_loads(mA2, n_res >= 2, mB2, c); };
       for (int pass = 0; pass < passes && ok; ++pass) {
         const int oc0 = pass * kMaxAccChunks;
         const int oc_n = max(0, min(kMaxAccChunks, own_n - oc0));
@@ -328,7 +350,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (c + 1 < g.ncols) x1_loads(c + 1);
           int ch, cr0;
           column<MODE>(g, p, c, &ch, &cr0);
-          for (int oc = 0; oc < oc_n; ++oc) load(mB3, (own0 + oc0 + oc) * kChunk, cr0, ch);
+          for (int oc = 0; oc < oc_n; oc += G) load_run(mB3, own0 + oc0 + oc, min(G, oc_n - oc), cr0, ch);
           if (two && c + 1 < g.ncols) x2_loads(c + 1);
         }
       }
@@ -358,31 +380,56 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       uint32_t it = 0;
       int t0 = 0;
-      // one score-like product: X (+)= A B^T over the chunks s0 .. s0+s_n-1
+      // one score-like product: X (+)= A B^T over the chunks s0 .. s0+s_n-1,
+      // consuming the ring in the producer's order (see product_loads)
       auto product = [&](uint32_t x_tm, int a_slot) {
         const bool resident = a_slot < n_res;
+        if (resident) {
+          for (int cc = 0; cc < s_n && ok; cc += G) {
+            const uint32_t sb = it % stages;
+            ok = mbar_wait(bar(bl.full + sb), (it / stages) & 1, status);
+            if (!ok) return;
+            ++it;
+            tc_fence_after();
+            const int cn = min(G, s_n - cc);
+            for (int i = 0; i < cn; ++i) {
+              const uint64_t a = sdesc_advance(da, (a_slot * plan.a_chunks + cc + i) * kChunkBytes);
+              const uint64_t bd = sdesc_advance(dk, sb * slot_bytes + i * kChunkBytes);
+#pragma unroll
+              for (int kk = 0; kk < 4; ++kk)
+                umma_ss(x_tm, sdesc_advance(a, kk * 32), sdesc_advance(bd, kk * 32), idesc_x, ((cc + i) | kk) != 0);
+            }
+            umma_commit(bar(bl.empty + sb));
+          }
+          return;
+        }
         for (int cc = 0; cc < s_n && ok; ++cc) {
-          uint64_t a;
-          uint32_t sa = 0;
-          if (resident) {
-            a = sdesc_advance(da, (a_slot * plan.a_chunks + cc) * kChunkBytes);
+          uint64_t a, bd;
+          uint32_t sa = 0, sb;
+          if (G == 2) {  // A and B chunk in one slot
+            sb = it % stages;
+            ok = mbar_wait(bar(bl.full + sb), (it / stages) & 1, status);
+            if (!ok) return;
+            ++it;
+            a = sdesc_advance(dk, sb * slot_bytes);
+            bd = sdesc_advance(dk, sb * slot_bytes + kChunkBytes);
           } else {
             sa = it % stages;
             ok = mbar_wait(bar(bl.full + sa), (it / stages) & 1, status);
             if (!ok) return;
             ++it;
+            sb = it % stages;
+            ok = mbar_wait(bar(bl.full + sb), (it / stages) & 1, status);
+            if (!ok) return;
+            ++it;
             a = sdesc_advance(dk, sa * kChunkBytes);
+            bd = sdesc_advance(dk, sb * kChunkBytes);
           }
-          const uint32_t sb = it % stages;
-          ok = mbar_wait(bar(bl.full + sb), (it / stages) & 1, status);
-          if (!ok) return;
-          ++it;
           tc_fence_after();
-          const uint64_t bd = sdesc_advance(dk, sb * kChunkBytes);
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
             umma_ss(x_tm, sdesc_advance(a, kk * 32), sdesc_advance(bd, kk * 32), idesc_x, (cc | kk) != 0);
-          if (!resident) umma_commit(bar(bl.empty + sa));
+          if (G == 1) umma_commit(bar(bl.empty + sa));
           umma_commit(bar(bl.empty + sb));
         }
       };
@@ -420,9 +467,26 @@ __global__ void __launch_bounds__(kThreads, 1)
           ok = mbar_wait(bar(bl.p_ready), t & 1, status);
           if (!ok) break;
           tc_fence_after();
-          // gradient += (P or dS) B3: two chunks per MMA (N=128) when they sit in adjacent ring slots
+          // gradient += (P or dS) B3: two chunks per MMA (N=128) when they share a
+          // ring slot, or (one chunk per slot) sit in adjacent slots
           for (int oc = 0; oc < oc_n && ok;) {
             const uint32_t s = it % stages;
+            if (G == 2) {
+              ok = mbar_wait(bar(bl.full + s), (it / stages) & 1, status);
+              if (!ok) break;
+              tc_fence_after();
+              const uint64_t bd = sdesc_advance(dm, s * slot_bytes);
+              const uint32_t acc0 = c > 0 ? 1u : 0u;
+              const uint32_t idesc = (oc + 1 < oc_n) ? idesc_acc2 : idesc_acc;
+#pragma unroll
+              for (int kk = 0; kk < 8; ++kk)
+                umma_ts(tbase + oc * kChunk, tbase + kX2 + kk * 8, sdesc_advance(bd, kk * 2048), idesc,
+                        acc0 | (kk > 0));
+              umma_commit(bar(bl.empty + s));
+              it += 1;
+              oc += 2;
+              continue;
+            }
             const bool pair = (oc + 1 < oc_n) && (s + 1 < static_cast<uint32_t>(stages));
             ok = mbar_wait(bar(bl.full + s), (it / stages) & 1, status);
             if (ok && pair) ok = mbar_wait(bar(bl.full + s + 1), ((it + 1) / stages) & 1, status);
@@ -725,17 +789,21 @@ cudaError_t launch_mode(const BwdParams& p_in, const BwdMaps& m, cudaStream_t st
   // Keep as many stationary operands resident as leave a ring of >= 3 stages
   // (>= 2 when nothing is resident).
   int n_res = (MODE == kDV) ? 1 : 2;
-  int stages = 0;
+  int room = 0;
   for (; n_res >= 0; --n_res) {
-    const Plan base = make_plan(p.n_chunks, FL, 0, n_res);
-    stages = (kMaxSmem - 1024 - base.total) / kChunkBytes;
-    if (stages >= 3) break;
+    const Plan base = make_plan(p.n_chunks, FL, 0, n_res, 1);
+    room = kMaxSmem - 1024 - base.total;
+    if (room / kChunkBytes >= 3) break;
   }
   if (n_res < 0) n_res = 0;
-  stages = stages > 8 ? 8 : stages;
+  // Two 16 KB tiles per ring slot when at least two such slots fit, else one.
+  const int G = (room / (2 * kChunkBytes) >= 2) ? 2 : 1;
+  int stages = room / (G * kChunkBytes);
+  stages = min(stages, G == 2 ? 6 : 8);
   if (stages < 2) return cudaErrorInvalidConfiguration;
   p.stages = stages;
-  const Plan plan = make_plan(p.n_chunks, FL, stages, n_res);
+  p.slot_chunks = G;
+  const Plan plan = make_plan(p.n_chunks, FL, stages, n_res, G);
   const int smem = plan.total + 1024;
   auto kern = bwd_main_kernel<MODE, FL, BF16>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);

@@ -84,12 +84,12 @@ struct SmemPlan {
   int q_chunks;  // resident Q chunks (the chunks this CTA reduces S over)
   int q_off, ring_off, land_off, bar_off, total;
 };
-__host__ __device__ inline SmemPlan smem_plan(int n_chunks, int fl, int stages) {
+__host__ __device__ inline SmemPlan smem_plan(int n_chunks, int fl, int stages, int slot_chunks) {
   SmemPlan s;
   s.q_chunks = (fl == kExchange) ? (n_chunks + 1) / 2 : n_chunks;
   s.q_off = 0;
   s.ring_off = s.q_chunks * kChunkBytes;
-  s.land_off = s.ring_off + stages * kChunkBytes;
+  s.land_off = s.ring_off + stages * slot_chunks * kChunkBytes;
   s.bar_off = s.land_off + (fl == kExchange ? kLandingBytes : 0);
   s.total = s.bar_off + 1024;  // barriers + TMEM slot
   return s;
@@ -121,9 +121,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int stages = p.stages;
+  const int G = p.slot_chunks;                  // chunk tiles per ring slot
+  const uint32_t slot_bytes = G * kChunkBytes;
   constexpr int CS = ctas_per_tile(FL);  // CTAs per query tile
   constexpr bool XCH = (FL == kExchange);
-  const SmemPlan plan = smem_plan(p.n_chunks, FL, stages);
+  const SmemPlan plan = smem_plan(p.n_chunks, FL, stages, G);
   const Bars bl = bar_layout(stages);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + plan.bar_off);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + bl.count);
@@ -198,13 +200,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       bool ok = true;
       uint32_t it = 0;
-      auto load = [&](const CUtensorMap* m, int dcol, int row) {
+      // One ring slot takes `cn` (<= G) consecutive 64-column chunk tiles under
+      // a single barrier phase.  Each phase of a slot (arm, land, wait, release)
+      // costs the SM a few hundred cycles whatever its size, so two 16 KB tiles
+      // per phase move nearly twice the bytes of one.
+      auto load = [&](const CUtensorMap* m, int c0, int cn, int row) {
         if (ok && static_cast<int>(it % nprod) == pi) {
           const uint32_t s = it % stages, r = it / stages;
           ok = mbar_wait(bar(bl.empty + s), (r & 1) ^ 1, status);
           if (ok) {
-            mbar_expect_tx(bar(bl.full + s), kChunkBytes);
-            tma_load_4d(ring_sm + s * kChunkBytes, m, bar(bl.full + s), dcol, row, kvh, b);
+            mbar_expect_tx(bar(bl.full + s), cn * kChunkBytes);
+            for (int i = 0; i < cn; ++i)
+              tma_load_4d(ring_sm + s * slot_bytes + i * kChunkBytes, m, bar(bl.full + s), (c0 + i) * kChunk, row,
+                          kvh, b);
           }
         }
         ++it;
@@ -214,9 +222,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int oc_n = max(0, min(kMaxOChunksPerPass, own_n - oc0));
         for (int j = 0; j <= ntiles && ok; ++j) {
           if (j < ntiles)
-            for (int c = 0; c < s_n; ++c) load(&map_k, (s0 + c) * kChunk, j * kTileRows);
+            for (int c = 0; c < s_n; c += G) load(&map_k, s0 + c, min(G, s_n - c), j * kTileRows);
           if (j >= 1)
-            for (int c = 0; c < oc_n; ++c) load(&map_v, (own0 + oc0 + c) * kChunk, (j - 1) * kTileRows);
+            for (int c = 0; c < oc_n; c += G) load(&map_v, own0 + oc0 + c, min(G, oc_n - c), (j - 1) * kTileRows);
         }
       }
       // Drain: wait for the last release of each ring slot whose last load was
@@ -239,8 +247,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t idesc_pv = idesc_f16(BF16, 128, 64, false, true);      // one V chunk
       const uint32_t idesc_pv2 = idesc_f16(BF16, 128, 128, false, true);    // two V chunks in adjacent slots
       const uint64_t dq = sdesc_sw128(q_sm, 16, 1024);                      // Q chunks, K-major
-      const uint64_t dk = sdesc_sw128(ring_sm, 16, 1024);                   // ring slots as K-major operands
-      const uint64_t dv = sdesc_sw128(ring_sm, kChunkBytes, 1024);          // ring slots as MN-major operands
+      const uint64_t dk = sdesc_sw128(ring_sm, 16, 1024);                   // ring tiles as K-major operands
+      const uint64_t dv = sdesc_sw128(ring_sm, kChunkBytes, 1024);          // ring tiles as MN-major operands
       bool ok = mbar_wait(bar(bl.q_full), 0, status);
       tc_fence_after();
       uint32_t it = 0;
@@ -266,15 +274,20 @@ __global__ void __launch_bounds__(kThreads, 1)
               if (!ok) break;
               tc_fence_after();
             }
-            for (int c = 0; c < s_n && ok; ++c) {
+            for (int c = 0; c < s_n && ok; c += G) {
               const uint32_t s = it % stages;
               ok = mbar_wait(bar(bl.full + s), (it / stages) & 1, status);
               if (!ok) break;
               tc_fence_after();
-              const uint64_t a = sdesc_advance(dq, c * kChunkBytes), bd = sdesc_advance(dk, s * kChunkBytes);
+              const int cn = min(G, s_n - c);
+              for (int i = 0; i < cn; ++i) {
+                const uint64_t a = sdesc_advance(dq, (c + i) * kChunkBytes);
+                const uint64_t bd = sdesc_advance(dk, s * slot_bytes + i * kChunkBytes);
 #pragma unroll
-              for (int kk = 0; kk < 4; ++kk)
-                umma_ss(s_tm, sdesc_advance(a, kk * 32), sdesc_advance(bd, kk * 32), idesc_s128, (c | kk) != 0);
+                for (int kk = 0; kk < 4; ++kk)
+                  umma_ss(s_tm, sdesc_advance(a, kk * 32), sdesc_advance(bd, kk * 32), idesc_s128,
+                          ((c + i) | kk) != 0);
+              }
               umma_commit(bar(bl.empty + s));
               ++it;
             }
@@ -287,9 +300,28 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!ok) break;
             tc_fence_after();
             const uint32_t p_tm = tbase + ((t & 1) ? kS1 : kS0);
-            // O[:, c..] += P V[:, c..]: two chunks per MMA (N=128) when they sit in adjacent ring slots
+            // O[:, c..] += P V[:, c..]: two chunks per MMA (N=128) when they share
+            // a ring slot, or (one chunk per slot) sit in adjacent slots
             for (int c = 0; c < oc_n && ok;) {
               const uint32_t s = it % stages;
+              if (G == 2) {
+                ok = mbar_wait(bar(bl.full + s), (it / stages) & 1, status);
+                if (!ok) break;
+                tc_fence_after();
+                const uint64_t bd = sdesc_advance(dv, s * slot_bytes);
+                const uint32_t acc0 = (j - 1 > 0) ? 1u : 0u;
+                const uint32_t idesc = (c + 1 < oc_n) ? idesc_pv2 : idesc_pv;
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk)
+                  umma_ts(tbase + c * kChunk, p_tm + kk * 8, sdesc_advance(bd, kk * 2048), idesc, acc0 | (kk > 0));
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk)  // the P_lo term
+                  umma_ts(tbase + c * kChunk, p_tm + 64 + kk * 8, sdesc_advance(bd, kk * 2048), idesc, 1u);
+                umma_commit(bar(bl.empty + s));
+                it += 1;
+                c += 2;
+                continue;
+              }
               const bool two = (c + 1 < oc_n) && (s + 1 < static_cast<uint32_t>(stages));
               ok = mbar_wait(bar(bl.full + s), (it / stages) & 1, status);
               if (ok && two) ok = mbar_wait(bar(bl.full + s + 1), ((it + 1) / stages) & 1, status);
@@ -532,12 +564,16 @@ cudaError_t launch_impl(const FwdParams& p_in, const FwdMaps& m, cudaStream_t st
   FwdParams p = p_in;
   constexpr int CS = ctas_per_tile(FL);
   constexpr int kMaxSmem = 232448;  // 227 KB opt-in per block
-  const SmemPlan base = smem_plan(p.n_chunks, FL, 0);
-  int stages = (kMaxSmem - 1024 - base.total) / kChunkBytes;
-  stages = stages > 8 ? 8 : stages;
+  const SmemPlan base = smem_plan(p.n_chunks, FL, 0, 1);
+  const int room = kMaxSmem - 1024 - base.total;
+  // Two chunk tiles per ring slot when at least two such slots fit, else one.
+  int G = (room / (2 * kChunkBytes) >= 2) ? 2 : 1;
+  int stages = room / (G * kChunkBytes);
+  stages = min(stages, G == 2 ? 6 : 8);
   if (stages < 2) return cudaErrorInvalidConfiguration;
   p.stages = stages;
-  const SmemPlan plan = smem_plan(p.n_chunks, FL, stages);
+  p.slot_chunks = G;
+  const SmemPlan plan = smem_plan(p.n_chunks, FL, stages, G);
   const int smem = plan.total + 1024;  // + alignment slack
   auto kern = fwd_main_kernel<FL, BF16>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);

@@ -23,7 +23,8 @@ struct FwdParams {
   int causal;
   float scale_log2;   // scale * log2(e)
   int n_chunks;       // D / 64
-  int stages;         // ring stages of 16 KB
+  int stages;         // ring slots
+  int slot_chunks;    // 64-column chunk tiles per ring slot (1 or 2), loaded under one barrier phase
   int q_tiles;        // ceil(Nq / 128)
   uint32_t* status;   // device status word
 };
@@ -78,7 +79,8 @@ struct BwdParams {
   float scale;
   float scale_log2;
   int n_chunks;
-  int stages;
+  int stages;         // ring slots
+  int slot_chunks;    // 16 KB tiles per ring slot (1 or 2), loaded under one barrier phase
   int q_tiles, kv_tiles;
   uint32_t* status;
 };
