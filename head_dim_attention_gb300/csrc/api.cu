@@ -94,7 +94,7 @@ void tma_strides(const ffpa_tensor_t* t, int64_t out[3]) {
   out[2] = sb;
 }
 
-int encode_map(CUtensorMap* m, const ffpa_tensor_t* t) {
+int encode_map(CUtensorMap* m, const ffpa_tensor_t* t, int box_rows = kTileRows) {
   EncodeTiledFn enc = encode_fn();
   if (!enc) return FFPA_ERR_CUDA;
   int64_t st[3];
@@ -102,7 +102,7 @@ int encode_map(CUtensorMap* m, const ffpa_tensor_t* t) {
   const cuuint64_t dims[4] = {(cuuint64_t)t->shape[3], (cuuint64_t)t->shape[2], (cuuint64_t)t->shape[1],
                               (cuuint64_t)t->shape[0]};
   const cuuint64_t strides[3] = {(cuuint64_t)st[0] * 2, (cuuint64_t)st[1] * 2, (cuuint64_t)st[2] * 2};
-  const cuuint32_t box[4] = {(cuuint32_t)kChunk, (cuuint32_t)kTileRows, 1, 1};
+  const cuuint32_t box[4] = {(cuuint32_t)kChunk, (cuuint32_t)box_rows, 1, 1};
   const cuuint32_t es[4] = {1, 1, 1, 1};
   const CUtensorMapDataType dt =
       t->dtype == FFPA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
@@ -246,7 +246,9 @@ extern "C" int ffpa_fwd(const ffpa_tensor_t* q, const ffpa_tensor_t* k, const ff
   p.q_tiles = (int)((c.Nq + kTileRows - 1) / kTileRows);
   p.status = status;
   FwdMaps m;
-  if ((rc = encode_map(&m.q, q)) || (rc = encode_map(&m.k, k)) || (rc = encode_map(&m.v, v))) return rc;
+  if ((rc = encode_map(&m.q, q)) || (rc = encode_map(&m.k, k)) || (rc = encode_map(&m.v, v)) ||
+      (rc = encode_map(&m.k_half, k, kTileRows / 2)))
+    return rc;
   return cuda_rc(launch_fwd_main(p, m, bf16, st));
 }
 

@@ -51,6 +51,9 @@ constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kS0 = 256, kS1 = 384;  // TMEM columns of the two S/P buffers
 constexpr int kMaxOChunksPerPass = 4;     // O columns per pass: 4 x 64 = 256
 constexpr float kRescaleLog2 = 8.0f;      // rescale O only when the max grows by > 2^8
+// A key tile feeds P to P V as two 16-bit terms only when some row of it holds
+// a probability above this fraction of the row's running sum (see below).
+constexpr float kLoFrac = 1.0f / 64.0f;
 constexpr int kLandingBytes = kTileRows * kTileRows * 4;  // 64 KB partial-S landing buffer
 
 struct Bars {
@@ -129,6 +132,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   const Bars bl = bar_layout(stages);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + plan.bar_off);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + bl.count);
+  // lo_flag[t & 1] == t + 1: tile t carries the residual term of P (written by
+  // the softmax warps before they arrive on p_ready, read by the MMA thread after)
+  volatile uint32_t* lo_flag = tmem_slot + 1;
   auto bar = [&](int i) { return smem_u32(&bars[i]); };
   const uint32_t s_base = smem_u32(smem);
   const uint32_t q_sm = s_base + plan.q_off, ring_sm = s_base + plan.ring_off, land_sm = s_base + plan.land_off;
@@ -165,6 +171,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(bar(bl.xfull), kTileRows);  // one arrive per peer row: "my partial is in your buffer"
     mbar_init(bar(bl.xfree), kTileRows);  // one arrive per peer row: "your buffer is free again"
     mbar_init(bar(bl.drain), 1);
+    lo_flag[0] = 0;
+    lo_flag[1] = 0;
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -299,6 +307,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             ok = mbar_wait(bar(bl.p_ready + (t & 1)), (t >> 1) & 1, status);
             if (!ok) break;
             tc_fence_after();
+            const bool use_lo = lo_flag[t & 1] == static_cast<uint32_t>(t + 1);
             const uint32_t p_tm = tbase + ((t & 1) ? kS1 : kS0);
             // O[:, c..] += P V[:, c..]: two chunks per MMA (N=128) when they share
             // a ring slot, or (one chunk per slot) sit in adjacent slots
@@ -314,9 +323,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk)
                   umma_ts(tbase + c * kChunk, p_tm + kk * 8, sdesc_advance(bd, kk * 2048), idesc, acc0 | (kk > 0));
+                if (use_lo) {
 #pragma unroll
-                for (int kk = 0; kk < 8; ++kk)  // the P_lo term
-                  umma_ts(tbase + c * kChunk, p_tm + 64 + kk * 8, sdesc_advance(bd, kk * 2048), idesc, 1u);
+                  for (int kk = 0; kk < 8; ++kk)  // the P_lo term
+                    umma_ts(tbase + c * kChunk, p_tm + 64 + kk * 8, sdesc_advance(bd, kk * 2048), idesc, 1u);
+                }
                 umma_commit(bar(bl.empty + s));
                 it += 1;
                 c += 2;
@@ -333,9 +344,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk)
                   umma_ts(tbase + c * kChunk, p_tm + kk * 8, sdesc_advance(bd, kk * 2048), idesc_pv2, acc0 | (kk > 0));
+                if (use_lo) {
 #pragma unroll
-                for (int kk = 0; kk < 8; ++kk)  // the P_lo term
-                  umma_ts(tbase + c * kChunk, p_tm + 64 + kk * 8, sdesc_advance(bd, kk * 2048), idesc_pv2, 1u);
+                  for (int kk = 0; kk < 8; ++kk)  // the P_lo term
+                    umma_ts(tbase + c * kChunk, p_tm + 64 + kk * 8, sdesc_advance(bd, kk * 2048), idesc_pv2, 1u);
+                }
                 umma_commit(bar(bl.empty + s));
                 umma_commit(bar(bl.empty + s + 1));
                 it += 2;
@@ -344,9 +357,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk)
                   umma_ts(tbase + c * kChunk, p_tm + kk * 8, sdesc_advance(bd, kk * 2048), idesc_pv, acc0 | (kk > 0));
+                if (use_lo) {
 #pragma unroll
-                for (int kk = 0; kk < 8; ++kk)  // the P_lo term
-                  umma_ts(tbase + c * kChunk, p_tm + 64 + kk * 8, sdesc_advance(bd, kk * 2048), idesc_pv, 1u);
+                  for (int kk = 0; kk < 8; ++kk)  // the P_lo term
+                    umma_ts(tbase + c * kChunk, p_tm + 64 + kk * 8, sdesc_advance(bd, kk * 2048), idesc_pv, 1u);
+                }
                 umma_commit(bar(bl.empty + s));
                 it += 1;
                 c += 1;
@@ -462,6 +477,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           ls[i & 3] += s[i];
         }
         l_sum = l_sum * alpha + ((ls[0] + ls[1]) + (ls[2] + ls[3]));
+        // Rounding P to 16 bits perturbs each weight by up to 2^-8 of itself
+        // (bf16).  That matters only for rows where a few keys carry much of
+        // the weight (outputs that are sums of a few nearly cancelling V rows);
+        // in a row whose weight is spread, the rounding errors of many small
+        // terms average out far below the tolerance.  So the residual term is
+        // fed only when this tile's largest probability exceeds kLoFrac of the
+        // row's running sum (the final sum is larger still).
+        const bool warp_lo = __any_sync(0xffffffffu, ex2(m_tile - m_ref) > kLoFrac * l_sum);
         if (j >= 1) {
           // Wait for the previous P V MMA before touching TMEM again: storing P
           // while that MMA ran gave wrong O on GB300 (found by testing, single-
@@ -489,25 +512,43 @@ __global__ void __launch_bounds__(kThreads, 1)
         // P goes to TMEM as two terms of the input type, P = P_hi + P_lo with
         // P_lo the rounding residual of P_hi (columns 0..63 and 64..127 of the
         // score buffer); the P V product sums both, so the 16-bit operand costs
-        // about 2^-17 of P instead of 2^-9 (bf16), which matters for outputs
-        // that are sums of nearly cancelling V rows.
+        // about 2^-17 of P instead of 2^-8 (bf16).  A warp whose rows do not
+        // need the residual stores zeros there, in case another warp's rows
+        // make the MMA thread issue the residual product for the whole tile.
+        if (warp_lo) {
 #pragma unroll
-        for (int g = 0; g < 4; ++g) {
-          uint32_t hi[16], lo[16];
+          for (int g = 0; g < 4; ++g) {
+            uint32_t hi[16], lo[16];
 #pragma unroll
-          for (int e = 0; e < 16; ++e) {
-            const float p0 = s[32 * g + 2 * e], p1 = s[32 * g + 2 * e + 1];
-            hi[e] = pack2<BF16>(p0, p1);
-            const float2 h = unpack2<BF16>(hi[e]);
-            lo[e] = pack2<BF16>(p0 - h.x, p1 - h.y);
+            for (int e = 0; e < 16; ++e) {
+              const float p0 = s[32 * g + 2 * e], p1 = s[32 * g + 2 * e + 1];
+              hi[e] = pack2<BF16>(p0, p1);
+              const float2 h = unpack2<BF16>(hi[e]);
+              lo[e] = pack2<BF16>(p0 - h.x, p1 - h.y);
+            }
+            tmem_st16(tbase + lane_off + s_col + 16 * g, hi);
+            tmem_st16(tbase + lane_off + s_col + 64 + 16 * g, lo);
           }
-          tmem_st16(tbase + lane_off + s_col + 16 * g, hi);
-          tmem_st16(tbase + lane_off + s_col + 64 + 16 * g, lo);
+        } else {
+          uint32_t zero[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e) zero[e] = 0u;
+#pragma unroll
+          for (int g = 0; g < 4; ++g) {
+            uint32_t hi[16];
+#pragma unroll
+            for (int e = 0; e < 16; ++e) hi[e] = pack2<BF16>(s[32 * g + 2 * e], s[32 * g + 2 * e + 1]);
+            tmem_st16(tbase + lane_off + s_col + 16 * g, hi);
+            tmem_st16(tbase + lane_off + s_col + 64 + 16 * g, zero);
+          }
         }
         tmem_st_wait();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(bar(bl.p_ready + (t & 1)));
+        if (lane == 0) {
+          if (warp_lo) lo_flag[t & 1] = static_cast<uint32_t>(t + 1);
+          mbar_arrive(bar(bl.p_ready + (t & 1)));  // release: the flag store is visible first
+        }
       }
       if (!ok) break;
       // ---------------------------------------------------------- epilogue
@@ -599,6 +640,7 @@ cudaError_t launch_impl(const FwdParams& p_in, const FwdMaps& m, cudaStream_t st
 }  // namespace
 
 cudaError_t launch_fwd_main(const FwdParams& p, const FwdMaps& m, bool bf16, cudaStream_t s) {
+  if (fwd_pair_supported(p)) return launch_fwd_pair(p, m, bf16, s);
   if (p.n_chunks <= 4) return bf16 ? launch_impl<kSolo, true>(p, m, s) : launch_impl<kSolo, false>(p, m, s);
   if (p.n_chunks <= 8)
     return bf16 ? launch_impl<kRecompute, true>(p, m, s) : launch_impl<kRecompute, false>(p, m, s);

@@ -1,0 +1,492 @@
+// Fused attention forward, CTA-pair flavour, for D = 512.
+//
+// Same computation as fwd_main.cu (O = softmax(scale * Q K^T + bias) V and the
+// row logsumexp, keys streamed in tiles of 128 with an online softmax), laid
+// out for GB300's paired tensor cores.
+//
+// TMEM (512 fp32 columns per SM) cannot hold a 128 x 512 fp32 O accumulator
+// next to the score tiles, so O is split by D in two halves of 256 columns
+// (the FFPA pages' fine tiling along D, FFPA-Attn Performance Benchmarks page,
+// "Why the Trends Look Like This"), and the scores are reduced over the whole
+// of D by every CTA that owns a half.  In this flavour two CTAs that own the
+// SAME half of D for two different 128-row query tiles form a cluster and
+// issue their MMAs as one pair (tcgen05 cta_group::2, M = 256):
+//   * S = Q K^T: each CTA supplies its own query tile (A, resident) and HALF
+//     of the key tile (B, 64 keys x 512); each receives its 128 x 128 scores;
+//   * O += P V: each CTA supplies its own P (A, from its TMEM) and HALF of the
+//     V columns of the shared O half (B, 128 keys x 128); each accumulates its
+//     128 x 256 slice of O.
+// So every SM loads 96 KB per key tile instead of 192 KB, and its shared
+// memory serves 3 KB of MMA operands per 64-row-equivalent step instead of 4.
+//
+// Warp roles (256 threads per CTA): warps 0, 2, 3 TMA producers (each CTA
+// loads its own halves), warp 1 TMEM owner (both CTAs) and, in the first CTA
+// of the pair only, the MMA issuer; warps 4-7 softmax / correction / epilogue
+// for the CTA's own 128 query rows (thread = row = TMEM lane).
+//
+// Synchronisation across the pair: the issuing CTA's `full` barriers count
+// the bytes of both CTAs' loads; its commits arrive on the `empty`, `s_full`
+// and `o_ready` barriers of both CTAs; both CTAs' softmax warps arrive on the
+// issuing CTA's `p_ready`.  Every wait is bounded (see ptx.cuh).
+#include <type_traits>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace ffpa {
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kProducers = 3;                 // warps 0, 2 and 3
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kS0 = 256, kS1 = 384;      // TMEM columns of the two S/P buffers; O in [0, 256)
+constexpr float kRescaleLog2 = 8.0f;          // rescale O only when the max grows by > 2^8
+constexpr float kLoFrac = 1.0f / 64.0f;       // see fwd_main.cu: residual term of P only where needed
+constexpr int kChunks = 8;                    // D = 512: eight 64-column chunks
+constexpr int kQBytes = kChunks * kChunkBytes;        // resident query tile, 128 KB
+constexpr int kSlotBytes = 2 * kChunkBytes;           // ring slot: 4 half-key-tile K chunks or 2 V chunks
+constexpr int kHalfChunkBytes = kChunkBytes / 2;      // 64 keys x 64 columns
+
+struct Bars {
+  int full, empty, q_full, s_full, p_ready, o_ready, drain, count;
+};
+__host__ __device__ inline Bars bar_layout(int stages) {
+  Bars b;
+  b.full = 0;
+  b.empty = stages;
+  b.q_full = 2 * stages;
+  b.s_full = b.q_full + 1;   // 2
+  b.p_ready = b.s_full + 2;  // 2
+  b.o_ready = b.p_ready + 2;
+  b.drain = b.o_ready + 1;
+  b.count = b.drain + 1;
+  return b;
+}
+
+__host__ __device__ constexpr int smem_bytes(int stages) { return kQBytes + stages * kSlotBytes + 1024 + 1024; }
+
+template <bool BF16>
+__device__ __forceinline__ float2 unpack2(uint32_t w) {
+  if constexpr (BF16)
+    return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w));
+  else
+    return __half22float2(*reinterpret_cast<const __half2*>(&w));
+}
+
+template <bool BF16>
+__device__ __forceinline__ uint32_t pack2(float a, float b) {
+  if constexpr (BF16) {
+    __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+    return *reinterpret_cast<uint32_t*>(&h);
+  } else {
+    __half2 h = __floats2half2_rn(a, b);
+    return *reinterpret_cast<uint32_t*>(&h);
+  }
+}
+
+template <bool BF16>
+__global__ void __launch_bounds__(kThreads, 1)
+    fwd_pair_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_kh,
+                    const __grid_constant__ CUtensorMap map_v, const __grid_constant__ FwdParams p) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int stages = p.stages;
+  const Bars bl = bar_layout(stages);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kQBytes + stages * kSlotBytes);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + bl.count);
+  // lo_flag[t & 1] == t + 1: tile t carries the residual term of P.  Only the
+  // issuing CTA's copy is read; the peer's softmax warps write it remotely.
+  volatile uint32_t* lo_flag = tmem_slot + 1;
+  auto bar = [&](int i) { return smem_u32(&bars[i]); };
+  const uint32_t q_sm = smem_u32(smem), ring_sm = q_sm + kQBytes;
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const uint32_t rank = cluster_ctarank();  // 0 issues the pair's MMAs
+  const int cl = static_cast<int>(blockIdx.x) >> 1;
+  const int dh = cl & 1;                    // which half of D (O columns) the pair owns
+  const int npairs = (p.q_tiles + 1) >> 1;
+  const int pr = npairs - 1 - (cl >> 1);    // query-tile pair, heavy causal pairs first
+  const int q0 = (2 * pr + static_cast<int>(rank)) * kTileRows;
+  const int h = blockIdx.y, b = blockIdx.z;
+  const int kvh = h / p.group;
+  // Both CTAs sweep the key tiles that the pair's later query tile needs.
+  const int kv_end = p.causal ? min(p.Nkv, (2 * pr + 2) * kTileRows) : p.Nkv;
+  const int ntiles = (kv_end + kTileRows - 1) / kTileRows;
+  uint32_t* status = p.status;
+  // A barrier of the issuing CTA, addressed from this CTA.
+  auto lead = [&](int i) { return rank == 0 ? bar(i) : mapa(bar(i), 0); };
+
+  if (tid == 0) {
+    for (int i = 0; i < stages; ++i) {
+      mbar_init(bar(bl.full + i), 1);
+      mbar_init(bar(bl.empty + i), 1);
+    }
+    mbar_init(bar(bl.q_full), 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(bar(bl.s_full + i), 1);
+      mbar_init(bar(bl.p_ready + i), 8);  // four softmax warps in each CTA
+    }
+    mbar_init(bar(bl.o_ready), 1);
+    mbar_init(bar(bl.drain), 1);
+    lo_flag[0] = 0;
+    lo_flag[1] = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc_pair(smem_u32(tmem_slot), kTmemCols);
+    tmem_relinquish_pair();
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();
+  tc_fence_after();
+  const uint32_t tbase = *tmem_slot;
+
+  if (warp == 0 || warp == 2 || warp == 3) {
+    // ------------------------------------------------------------ TMA producers
+    // As in fwd_main.cu: producer pi issues every nprod-th slot load and waits
+    // only for its own slot; nprod <= stages keeps parity waits unambiguous.
+    // This CTA's slot s is free once the pair's MMAs reading it completed (the
+    // issuing CTA's commit arrives on empty[s] here); the bytes are counted on
+    // the issuing CTA's full[s], which that CTA arms for both halves.
+    const int nprod = min(kProducers, stages);
+    const int pi = (warp == 0) ? 0 : warp - 1;
+    if (lane == 0 && pi < nprod) {
+      tma_prefetch_desc(&map_q);
+      tma_prefetch_desc(&map_kh);
+      tma_prefetch_desc(&map_v);
+      if (pi == 0) {
+        if (rank == 0) mbar_expect_tx(bar(bl.q_full), 2 * kQBytes);
+        for (int c = 0; c < kChunks; ++c)
+          tma_load_4d_pair(q_sm + c * kChunkBytes, &map_q, lead(bl.q_full), c * kChunk, q0, h, b);
+      }
+      bool ok = true;
+      uint32_t it = 0;
+      auto slot = [&](bool is_k, int j) {
+        if (ok && static_cast<int>(it % nprod) == pi) {
+          const uint32_t s = it % stages, r = it / stages;
+          ok = mbar_wait(bar(bl.empty + s), (r & 1) ^ 1, status);
+          if (ok) {
+            if (rank == 0) mbar_expect_tx(bar(bl.full + s), 2 * kSlotBytes);
+            const uint32_t dst = ring_sm + s * kSlotBytes, fb = lead(bl.full + s);
+            if (is_k) {
+              // chunks 4m .. 4m+3 of this CTA's 64 keys of key tile j (m = slot parity within the tile)
+              const int m = j & 1, jt = j >> 1;
+              for (int i = 0; i < 4; ++i)
+                tma_load_4d_pair(dst + i * kHalfChunkBytes, &map_kh, fb, (4 * m + i) * kChunk,
+                                 jt * kTileRows + 64 * static_cast<int>(rank), kvh, b);
+            } else {
+              // this CTA's two V chunks of the pair's O half, key tile j
+              for (int i = 0; i < 2; ++i)
+                tma_load_4d_pair(dst + i * kChunkBytes, &map_v, fb, (4 * dh + 2 * static_cast<int>(rank) + i) * kChunk,
+                                 j * kTileRows, kvh, b);
+            }
+          }
+        }
+        ++it;
+      };
+      for (int j = 0; j <= ntiles && ok; ++j) {
+        if (j < ntiles) {
+          slot(true, 2 * j);
+          slot(true, 2 * j + 1);
+        }
+        if (j >= 1) slot(false, j - 1);
+      }
+      // Drain: wait for the last release of each slot whose last load was ours,
+      // so no commit arrival is in flight when the CTA exits.
+      for (uint32_t s = 0; s < static_cast<uint32_t>(stages) && s < it; ++s) {
+        const uint32_t last = s + ((it - 1 - s) / stages) * stages;
+        if (static_cast<int>(last % nprod) == pi) mbar_wait(bar(bl.empty + s), (last / stages) & 1, status);
+      }
+      if (pi == 0 && rank == 0) mbar_wait(bar(bl.q_full), 0, status);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer (first CTA of the pair)
+    if (lane == 0 && rank == 0) {
+      const uint32_t idesc_s = idesc_f16(BF16, 256, 128, false, false);  // 2 x 128 query rows x 128 keys
+      const uint32_t idesc_pv = idesc_f16(BF16, 256, 256, false, true);  // 2 x 128 query rows x 256 O columns
+      const uint64_t dq = sdesc_sw128(q_sm, 16, 1024);                    // Q chunks, K-major
+      const uint64_t dk = sdesc_sw128(ring_sm, 16, 1024);                 // half-tile K chunks, K-major
+      const uint64_t dv = sdesc_sw128(ring_sm, kChunkBytes, 1024);        // V chunks, MN-major
+      bool ok = mbar_wait(bar(bl.q_full), 0, status);
+      tc_fence_after();
+      uint32_t it = 0;
+      for (int j = 0; j <= ntiles && ok; ++j) {
+        if (j < ntiles) {
+          // S_j lands in the buffer that held P_{j-2}; it is issued once the
+          // P_{j-2} V product that read that buffer has completed.
+          const int t = j;
+          const uint32_t s_tm = tbase + ((t & 1) ? kS1 : kS0);
+          if (j >= 2) {
+            ok = mbar_wait(bar(bl.o_ready), (t - 2) & 1, status);
+            if (!ok) break;
+            tc_fence_after();
+          }
+          for (int m = 0; m < 2 && ok; ++m) {
+            const uint32_t s = it % stages;
+            ok = mbar_wait(bar(bl.full + s), (it / stages) & 1, status);
+            if (!ok) break;
+            tc_fence_after();
+            for (int i = 0; i < 4; ++i) {
+              const int c = 4 * m + i;
+              const uint64_t a = sdesc_advance(dq, c * kChunkBytes);
+              const uint64_t bd = sdesc_advance(dk, s * kSlotBytes + i * kHalfChunkBytes);
+#pragma unroll
+              for (int kk = 0; kk < 4; ++kk)
+                umma_ss_pair(s_tm, sdesc_advance(a, kk * 32), sdesc_advance(bd, kk * 32), idesc_s, (c | kk) != 0);
+            }
+            umma_commit_pair(bar(bl.empty + s), 3);
+            ++it;
+          }
+          if (!ok) break;
+          umma_commit_pair(bar(bl.s_full + (t & 1)), 3);
+        }
+        if (j >= 1) {
+          const int t = j - 1;
+          ok = mbar_wait(bar(bl.p_ready + (t & 1)), (t >> 1) & 1, status);
+          if (!ok) break;
+          tc_fence_after();
+          const bool use_lo = lo_flag[t & 1] == static_cast<uint32_t>(t + 1);
+          const uint32_t p_tm = tbase + ((t & 1) ? kS1 : kS0);
+          const uint32_t s = it % stages;
+          ok = mbar_wait(bar(bl.full + s), (it / stages) & 1, status);
+          if (!ok) break;
+          tc_fence_after();
+          const uint64_t bd = sdesc_advance(dv, s * kSlotBytes);
+          const uint32_t acc0 = t > 0 ? 1u : 0u;
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk)
+            umma_ts_pair(tbase, p_tm + kk * 8, sdesc_advance(bd, kk * 2048), idesc_pv, acc0 | (kk > 0));
+          if (use_lo) {
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk)  // the P_lo term
+              umma_ts_pair(tbase, p_tm + 64 + kk * 8, sdesc_advance(bd, kk * 2048), idesc_pv, 1u);
+          }
+          umma_commit_pair(bar(bl.empty + s), 3);
+          ++it;
+          umma_commit_pair(bar(bl.o_ready), 3);
+        }
+      }
+      umma_commit_pair(bar(bl.drain), 1);
+      mbar_wait(bar(bl.drain), 0, status);
+    }
+  } else if (warp >= 4) {
+    // ------------------------------------------------------------ softmax / correction / epilogue
+    const int r = tid - 128;  // query row within this CTA's tile == TMEM lane
+    const int row = q0 + r;
+    const uint32_t lane_off = static_cast<uint32_t>((warp - 4) * 32) << 16;
+    const float* bias_row = nullptr;
+    if (p.bias)
+      bias_row = p.bias + b * p.bias_sb + h * p.bias_sh + static_cast<int64_t>(min(row, p.Nq - 1)) * p.bias_sq;
+    constexpr float kLog2e = 1.4426950408889634f;
+    const uint32_t p_ready_lead0 = lead(bl.p_ready), p_ready_lead1 = lead(bl.p_ready + 1);
+    const uint32_t lo_flag_lead = rank == 0 ? 0u : mapa(smem_u32(const_cast<uint32_t*>(lo_flag)), 0);
+    bool ok = true;
+    float m_used = -INFINITY, l_sum = 0.f;
+    for (int j = 0; j < ntiles; ++j) {
+      const int t = j;
+      const uint32_t s_col = (t & 1) ? kS1 : kS0;
+      ok = __all_sync(0xffffffffu, mbar_wait(bar(bl.s_full + (t & 1)), (t >> 1) & 1, status));
+      if (!ok) break;
+      tc_fence_after();
+      float s[128];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint32_t v[32];
+        tmem_ld32(tbase + lane_off + s_col + c * 32, v);
+        tmem_ld_wait();
+#pragma unroll
+        for (int i = 0; i < 32; ++i) s[c * 32 + i] = __uint_as_float(v[i]);
+      }
+      const int kv0 = j * kTileRows;
+      const bool masked = (kv0 + kTileRows > p.Nkv) || (p.causal && kv0 + kTileRows - 1 > row);
+      const float c_scale = p.scale_log2;
+      if (bias_row) {
+#pragma unroll
+        for (int i = 0; i < 128; ++i)
+          s[i] = fmaf(__ldg(bias_row + static_cast<int64_t>(kv0 + min(i, p.Nkv - 1 - kv0)) * p.bias_sk), kLog2e,
+                      s[i] * c_scale);
+      } else {
+#pragma unroll
+        for (int i = 0; i < 128; ++i) s[i] *= c_scale;
+      }
+      if (masked) {
+#pragma unroll
+        for (int i = 0; i < 128; ++i) {
+          const int kv = kv0 + i;
+          if (kv >= p.Nkv || (p.causal && kv > row)) s[i] = -INFINITY;
+        }
+      }
+      float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+      for (int i = 0; i < 128; ++i) mx[i & 3] = fmaxf(mx[i & 3], s[i]);
+      const float m_tile = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+      float alpha = 1.f;
+      bool rescale = false;
+      if (m_used == -INFINITY) {
+        m_used = m_tile;
+      } else if (m_tile > m_used + kRescaleLog2) {
+        alpha = ex2(m_used - m_tile);
+        m_used = m_tile;
+        rescale = true;
+      }
+      const float m_ref = (m_used == -INFINITY) ? 0.f : m_used;
+      float ls[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int i = 0; i < 128; ++i) {
+        s[i] = ex2(s[i] - m_ref);  // P, in place
+        ls[i & 3] += s[i];
+      }
+      l_sum = l_sum * alpha + ((ls[0] + ls[1]) + (ls[2] + ls[3]));
+      const bool warp_lo = __any_sync(0xffffffffu, ex2(m_tile - m_ref) > kLoFrac * l_sum);
+      if (j >= 1) {
+        // P_j overwrites TMEM that the P_{j-1} V product may still read, and
+        // the correction below rewrites O: wait for that product first.
+        ok = __all_sync(0xffffffffu, mbar_wait(bar(bl.o_ready), (t - 1) & 1, status));
+        if (!ok) break;
+        tc_fence_after();
+      }
+      if (__any_sync(0xffffffffu, rescale) && j >= 1) {
+        for (int c = 0; c < 4; ++c) {  // O of this row *= alpha
+#pragma unroll
+          for (int hh = 0; hh < 2; ++hh) {
+            uint32_t v[32];
+            const uint32_t a = tbase + lane_off + c * kChunk + hh * 32;
+            tmem_ld32(a, v);
+            tmem_ld_wait();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * alpha);
+            tmem_st32(a, v);
+          }
+        }
+      }
+      // P as the rounded value (columns 0..63) and, where needed, its rounding
+      // residual (columns 64..127; zeros from warps that do not need it).
+      if (warp_lo) {
+#pragma unroll
+        for (int g = 0; g < 4; ++g) {
+          uint32_t hi[16], lo[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            const float p0 = s[32 * g + 2 * e], p1 = s[32 * g + 2 * e + 1];
+            hi[e] = pack2<BF16>(p0, p1);
+            const float2 hv = unpack2<BF16>(hi[e]);
+            lo[e] = pack2<BF16>(p0 - hv.x, p1 - hv.y);
+          }
+          tmem_st16(tbase + lane_off + s_col + 16 * g, hi);
+          tmem_st16(tbase + lane_off + s_col + 64 + 16 * g, lo);
+        }
+      } else {
+        uint32_t zero[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) zero[e] = 0u;
+#pragma unroll
+        for (int g = 0; g < 4; ++g) {
+          uint32_t hi[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e) hi[e] = pack2<BF16>(s[32 * g + 2 * e], s[32 * g + 2 * e + 1]);
+          tmem_st16(tbase + lane_off + s_col + 16 * g, hi);
+          tmem_st16(tbase + lane_off + s_col + 64 + 16 * g, zero);
+        }
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        const uint32_t pr_bar = (t & 1) ? p_ready_lead1 : p_ready_lead0;
+        if (rank == 0) {
+          if (warp_lo) lo_flag[t & 1] = static_cast<uint32_t>(t + 1);
+          mbar_arrive(pr_bar);
+        } else {
+          if (warp_lo) st_cluster_u32(lo_flag_lead + 4 * (t & 1), static_cast<uint32_t>(t + 1));
+          mbar_arrive_remote(pr_bar);  // release.cluster: the flag store is visible first
+        }
+      }
+    }
+    if (ok) {
+      // ---------------------------------------------------------- epilogue
+      ok = __all_sync(0xffffffffu, mbar_wait(bar(bl.o_ready), (ntiles - 1) & 1, status));
+      if (ok) {
+        tc_fence_after();
+        const float inv_l = l_sum > 0.f ? 1.f / l_sum : 0.f;
+        typedef typename std::conditional<BF16, __nv_bfloat16, __half>::type T;
+        T* orow = reinterpret_cast<T*>(p.out) + b * p.o_sb + h * p.o_sh + static_cast<int64_t>(row) * p.o_sn;
+        for (int c = 0; c < 4; ++c) {
+#pragma unroll
+          for (int hh = 0; hh < 2; ++hh) {
+            uint32_t v[32];
+            tmem_ld32(tbase + lane_off + c * kChunk + hh * 32, v);
+            tmem_ld_wait();
+            if (row < p.Nq) {
+              uint4* dst = reinterpret_cast<uint4*>(orow + (4 * dh + c) * kChunk + hh * 32);
+#pragma unroll
+              for (int g = 0; g < 4; ++g) {
+                uint4 w;
+                w.x = pack2<BF16>(__uint_as_float(v[8 * g + 0]) * inv_l, __uint_as_float(v[8 * g + 1]) * inv_l);
+                w.y = pack2<BF16>(__uint_as_float(v[8 * g + 2]) * inv_l, __uint_as_float(v[8 * g + 3]) * inv_l);
+                w.z = pack2<BF16>(__uint_as_float(v[8 * g + 4]) * inv_l, __uint_as_float(v[8 * g + 5]) * inv_l);
+                w.w = pack2<BF16>(__uint_as_float(v[8 * g + 6]) * inv_l, __uint_as_float(v[8 * g + 7]) * inv_l);
+                dst[g] = w;
+              }
+            }
+          }
+        }
+        if (dh == 0 && p.lse && row < p.Nq) {
+          constexpr float kLn2 = 0.6931471805599453f;
+          p.lse[(static_cast<int64_t>(b) * p.Hq + h) * p.Nq + row] =
+              l_sum > 0.f ? (m_used + __log2f(l_sum)) * kLn2 : -INFINITY;
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc_pair(tbase, kTmemCols);
+  }
+}
+
+template <bool BF16>
+cudaError_t launch_impl(const FwdParams& p_in, const FwdMaps& m, cudaStream_t st) {
+  FwdParams p = p_in;
+  constexpr int kMaxSmem = 232448;  // 227 KB opt-in per block
+  int stages = (kMaxSmem - smem_bytes(0)) / kSlotBytes;
+  stages = min(stages, 4);
+  if (stages < 2) return cudaErrorInvalidConfiguration;
+  p.stages = stages;
+  p.slot_chunks = 2;
+  const int smem = smem_bytes(stages);
+  auto kern = fwd_pair_kernel<BF16>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  const int npairs = (p.q_tiles + 1) / 2;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(4 * npairs, p.Hq, p.B);  // (pair rank, D half, query-tile pair)
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  timing_mark(st);
+  e = cudaLaunchKernelEx(&cfg, kern, m.q, m.k_half, m.v, p);
+  timing_mark(st);
+  return e;
+}
+
+}  // namespace
+
+bool fwd_pair_supported(const FwdParams& p) { return p.n_chunks == kChunks; }
+
+cudaError_t launch_fwd_pair(const FwdParams& p, const FwdMaps& m, bool bf16, cudaStream_t s) {
+  return bf16 ? launch_impl<true>(p, m, s) : launch_impl<false>(p, m, s);
+}
+
+}  // namespace ffpa

@@ -31,6 +31,7 @@ struct FwdParams {
 
 struct FwdMaps {
   CUtensorMap q, k, v;  // 4-D {D, N, H, B}, box {64, 128, 1, 1}, 128-byte swizzle
+  CUtensorMap k_half;   // K with box {64, 64, 1, 1}: one CTA's half of a key tile in the CTA-pair kernel
 };
 
 // Decode (small Nq) path.
@@ -92,6 +93,9 @@ struct BwdMaps {
 bool dtype_is_bf16(int dtype);
 
 cudaError_t launch_fwd_main(const FwdParams& p, const FwdMaps& m, bool bf16, cudaStream_t s);
+// CTA-pair forward (fwd_pair.cu): D = 512.
+bool fwd_pair_supported(const FwdParams& p);
+cudaError_t launch_fwd_pair(const FwdParams& p, const FwdMaps& m, bool bf16, cudaStream_t s);
 cudaError_t launch_fwd_decode(const DecodeParams& p, bool bf16, cudaStream_t s);
 // Same kernels, partials in the library's fixed device array (no allocation).
 cudaError_t launch_fwd_decode_noalloc(const DecodeParams& p, bool bf16, cudaStream_t s);

@@ -53,9 +53,9 @@ def gpu_fwd(inp, causal, scale):
     return out, lse
 
 
-def check_fwd_full(B, Hq, Hkv, Nq, Nkv, D, dtype, causal=False, bias=False, seed=0):
+def check_fwd_full(B, Hq, Hkv, Nq, Nkv, D, dtype, causal=False, bias=False, seed=0, scale=None):
     inp = make_inputs(B, Hq, Hkv, Nq, Nkv, D, dtype, bias=bias, seed=seed)
-    scale = D ** -0.5
+    scale = D ** -0.5 if scale is None else scale
     out, lse = gpu_fwd(inp, causal, scale)
     o_ref, lse_ref = ref.attn_fwd(f64(inp.q), f64(inp.k), f64(inp.v), bias=f64(inp.bias), causal=causal,
                                   scale=scale)
@@ -64,10 +64,10 @@ def check_fwd_full(B, Hq, Hkv, Nq, Nkv, D, dtype, causal=False, bias=False, seed
     assert_close(lse.cpu().numpy(), lse_ref, LSE_ATOL, 0.0, "lse")
 
 
-def check_fwd_sampled(B, Hq, Hkv, Nq, Nkv, D, dtype, causal=False, bias=False, rows=64, seed=0):
+def check_fwd_sampled(B, Hq, Hkv, Nq, Nkv, D, dtype, causal=False, bias=False, rows=64, seed=0, scale=None):
     """Large shapes: the oracle computes `rows` seeded query rows per head, one by one."""
     inp = make_inputs(B, Hq, Hkv, Nq, Nkv, D, dtype, bias=bias, seed=seed)
-    scale = D ** -0.5
+    scale = D ** -0.5 if scale is None else scale
     out, lse = gpu_fwd(inp, causal, scale)
     out = out.float().cpu().numpy()
     lse = lse.cpu().numpy()

@@ -45,6 +45,19 @@ def test_fused_small(B, Hq, Hkv, Nq, Nkv, D, dtype, causal, bias):
     check_fwd_full(B, Hq, Hkv, Nq, Nkv, D, dtype, causal=causal, bias=bias)
 
 
+@pytest.mark.parametrize("sharp,dtype", [(1.5, BF), (2.0, BF), (3.0, BF), (2.0, FP), (6.0, FP)])
+def test_sharp_softmax(sharp, dtype):
+    # Scores with standard deviation `sharp`: from rows whose weight is spread
+    # over many keys to rows that a few keys dominate, so key tiles that feed P
+    # as one 16-bit term and tiles that add its rounding residual mix within a
+    # row and within a tile.
+    check_fwd_full(1, 2, 2, 700, 1100, 512, dtype, scale=sharp * 512 ** -0.5)
+
+
+def test_sharp_softmax_8k_bf16():
+    check_fwd_sampled(1, 2, 2, 8192, 8192, 512, BF, scale=2.0 * 512 ** -0.5)
+
+
 def test_fused_query_bias_small():
     # [1, 1, Nq, Nkv] per-query bias
     check_fwd_full(1, 2, 2, 150, 260, 512, torch.bfloat16, bias="query")
