@@ -297,7 +297,9 @@ extern "C" int ffpa_bwd(const ffpa_tensor_t* q, const ffpa_tensor_t* k, const ff
   p.status = status;
   BwdMaps m;
   if ((rc = encode_map(&m.q, q)) || (rc = encode_map(&m.k, k)) || (rc = encode_map(&m.v, v)) ||
-      (rc = encode_map(&m.dout, dout)))
+      (rc = encode_map(&m.dout, dout)) || (rc = encode_map(&m.q_half, q, kTileRows / 2)) ||
+      (rc = encode_map(&m.k_half, k, kTileRows / 2)) || (rc = encode_map(&m.v_half, v, kTileRows / 2)) ||
+      (rc = encode_map(&m.dout_half, dout, kTileRows / 2)))
     return rc;
   const size_t rows = (size_t)c.B * c.Hq * c.Nq;
   timing_begin();

@@ -825,13 +825,18 @@ cudaError_t launch_mode(const BwdParams& p_in, const BwdMaps& m, cudaStream_t st
   return e;
 }
 
-template <int FL, bool BF16>
-cudaError_t launch_all(const BwdParams& p, const BwdMaps& m, cudaStream_t st) {
+template <bool BF16>
+cudaError_t launch_preprocess(const BwdParams& p, cudaStream_t st) {
   const int64_t rows = static_cast<int64_t>(p.B) * p.Hq * p.Nq;
   timing_mark(st);
   bwd_preprocess_kernel<BF16><<<static_cast<unsigned>((rows + 7) / 8), 256, 0, st>>>(p);
   timing_mark(st);
-  cudaError_t e = cudaGetLastError();
+  return cudaGetLastError();
+}
+
+template <int FL, bool BF16>
+cudaError_t launch_all(const BwdParams& p, const BwdMaps& m, cudaStream_t st) {
+  cudaError_t e = launch_preprocess<BF16>(p, st);
   if (e != cudaSuccess) return e;
   if ((e = launch_mode<kDV, FL, BF16>(p, m, st)) != cudaSuccess) return e;
   if ((e = launch_mode<kDK, FL, BF16>(p, m, st)) != cudaSuccess) return e;
@@ -841,6 +846,10 @@ cudaError_t launch_all(const BwdParams& p, const BwdMaps& m, cudaStream_t st) {
 }  // namespace
 
 cudaError_t launch_bwd(const BwdParams& p, const BwdMaps& m, bool bf16, cudaStream_t s) {
+  if (bwd_pair_supported(p)) {
+    cudaError_t e = bf16 ? launch_preprocess<true>(p, s) : launch_preprocess<false>(p, s);
+    return e != cudaSuccess ? e : launch_bwd_pair(p, m, bf16, s);
+  }
   if (p.n_chunks <= 4) return bf16 ? launch_all<kSolo, true>(p, m, s) : launch_all<kSolo, false>(p, m, s);
   if (p.n_chunks <= 8) return bf16 ? launch_all<kRecompute, true>(p, m, s) : launch_all<kRecompute, false>(p, m, s);
   return bf16 ? launch_all<kExchange, true>(p, m, s) : launch_all<kExchange, false>(p, m, s);

@@ -87,7 +87,8 @@ struct BwdParams {
 };
 
 struct BwdMaps {
-  CUtensorMap q, k, v, dout;
+  CUtensorMap q, k, v, dout;                  // box {64, 128, 1, 1}
+  CUtensorMap q_half, k_half, v_half, dout_half;  // box {64, 64, 1, 1}: one CTA's half of a column tile (CTA pair)
 };
 
 bool dtype_is_bf16(int dtype);
@@ -102,6 +103,9 @@ cudaError_t launch_fwd_decode_noalloc(const DecodeParams& p, bool bf16, cudaStre
 size_t decode_scratch_bytes(const DecodeParams& p);
 size_t decode_noalloc_capacity_bytes();
 cudaError_t launch_bwd(const BwdParams& p, const BwdMaps& m, bool bf16, cudaStream_t s);
+// CTA-pair dV, dK, dQ kernels (bwd_pair.cu): D = 512; the preprocess runs first.
+bool bwd_pair_supported(const BwdParams& p);
+cudaError_t launch_bwd_pair(const BwdParams& p, const BwdMaps& m, bool bf16, cudaStream_t s);
 
 uint32_t* device_status_word();  // per current device
 

@@ -28,6 +28,13 @@ BF, FP = torch.bfloat16, torch.float16
     (1, 1, 1, 17, 140, 768, BF, False, True),
     (1, 2, 2, 5, 200, 512, BF, False, False),
     (1, 4, 1, 384, 384, 640, FP, True, True),
+    # D = 512 runs as CTA pairs over neighbouring stationary tiles: odd tile
+    # counts (the last pair's second tile is empty), causal with Nq != Nkv,
+    # GQA with bias, a single query row
+    (1, 4, 2, 300, 500, 512, BF, True, True),
+    (1, 2, 1, 500, 300, 512, FP, True, False),
+    (2, 2, 2, 384, 384, 512, BF, False, False),
+    (1, 1, 1, 1, 129, 512, BF, False, False),
 ])
 def test_bwd_small(B, Hq, Hkv, Nq, Nkv, D, dtype, causal, bias):
     check_bwd_full(B, Hq, Hkv, Nq, Nkv, D, dtype, causal=causal, bias=bias)
