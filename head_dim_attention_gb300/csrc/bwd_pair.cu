@@ -19,11 +19,13 @@
 // pair instead of twice, and its shared memory serves half of each B operand.
 //
 // TMEM per CTA: gradient [0, 256), X1 [256, 384), X2 [384, 512).  Shared
-// memory: the first stationary operand (K for dV/dK, Q for dQ) resident,
-// 128 KB; a ring of 32 KB slots holding four 64-row column half-chunks, one
-// 128-row chunk of the second stationary operand (V for dK, dO for dQ, which
-// does not fit resident) next to the matching column half-chunk, or the two
-// gradient-operand chunks of this CTA.
+// memory, dV: K resident (128 KB) and a ring of three 32 KB slots, each
+// holding four 64-row column half-chunks or this CTA's two gradient-operand
+// chunks.  dK and dQ need two stationary operands (K and V, or Q and dO) that
+// do not both fit, and streaming one of them through a short ring left the
+// second product waiting on loads; so both stream, through four 48 KB slots
+// that each hold two 128-row stationary chunks next to the matching two
+// column half-chunks (or the two gradient-operand chunks).
 // Warp roles as in bwd.cu; the first CTA of the pair issues the MMAs.
 #include <type_traits>
 
@@ -40,9 +42,10 @@ constexpr int kProducers = 3;  // warps 0, 2 and 3
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kX1 = 256, kX2 = 384;
 constexpr int kChunks = 8;                       // D = 512
-constexpr int kResBytes = kChunks * kChunkBytes;  // resident stationary operand, 128 KB
-constexpr int kSlotBytes = 2 * kChunkBytes;
 constexpr int kHalfChunkBytes = kChunkBytes / 2;  // 64 rows x 64 columns
+// dV: resident K and 32 KB slots; dK/dQ: nothing resident and 48 KB slots
+__host__ __device__ constexpr int res_bytes(int mode) { return mode == kDV ? kChunks * kChunkBytes : 0; }
+__host__ __device__ constexpr int slot_bytes(int mode) { return mode == kDV ? 2 * kChunkBytes : 3 * kChunkBytes; }
 constexpr float kLog2e = 1.4426950408889634f;
 
 struct Bars {
@@ -61,7 +64,9 @@ __host__ __device__ inline Bars bar_layout(int stages) {
   b.count = b.drain + 1;
   return b;
 }
-__host__ __device__ constexpr int smem_bytes(int stages) { return kResBytes + stages * kSlotBytes + 1024 + 1024; }
+__host__ __device__ constexpr int smem_bytes(int mode, int stages) {
+  return res_bytes(mode) + stages * slot_bytes(mode) + 1024 + 1024;
+}
 
 template <bool BF16>
 __device__ __forceinline__ uint32_t pack2(float a, float b) {
@@ -142,6 +147,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int stages = p.stages;
+  constexpr bool RES = (MODE == kDV);  // A1 resident
+  constexpr int kResBytes = res_bytes(MODE);
+  constexpr int kSlotBytes = slot_bytes(MODE);
   const Bars bl = bar_layout(stages);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kResBytes + stages * kSlotBytes);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + bl.count);
@@ -155,7 +163,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint32_t* status = p.status;
   auto lead = [&](int i) { return rank == 0 ? bar(i) : mapa(bar(i), 0); };
 
-  // resident A1, streamed A2 (stationary); column operands: half-row B1, B2; gradient B3
+  // stationary A1, A2 (A1 resident for dV); column operands: half-row B1, B2; gradient B3
   const CUtensorMap* mA1 = (MODE == kDQ) ? &map_q : &map_k;
   const CUtensorMap* mA2 = (MODE == kDQ) ? &map_do : &map_v;
   const CUtensorMap* mB1 = (MODE == kDQ) ? &map_kh : &map_qh;
@@ -198,16 +206,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_prefetch_desc(mB1);
       tma_prefetch_desc(mB2);
       tma_prefetch_desc(mB3);
-      if (pi == 0) {
+      if (RES && pi == 0) {
         if (rank == 0) mbar_expect_tx(bar(bl.a_full), 2 * kResBytes);
         for (int c = 0; c < kChunks; ++c)
           tma_load_4d_pair(a_sm + c * kChunkBytes, mA1, lead(bl.a_full), c * kChunk, g.s_row0, g.s_head, g.b);
       }
       bool ok = true;
       uint32_t it = 0;
-      // kind 0: column half-chunks 4m..4m+3 of B (m = 0, 1); kind 1: A2 chunk m
-      // with B2 half-chunk m; kind 2: this CTA's two gradient-operand chunks
-      auto slot = [&](int kind, const CUtensorMap* mb, int m, int c) {
+      // kind 0: column half-chunks 4m..4m+3 of B (m = 0, 1); kind 1: stationary
+      // chunks 2m, 2m+1 of A with column half-chunks 2m, 2m+1 of B (m = 0..3);
+      // kind 2: this CTA's two gradient-operand chunks
+      auto slot = [&](int kind, const CUtensorMap* ma, const CUtensorMap* mb, int m, int c) {
         if (ok && static_cast<int>(it % nprod) == pi) {
           const uint32_t s = it % stages, r = it / stages;
           ok = mbar_wait(bar(bl.empty + s), (r & 1) ^ 1, status);
@@ -221,9 +230,12 @@ __global__ void __launch_bounds__(kThreads, 1)
               for (int i = 0; i < 4; ++i)
                 tma_load_4d_pair(dst + i * kHalfChunkBytes, mb, fb, (4 * m + i) * kChunk, half_row, ch, g.b);
             } else if (kind == 1) {
-              if (rank == 0) mbar_expect_tx(bar(bl.full + s), 2 * (kChunkBytes + kHalfChunkBytes));
-              tma_load_4d_pair(dst, mA2, fb, m * kChunk, g.s_row0, g.s_head, g.b);
-              tma_load_4d_pair(dst + kChunkBytes, mb, fb, m * kChunk, half_row, ch, g.b);
+              if (rank == 0) mbar_expect_tx(bar(bl.full + s), 2 * 2 * (kChunkBytes + kHalfChunkBytes));
+              for (int i = 0; i < 2; ++i) {
+                tma_load_4d_pair(dst + i * kChunkBytes, ma, fb, (2 * m + i) * kChunk, g.s_row0, g.s_head, g.b);
+                tma_load_4d_pair(dst + 2 * kChunkBytes + i * kHalfChunkBytes, mb, fb, (2 * m + i) * kChunk, half_row,
+                                 ch, g.b);
+              }
             } else {
               if (rank == 0) mbar_expect_tx(bar(bl.full + s), 2 * 2 * kChunkBytes);
               for (int i = 0; i < 2; ++i)
@@ -237,11 +249,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       // Loads follow the MMA thread's order of use: X1 and X2 of column 0, then
       // for each column c: X1 of c + 1, the gradient of c, X2 of c + 1.
       auto x1_loads = [&](int c) {
-        slot(0, mB1, 0, c);
-        slot(0, mB1, 1, c);
+        if (RES) {
+          slot(0, nullptr, mB1, 0, c);
+          slot(0, nullptr, mB1, 1, c);
+        } else {
+          for (int m = 0; m < kChunks / 2; ++m) slot(1, mA1, mB1, m, c);
+        }
       };
       auto x2_loads = [&](int c) {
-        for (int m = 0; m < kChunks; ++m) slot(1, mB2, m, c);
+        for (int m = 0; m < kChunks / 2; ++m) slot(1, mA2, mB2, m, c);
       };
       if (g.ncols > 0) {
         x1_loads(0);
@@ -249,14 +265,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       for (int c = 0; c < g.ncols && ok; ++c) {
         if (c + 1 < g.ncols) x1_loads(c + 1);
-        slot(2, nullptr, 0, c);
+        slot(2, nullptr, nullptr, 0, c);
         if (two && c + 1 < g.ncols) x2_loads(c + 1);
       }
       for (uint32_t s = 0; s < static_cast<uint32_t>(stages) && s < it; ++s) {
         const uint32_t last = s + ((it - 1 - s) / stages) * stages;
         if (static_cast<int>(last % nprod) == pi) mbar_wait(bar(bl.empty + s), (last / stages) & 1, status);
       }
-      if (pi == 0 && rank == 0) mbar_wait(bar(bl.a_full), 0, status);
+      if (RES && pi == 0 && rank == 0) mbar_wait(bar(bl.a_full), 0, status);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer (first CTA of the pair)
@@ -266,7 +282,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t da = sdesc_sw128(a_sm, 16, 1024);                     // resident A1, K-major
       const uint64_t dk = sdesc_sw128(ring_sm, 16, 1024);                  // ring tiles, K-major
       const uint64_t dm = sdesc_sw128(ring_sm, kChunkBytes, 1024);         // ring tiles, MN-major
-      bool ok = mbar_wait(bar(bl.a_full), 0, status);
+      bool ok = RES ? mbar_wait(bar(bl.a_full), 0, status) : true;
       tc_fence_after();
       uint32_t it = 0;
       auto wait_slot = [&]() -> uint32_t {
@@ -276,8 +292,29 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         return s;
       };
+      // X (+)= A B^T over the eight chunks, A and B streamed: chunks 2m, 2m+1 of
+      // both in slot m
+      auto product_streamed = [&](uint32_t x_tm) {
+        for (int m = 0; m < kChunks / 2 && ok; ++m) {
+          const uint32_t s = wait_slot();
+          if (!ok) return;
+          for (int i = 0; i < 2; ++i) {
+            const int c = 2 * m + i;
+            const uint64_t a = sdesc_advance(dk, s * kSlotBytes + i * kChunkBytes);
+            const uint64_t bd = sdesc_advance(dk, s * kSlotBytes + 2 * kChunkBytes + i * kHalfChunkBytes);
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+              umma_ss_pair(x_tm, sdesc_advance(a, kk * 32), sdesc_advance(bd, kk * 32), idesc_x, (c | kk) != 0);
+          }
+          umma_commit_pair(bar(bl.empty + s), 3);
+        }
+      };
       // X1 (+)= A1 B1^T over the eight chunks: B1 half-chunks in two slots
       auto product1 = [&]() {
+        if (!RES) {
+          product_streamed(tbase + kX1);
+          return;
+        }
         for (int m = 0; m < 2 && ok; ++m) {
           const uint32_t s = wait_slot();
           if (!ok) return;
@@ -292,19 +329,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           umma_commit_pair(bar(bl.empty + s), 3);
         }
       };
-      // X2 (+)= A2 B2^T: A2 chunk m and B2 half-chunk m share a slot
-      auto product2 = [&]() {
-        for (int m = 0; m < kChunks && ok; ++m) {
-          const uint32_t s = wait_slot();
-          if (!ok) return;
-          const uint64_t a = sdesc_advance(dk, s * kSlotBytes);
-          const uint64_t bd = sdesc_advance(dk, s * kSlotBytes + kChunkBytes);
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk)
-            umma_ss_pair(tbase + kX2, sdesc_advance(a, kk * 32), sdesc_advance(bd, kk * 32), idesc_x, (m | kk) != 0);
-          umma_commit_pair(bar(bl.empty + s), 3);
-        }
-      };
+      auto product2 = [&]() { product_streamed(tbase + kX2); };
       // X1 is read only by the elementwise warps, which free it before computing
       // P and dS; X2 ends up holding P or dS, the A operand of the gradient.  So
       // the next column's X1 product overlaps this column's elementwise work,
@@ -545,12 +570,12 @@ template <int MODE, bool BF16>
 cudaError_t launch_mode(const BwdParams& p_in, const BwdMaps& m, cudaStream_t st) {
   BwdParams p = p_in;
   constexpr int kMaxSmem = 232448;
-  int stages = (kMaxSmem - smem_bytes(0)) / kSlotBytes;
+  int stages = (kMaxSmem - smem_bytes(MODE, 0)) / slot_bytes(MODE);
   stages = min(stages, 4);
   if (stages < 2) return cudaErrorInvalidConfiguration;
   p.stages = stages;
-  p.slot_chunks = 2;
-  const int smem = smem_bytes(stages);
+  p.slot_chunks = slot_bytes(MODE) / kChunkBytes;
+  const int smem = smem_bytes(MODE, stages);
   auto kern = bwd_pair_kernel<MODE, BF16>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
