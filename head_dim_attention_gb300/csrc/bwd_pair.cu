@@ -309,31 +309,33 @@ __global__ void __launch_bounds__(kThreads, 1)
           umma_commit_pair(bar(bl.empty + s), 3);
         }
       };
-      // X1 (+)= A1 B1^T over the eight chunks: B1 half-chunks in two slots
+      // X1 (+)= A1 B1^T over the eight chunks: with A1 resident (dV), B1
+      // half-chunks in two slots; otherwise both streamed
       auto product1 = [&]() {
-        if (!RES) {
+        if constexpr (!RES) {
           product_streamed(tbase + kX1);
-          return;
-        }
-        for (int m = 0; m < 2 && ok; ++m) {
-          const uint32_t s = wait_slot();
-          if (!ok) return;
-          for (int i = 0; i < 4; ++i) {
-            const int c = 4 * m + i;
-            const uint64_t a = sdesc_advance(da, c * kChunkBytes);
-            const uint64_t bd = sdesc_advance(dk, s * kSlotBytes + i * kHalfChunkBytes);
+        } else {
+          for (int m = 0; m < 2 && ok; ++m) {
+            const uint32_t s = wait_slot();
+            if (!ok) return;
+            for (int i = 0; i < 4; ++i) {
+              const int c = 4 * m + i;
+              const uint64_t a = sdesc_advance(da, c * kChunkBytes);
+              const uint64_t bd = sdesc_advance(dk, s * kSlotBytes + i * kHalfChunkBytes);
 #pragma unroll
-            for (int kk = 0; kk < 4; ++kk)
-              umma_ss_pair(tbase + kX1, sdesc_advance(a, kk * 32), sdesc_advance(bd, kk * 32), idesc_x, (c | kk) != 0);
+              for (int kk = 0; kk < 4; ++kk)
+                umma_ss_pair(tbase + kX1, sdesc_advance(a, kk * 32), sdesc_advance(bd, kk * 32), idesc_x,
+                             (c | kk) != 0);
+            }
+            umma_commit_pair(bar(bl.empty + s), 3);
           }
-          umma_commit_pair(bar(bl.empty + s), 3);
         }
       };
       auto product2 = [&]() { product_streamed(tbase + kX2); };
       // X1 is read only by the elementwise warps, which free it before computing
       // P and dS; X2 ends up holding P or dS, the A operand of the gradient.  So
       // the next column's X1 product overlaps this column's elementwise work,
-      // and X2 is rewritten only after the gradient MMAs reading it completed.
+      // and X2 is rewritten by the next product right after the gradient MMAs.
       if (g.ncols > 0) {
         product1();
         if (two && ok) product2();
@@ -364,9 +366,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         umma_commit_pair(bar(bl.acc_ready), 3);
         if (more && two) {
-          ok = mbar_wait(bar(bl.acc_ready), c & 1, status);
-          if (!ok) break;
-          tc_fence_after();
+          // X2 still holds dS of this column, read by the gradient MMAs just
+          // issued; MMAs issued by one thread execute in issue order, so the
+          // next column's X2 product may follow them without a wait.
           product2();
           if (!ok) break;
           umma_commit_pair(bar(bl.x_full), 3);

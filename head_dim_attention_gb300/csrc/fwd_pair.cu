@@ -213,15 +213,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t it = 0;
       for (int j = 0; j <= ntiles && ok; ++j) {
         if (j < ntiles) {
-          // S_j lands in the buffer that held P_{j-2}; it is issued once the
-          // P_{j-2} V product that read that buffer has completed.
+          // S_j lands in the buffer that held P_{j-2}, which the P_{j-2} V
+          // product (issued earlier by this thread) reads.  MMAs issued by one
+          // thread form an implicitly pipelined sequence that executes in issue
+          // order, so no wait is needed between that read and this write.
           const int t = j;
           const uint32_t s_tm = tbase + ((t & 1) ? kS1 : kS0);
-          if (j >= 2) {
-            ok = mbar_wait(bar(bl.o_ready), (t - 2) & 1, status);
-            if (!ok) break;
-            tc_fence_after();
-          }
           for (int m = 0; m < 2 && ok; ++m) {
             const uint32_t s = it % stages;
             ok = mbar_wait(bar(bl.full + s), (it / stages) & 1, status);
