@@ -430,22 +430,37 @@ __global__ void __launch_bounds__(kThreads, 1)
       else
         plain = srow < p.Nkv && cr0 + kTileRows <= p.Nq && (!p.causal || srow <= cr0);
       plain = __all_sync(0xffffffffu, plain) && p.bias == nullptr;
+      // Copy the raw scores out of TMEM first and free X1 at once, so the next
+      // column's score product runs while this thread computes the exponentials
+      // (they are limited by the special-function unit's throughput).
+      uint32_t raw0[32], raw1[32], raw2[32], raw3[32];
+      tmem_ld32(tbase + lane_off + kX1, raw0);
+      tmem_ld32(tbase + lane_off + kX1 + 32, raw1);
+      tmem_ld32(tbase + lane_off + kX1 + 64, raw2);
+      tmem_ld32(tbase + lane_off + kX1 + 96, raw3);
+      tmem_ld_wait();
+#pragma unroll
+      for (int e = 0; e < 32; ++e) {
+        pv[e] = __uint_as_float(raw0[e]);
+        pv[32 + e] = __uint_as_float(raw1[e]);
+        pv[64 + e] = __uint_as_float(raw2[e]);
+        pv[96 + e] = __uint_as_float(raw3[e]);
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) arrive_lead(x1_free_lead);
       if (plain) {
 #pragma unroll
         for (int c4 = 0; c4 < 4; ++c4) {
-          float f[32];
-          chunk(kX1, c4, f);
 #pragma unroll
           for (int e = 0; e < 32; ++e) {
             const float l2 = (MODE == kDQ) ? lse2_row : __shfl_sync(0xffffffffu, l2v[c4], e);
-            pv[c4 * 32 + e] = ex2(fmaf(f[e], p.scale_log2, -l2));
+            pv[c4 * 32 + e] = ex2(fmaf(pv[c4 * 32 + e], p.scale_log2, -l2));
           }
         }
       } else {
 #pragma unroll
         for (int c4 = 0; c4 < 4; ++c4) {
-          float f[32];
-          chunk(kX1, c4, f);
 #pragma unroll
           for (int e = 0; e < 32; ++e) {
             const int ci = c4 * 32 + e;
@@ -464,7 +479,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             const int hq = (MODE == kDQ) ? g.h : ch;
             const bool valid = i < p.Nq && j < p.Nkv && !(p.causal && j > i) && l2 > -INFINITY;
-            float xv = fmaf(f[e], p.scale_log2, -l2);
+            float xv = fmaf(pv[ci], p.scale_log2, -l2);
             if (p.bias)
               xv = fmaf(__ldg(p.bias + g.b * p.bias_sb + hq * p.bias_sh + static_cast<int64_t>(ic) * p.bias_sq +
                               static_cast<int64_t>(min(j, p.Nkv - 1)) * p.bias_sk),
@@ -473,10 +488,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
-      // The scores have been read: X1 may take the next column's.
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) arrive_lead(x1_free_lead);
       if (two) {
 #pragma unroll
         for (int c4 = 0; c4 < 4; ++c4) {
