@@ -49,15 +49,16 @@ __host__ __device__ constexpr int slot_bytes(int mode) { return mode == kDV ? 2 
 constexpr float kLog2e = 1.4426950408889634f;
 
 struct Bars {
-  int full, empty, a_full, x_full, x1_free, p_ready, acc_ready, drain, count;
+  int full, empty, a_full, x1_full, x2_full, x1_free, p_ready, acc_ready, drain, count;
 };
 __host__ __device__ inline Bars bar_layout(int stages) {
   Bars b;
   b.full = 0;
   b.empty = stages;
   b.a_full = 2 * stages;
-  b.x_full = b.a_full + 1;
-  b.x1_free = b.x_full + 1;
+  b.x1_full = b.a_full + 1;
+  b.x2_full = b.x1_full + 1;
+  b.x1_free = b.x2_full + 1;
   b.p_ready = b.x1_free + 1;
   b.acc_ready = b.p_ready + 1;
   b.drain = b.acc_ready + 1;
@@ -176,7 +177,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar(bl.empty + i), 1);
     }
     mbar_init(bar(bl.a_full), 1);
-    mbar_init(bar(bl.x_full), 1);
+    mbar_init(bar(bl.x1_full), 1);
+    mbar_init(bar(bl.x2_full), 1);
     mbar_init(bar(bl.x1_free), 8);  // four elementwise warps in each CTA
     mbar_init(bar(bl.p_ready), 8);
     mbar_init(bar(bl.acc_ready), 1);
@@ -336,10 +338,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       // P and dS; X2 ends up holding P or dS, the A operand of the gradient.  So
       // the next column's X1 product overlaps this column's elementwise work,
       // and X2 is rewritten by the next product right after the gradient MMAs.
+      // X1 and X2 each signal their own barrier, so the elementwise warps copy
+      // the scores out (and free X1) while the gradient and dP MMAs still run.
       if (g.ncols > 0) {
         product1();
+        if (ok) umma_commit_pair(bar(bl.x1_full), 3);
         if (two && ok) product2();
-        if (ok) umma_commit_pair(bar(bl.x_full), 3);
+        if (two && ok) umma_commit_pair(bar(bl.x2_full), 3);
       }
       for (int c = 0; c < g.ncols && ok; ++c) {
         const bool more = c + 1 < g.ncols;
@@ -349,7 +354,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc_fence_after();
           product1();
           if (!ok) break;
-          if (!two) umma_commit_pair(bar(bl.x_full), 3);
+          umma_commit_pair(bar(bl.x1_full), 3);
         }
         ok = mbar_wait(bar(bl.p_ready), c & 1, status);
         if (!ok) break;
@@ -371,7 +376,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           // next column's X2 product may follow them without a wait.
           product2();
           if (!ok) break;
-          umma_commit_pair(bar(bl.x_full), 3);
+          umma_commit_pair(bar(bl.x2_full), 3);
         }
       }
       umma_commit_pair(bar(bl.drain), 1);
@@ -419,7 +424,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (two) dlv[c4] = p.delta[i];
         }
       }
-      ok = __all_sync(0xffffffffu, mbar_wait(bar(bl.x_full), c & 1, status));
+      ok = __all_sync(0xffffffffu, mbar_wait(bar(bl.x1_full), c & 1, status));
       if (!ok) break;
       tc_fence_after();
       float pv[128];
@@ -489,6 +494,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       if (two) {
+        ok = __all_sync(0xffffffffu, mbar_wait(bar(bl.x2_full), c & 1, status));
+        if (!ok) break;
+        tc_fence_after();
 #pragma unroll
         for (int c4 = 0; c4 < 4; ++c4) {
           float f[32];
