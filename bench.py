@@ -286,12 +286,10 @@ def run_ffpa(args, rank, world):
         print(json.dumps(line), flush=True)
 
 
-# DRAM bytes per launch of each kernel from the committed ncu capture of the
-# current kernels (profiles/); None until a capture of the current code exists.
 # DRAM bytes (read + write) per launch from the ncu capture summarised in
 # profiles/ncu_full_fwd_bwd_N8192_D512_bf16.md (same workload); only kernels
 # unchanged since that capture are listed.
-TRAFFIC: dict = {"fwd_main": 253895936, "bwd_dv": 253783296, "bwd_dk": 334875392, "bwd_dq": 339085056}
+TRAFFIC: dict = {"fwd_main": 252820224, "bwd_dv": 253036032, "bwd_dk": 346558464, "bwd_dq": 353302016}
 
 
 def measure_e2e(step, inp, dev_in, dev_out, world, dev, steps=3):
