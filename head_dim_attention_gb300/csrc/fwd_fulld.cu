@@ -14,21 +14,23 @@
 //
 // Per CTA c of the pair (query rows q0 + 64c .. q0 + 64c + 63):
 //   * Q resident in shared memory: 8 chunk tiles of 64 rows x 64 columns;
-//   * key tiles of 256 keys: S = Q K^T with M=128, N=256: B split by N, this
-//     CTA loads keys 128c .. 128c+127 of the tile (128 KB over all of D);
-//     TMEM S buffer (128 columns): lane r holds keys 0..127 of row r, lane
-//     r + 64 keys 128..255 (double-buffered);
+//   * key tiles of 128 keys: S = Q K^T with M=128, N=128: B split by N, this
+//     CTA loads keys 64c .. 64c+63 of the tile (64 KB over all of D); TMEM S
+//     buffer (64 columns): lane r holds keys 0..63 of row r, lane r + 64 keys
+//     64..127 (double-buffered);
 //   * softmax by 128 threads, two per row (thread t: row t mod 64, key half
 //     t / 64); the row maximum is exchanged between the two through shared
-//     memory; each thread keeps its half's running sum, added at the end;
+//     memory, and each keeps its half's running sum, added at the end;
 //   * P (and, on tiles that need it, its rounding residual) is written to
-//     shared memory as the K-major A operand (64 rows x 256 keys, 32 KB):
-//     the A operand of an M=128 pair MMA taken from TMEM would need a layout
-//     other than the one S arrives in;
+//     shared memory as the K-major A operand (64 rows x 128 keys, 16 KB): a
+//     probe of the TMEM form of this MMA's A operand did not match the layout
+//     S arrives in, so P goes through shared memory;
 //   * O += P V: two MMAs per 16-key step (D columns 0..255 and 256..511),
 //     M=128, N=256, B split by N: this CTA loads 128 of each half's columns
-//     (256 keys x 256 columns = 128 KB per key tile); TMEM columns [0, 128)
+//     (128 keys x 256 columns = 64 KB per key tile); TMEM columns [0, 128)
 //     hold D 128c'.. of half 0, [128, 256) of half 1 (c' = lane / 64).
+// With Q (64 KB) and P (32 KB) resident, four 32 KB ring slots hold one key
+// tile's K and V loads together.
 //
 // Warp roles: warps 0, 2, 3 TMA producers (each CTA its own halves), warp 1
 // TMEM owner and, in the first CTA, the MMA issuer; warps 4-7 softmax.
@@ -46,16 +48,16 @@ namespace {
 constexpr int kThreads = 256;
 constexpr int kProducers = 3;
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kS0 = 256, kS1 = 384;      // S/P score buffers; O in [0, 256)
+constexpr uint32_t kS0 = 256, kS1 = 320;      // S score buffers (64 columns each); O in [0, 256)
 constexpr float kRescaleLog2 = 8.0f;
 constexpr float kLoFrac = 1.0f / 64.0f;       // residual term of P only where a weight exceeds this share
 constexpr int kChunks = 8;                    // D = 512
-constexpr int kKeys = 256;                    // keys per tile
+constexpr int kKeys = 128;                    // keys per tile
 constexpr int kHalfBytes = kChunkBytes / 2;   // 64 rows x 64 columns
 constexpr int kQBytes = kChunks * kHalfBytes;  // 64 KB
-constexpr int kPBytes = 4 * kHalfBytes;        // 64 rows x 256 keys, 32 KB
+constexpr int kPBytes = 2 * kHalfBytes;        // 64 rows x 128 keys, 16 KB
 constexpr int kSlotBytes = 2 * kChunkBytes;    // 32 KB
-constexpr int kStages = 3;
+constexpr int kStages = 4;
 // shared memory: Q | P_hi | P_lo | ring | barriers + exchange
 constexpr int kPHiOff = kQBytes, kPLoOff = kPHiOff + kPBytes, kRingOff = kPLoOff + kPBytes;
 constexpr int kMiscOff = kRingOff + kStages * kSlotBytes;
@@ -99,7 +101,7 @@ __device__ __forceinline__ void store_row64(uint32_t tile, int r, const uint32_t
 
 template <bool BF16>
 __global__ void __launch_bounds__(kThreads, 1)
-    fwd_fulld_kernel(const __grid_constant__ CUtensorMap map_qh, const __grid_constant__ CUtensorMap map_k,
+    fwd_fulld_kernel(const __grid_constant__ CUtensorMap map_qh, const __grid_constant__ CUtensorMap map_kh,
                      const __grid_constant__ CUtensorMap map_v, const __grid_constant__ FwdParams p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -157,7 +159,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int pi = (warp == 0) ? 0 : warp - 1;
     if (lane == 0) {
       tma_prefetch_desc(&map_qh);
-      tma_prefetch_desc(&map_k);
+      tma_prefetch_desc(&map_kh);
       tma_prefetch_desc(&map_v);
       if (pi == 0) {
         if (rank == 0) mbar_expect_tx(bar(bl.q_full), 2 * kQBytes);
@@ -167,8 +169,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       bool ok = true;
       uint32_t it = 0;
-      // kind 0: K chunks 2m, 2m+1 of this CTA's 128 keys of tile j;
-      // kind 1: V chunks (this CTA's two of D half m>>1) of keys 128(m&1).. of tile j
+      // kind 0: K chunks 4m .. 4m+3 of this CTA's 64 keys of tile j (m = 0, 1);
+      // kind 1: V chunks (this CTA's two of D half m) of the 128 keys of tile j
       auto slot = [&](int kind, int j, int m) {
         if (ok && static_cast<int>(it % nprod) == pi) {
           const uint32_t s = it % kStages, r = it / kStages;
@@ -177,14 +179,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (rank == 0) mbar_expect_tx(bar(bl.full + s), 2 * kSlotBytes);
             const uint32_t dst = ring_sm + s * kSlotBytes, fb = lead(bl.full + s);
             if (kind == 0) {
-              for (int i = 0; i < 2; ++i)
-                tma_load_4d_pair(dst + i * kChunkBytes, &map_k, fb, (2 * m + i) * kChunk,
-                                 j * kKeys + kTileRows * static_cast<int>(rank), kvh, b);
+              for (int i = 0; i < 4; ++i)
+                tma_load_4d_pair(dst + i * kHalfBytes, &map_kh, fb, (4 * m + i) * kChunk,
+                                 j * kKeys + 64 * static_cast<int>(rank), kvh, b);
             } else {
-              const int dh = m >> 1, kh = m & 1;
               for (int i = 0; i < 2; ++i)
-                tma_load_4d_pair(dst + i * kChunkBytes, &map_v, fb, (4 * dh + 2 * static_cast<int>(rank) + i) * kChunk,
-                                 j * kKeys + kTileRows * kh, kvh, b);
+                tma_load_4d_pair(dst + i * kChunkBytes, &map_v, fb, (4 * m + 2 * static_cast<int>(rank) + i) * kChunk,
+                                 j * kKeys, kvh, b);
             }
           }
         }
@@ -192,9 +193,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       };
       for (int j = 0; j <= ntiles && ok; ++j) {
         if (j < ntiles)
-          for (int m = 0; m < 4; ++m) slot(0, j, m);
+          for (int m = 0; m < 2; ++m) slot(0, j, m);
         if (j >= 1)
-          for (int m = 0; m < 4; ++m) slot(1, j - 1, m);
+          for (int m = 0; m < 2; ++m) slot(1, j - 1, m);
       }
       for (uint32_t s = 0; s < static_cast<uint32_t>(kStages) && s < it; ++s) {
         const uint32_t last = s + ((it - 1 - s) / kStages) * kStages;
@@ -205,12 +206,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer (first CTA of the pair)
     if (lane == 0 && rank == 0) {
-      const uint32_t idesc_s = idesc_f16(BF16, 128, 256, false, false);   // 128 rows x 256 keys
+      const uint32_t idesc_s = idesc_f16(BF16, 128, 128, false, false);   // 128 rows x 128 keys
       const uint32_t idesc_pv = idesc_f16(BF16, 128, 256, false, true);   // 128 rows x 256 O columns
       const uint64_t dq = sdesc_sw128(q_sm, 16, 1024);                     // Q chunks (64 rows), K-major
-      const uint64_t dk = sdesc_sw128(ring_sm, 16, 1024);                  // K chunks (128 keys), K-major
+      const uint64_t dk = sdesc_sw128(ring_sm, 16, 1024);                  // K chunks (64 keys), K-major
       const uint64_t dv = sdesc_sw128(ring_sm, kChunkBytes, 1024);         // V chunks, MN-major
-      const uint64_t dphi = sdesc_sw128(phi_sm, 16, 1024);                 // P (64 rows x 256 keys), K-major
+      const uint64_t dphi = sdesc_sw128(phi_sm, 16, 1024);                 // P (64 rows x 128 keys), K-major
       const uint64_t dplo = sdesc_sw128(plo_sm, 16, 1024);
       bool ok = mbar_wait(bar(bl.q_full), 0, status);
       tc_fence_after();
@@ -221,15 +222,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           // shared memory; the softmax warps read S_{j-2} before P_{j-1} could
           // be issued).
           const uint32_t s_tm = tbase + ((j & 1) ? kS1 : kS0);
-          for (int m = 0; m < 4 && ok; ++m) {
+          for (int m = 0; m < 2 && ok; ++m) {
             const uint32_t s = it % kStages;
             ok = mbar_wait(bar(bl.full + s), (it / kStages) & 1, status);
             if (!ok) break;
             tc_fence_after();
-            for (int i = 0; i < 2; ++i) {
-              const int c = 2 * m + i;
+            for (int i = 0; i < 4; ++i) {
+              const int c = 4 * m + i;
               const uint64_t a = sdesc_advance(dq, c * kHalfBytes);
-              const uint64_t bd = sdesc_advance(dk, s * kSlotBytes + i * kChunkBytes);
+              const uint64_t bd = sdesc_advance(dk, s * kSlotBytes + i * kHalfBytes);
 #pragma unroll
               for (int kk = 0; kk < 4; ++kk)
                 umma_ss_pair(s_tm, sdesc_advance(a, kk * 32), sdesc_advance(bd, kk * 32), idesc_s, (c | kk) != 0);
@@ -246,16 +247,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!ok) break;
           tc_fence_after();
           const bool use_lo = lo_flag[t & 1] == static_cast<uint32_t>(t + 1);
-          for (int m = 0; m < 4 && ok; ++m) {
-            const int dh = m >> 1, kh = m & 1;
+          for (int dh = 0; dh < 2 && ok; ++dh) {
             const uint32_t s = it % kStages;
             ok = mbar_wait(bar(bl.full + s), (it / kStages) & 1, status);
             if (!ok) break;
             tc_fence_after();
             const uint64_t bd = sdesc_advance(dv, s * kSlotBytes);
 #pragma unroll
-            for (int k8 = 0; k8 < 8; ++k8) {
-              const int kk = 8 * kh + k8;  // 16-key step within the tile
+            for (int kk = 0; kk < 8; ++kk) {  // 16-key step within the tile
+              const int k8 = kk;
               const uint32_t aoff = (kk >> 2) * kHalfBytes + (kk & 3) * 32;
               const uint32_t acc = (t > 0 || kk > 0) ? 1u : 0u;
               umma_ss_pair(tbase + 128 * dh, sdesc_advance(dphi, aoff), sdesc_advance(bd, k8 * 2048), idesc_pv, acc);
@@ -276,7 +276,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ softmax / correction / epilogue
     const int t = tid - 128;      // TMEM lane
     const int r = t & 63;         // row within this CTA's 64
-    const int kh = t >> 6;        // which 128 keys of each tile this thread scores
+    const int kh = t >> 6;        // which 64 keys of each tile this thread scores
     const int row = q0 + 64 * static_cast<int>(rank) + r;
     const uint32_t lane_off = static_cast<uint32_t>((warp - 4) * 32) << 16;
     const float* bias_row = nullptr;
@@ -291,40 +291,40 @@ __global__ void __launch_bounds__(kThreads, 1)
       ok = __all_sync(0xffffffffu, mbar_wait(bar(bl.s_full + (j & 1)), (j >> 1) & 1, status));
       if (!ok) break;
       tc_fence_after();
-      float s[128];
+      float s[64];
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
+      for (int c = 0; c < 2; ++c) {
         uint32_t v[32];
         tmem_ld32(tbase + lane_off + s_col + c * 32, v);
         tmem_ld_wait();
 #pragma unroll
         for (int i = 0; i < 32; ++i) s[c * 32 + i] = __uint_as_float(v[i]);
       }
-      const int kv0 = j * kKeys + kTileRows * kh;  // key of s[0]
-      const bool masked = (kv0 + kTileRows > p.Nkv) || (p.causal && kv0 + kTileRows - 1 > row);
+      const int kv0 = j * kKeys + 64 * kh;  // key of s[0]
+      const bool masked = (kv0 + 64 > p.Nkv) || (p.causal && kv0 + 63 > row);
       const float c_scale = p.scale_log2;
       if (bias_row) {
 #pragma unroll
-        for (int i = 0; i < 128; ++i)
+        for (int i = 0; i < 64; ++i)
           s[i] = fmaf(__ldg(bias_row + static_cast<int64_t>(min(kv0 + i, p.Nkv - 1)) * p.bias_sk), kLog2e,
                       s[i] * c_scale);
       } else {
 #pragma unroll
-        for (int i = 0; i < 128; ++i) s[i] *= c_scale;
+        for (int i = 0; i < 64; ++i) s[i] *= c_scale;
       }
       if (masked) {
 #pragma unroll
-        for (int i = 0; i < 128; ++i) {
+        for (int i = 0; i < 64; ++i) {
           const int kv = kv0 + i;
           if (kv >= p.Nkv || (p.causal && kv > row)) s[i] = -INFINITY;
         }
       }
       float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-      for (int i = 0; i < 128; ++i) mx4[i & 3] = fmaxf(mx4[i & 3], s[i]);
+      for (int i = 0; i < 64; ++i) mx4[i & 3] = fmaxf(mx4[i & 3], s[i]);
       const float m_half = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
       // the row's maximum over both halves: exchange with the thread holding
-      // the other 128 keys of this row (t ^ 64, in warp w ^ 2)
+      // the other 64 keys of this row (t ^ 64, in warp w ^ 2)
       xm[(j & 1) * 128 + t] = m_half;
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(bl.mx + (j & 1)));
@@ -343,7 +343,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float m_ref = (m_used == -INFINITY) ? 0.f : m_used;
       float ls[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int i = 0; i < 128; ++i) {
+      for (int i = 0; i < 64; ++i) {
         s[i] = ex2(s[i] - m_ref);
         ls[i & 3] += s[i];
       }
@@ -370,13 +370,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tmem_st_wait();
       }
-      // P of keys 128 kh .. 128 kh + 127 of row r: K-chunks 2 kh and 2 kh + 1
-#pragma unroll
-      for (int g = 0; g < 2; ++g) {
+      // P of keys 64 kh .. 64 kh + 63 of row r: K-chunk kh of the P tile
+      {
         uint32_t hi[32], lo[32];
 #pragma unroll
         for (int e = 0; e < 32; ++e) {
-          const float p0 = s[64 * g + 2 * e], p1 = s[64 * g + 2 * e + 1];
+          const float p0 = s[2 * e], p1 = s[2 * e + 1];
           hi[e] = pack2<BF16>(p0, p1);
           if (warp_lo) {
             const float2 hv = unpack2<BF16>(hi[e]);
@@ -385,8 +384,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             lo[e] = 0u;
           }
         }
-        store_row64(phi_sm + (2 * kh + g) * kHalfBytes, r, hi);
-        store_row64(plo_sm + (2 * kh + g) * kHalfBytes, r, lo);
+        store_row64(phi_sm + kh * kHalfBytes, r, hi);
+        store_row64(plo_sm + kh * kHalfBytes, r, lo);
       }
       fence_proxy_async_smem();
       tc_fence_before();
@@ -474,7 +473,7 @@ cudaError_t launch_impl(const FwdParams& p_in, const FwdMaps& m, cudaStream_t st
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   timing_mark(st);
-  e = cudaLaunchKernelEx(&cfg, kern, m.q_half, m.k, m.v, p);
+  e = cudaLaunchKernelEx(&cfg, kern, m.q_half, m.k_half, m.v, p);
   timing_mark(st);
   return e;
 }
