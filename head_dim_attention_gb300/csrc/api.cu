@@ -247,7 +247,7 @@ extern "C" int ffpa_fwd(const ffpa_tensor_t* q, const ffpa_tensor_t* k, const ff
   p.status = status;
   FwdMaps m;
   if ((rc = encode_map(&m.q, q)) || (rc = encode_map(&m.k, k)) || (rc = encode_map(&m.v, v)) ||
-      (rc = encode_map(&m.k_half, k, kTileRows / 2)) || (rc = encode_map(&m.q_half, q, kTileRows / 2)))
+      (rc = encode_map(&m.k_half, k, kTileRows / 2)))
     return rc;
   return cuda_rc(launch_fwd_main(p, m, bf16, st));
 }

@@ -32,7 +32,6 @@ struct FwdParams {
 struct FwdMaps {
   CUtensorMap q, k, v;  // 4-D {D, N, H, B}, box {64, 128, 1, 1}, 128-byte swizzle
   CUtensorMap k_half;   // K with box {64, 64, 1, 1}: one CTA's half of a key tile in the CTA-pair kernel
-  CUtensorMap q_half;   // Q with box {64, 64, 1, 1}: one CTA's half of a query tile in the full-D pair kernel
 };
 
 // Decode (small Nq) path.
@@ -95,9 +94,6 @@ struct BwdMaps {
 bool dtype_is_bf16(int dtype);
 
 cudaError_t launch_fwd_main(const FwdParams& p, const FwdMaps& m, bool bf16, cudaStream_t s);
-// Full-D CTA-pair forward (fwd_fulld.cu): D = 512, each pair holding all of O for one query tile.
-bool fwd_fulld_supported(const FwdParams& p);
-cudaError_t launch_fwd_fulld(const FwdParams& p, const FwdMaps& m, bool bf16, cudaStream_t s);
 // CTA-pair forward (fwd_pair.cu): D = 512.
 bool fwd_pair_supported(const FwdParams& p);
 cudaError_t launch_fwd_pair(const FwdParams& p, const FwdMaps& m, bool bf16, cudaStream_t s);
