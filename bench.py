@@ -365,12 +365,33 @@ def measure_e2e(inp, scale, world, dev, steps=8):
             "overlap": "double-buffered: each step's copies overlap the neighbouring steps' kernels"}
 
 
-def measure_decode(dev, peaks, iters=20):
-    """Decode-shaped forward (Nq=1, Nkv=8192, H=8, D=512, bf16): HBM-bound; L2
-    flushed with a 256 MiB write before every call.  The GB/s figure uses the
-    device time of the library's own launches (split + combine), taken with the
-    library's timing hook; `call_us` is the whole API call, host marshalling
-    and scratch allocation included."""
+def _call_times(sets, out, lse, ffpa_fwd, iters=10):
+    """Wall time of whole decode API calls (host marshalling, scratch
+    allocation and launches included), GPU idle before each."""
+    import torch
+
+    times = []
+    for i in range(iters):
+        q, k, v = sets[i % 3]
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        ffpa_fwd(q, k, v, None, 0, 512 ** -0.5, out, lse)
+        e1.record()
+        torch.cuda.synchronize()
+        times.append(e0.elapsed_time(e1))
+    return times
+
+
+def measure_decode(dev, peaks, iters=21):
+    """Decode-shaped forward (Nq=1, Nkv=8192, H=8, D=512, bf16): HBM-bound.
+    Every call reads K and V that are not resident in L2: three separate input
+    sets of 134 MB are used in turn (inputs larger than L2), so no flush write
+    leaves dirty lines for the call to write back.  For comparison the same
+    calls are also timed after a 256 MiB flush write (dirty L2).  The GB/s
+    figures use the device time of the library's own launches (split +
+    combine), taken with the library's timing hook; `call_us` is the whole API
+    call, host marshalling and scratch allocation included."""
     import torch
 
     from head_dim_attention_gb300 import ffpa_fwd
@@ -378,32 +399,48 @@ def measure_decode(dev, peaks, iters=20):
     from head_dim_attention_gb300.synth import make_inputs
 
     inp = make_inputs(1, 8, 8, 1, 8192, 512, torch.bfloat16, seed=7)
-    q, k, v = (t.to(dev) for t in (inp.q, inp.k, inp.v))
-    out = torch.empty_like(q)
+    sets = [tuple(t.to(dev).clone() for t in (inp.q, inp.k, inp.v)) for _ in range(3)]
+    out = torch.empty_like(sets[0][0])
     lse = torch.empty(1, 8, 1, dtype=torch.float32, device=dev)
     flush = torch.empty(64 << 20, dtype=torch.float32, device=dev)
     hook = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
     for e in hook:
         e.record()  # the hook needs events that exist on the device
-    kern, call = [], []
-    for i in range(iters + 3):
-        flush.fill_(float(i))
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record()
-        ffpa_set_timing_events(hook)
-        ffpa_fwd(q, k, v, None, 0, 512 ** -0.5, out, lse)
-        ffpa_set_timing_events(None)
-        e1.record()
-        torch.cuda.synchronize()
-        if i >= 3:
-            kern.append(hook[0].elapsed_time(hook[2]))
-            call.append(e0.elapsed_time(e1))
-    ms = statistics.median(kern)
+
+    def timed(dirty):
+        kern, split, call = [], [], []
+        for i in range(iters + 3):
+            q, k, v = sets[i % 3]
+            if dirty:
+                flush.fill_(float(i))
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            # keep the GPU busy while the host enqueues the call, so the
+            # library's events bracket GPU work, not host-side gaps
+            torch.cuda._sleep(1000000)
+            ffpa_set_timing_events(hook)
+            ffpa_fwd(q, k, v, None, 0, 512 ** -0.5, out, lse)
+            ffpa_set_timing_events(None)
+            e1.record()
+            torch.cuda.synchronize()
+            if i >= 3:
+                kern.append(hook[0].elapsed_time(hook[2]))
+                split.append(hook[0].elapsed_time(hook[1]))
+                call.append(e0.elapsed_time(e1))
+        return statistics.median(kern), statistics.median(split), statistics.median(call)
+
+    ms, split_ms, _ = timed(False)
+    ms_dirty, _, _ = timed(True)
+    call_ms = statistics.median(_call_times(sets, out, lse, ffpa_fwd))
+    q, k, v = sets[0]
     nbytes = sum(t.numel() * t.element_size() for t in (q, k, v, out))
     gbs = nbytes / (ms / 1e3) / 1e9
     return {"workload": "decode Nq=1, Nkv=8192, H=8, D=512, bf16", "us": ms * 1e3, "bytes": nbytes,
-            "gbps": gbs, "frac_of_hbm": gbs / peaks["hbm_gbs"], "call_us": statistics.median(call) * 1e3,
-            "l2": "flushed before each call", "timing": "device time of split + combine launches"}
+            "gbps": gbs, "frac_of_hbm": gbs / peaks["hbm_gbs"], "split_us": split_ms * 1e3,
+            "combine_us": (ms - split_ms) * 1e3, "call_us": call_ms * 1e3,
+            "l2": "cold: three 134 MB input sets used in turn (no flush writes)",
+            "us_after_dirty_flush": ms_dirty * 1e3, "gbps_after_dirty_flush": nbytes / (ms_dirty / 1e3) / 1e9,
+            "timing": "device time of split + combine launches"}
 
 
 def main():

@@ -221,6 +221,7 @@ extern "C" int ffpa_fwd(const ffpa_tensor_t* q, const ffpa_tensor_t* k, const ff
     p.scale_log2 = scale * kLog2e;
     p.split_len = 128;
     p.n_splits = (int)((c.Nkv + p.split_len - 1) / p.split_len);
+    p.status = status;
     const size_t n_rows = (size_t)c.B * c.Hq * c.Nq * p.n_splits;
     void* scratch = nullptr;
     const size_t o_bytes = n_rows * c.D * sizeof(float), ml_bytes = n_rows * 2 * sizeof(float);
@@ -345,6 +346,7 @@ extern "C" int ffpa_fwd_decode_noalloc(const ffpa_tensor_t* q, const ffpa_tensor
   p.scale_log2 = scale * kLog2e;
   p.split_len = 128;
   p.n_splits = (int)((c.Nkv + p.split_len - 1) / p.split_len);
+  p.status = device_status_word();  // fetched with cudaGetSymbolAddress, no allocation
   if (decode_scratch_bytes(p) > decode_noalloc_capacity_bytes()) return FFPA_ERR_SCRATCH_LIMIT;
   timing_begin();
   return cuda_rc(launch_fwd_decode_noalloc(p, dtype_is_bf16(c.dtype), reinterpret_cast<cudaStream_t>(stream)));

@@ -394,6 +394,240 @@ __global__ void __launch_bounds__(kDecThreads) decode_stream_kernel(const __grid
   }
 }
 
+
+// Streaming decode through shared memory (Nq <= 2, K and V rows contiguous).
+// The register-fed kernel above keeps only 8 KB per warp in flight and walks
+// its keys in dependent rounds, which left HBM at ~40% of its copy rate.  Here
+// one thread streams the slice's K and V rows into a ring of shared-memory
+// stages with 1-D bulk TMA copies (16 keys of K and of V per stage, three
+// stages in flight per CTA), and the eight warps read them from shared memory:
+// warp w scores keys 2w and 2w+1 of each stage and keeps its own online
+// softmax, merged at the end exactly as above.
+constexpr int kBulkStages = 3;
+constexpr int kBulkKeys = 16;  // keys per stage
+
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+               "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
+               : "memory");
+}
+
+template <int R, int G, bool BF16>
+__global__ void __launch_bounds__(kDecThreads) decode_bulk_kernel(const __grid_constant__ DecodeParams p) {
+  extern __shared__ __align__(128) uint8_t bsm[];
+  const int split = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+  const int g = h / p.group;
+  const int D = p.D, Nq = p.Nq, L = p.split_len;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int groups = D / 8;
+  const int kv_begin = split * L;
+  const int kv_len = min(L, p.Nkv - kv_begin);
+  const int nst = (kv_len + kBulkKeys - 1) / kBulkKeys;
+  const uint32_t half_bytes = static_cast<uint32_t>(kBulkKeys * D * 2);  // one stage's K (or V) rows
+  const uint32_t stage_bytes = 2 * half_bytes;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(bsm + kBulkStages * stage_bytes);
+  auto full = [&](int s) { return smem_u32(&bars[s]); };
+  auto empty = [&](int s) { return smem_u32(&bars[kBulkStages + s]); };
+  const uint32_t ring = smem_u32(bsm);
+  uint32_t* status = p.status;
+  typedef typename std::conditional<BF16, __nv_bfloat16, __half>::type T;
+  constexpr float kLog2e = 1.4426950408889634f;
+  const T* kbase = reinterpret_cast<const T*>(p.k) + b * p.k_sb + g * p.k_sh + static_cast<int64_t>(kv_begin) * D;
+  const T* vbase = reinterpret_cast<const T*>(p.v) + b * p.v_sb + g * p.v_sh + static_cast<int64_t>(kv_begin) * D;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kBulkStages; ++s) {
+      mbar_init(full(s), 1);
+      mbar_init(empty(s), kDecThreads / 32);
+    }
+    fence_mbar_init();
+  }
+  __syncthreads();
+  // stage i: keys 16 i .. 16 i + 15 of the slice (fewer in the last one)
+  auto issue = [&](int i) {
+    const int s = i % kBulkStages;
+    const int n = min(kBulkKeys, kv_len - i * kBulkKeys);
+    const uint32_t bytes = static_cast<uint32_t>(n * D * 2);
+    mbar_expect_tx(full(s), 2 * bytes);
+    bulk_load(ring + s * stage_bytes, kbase + static_cast<int64_t>(i) * kBulkKeys * D, bytes, full(s));
+    bulk_load(ring + s * stage_bytes + half_bytes, vbase + static_cast<int64_t>(i) * kBulkKeys * D, bytes, full(s));
+  };
+  if (threadIdx.x == 0)
+    for (int i = 0; i < min(kBulkStages, nst); ++i) issue(i);
+
+  float qf[R][G][8];
+#pragma unroll
+  for (int r = 0; r < R; ++r)
+#pragma unroll
+    for (int k = 0; k < G; ++k) {
+      const int c = lane + 32 * k;
+      if (r < Nq && c < groups)
+        Vec8<BF16>::load(reinterpret_cast<const T*>(p.q) + b * p.q_sb + h * p.q_sh + static_cast<int64_t>(r) * p.q_sn +
+                             c * 8,
+                         qf[r][k]);
+      else
+#pragma unroll
+        for (int e = 0; e < 8; ++e) qf[r][k][e] = 0.f;
+    }
+  float m[R], l[R], o[R][G][8];
+#pragma unroll
+  for (int r = 0; r < R; ++r) {
+    m[r] = -INFINITY;
+    l[r] = 0.f;
+#pragma unroll
+    for (int k = 0; k < G; ++k)
+#pragma unroll
+      for (int e = 0; e < 8; ++e) o[r][k][e] = 0.f;
+  }
+  bool ok = true;
+  for (int i = 0; i < nst; ++i) {
+    const int s = i % kBulkStages;
+    ok = __all_sync(0xffffffffu, mbar_wait(full(s), (i / kBulkStages) & 1, status));
+    if (!ok) break;
+    const int n = min(kBulkKeys, kv_len - i * kBulkKeys);
+    const uint8_t* kst = bsm + s * stage_bytes;
+    const uint8_t* vst = kst + half_bytes;
+    float sc[2][R];
+    int jj[2];
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      const int kk = 2 * warp + u;             // key within the stage
+      jj[u] = min(kk, n - 1);                  // rows past the slice end read a valid row, weight 0
+      const uint8_t* krow = kst + static_cast<size_t>(jj[u]) * D * 2;
+#pragma unroll
+      for (int r = 0; r < R; ++r) sc[u][r] = 0.f;
+#pragma unroll
+      for (int k = 0; k < G; ++k) {
+        const int c = lane + 32 * k;
+        if (c < groups) {
+          const uint4 w4 = *reinterpret_cast<const uint4*>(krow + c * 16);
+          const uint32_t w[4] = {w4.x, w4.y, w4.z, w4.w};
+          float kf[8];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            float2 x;
+            if constexpr (BF16)
+              x = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[e]));
+            else
+              x = __half22float2(*reinterpret_cast<const __half2*>(&w[e]));
+            kf[2 * e] = x.x;
+            kf[2 * e + 1] = x.y;
+          }
+#pragma unroll
+          for (int r = 0; r < R; ++r)
+#pragma unroll
+            for (int e = 0; e < 8; ++e) sc[u][r] = fmaf(qf[r][k][e], kf[e], sc[u][r]);
+        }
+      }
+#pragma unroll
+      for (int r = 0; r < R; ++r) {
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) sc[u][r] += __shfl_xor_sync(0xffffffffu, sc[u][r], off);
+        const int kv = kv_begin + i * kBulkKeys + kk;
+        float x = sc[u][r] * p.scale_log2;
+        if (p.bias)
+          x = fmaf(__ldg(p.bias + b * p.bias_sb + h * p.bias_sh + static_cast<int64_t>(r) * p.bias_sq +
+                         static_cast<int64_t>(min(kv, p.Nkv - 1)) * p.bias_sk),
+                   kLog2e, x);
+        const bool valid = kk < n && r < Nq && !(p.causal && kv > r);
+        sc[u][r] = valid ? x : -INFINITY;
+      }
+    }
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+      const float mx = fmaxf(m[r], fmaxf(sc[0][r], sc[1][r]));
+      if (mx == -INFINITY) continue;  // nothing visible yet for this row
+      const float alpha = ex2(m[r] - mx);
+      const float p0 = ex2(sc[0][r] - mx), p1 = ex2(sc[1][r] - mx);
+      l[r] = l[r] * alpha + p0 + p1;
+      m[r] = mx;
+#pragma unroll
+      for (int k = 0; k < G; ++k) {
+        const int c = lane + 32 * k;
+        if (c < groups) {
+          const uint4 a4 = *reinterpret_cast<const uint4*>(vst + static_cast<size_t>(jj[0]) * D * 2 + c * 16);
+          const uint4 b4 = *reinterpret_cast<const uint4*>(vst + static_cast<size_t>(jj[1]) * D * 2 + c * 16);
+          const uint32_t wa[4] = {a4.x, a4.y, a4.z, a4.w}, wb[4] = {b4.x, b4.y, b4.z, b4.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            float2 xa, xb;
+            if constexpr (BF16) {
+              xa = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&wa[e]));
+              xb = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&wb[e]));
+            } else {
+              xa = __half22float2(*reinterpret_cast<const __half2*>(&wa[e]));
+              xb = __half22float2(*reinterpret_cast<const __half2*>(&wb[e]));
+            }
+            o[r][k][2 * e] = fmaf(p1, xb.x, fmaf(p0, xa.x, o[r][k][2 * e] * alpha));
+            o[r][k][2 * e + 1] = fmaf(p1, xb.y, fmaf(p0, xa.y, o[r][k][2 * e + 1] * alpha));
+          }
+        }
+      }
+    }
+    // release the stage; thread 0 refills it once all eight warps are done
+    __syncwarp();
+    if (lane == 0) mbar_arrive(empty(s));
+    if (threadIdx.x == 0 && i + kBulkStages < nst) {
+      ok = mbar_wait(empty(s), (i / kBulkStages) & 1, status);
+      if (ok) issue(i + kBulkStages);
+    }
+  }
+  // every issued stage was waited on above, so no copy is still in flight; the
+  // ring's first bytes now take the warps' partials
+  __syncthreads();
+  float* so = reinterpret_cast<float*>(bsm);  // [8][R][D]
+  float* sm = so + 8 * R * D;                 // [8][R]
+  float* sl = sm + 8 * R;                     // [8][R]
+#pragma unroll
+  for (int r = 0; r < R; ++r) {
+#pragma unroll
+    for (int k = 0; k < G; ++k) {
+      const int c = lane + 32 * k;
+      if (c < groups) {
+        float4* dst = reinterpret_cast<float4*>(so + (warp * R + r) * D + c * 8);
+        dst[0] = make_float4(o[r][k][0], o[r][k][1], o[r][k][2], o[r][k][3]);
+        dst[1] = make_float4(o[r][k][4], o[r][k][5], o[r][k][6], o[r][k][7]);
+      }
+    }
+    if (lane == 0) {
+      sm[warp * R + r] = m[r];
+      sl[warp * R + r] = l[r];
+    }
+  }
+  __syncthreads();
+  for (int r = 0; r < Nq; ++r) {
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < 8; ++w) M = fmaxf(M, sm[w * R + r]);
+    const float Mref = (M == -INFINITY) ? 0.f : M;
+    float wgt[8];
+    float Ls = 0.f;
+#pragma unroll
+    for (int w = 0; w < 8; ++w) {
+      wgt[w] = ex2(sm[w * R + r] - Mref);
+      Ls += wgt[w] * sl[w * R + r];
+    }
+    float* dst = p.part_o + ((((static_cast<int64_t>(b) * p.Hq + h) * Nq + r) * p.n_splits + split) * D);
+    for (int d = threadIdx.x * 4; d < D; d += kDecThreads * 4) {
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int w = 0; w < 8; ++w) {
+        const float4 v = *reinterpret_cast<const float4*>(so + (w * R + r) * D + d);
+        acc.x = fmaf(wgt[w], v.x, acc.x);
+        acc.y = fmaf(wgt[w], v.y, acc.y);
+        acc.z = fmaf(wgt[w], v.z, acc.z);
+        acc.w = fmaf(wgt[w], v.w, acc.w);
+      }
+      *reinterpret_cast<float4*>(dst + d) = acc;
+    }
+    if (threadIdx.x == 0) {
+      float* ml = p.part_ml + (((static_cast<int64_t>(b) * p.Hq + h) * Nq + r) * p.n_splits + split) * 2;
+      ml[0] = M;
+      ml[1] = Ls;
+    }
+  }
+}
+
 // Merge the slices.  One CTA per (row, 128-column chunk of D, query head,
 // batch): the block reduces the slices' (m, l) to M and L, then warp w sums
 // slices w, w+8, ... for its lane's four columns (all its loads in flight) and
@@ -485,11 +719,28 @@ cudaError_t launch_stream(const DecodeParams& p, cudaStream_t st) {
   return cudaSuccess;
 }
 
+template <int R, int G, bool BF16>
+cudaError_t launch_bulk(const DecodeParams& p, cudaStream_t st) {
+  const size_t ring = static_cast<size_t>(kBulkStages) * 2 * kBulkKeys * p.D * 2;
+  const size_t merge = (static_cast<size_t>(8) * R * p.D + 16 * R) * 4;
+  const size_t smem = (ring > merge ? ring : merge) + 2 * kBulkStages * 8;
+  auto k1 = decode_bulk_kernel<R, G, BF16>;
+  cudaError_t e = cudaFuncSetAttribute(k1, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  k1<<<dim3(p.n_splits, p.Hq, p.B), kDecThreads, smem, st>>>(p);
+  return cudaSuccess;
+}
+
 template <bool BF16>
 cudaError_t launch_decode_impl(const DecodeParams& p, cudaStream_t st) {
   cudaError_t e = cudaSuccess;
   timing_mark(st);
-  if (p.Nq <= 2 && p.D <= 512) {
+  // rows of K and V contiguous (row stride D): the slice streams through
+  // shared memory with bulk copies
+  const bool rows_contiguous = p.k_sn == p.D && p.v_sn == p.D;
+  if (p.Nq <= 2 && p.D <= 512 && rows_contiguous && p.split_len % kBulkKeys == 0) {
+    e = p.Nq == 1 ? launch_bulk<1, 2, BF16>(p, st) : launch_bulk<2, 2, BF16>(p, st);
+  } else if (p.Nq <= 2 && p.D <= 512) {
     e = p.Nq == 1 ? launch_stream<1, 2, 4, BF16>(p, st) : launch_stream<2, 2, 4, BF16>(p, st);
   } else if (p.Nq <= 2) {
     e = p.Nq == 1 ? launch_stream<1, 4, 2, BF16>(p, st) : launch_stream<2, 4, 2, BF16>(p, st);

@@ -55,6 +55,7 @@ struct DecodeParams {
   int n_splits;
   float* part_o;      // [B, Hq, Nq, n_splits, D] fp32 scratch
   float* part_ml;     // [B, Hq, Nq, n_splits, 2] fp32 scratch (max, sum), log2 domain
+  uint32_t* status;   // device status word (bounded waits of the streaming kernel)
 };
 
 // Backward.

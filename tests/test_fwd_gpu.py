@@ -74,6 +74,13 @@ def test_head_dim_sweep_small(D):
     (2, 2, 2, 16, 130, 1024, BF, False, False),
     (1, 2, 1, 5, 1, 320, FP, False, True),
     (1, 1, 1, 16, 16, 64, BF, True, False),
+    # one or two query rows with contiguous K/V rows stream the slice through
+    # shared memory: GQA + bias + causal, head dimensions whose 16-byte groups
+    # do not fill every lane, ragged slices, a slice of a single partial stage
+    (1, 4, 2, 2, 1000, 512, BF, True, True),
+    (2, 3, 3, 1, 777, 320, FP, False, True),
+    (1, 2, 1, 2, 8191, 448, BF, False, False),
+    (1, 1, 1, 1, 17, 512, FP, True, False),
 ])
 def test_decode_small(B, Hq, Hkv, Nq, Nkv, D, dtype, causal, bias):
     check_fwd_full(B, Hq, Hkv, Nq, Nkv, D, dtype, causal=causal, bias=bias)
