@@ -65,8 +65,11 @@ __host__ __device__ inline Bars bar_layout(int stages) {
   b.count = b.drain + 1;
   return b;
 }
+// dK: each elementwise warp stages its column tile's statistics (lse2 and
+// Delta of 128 column rows, 1 KB) in shared memory
+__host__ __device__ constexpr int stat_bytes(int mode) { return mode == kDK ? 4 * 1024 : 0; }
 __host__ __device__ constexpr int smem_bytes(int mode, int stages) {
-  return res_bytes(mode) + stages * slot_bytes(mode) + 1024 + 1024;
+  return res_bytes(mode) + stages * slot_bytes(mode) + 1024 + stat_bytes(mode) + 1024;
 }
 
 template <bool BF16>
@@ -154,6 +157,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const Bars bl = bar_layout(stages);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kResBytes + stages * kSlotBytes);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + bl.count);
+  float* stat_sm = reinterpret_cast<float*>(smem + kResBytes + stages * kSlotBytes + 1024);  // dK: [4 warps][2][128]
   auto bar = [&](int i) { return smem_u32(&bars[i]); };
   const uint32_t a_sm = smem_u32(smem), ring_sm = a_sm + kResBytes;
 
@@ -413,8 +417,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       int ch, cr0;
       column<MODE>(g, p, c, &ch, &cr0);
       // Column statistics (dV, dK): lane l of every warp loads lse2 and Delta of
-      // column rows cr0 + l + 32 c4, and threads take theirs with shuffles.
+      // column rows cr0 + l + 32 c4.  dV's threads take theirs with shuffles;
+      // dK's warps stage them in their own 1 KB of shared memory and read them
+      // back four at a time with broadcast loads (a quarter of the shuffle
+      // traffic, which shares the shared-memory pipe with the MMA operands).
       float l2v[4] = {0.f, 0.f, 0.f, 0.f}, dlv[4] = {0.f, 0.f, 0.f, 0.f};
+      float* wst = stat_sm + (warp - 4) * 256;  // dK: [lse2 x 128 | Delta x 128] of this warp
       if (MODE != kDQ) {
         const int64_t sbase = (static_cast<int64_t>(g.b) * p.Hq + ch) * p.Nq;
 #pragma unroll
@@ -423,7 +431,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           l2v[c4] = p.lse2[i];
           if (two) dlv[c4] = p.delta[i];
         }
+        if constexpr (MODE == kDK) {
+#pragma unroll
+          for (int c4 = 0; c4 < 4; ++c4) {
+            wst[c4 * 32 + lane] = l2v[c4];
+            wst[128 + c4 * 32 + lane] = dlv[c4];
+          }
+          __syncwarp();
+        }
       }
+      const float4* wst4 = reinterpret_cast<const float4*>(wst);
       ok = __all_sync(0xffffffffu, mbar_wait(bar(bl.x1_full), c & 1, status));
       if (!ok) break;
       tc_fence_after();
@@ -454,7 +471,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) arrive_lead(x1_free_lead);
-      if (plain) {
+      if (MODE == kDK && plain) {
+#pragma unroll
+        for (int e4 = 0; e4 < 32; ++e4) {
+          const float4 l2 = wst4[e4];
+          pv[4 * e4 + 0] = ex2(fmaf(pv[4 * e4 + 0], p.scale_log2, -l2.x));
+          pv[4 * e4 + 1] = ex2(fmaf(pv[4 * e4 + 1], p.scale_log2, -l2.y));
+          pv[4 * e4 + 2] = ex2(fmaf(pv[4 * e4 + 2], p.scale_log2, -l2.z));
+          pv[4 * e4 + 3] = ex2(fmaf(pv[4 * e4 + 3], p.scale_log2, -l2.w));
+        }
+      } else if (plain) {
 #pragma unroll
         for (int c4 = 0; c4 < 4; ++c4) {
 #pragma unroll
@@ -480,7 +506,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               i = cr0 + ci;
               j = srow;
               ic = min(i, p.Nq - 1);
-              l2 = __shfl_sync(0xffffffffu, l2v[c4], e);
+              l2 = (MODE == kDK) ? wst[ci] : __shfl_sync(0xffffffffu, l2v[c4], e);
             }
             const int hq = (MODE == kDQ) ? g.h : ch;
             const bool valid = i < p.Nq && j < p.Nkv && !(p.causal && j > i) && l2 > -INFINITY;
@@ -501,11 +527,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int c4 = 0; c4 < 4; ++c4) {
           float f[32];
           chunk(kX2, c4, f);
+          if constexpr (MODE == kDK) {
 #pragma unroll
-          for (int e = 0; e < 32; ++e) {
-            const int ci = c4 * 32 + e;
-            const float dl = (MODE == kDQ) ? delta_row : __shfl_sync(0xffffffffu, dlv[c4], e);
-            pv[ci] = pv[ci] * (f[e] - dl);
+            for (int e4 = 0; e4 < 8; ++e4) {
+              const float4 dl = wst4[32 + c4 * 8 + e4];
+              pv[c4 * 32 + 4 * e4 + 0] *= f[4 * e4 + 0] - dl.x;
+              pv[c4 * 32 + 4 * e4 + 1] *= f[4 * e4 + 1] - dl.y;
+              pv[c4 * 32 + 4 * e4 + 2] *= f[4 * e4 + 2] - dl.z;
+              pv[c4 * 32 + 4 * e4 + 3] *= f[4 * e4 + 3] - dl.w;
+            }
+          } else {
+#pragma unroll
+            for (int e = 0; e < 32; ++e) {
+              const int ci = c4 * 32 + e;
+              const float dl = (MODE == kDQ) ? delta_row : __shfl_sync(0xffffffffu, dlv[c4], e);
+              pv[ci] = pv[ci] * (f[e] - dl);
+            }
           }
         }
       }
