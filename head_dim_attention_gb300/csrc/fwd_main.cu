@@ -26,13 +26,17 @@
 // When a CTA owns more than 4 chunks (D > 512) it sweeps the keys once per
 // 4-chunk slice of its O columns ("passes"), recomputing S each time.
 //
-// Split without exchange (320 <= D <= 640).  The exchange moves 64 KB per key
+// Split without exchange (320 <= D <= 768).  The exchange moves 64 KB per key
 // tile and CTA through distributed shared memory, whose bandwidth is far
 // below the tensor pipe's.  So for D <= 512 two CTAs per query tile, and for
-// 576 <= D <= 640 three, each reduce S over the whole of D themselves (Q fully
+// 576 <= D <= 768 three, each reduce S over the whole of D themselves (Q fully
 // resident, every K chunk streamed) and own at most four 64-column chunks of O:
 // more MMA work than the exchange (1.5x for two CTAs), but no cluster and no
 // DSMEM traffic.
+//
+// D = 512 itself does not run here: launch_fwd_main hands it to the CTA-pair
+// kernel of fwd_pair.cu, which pairs two query tiles that own the same half
+// of O so that each SM loads half of every K tile and half of the V columns.
 //
 // Warp roles (256 threads): warp 0 = TMA producer, warp 1 = TMEM owner and
 // MMA issuer, warps 4-7 = softmax / correction / epilogue (one query row per
