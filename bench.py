@@ -289,7 +289,7 @@ def run_ffpa(args, rank, world):
 # DRAM bytes (read + write) per launch from the ncu capture summarised in
 # profiles/ncu_full_fwd_bwd_N8192_D512_bf16.md (same workload); only kernels
 # unchanged since that capture are listed.
-TRAFFIC: dict = {"fwd_main": 252820224, "bwd_dv": 253036032, "bwd_dk": 346558464, "bwd_dq": 353302016}
+TRAFFIC: dict = {"fwd_main": 251212288, "bwd_dv": 253638144, "bwd_dk": 357611520, "bwd_dq": 362597632}
 
 
 def measure_e2e(inp, scale, world, dev, steps=8):
