@@ -177,6 +177,39 @@ void bias_strides(const ffpa_tensor_t* bias, int64_t* sb, int64_t* sh, int64_t* 
 int cuda_rc(cudaError_t e) { return e == cudaSuccess ? FFPA_OK : FFPA_ERR_CUDA; }
 
 constexpr int kDecodeMaxRows = 16;
+
+// Keys per decode slice: the multiple of 16 in [128, 256] for which the
+// decode CTAs (one per batch, query head and slice; two fit on an SM) fill
+// their last wave best on the current device.  Ties go to the longer slice.
+// Slices of at least 128 keys keep a call's partials within what 128-key
+// slices would take (the no-allocation entry point's capacity check).
+int decode_split_len(int64_t B, int64_t Hq, int64_t Nkv) {
+  static std::mutex mu;
+  static int sms_cache[64] = {};
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) == cudaSuccess && dev >= 0 && dev < 64) {
+    std::lock_guard<std::mutex> lock(mu);
+    if (!sms_cache[dev]) {
+      int v = 0;
+      if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess) sms_cache[dev] = v;
+    }
+    sms = sms_cache[dev];
+  }
+  if (sms <= 0) return 128;
+  const int64_t slots = 2 * static_cast<int64_t>(sms);
+  int best = 128;
+  double best_fill = -1.0;
+  for (int L = 256; L >= 128; L -= 16) {
+    const int64_t ctas = B * Hq * ((Nkv + L - 1) / L);
+    const int64_t waves = (ctas + slots - 1) / slots;
+    const double fill = static_cast<double>(ctas) / static_cast<double>(waves * slots);
+    if (fill > best_fill + 1e-9) {
+      best_fill = fill;
+      best = L;
+    }
+  }
+  return best;
+}
 constexpr float kLog2e = 1.4426950408889634f;
 
 }  // namespace
@@ -219,7 +252,7 @@ extern "C" int ffpa_fwd(const ffpa_tensor_t* q, const ffpa_tensor_t* k, const ff
     p.group = (int)(c.Hq / c.Hkv);
     p.causal = causal;
     p.scale_log2 = scale * kLog2e;
-    p.split_len = 128;
+    p.split_len = decode_split_len(c.B, c.Hq, c.Nkv);
     p.n_splits = (int)((c.Nkv + p.split_len - 1) / p.split_len);
     p.status = status;
     const size_t n_rows = (size_t)c.B * c.Hq * c.Nq * p.n_splits;
@@ -344,7 +377,7 @@ extern "C" int ffpa_fwd_decode_noalloc(const ffpa_tensor_t* q, const ffpa_tensor
   p.group = (int)(c.Hq / c.Hkv);
   p.causal = causal;
   p.scale_log2 = scale * kLog2e;
-  p.split_len = 128;
+  p.split_len = decode_split_len(c.B, c.Hq, c.Nkv);
   p.n_splits = (int)((c.Nkv + p.split_len - 1) / p.split_len);
   p.status = device_status_word();  // fetched with cudaGetSymbolAddress, no allocation
   if (decode_scratch_bytes(p) > decode_noalloc_capacity_bytes()) return FFPA_ERR_SCRATCH_LIMIT;

@@ -123,7 +123,8 @@ int ffpa_bwd(const ffpa_tensor_t* q, const ffpa_tensor_t* k, const ffpa_tensor_t
  *   Arguments, layouts, results and validation exactly as ffpa_fwd, plus:
  *   - Nq must be <= 16, else FFPA_ERR_UNSUPPORTED.
  *   - The partials take (D + 2) * 4 bytes per (batch, query head, query row,
- *     slice of 128 keys); a call that needs more than 8 MiB returns
+ *     slice of keys; slices hold 128 to 256 keys, chosen per call so the
+ *     decode CTAs fill whole waves); a call that needs more than 8 MiB returns
  *     FFPA_ERR_SCRATCH_LIMIT and launches nothing (e.g. B=1, Hq=8, Nq=1,
  *     Nkv=8192, D=512 needs 1.05 MB).
  *   - The first call on a device looks up the array's device address (one

@@ -51,7 +51,8 @@ def test_noalloc_matches_decode_path_twice(B, Hq, Hkv, Nq, Nkv, D, dtype, causal
 
 
 def test_noalloc_refuses_oversized_call():
-    # B=8, Hq=8, Nq=16, Nkv=2048, D=1024: 8*8*16*16 slice rows * 1026 floats > 8 MiB
+    # B=8, Hq=8, Nq=16, Nkv=2048, D=1024: slices hold at most 256 keys, so at least
+    # 8*8*16*8 slice rows * 1026 floats (33.6 MB) > 8 MiB
     dev = torch.device("cuda")
     q = torch.zeros(8, 8, 16, 1024, dtype=torch.bfloat16, device=dev)
     k = torch.zeros(8, 8, 2048, 1024, dtype=torch.bfloat16, device=dev)
