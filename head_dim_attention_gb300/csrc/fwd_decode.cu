@@ -652,6 +652,10 @@ __device__ __forceinline__ float block_reduce(float v, bool is_max, float* red) 
 
 template <bool BF16>
 __global__ void __launch_bounds__(kCombThreads) decode_combine_kernel(const __grid_constant__ DecodeParams p) {
+  // Launched as a programmatic dependent of the split kernel: it may be
+  // scheduled before that grid ends, and waits here until the split grid has
+  // completed and its partials are visible.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   __shared__ float red[kCombThreads / 32];
   __shared__ float4 part[kCombThreads / 32][32];
   const int S = p.n_splits, D = p.D;
@@ -755,9 +759,21 @@ cudaError_t launch_decode_impl(const DecodeParams& p, cudaStream_t st) {
   timing_mark(st);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  decode_combine_kernel<BF16><<<dim3(p.Nq * ((p.D + 127) / 128), p.Hq, p.B), kCombThreads, 0, st>>>(p);
+  // programmatic dependent launch: the combine grid's launch overlaps the end
+  // of the split grid (it waits for the split grid's results in the kernel)
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(p.Nq * ((p.D + 127) / 128), p.Hq, p.B);
+  cfg.blockDim = dim3(kCombThreads, 1, 1);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, decode_combine_kernel<BF16>, p);
   timing_mark(st);
-  return cudaGetLastError();
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 }  // namespace
