@@ -107,7 +107,7 @@ def pin_gqa_repeat_interleave(m=ref):
 
 
 def _torch_sdpa(q, k, v, bias, causal, scale, gqa):
-    t = lambda x: torch.from_numpy(np.ascontiguousarray(x))
+    t = lambda x: torch.from_numpy(np.array(x, dtype=np.float64, copy=True))
     mask = None if bias is None else t(np.broadcast_to(bias, (q.shape[0], q.shape[1], q.shape[2], k.shape[2])))
     if causal:
         tri = torch.ones(q.shape[2], k.shape[2], dtype=torch.bool).tril()
