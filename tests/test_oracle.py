@@ -248,19 +248,6 @@ def test_lse_magnitude():
 
 
 # ---------------------------------------------------------------- the pins bite
-class _Mutant:
-    """A copy of the oracle's module namespace with one function replaced."""
-
-    def __init__(self, **over):
-        for name in dir(ref):
-            if not name.startswith("__"):
-                setattr(self, name, getattr(ref, name))
-        for name, fn in over.items():
-            setattr(self, name, fn)
-        # rebind the module-level helpers the public functions use
-        self._bound = over
-
-
 def _mutant_module(**over):
     import importlib.util
     spec = importlib.util.spec_from_file_location("attn_ref_mutant", ref.__file__)
@@ -337,6 +324,41 @@ def _mut_pv_transposed_v(mod):
     return f
 
 
+def _mut_sampled_dk_unscaled(mod):
+    orig = mod.attn_bwd_sampled
+
+    def f(q, k, v, do, b, h_kv, q_rows, kv_rows, bias=None, causal=False, scale=None, block=1024):
+        dq, dk, dv = orig(q, k, v, do, b, h_kv, q_rows, kv_rows, bias, causal, scale, block)
+        s = 1.0 / math.sqrt(np.shape(q)[3]) if scale is None else scale
+        return dq, dk / s, dv                             # scale dropped from dK
+    return f
+
+
+def _mut_sampled_dv_one_head(mod):
+    orig = mod.attn_bwd_sampled
+
+    def f(q, k, v, do, b, h_kv, q_rows, kv_rows, bias=None, causal=False, scale=None, block=1024):
+        # dV from the group's first query head only, scaled up: GQA sum replaced by a copy
+        q, do = np.asarray(q, dtype=np.float64), np.asarray(do, dtype=np.float64)
+        group = q.shape[1] // np.shape(k)[1]
+        first = h_kv * group
+        qq, dd = q.copy(), do.copy()
+        for h in range(first + 1, first + group):
+            qq[:, h], dd[:, h] = q[:, first], do[:, first]
+        dq, dk, _ = orig(q, k, v, do, b, h_kv, q_rows, kv_rows, bias, causal, scale, block)
+        _, _, dv = orig(qq, k, v, dd, b, h_kv, q_rows, kv_rows, bias, causal, scale, block)
+        return dq, dk, dv
+    return f
+
+
+def _mut_fwd_rows_next_head(mod):
+    orig = mod.attn_fwd_rows
+
+    def f(q, k, v, b, h, rows, bias=None, causal=False, scale=None):
+        return orig(q, k, v, b, (h + 1) % np.shape(q)[1], rows, bias, causal, scale)
+    return f
+
+
 MUTANTS = {
     "no_scale": {"scores_head": _mut_no_scale},
     "causal_flipped": {"scores_head": _mut_causal_flipped},
@@ -345,6 +367,9 @@ MUTANTS = {
     "bias_sign": {"_bias_rows": _mut_bias_sign},
     "bwd_delta_dropped": {"attn_bwd": _mut_bwd_delta_dropped},
     "pv_wrong_v": {"attn_fwd": _mut_pv_transposed_v},
+    "sampled_dk_unscaled": {"attn_bwd_sampled": _mut_sampled_dk_unscaled},
+    "sampled_dv_one_head": {"attn_bwd_sampled": _mut_sampled_dv_one_head},
+    "fwd_rows_next_head": {"attn_fwd_rows": _mut_fwd_rows_next_head},
 }
 
 
