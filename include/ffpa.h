@@ -102,8 +102,9 @@ int ffpa_fwd(const ffpa_tensor_t* q, const ffpa_tensor_t* k, const ffpa_tensor_t
  *   dq    [B, Hq, Nq, D]  written
  *   dk, dv [B, Hkv, Nkv, D] written (summed over the query heads of a group)
  *
- * No gradient is produced for the bias.  Delta (f32 [B, Hq, Nq]) lives in
- * stream-ordered scratch from cudaMallocAsync on `stream`.
+ * No gradient is produced for the bias.  Delta and lse in log2 units (f32
+ * [B, Hq, Nq] each) live in stream-ordered scratch from cudaMallocAsync on
+ * `stream`.
  */
 int ffpa_bwd(const ffpa_tensor_t* q, const ffpa_tensor_t* k, const ffpa_tensor_t* v,
              const ffpa_tensor_t* bias, int causal, float scale, const ffpa_tensor_t* out,
@@ -126,7 +127,7 @@ int ffpa_bwd(const ffpa_tensor_t* q, const ffpa_tensor_t* k, const ffpa_tensor_t
  *     slice of keys; slices hold 128 to 256 keys, chosen per call so the
  *     decode CTAs fill whole waves); a call that needs more than 8 MiB returns
  *     FFPA_ERR_SCRATCH_LIMIT and launches nothing (e.g. B=1, Hq=8, Nq=1,
- *     Nkv=8192, D=512 needs 1.05 MB).
+ *     Nkv=8192, D=512 takes 37 slices of 224 keys and needs 0.61 MB).
  *   - The first call on a device looks up the array's device address (one
  *     cudaGetSymbolAddress for that device); make that first call before
  *     any stream capture on the device.
