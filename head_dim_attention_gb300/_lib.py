@@ -72,6 +72,8 @@ def describe(t, as_lse: bool = False):
     """ffpa_tensor_t for a torch tensor (4-D; an lse [B,H,N] gets a trailing size-1 dim)."""
     if t is None:
         return None
+    if not t.is_cuda:
+        raise ValueError("ffpa tensors must be CUDA tensors (the library takes device pointers)")
     d = FfpaTensor()
     d.data = t.data_ptr()
     d.dtype = _dtype_code(t)

@@ -131,3 +131,11 @@ def test_bwd_rejects(lib):
     assert call(lse=None) == INVALID          # lse is required by the backward
     assert call(dk=t4([1, 4, 200, 512])) == INVALID
     assert call(q=t4([1, 4, 100, 320])) == INVALID
+
+
+def test_binding_rejects_host_tensors():
+    # the binding passes data pointers as device addresses: host tensors never reach the library
+    import torch
+    with pytest.raises(ValueError):
+        _lib.describe(torch.zeros(1, 1, 4, 64, dtype=torch.bfloat16))
+    assert _lib.describe(None) is None
