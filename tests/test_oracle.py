@@ -215,9 +215,53 @@ def pin_query_bias(m=ref):
     assert np.allclose(o1, o2, atol=1e-12) and np.allclose(l1, l2, atol=1e-12)
 
 
+def pin_torch_bias_broadcast(m=ref):
+    # Every broadcast form of the additive bias ([1,1,Nq,Nkv] per-query, [B,Hq,1,Nkv],
+    # [B,1,Nq,Nkv], [1,Hq,Nq,Nkv], [B,Hq,Nq,Nkv]) with distinct rows, heads and batches,
+    # against torch SDPA and autograd in fp64 (torch broadcasts the float mask itself);
+    # then the row-sampled forms of the oracle on the same biases against its full forms.
+    b, hq, hkv, nq, nkv, d = 2, 4, 2, 6, 9, 8
+    q, k, v, do = rand(b, hq, nq, d), rand(b, hkv, nkv, d), rand(b, hkv, nkv, d), rand(b, hq, nq, d)
+    scale = 1.0 / math.sqrt(d)
+    for shape in [(1, 1, nq, nkv), (b, hq, 1, nkv), (b, 1, nq, nkv), (1, hq, nq, nkv), (b, hq, nq, nkv)]:
+        bias = rand(*shape)
+        for causal in (False, True):
+            o, lse = m.attn_fwd(q, k, v, bias=bias, causal=causal)
+            tq, tk, tv = (torch.from_numpy(x.copy()).requires_grad_(True) for x in (q, k, v))
+            mask = torch.from_numpy(bias.copy())
+            if causal:
+                mask = mask + torch.zeros(nq, nkv, dtype=torch.float64).masked_fill(
+                    ~torch.ones(nq, nkv, dtype=torch.bool).tril(), float("-inf"))
+            out = torch.nn.functional.scaled_dot_product_attention(tq, tk, tv, attn_mask=mask, scale=scale,
+                                                                   enable_gqa=True)
+            assert np.allclose(o, out.detach().numpy(), atol=1e-12, rtol=1e-12), (shape, causal)
+            st = (torch.from_numpy(q) @ torch.from_numpy(k).repeat_interleave(hq // hkv, dim=1).transpose(-1, -2)
+                  * scale + mask)
+            assert np.allclose(lse, torch.logsumexp(st, dim=-1).numpy(), atol=1e-12), (shape, causal)
+            out.backward(torch.from_numpy(do))
+            dq, dk, dv = m.attn_bwd(q, k, v, do, bias=bias, causal=causal)
+            for mine, theirs in ((dq, tq), (dk, tk), (dv, tv)):
+                assert np.allclose(mine, theirs.grad.numpy(), atol=1e-11), (shape, causal)
+            rows = np.array([4, 1, 5])
+            for bi in range(b):
+                for h in range(hq):
+                    orow, lrow = m.attn_fwd_rows(q, k, v, bi, h, rows, bias=bias, causal=causal)
+                    assert np.allclose(orow, o[bi, h, rows], atol=1e-12), (shape, causal, bi, h)
+                    assert np.allclose(lrow, lse[bi, h, rows], atol=1e-12), (shape, causal, bi, h)
+            kr = np.array([8, 0, 3])
+            for bi in range(b):
+                for g in range(hkv):
+                    sdq, sdk, sdv = m.attn_bwd_sampled(q, k, v, do, bi, g, rows, kr, bias=bias, causal=causal,
+                                                       block=4)
+                    for h, val in sdq.items():
+                        assert np.allclose(val, dq[bi, h, rows], atol=1e-12), (shape, causal, bi, h)
+                    assert np.allclose(sdk, dk[bi, g, kr], atol=1e-12), (shape, causal, bi, g)
+                    assert np.allclose(sdv, dv[bi, g, kr], atol=1e-12), (shape, causal, bi, g)
+
+
 PINS = [pin_rows_sum_to_one, pin_constant_v, pin_zero_q, pin_causal_row0, pin_single_key, pin_bias_shift,
         pin_permutation, pin_gqa_repeat_interleave, pin_torch_sdpa, pin_torch_autograd, pin_finite_differences,
-        pin_bwd_sums, pin_sampled_bwd, pin_query_bias]
+        pin_bwd_sums, pin_sampled_bwd, pin_query_bias, pin_torch_bias_broadcast]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=[p.__name__ for p in PINS])
@@ -359,6 +403,38 @@ def _mut_fwd_rows_next_head(mod):
     return f
 
 
+def _bias_head(mod, pick_rows):
+    # _bias_rows with the broadcast done by hand, so a mutant can change one index
+    def f(bias, b, h, rows, nkv):
+        if bias is None:
+            return 0.0
+        bias = np.asarray(bias, dtype=np.float64)
+        bb = bias[b if bias.shape[0] > 1 else 0, h if bias.shape[1] > 1 else 0]
+        return pick_rows(bb, np.asarray(rows), nkv)
+    return f
+
+
+def _mut_bias_first_row(mod):
+    # a per-query bias read as if its first row applied to every query
+    return _bias_head(mod, lambda bb, rows, nkv: np.broadcast_to(bb[0], (len(rows), nkv)))
+
+
+def _mut_bias_row_shifted(mod):
+    # a per-query bias read one row late (clamped at the last row)
+    return _bias_head(mod, lambda bb, rows, nkv: bb[np.minimum(rows + 1, bb.shape[0] - 1)]
+                      if bb.shape[0] > 1 else np.broadcast_to(bb[0], (len(rows), nkv)))
+
+
+def _mut_bias_head_ignored(mod):
+    orig = mod._bias_rows
+    return lambda bias, b, h, rows, nkv: orig(bias, b, 0, rows, nkv)
+
+
+def _mut_bias_batch_ignored(mod):
+    orig = mod._bias_rows
+    return lambda bias, b, h, rows, nkv: orig(bias, 0, h, rows, nkv)
+
+
 MUTANTS = {
     "no_scale": {"scores_head": _mut_no_scale},
     "causal_flipped": {"scores_head": _mut_causal_flipped},
@@ -370,6 +446,10 @@ MUTANTS = {
     "sampled_dk_unscaled": {"attn_bwd_sampled": _mut_sampled_dk_unscaled},
     "sampled_dv_one_head": {"attn_bwd_sampled": _mut_sampled_dv_one_head},
     "fwd_rows_next_head": {"attn_fwd_rows": _mut_fwd_rows_next_head},
+    "bias_first_row": {"_bias_rows": _mut_bias_first_row},
+    "bias_row_shifted": {"_bias_rows": _mut_bias_row_shifted},
+    "bias_head_ignored": {"_bias_rows": _mut_bias_head_ignored},
+    "bias_batch_ignored": {"_bias_rows": _mut_bias_batch_ignored},
 }
 
 
@@ -385,3 +465,18 @@ def test_pins_catch_planted_mistake(name):
         except Exception:
             caught.append(pin.__name__ + "!")
     assert caught, f"no pin catches mutant {name}"
+
+
+@pytest.mark.parametrize("name", ["bias_first_row", "bias_row_shifted", "bias_head_ignored", "bias_batch_ignored"])
+def test_bias_broadcast_mutants_need_the_broadcast_pin(name):
+    # These mistakes in the per-query / per-head / per-batch bias branches slip past
+    # every pin that uses a key-position bias or equal rows; the broadcast pin alone
+    # catches them.
+    mod = _mutant_module(**MUTANTS[name])
+    caught = []
+    for pin in PINS:
+        try:
+            pin(mod)
+        except AssertionError:
+            caught.append(pin.__name__)
+    assert caught == ["pin_torch_bias_broadcast"], caught
