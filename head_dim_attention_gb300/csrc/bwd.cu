@@ -849,9 +849,9 @@ cudaError_t launch_all(const BwdParams& p, const BwdMaps& m, cudaStream_t st) {
 }  // namespace
 
 cudaError_t launch_bwd(const BwdParams& p, const BwdMaps& m, bool bf16, cudaStream_t s) {
-  if (bwd_pair_supported(p)) {
+  if (bwd_fulld_supported(p)) {
     cudaError_t e = bf16 ? launch_preprocess<true>(p, s) : launch_preprocess<false>(p, s);
-    return e != cudaSuccess ? e : launch_bwd_pair(p, m, bf16, s);
+    return e != cudaSuccess ? e : launch_bwd_fulld(p, m, bf16, s);
   }
   if (p.n_chunks <= 4) return bf16 ? launch_all<kSolo, true>(p, m, s) : launch_all<kSolo, false>(p, m, s);
   if (p.n_chunks <= 8) return bf16 ? launch_all<kRecompute, true>(p, m, s) : launch_all<kRecompute, false>(p, m, s);

@@ -107,6 +107,9 @@ cudaError_t launch_bwd(const BwdParams& p, const BwdMaps& m, bool bf16, cudaStre
 // CTA-pair dV, dK, dQ kernels (bwd_pair.cu): D = 512; the preprocess runs first.
 bool bwd_pair_supported(const BwdParams& p);
 cudaError_t launch_bwd_pair(const BwdParams& p, const BwdMaps& m, bool bf16, cudaStream_t s);
+// Full-D CTA-pair dV, dK, dQ kernels (bwd_fulld.cu): D = 512; the preprocess runs first.
+bool bwd_fulld_supported(const BwdParams& p);
+cudaError_t launch_bwd_fulld(const BwdParams& p, const BwdMaps& m, bool bf16, cudaStream_t s);
 
 uint32_t* device_status_word();  // per current device
 
