@@ -19,15 +19,25 @@
 // So every SM loads 96 KB per key tile instead of 192 KB, and its shared
 // memory serves 3 KB of MMA operands per 64-row-equivalent step instead of 4.
 //
-// Warp roles (256 threads per CTA): warps 0, 2, 3 TMA producers (each CTA
-// loads its own halves), warp 1 TMEM owner (both CTAs) and, in the first CTA
-// of the pair only, the MMA issuer; warps 4-7 softmax / correction / epilogue
-// for the CTA's own 128 query rows (thread = row = TMEM lane).
+// Two threads of the first CTA issue the pair's MMAs: a single thread spends
+// longer issuing a pair MMA, and waiting on a barrier, than the tensor core
+// needs for the MMA, so one issuer leaves the tensor core idle.  Thread A
+// issues the S products from a ring of K tiles, thread B the P V products
+// from a ring of V tiles; each ring has its own TMA producer.
+//
+// Warp roles (256 threads per CTA): warp 0 K producer, warp 3 V producer
+// (each CTA loads its own halves), warp 1 TMEM owner (both CTAs) and, in the
+// first CTA of the pair, MMA issuer A; warp 2 MMA issuer B (first CTA);
+// warps 4-7 softmax / correction / epilogue for the CTA's own 128 query rows
+// (thread = row = TMEM lane).
 //
 // Synchronisation across the pair: the issuing CTA's `full` barriers count
 // the bytes of both CTAs' loads; its commits arrive on the `empty`, `s_full`
-// and `o_ready` barriers of both CTAs; both CTAs' softmax warps arrive on the
-// issuing CTA's `p_ready`.  Every wait is bounded (see ptx.cuh).
+// and `pv_done` barriers of both CTAs; both CTAs' softmax warps arrive on the
+// issuing CTA's `p_ready`.  S_j and P_j share TMEM buffer j mod 2, so thread A
+// writes S_j only after P_{j-2} V completed (pv_done of that buffer), and the
+// softmax warps rescale O only after the previous P V completed.  Every wait
+// is bounded (see ptx.cuh).
 #include <type_traits>
 
 #include "internal.h"
@@ -37,7 +47,6 @@ namespace ffpa {
 namespace {
 
 constexpr int kThreads = 256;
-constexpr int kProducers = 3;                 // warps 0, 2 and 3
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kS0 = 256, kS1 = 384;      // TMEM columns of the two S/P buffers; O in [0, 256)
 constexpr float kRescaleLog2 = 8.0f;          // rescale O only when the max grows by > 2^8
@@ -46,24 +55,26 @@ constexpr int kChunks = 8;                    // D = 512: eight 64-column chunks
 constexpr int kQBytes = kChunks * kChunkBytes;        // resident query tile, 128 KB
 constexpr int kSlotBytes = 2 * kChunkBytes;           // ring slot: 4 half-key-tile K chunks or 2 V chunks
 constexpr int kHalfChunkBytes = kChunkBytes / 2;      // 64 keys x 64 columns
+constexpr int kKSlots = 2, kVSlots = 1;               // K ring (one key tile) and V ring
 
 struct Bars {
-  int full, empty, q_full, s_full, p_ready, o_ready, drain, count;
+  int full_k, empty_k, full_v, empty_v, q_full, s_full, p_ready, pv_done, drain_a, drain_b, count;
 };
-__host__ __device__ inline Bars bar_layout(int stages) {
-  Bars b;
-  b.full = 0;
-  b.empty = stages;
-  b.q_full = 2 * stages;
-  b.s_full = b.q_full + 1;   // 2
-  b.p_ready = b.s_full + 2;  // 2
-  b.o_ready = b.p_ready + 2;
-  b.drain = b.o_ready + 1;
-  b.count = b.drain + 1;
-  return b;
+__host__ __device__ constexpr Bars bar_layout() {
+  return Bars{0,
+              kKSlots,
+              2 * kKSlots,
+              2 * kKSlots + kVSlots,
+              2 * (kKSlots + kVSlots),
+              2 * (kKSlots + kVSlots) + 1,  // 2
+              2 * (kKSlots + kVSlots) + 3,  // 2
+              2 * (kKSlots + kVSlots) + 5,  // 2
+              2 * (kKSlots + kVSlots) + 7,
+              2 * (kKSlots + kVSlots) + 8,
+              2 * (kKSlots + kVSlots) + 9};
 }
 
-__host__ __device__ constexpr int smem_bytes(int stages) { return kQBytes + stages * kSlotBytes + 1024 + 1024; }
+__host__ __device__ constexpr int smem_bytes() { return kQBytes + (kKSlots + kVSlots) * kSlotBytes + 1024 + 1024; }
 
 template <bool BF16>
 __device__ __forceinline__ float2 unpack2(uint32_t w) {
@@ -90,15 +101,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const __grid_constant__ CUtensorMap map_v, const __grid_constant__ FwdParams p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  const int stages = p.stages;
-  const Bars bl = bar_layout(stages);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kQBytes + stages * kSlotBytes);
+  constexpr Bars bl = bar_layout();
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kQBytes + (kKSlots + kVSlots) * kSlotBytes);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + bl.count);
   // lo_flag[t & 1] == t + 1: tile t carries the residual term of P.  Only the
   // issuing CTA's copy is read; the peer's softmax warps write it remotely.
   volatile uint32_t* lo_flag = tmem_slot + 1;
   auto bar = [&](int i) { return smem_u32(&bars[i]); };
-  const uint32_t q_sm = smem_u32(smem), ring_sm = q_sm + kQBytes;
+  const uint32_t q_sm = smem_u32(smem), ring_k = q_sm + kQBytes, ring_v = ring_k + kKSlots * kSlotBytes;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const uint32_t rank = cluster_ctarank();  // 0 issues the pair's MMAs
@@ -117,17 +127,22 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto lead = [&](int i) { return rank == 0 ? bar(i) : mapa(bar(i), 0); };
 
   if (tid == 0) {
-    for (int i = 0; i < stages; ++i) {
-      mbar_init(bar(bl.full + i), 1);
-      mbar_init(bar(bl.empty + i), 1);
+    for (int i = 0; i < kKSlots; ++i) {
+      mbar_init(bar(bl.full_k + i), 1);
+      mbar_init(bar(bl.empty_k + i), 1);
+    }
+    for (int i = 0; i < kVSlots; ++i) {
+      mbar_init(bar(bl.full_v + i), 1);
+      mbar_init(bar(bl.empty_v + i), 1);
     }
     mbar_init(bar(bl.q_full), 1);
     for (int i = 0; i < 2; ++i) {
       mbar_init(bar(bl.s_full + i), 1);
       mbar_init(bar(bl.p_ready + i), 8);  // four softmax warps in each CTA
+      mbar_init(bar(bl.pv_done + i), 1);
     }
-    mbar_init(bar(bl.o_ready), 1);
-    mbar_init(bar(bl.drain), 1);
+    mbar_init(bar(bl.drain_a), 1);
+    mbar_init(bar(bl.drain_b), 1);
     lo_flag[0] = 0;
     lo_flag[1] = 0;
     fence_mbar_init();
@@ -142,131 +157,121 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tbase = *tmem_slot;
 
-  if (warp == 0 || warp == 2 || warp == 3) {
-    // ------------------------------------------------------------ TMA producers
-    // As in fwd_main.cu: producer pi issues every nprod-th slot load and waits
-    // only for its own slot; nprod <= stages keeps parity waits unambiguous.
+  if ((warp == 0 || warp == 3) && lane == 0) {
+    // ------------------------------------------------------------ TMA producers (K: warp 0, V: warp 3)
     // This CTA's slot s is free once the pair's MMAs reading it completed (the
     // issuing CTA's commit arrives on empty[s] here); the bytes are counted on
     // the issuing CTA's full[s], which that CTA arms for both halves.
-    const int nprod = min(kProducers, stages);
-    const int pi = (warp == 0) ? 0 : warp - 1;
-    if (lane == 0 && pi < nprod) {
+    const bool is_k = warp == 0;
+    const int S = is_k ? kKSlots : kVSlots;
+    const int full0 = is_k ? bl.full_k : bl.full_v, empty0 = is_k ? bl.empty_k : bl.empty_v;
+    const uint32_t ring = is_k ? ring_k : ring_v;
+    if (is_k) {
       tma_prefetch_desc(&map_q);
       tma_prefetch_desc(&map_kh);
+      if (rank == 0) mbar_expect_tx(bar(bl.q_full), 2 * kQBytes);
+      for (int c = 0; c < kChunks; ++c)
+        tma_load_4d_pair(q_sm + c * kChunkBytes, &map_q, lead(bl.q_full), c * kChunk, q0, h, b);
+    } else {
       tma_prefetch_desc(&map_v);
-      if (pi == 0) {
-        if (rank == 0) mbar_expect_tx(bar(bl.q_full), 2 * kQBytes);
-        for (int c = 0; c < kChunks; ++c)
-          tma_load_4d_pair(q_sm + c * kChunkBytes, &map_q, lead(bl.q_full), c * kChunk, q0, h, b);
+    }
+    bool ok = true;
+    uint32_t it = 0;
+    const int nslots = is_k ? 2 * ntiles : ntiles;
+    for (int n = 0; n < nslots && ok; ++n) {
+      const uint32_t s = it % S, r = it / S;
+      ++it;
+      ok = mbar_wait(bar(empty0 + s), (r & 1) ^ 1, status);
+      if (!ok) break;
+      if (rank == 0) mbar_expect_tx(bar(full0 + s), 2 * kSlotBytes);
+      const uint32_t dst = ring + s * kSlotBytes, fb = lead(full0 + s);
+      if (is_k) {
+        // chunks 4m .. 4m+3 of this CTA's 64 keys of key tile n / 2 (m = n mod 2)
+        const int m = n & 1, jt = n >> 1;
+        for (int i = 0; i < 4; ++i)
+          tma_load_4d_pair(dst + i * kHalfChunkBytes, &map_kh, fb, (4 * m + i) * kChunk,
+                           jt * kTileRows + 64 * static_cast<int>(rank), kvh, b);
+      } else {
+        // this CTA's two V chunks of the pair's O half, key tile n
+        for (int i = 0; i < 2; ++i)
+          tma_load_4d_pair(dst + i * kChunkBytes, &map_v, fb, (4 * dh + 2 * static_cast<int>(rank) + i) * kChunk,
+                           n * kTileRows, kvh, b);
       }
-      bool ok = true;
-      uint32_t it = 0;
-      auto slot = [&](bool is_k, int j) {
-        if (ok && static_cast<int>(it % nprod) == pi) {
-          const uint32_t s = it % stages, r = it / stages;
-          ok = mbar_wait(bar(bl.empty + s), (r & 1) ^ 1, status);
-          if (ok) {
-            if (rank == 0) mbar_expect_tx(bar(bl.full + s), 2 * kSlotBytes);
-            const uint32_t dst = ring_sm + s * kSlotBytes, fb = lead(bl.full + s);
-            if (is_k) {
-              // chunks 4m .. 4m+3 of this CTA's 64 keys of key tile j (m = slot parity within the tile)
-              const int m = j & 1, jt = j >> 1;
-              for (int i = 0; i < 4; ++i)
-                tma_load_4d_pair(dst + i * kHalfChunkBytes, &map_kh, fb, (4 * m + i) * kChunk,
-                                 jt * kTileRows + 64 * static_cast<int>(rank), kvh, b);
-            } else {
-              // this CTA's two V chunks of the pair's O half, key tile j
-              for (int i = 0; i < 2; ++i)
-                tma_load_4d_pair(dst + i * kChunkBytes, &map_v, fb, (4 * dh + 2 * static_cast<int>(rank) + i) * kChunk,
-                                 j * kTileRows, kvh, b);
-            }
-          }
-        }
+    }
+    // Drain: wait for the last release of each slot, so no commit arrival is
+    // in flight when the CTA exits.
+    for (uint32_t s = 0; s < static_cast<uint32_t>(S) && s < it && ok; ++s) {
+      const uint32_t last = s + ((it - 1 - s) / S) * S;
+      mbar_wait(bar(empty0 + s), (last / S) & 1, status);
+    }
+  } else if (warp == 1 && lane == 0 && rank == 0) {
+    // ------------------------------------------------------------ MMA issuer A: S_j = Q K_j^T
+    constexpr uint32_t idesc_s = idesc_f16(BF16, 256, 128, false, false);  // 2 x 128 query rows x 128 keys
+    const uint64_t dq = sdesc_sw128(q_sm, 16, 1024);                        // Q chunks, K-major
+    const uint64_t dk = sdesc_sw128(ring_k, 16, 1024);                      // half-tile K chunks, K-major
+    bool ok = mbar_wait(bar(bl.q_full), 0, status);
+    tc_fence_after();
+    uint32_t it = 0;
+    for (int j = 0; j < ntiles && ok; ++j) {
+      // S_j lands in the TMEM buffer that held P_{j-2}: wait for P_{j-2} V.
+      if (j >= 2) {
+        ok = mbar_wait(bar(bl.pv_done + (j & 1)), ((j - 2) >> 1) & 1, status);
+        if (!ok) break;
+        tc_fence_after();
+      }
+      const uint32_t s_tm = tbase + ((j & 1) ? kS1 : kS0);
+      for (int m = 0; m < 2 && ok; ++m) {
+        const uint32_t s = it % kKSlots;
+        ok = mbar_wait(bar(bl.full_k + s), (it / kKSlots) & 1, status);
         ++it;
-      };
-      for (int j = 0; j <= ntiles && ok; ++j) {
-        if (j < ntiles) {
-          slot(true, 2 * j);
-          slot(true, 2 * j + 1);
+        if (!ok) break;
+        tc_fence_after();
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const uint64_t a = sdesc_advance(dq, (4 * m + i) * kChunkBytes);
+          const uint64_t bd = sdesc_advance(dk, s * kSlotBytes + i * kHalfChunkBytes);
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            umma_ss_pair(s_tm, sdesc_advance(a, kk * 32), sdesc_advance(bd, kk * 32), idesc_s, (m | i | kk) != 0);
         }
-        if (j >= 1) slot(false, j - 1);
+        umma_commit_pair(bar(bl.empty_k + s), 3);
       }
-      // Drain: wait for the last release of each slot whose last load was ours,
-      // so no commit arrival is in flight when the CTA exits.
-      for (uint32_t s = 0; s < static_cast<uint32_t>(stages) && s < it; ++s) {
-        const uint32_t last = s + ((it - 1 - s) / stages) * stages;
-        if (static_cast<int>(last % nprod) == pi) mbar_wait(bar(bl.empty + s), (last / stages) & 1, status);
-      }
-      if (pi == 0 && rank == 0) mbar_wait(bar(bl.q_full), 0, status);
+      if (!ok) break;
+      umma_commit_pair(bar(bl.s_full + (j & 1)), 3);
     }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer (first CTA of the pair)
-    if (lane == 0 && rank == 0) {
-      const uint32_t idesc_s = idesc_f16(BF16, 256, 128, false, false);  // 2 x 128 query rows x 128 keys
-      const uint32_t idesc_pv = idesc_f16(BF16, 256, 256, false, true);  // 2 x 128 query rows x 256 O columns
-      const uint64_t dq = sdesc_sw128(q_sm, 16, 1024);                    // Q chunks, K-major
-      const uint64_t dk = sdesc_sw128(ring_sm, 16, 1024);                 // half-tile K chunks, K-major
-      const uint64_t dv = sdesc_sw128(ring_sm, kChunkBytes, 1024);        // V chunks, MN-major
-      bool ok = mbar_wait(bar(bl.q_full), 0, status);
+    umma_commit_pair(bar(bl.drain_a), 1);
+    mbar_wait(bar(bl.drain_a), 0, status);
+  } else if (warp == 2 && lane == 0 && rank == 0) {
+    // ------------------------------------------------------------ MMA issuer B: O += P_t V_t
+    constexpr uint32_t idesc_pv = idesc_f16(BF16, 256, 256, false, true);  // 2 x 128 query rows x 256 O columns
+    const uint64_t dv = sdesc_sw128(ring_v, kChunkBytes, 1024);            // V chunks, MN-major
+    bool ok = true;
+    uint32_t it = 0;
+    for (int t = 0; t < ntiles && ok; ++t) {
+      ok = mbar_wait(bar(bl.p_ready + (t & 1)), (t >> 1) & 1, status);
+      if (!ok) break;
       tc_fence_after();
-      uint32_t it = 0;
-      for (int j = 0; j <= ntiles && ok; ++j) {
-        if (j < ntiles) {
-          // S_j lands in the buffer that held P_{j-2}, which the P_{j-2} V
-          // product (issued earlier by this thread) reads.  MMAs issued by one
-          // thread form an implicitly pipelined sequence that executes in issue
-          // order, so no wait is needed between that read and this write.
-          const int t = j;
-          const uint32_t s_tm = tbase + ((t & 1) ? kS1 : kS0);
-          for (int m = 0; m < 2 && ok; ++m) {
-            const uint32_t s = it % stages;
-            ok = mbar_wait(bar(bl.full + s), (it / stages) & 1, status);
-            if (!ok) break;
-            tc_fence_after();
-            for (int i = 0; i < 4; ++i) {
-              const int c = 4 * m + i;
-              const uint64_t a = sdesc_advance(dq, c * kChunkBytes);
-              const uint64_t bd = sdesc_advance(dk, s * kSlotBytes + i * kHalfChunkBytes);
+      const uint32_t p_tm = tbase + ((t & 1) ? kS1 : kS0);
+      const uint32_t s = it % kVSlots;
+      ok = mbar_wait(bar(bl.full_v + s), (it / kVSlots) & 1, status);
+      ++it;
+      if (!ok) break;
+      tc_fence_after();
+      const uint64_t bd = sdesc_advance(dv, s * kSlotBytes);
+      const uint32_t acc0 = t > 0 ? 1u : 0u;
 #pragma unroll
-              for (int kk = 0; kk < 4; ++kk)
-                umma_ss_pair(s_tm, sdesc_advance(a, kk * 32), sdesc_advance(bd, kk * 32), idesc_s, (c | kk) != 0);
-            }
-            umma_commit_pair(bar(bl.empty + s), 3);
-            ++it;
-          }
-          if (!ok) break;
-          umma_commit_pair(bar(bl.s_full + (t & 1)), 3);
-        }
-        if (j >= 1) {
-          const int t = j - 1;
-          ok = mbar_wait(bar(bl.p_ready + (t & 1)), (t >> 1) & 1, status);
-          if (!ok) break;
-          tc_fence_after();
-          const bool use_lo = lo_flag[t & 1] == static_cast<uint32_t>(t + 1);
-          const uint32_t p_tm = tbase + ((t & 1) ? kS1 : kS0);
-          const uint32_t s = it % stages;
-          ok = mbar_wait(bar(bl.full + s), (it / stages) & 1, status);
-          if (!ok) break;
-          tc_fence_after();
-          const uint64_t bd = sdesc_advance(dv, s * kSlotBytes);
-          const uint32_t acc0 = t > 0 ? 1u : 0u;
+      for (int kk = 0; kk < 8; ++kk)
+        umma_ts_pair(tbase, p_tm + kk * 8, sdesc_advance(bd, kk * 2048), idesc_pv, acc0 | (kk > 0));
+      if (lo_flag[t & 1] == static_cast<uint32_t>(t + 1)) {
 #pragma unroll
-          for (int kk = 0; kk < 8; ++kk)
-            umma_ts_pair(tbase, p_tm + kk * 8, sdesc_advance(bd, kk * 2048), idesc_pv, acc0 | (kk > 0));
-          if (use_lo) {
-#pragma unroll
-            for (int kk = 0; kk < 8; ++kk)  // the P_lo term
-              umma_ts_pair(tbase, p_tm + 64 + kk * 8, sdesc_advance(bd, kk * 2048), idesc_pv, 1u);
-          }
-          umma_commit_pair(bar(bl.empty + s), 3);
-          ++it;
-          umma_commit_pair(bar(bl.o_ready), 3);
-        }
+        for (int kk = 0; kk < 8; ++kk)  // the P_lo term
+          umma_ts_pair(tbase, p_tm + 64 + kk * 8, sdesc_advance(bd, kk * 2048), idesc_pv, 1u);
       }
-      umma_commit_pair(bar(bl.drain), 1);
-      mbar_wait(bar(bl.drain), 0, status);
+      umma_commit_pair(bar(bl.empty_v + s), 3);
+      umma_commit_pair(bar(bl.pv_done + (t & 1)), 3);
     }
+    umma_commit_pair(bar(bl.drain_b), 1);
+    mbar_wait(bar(bl.drain_b), 0, status);
   } else if (warp >= 4) {
     // ------------------------------------------------------------ softmax / correction / epilogue
     const int r = tid - 128;  // query row within this CTA's tile == TMEM lane
@@ -335,15 +340,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         ls[i & 3] += s[i];
       }
       l_sum = l_sum * alpha + ((ls[0] + ls[1]) + (ls[2] + ls[3]));
+      // the residual term of P on this tile if some row's largest weight
+      // exceeds 1/64 of its running sum (this tile included)
       const bool warp_lo = __any_sync(0xffffffffu, ex2(m_tile - m_ref) > kLoFrac * l_sum);
-      if (j >= 1) {
-        // P_j overwrites TMEM that the P_{j-1} V product may still read, and
-        // the correction below rewrites O: wait for that product first.
-        ok = __all_sync(0xffffffffu, mbar_wait(bar(bl.o_ready), (t - 1) & 1, status));
+      // The correction rewrites O: wait for P_{j-1} V first.  P_{j+1} V cannot
+      // have completed yet, so the parity of that phase is unambiguous even
+      // when earlier tiles skipped this wait.
+      const bool warp_rescale = __any_sync(0xffffffffu, rescale) && j >= 1;
+      if (warp_rescale) {
+        ok = __all_sync(0xffffffffu, mbar_wait(bar(bl.pv_done + ((t - 1) & 1)), ((t - 1) >> 1) & 1, status));
         if (!ok) break;
         tc_fence_after();
-      }
-      if (__any_sync(0xffffffffu, rescale) && j >= 1) {
         for (int c = 0; c < 4; ++c) {  // O of this row *= alpha
 #pragma unroll
           for (int hh = 0; hh < 2; ++hh) {
@@ -357,8 +364,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
-      // P as the rounded value (columns 0..63) and, where needed, its rounding
-      // residual (columns 64..127; zeros from warps that do not need it).
+      // P_j goes to the buffer S_j arrived in (its previous P V completed before
+      // S_j was issued): the rounded value (columns 0..63) and, where needed, its
+      // rounding residual (columns 64..127; zeros from warps that do not need it).
       if (warp_lo) {
 #pragma unroll
         for (int g = 0; g < 4; ++g) {
@@ -402,7 +410,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (ok) {
       // ---------------------------------------------------------- epilogue
-      ok = __all_sync(0xffffffffu, mbar_wait(bar(bl.o_ready), (ntiles - 1) & 1, status));
+      // the last P V of each buffer (their commits also arrive on the peer CTA)
+      ok = __all_sync(0xffffffffu, mbar_wait(bar(bl.pv_done + ((ntiles - 1) & 1)), ((ntiles - 1) >> 1) & 1, status));
+      if (ok && ntiles >= 2)
+        ok = __all_sync(0xffffffffu, mbar_wait(bar(bl.pv_done + (ntiles & 1)), ((ntiles - 2) >> 1) & 1, status));
       if (ok) {
         tc_fence_after();
         const float inv_l = l_sum > 0.f ? 1.f / l_sum : 0.f;
@@ -449,13 +460,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 template <bool BF16>
 cudaError_t launch_impl(const FwdParams& p_in, const FwdMaps& m, cudaStream_t st) {
   FwdParams p = p_in;
-  constexpr int kMaxSmem = 232448;  // 227 KB opt-in per block
-  int stages = (kMaxSmem - smem_bytes(0)) / kSlotBytes;
-  stages = min(stages, 4);
-  if (stages < 2) return cudaErrorInvalidConfiguration;
-  p.stages = stages;
+  constexpr int smem = smem_bytes();
+  static_assert(smem <= 232448, "227 KB opt-in per block");
+  p.stages = kKSlots + kVSlots;
   p.slot_chunks = 2;
-  const int smem = smem_bytes(stages);
   auto kern = fwd_pair_kernel<BF16>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
