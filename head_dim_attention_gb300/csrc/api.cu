@@ -405,7 +405,7 @@ extern "C" int ffpa_check_status(ffpa_stream_t stream) {
   if (v != 0) {
     const uint32_t zero = 0;
     if (cudaMemcpyToSymbol(g_status_word, &zero, sizeof(zero)) != cudaSuccess) return FFPA_ERR_CUDA;
-    return FFPA_ERR_TIMEOUT;
+    return v == FFPA_DEV_TIMEOUT ? FFPA_ERR_TIMEOUT : FFPA_ERR_CUDA;
   }
   return FFPA_OK;
 }

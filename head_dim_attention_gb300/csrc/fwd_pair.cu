@@ -25,11 +25,16 @@
 // issues the S products from a ring of K tiles, thread B the P V products
 // from a ring of V tiles; each ring has its own TMA producer.
 //
-// Warp roles (256 threads per CTA): warp 0 K producer, warp 3 V producer
+// Warp roles (384 threads per CTA): warp 0 K producer, warp 3 V producer
 // (each CTA loads its own halves), warp 1 TMEM owner (both CTAs) and, in the
 // first CTA of the pair, MMA issuer A; warp 2 MMA issuer B (first CTA);
-// warps 4-7 softmax / correction / epilogue for the CTA's own 128 query rows
-// (thread = row = TMEM lane).
+// warps 4-11 softmax / correction / epilogue for the CTA's own 128 query rows:
+// warps 4-7 take keys 0..63 of every key tile and O columns 0..127 of the
+// half, warps 8-11 keys 64..127 and O columns 128..255 (thread = row = TMEM
+// lane; two warps per row quadrant, so each SM sub-partition runs two softmax
+// warps that hide each other's latencies).  The two threads of a row swap
+// their partial row maxima and sums through shared memory at a named barrier
+// of the two warps.
 //
 // Synchronisation across the pair: the issuing CTA's `full` barriers count
 // the bytes of both CTAs' loads; its commits arrive on the `empty`, `s_full`
@@ -46,7 +51,7 @@
 namespace ffpa {
 namespace {
 
-constexpr int kThreads = 256;
+constexpr int kThreads = 384;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kS0 = 256, kS1 = 384;      // TMEM columns of the two S/P buffers; O in [0, 256)
 constexpr float kRescaleLog2 = 8.0f;          // rescale O only when the max grows by > 2^8
@@ -74,7 +79,25 @@ __host__ __device__ constexpr Bars bar_layout() {
               2 * (kKSlots + kVSlots) + 9};
 }
 
-__host__ __device__ constexpr int smem_bytes() { return kQBytes + (kKSlots + kVSlots) * kSlotBytes + 1024 + 1024; }
+// Q, the rings, 256 bytes of barriers and flags, and the row-statistics
+// exchange (2 x 2 x 128 floats).  There is no room for alignment padding: the
+// kernel checks that dynamic shared memory starts on a 1024-byte boundary.
+constexpr int kBarArea = 256, kXchBytes = 2 * 2 * 128 * 4;
+__host__ __device__ constexpr int smem_bytes() {
+  return kQBytes + (kKSlots + kVSlots) * kSlotBytes + kBarArea + kXchBytes;
+}
+
+// Named barrier of the two softmax warps of one row quadrant that returns the
+// AND of their predicates (both warps then take the same branch).
+__device__ __forceinline__ bool pair_bar_and(uint32_t id, bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\tbar.red.and.pred q, %2, 64, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"(static_cast<uint32_t>(v)), "r"(id)
+      : "memory");
+  return r != 0;
+}
 
 template <bool BF16>
 __device__ __forceinline__ float2 unpack2(uint32_t w) {
@@ -100,9 +123,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     fwd_pair_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_kh,
                     const __grid_constant__ CUtensorMap map_v, const __grid_constant__ FwdParams p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  if (smem_u32(smem_raw) & 1023u) {  // the same in both CTAs of the pair: both leave here
+    if (threadIdx.x == 0) record_error(p.status, FFPA_DEV_LAYOUT);
+    return;
+  }
+  uint8_t* smem = smem_raw;
   constexpr Bars bl = bar_layout();
+  static_assert(bl.count * 8 + 16 <= kBarArea, "barrier area");
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kQBytes + (kKSlots + kVSlots) * kSlotBytes);
+  float* xch = reinterpret_cast<float*>(smem + kQBytes + (kKSlots + kVSlots) * kSlotBytes + kBarArea);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + bl.count);
   // lo_flag[t & 1] == t + 1: tile t carries the residual term of P.  Only the
   // issuing CTA's copy is read; the peer's softmax warps write it remotely.
@@ -138,7 +167,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(bar(bl.q_full), 1);
     for (int i = 0; i < 2; ++i) {
       mbar_init(bar(bl.s_full + i), 1);
-      mbar_init(bar(bl.p_ready + i), 8);  // four softmax warps in each CTA
+      mbar_init(bar(bl.p_ready + i), 16);  // eight softmax warps in each CTA
       mbar_init(bar(bl.pv_done + i), 1);
     }
     mbar_init(bar(bl.drain_a), 1);
@@ -274,9 +303,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_wait(bar(bl.drain_b), 0, status);
   } else if (warp >= 4) {
     // ------------------------------------------------------------ softmax / correction / epilogue
-    const int r = tid - 128;  // query row within this CTA's tile == TMEM lane
+    const int wq = warp & 3;          // row quadrant (TMEM lanes 32 wq ..)
+    const int kh = (warp - 4) >> 2;   // 0: keys 0..63 and O columns 0..127; 1: keys 64..127, O 128..255
+    const int r = 32 * wq + lane;     // query row within this CTA's tile == TMEM lane
     const int row = q0 + r;
-    const uint32_t lane_off = static_cast<uint32_t>((warp - 4) * 32) << 16;
+    const uint32_t lane_off = static_cast<uint32_t>(32 * wq) << 16;
+    const uint32_t nb = 1 + wq;       // named barrier of this quadrant's two warps
+    float* xmax = xch + 0 * 256;      // [kh][row]
+    float* xsum = xch + 1 * 256;
     const float* bias_row = nullptr;
     if (p.bias)
       bias_row = p.bias + b * p.bias_sb + h * p.bias_sh + static_cast<int64_t>(min(row, p.Nq - 1)) * p.bias_sq;
@@ -284,45 +318,50 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t p_ready_lead0 = lead(bl.p_ready), p_ready_lead1 = lead(bl.p_ready + 1);
     const uint32_t lo_flag_lead = rank == 0 ? 0u : mapa(smem_u32(const_cast<uint32_t*>(lo_flag)), 0);
     bool ok = true;
-    float m_used = -INFINITY, l_sum = 0.f;
+    float m_used = -INFINITY, l_own = 0.f, l_sum = 0.f;  // l_sum: both halves of the row
     for (int j = 0; j < ntiles; ++j) {
       const int t = j;
       const uint32_t s_col = (t & 1) ? kS1 : kS0;
-      ok = __all_sync(0xffffffffu, mbar_wait(bar(bl.s_full + (t & 1)), (t >> 1) & 1, status));
-      if (!ok) break;
-      tc_fence_after();
-      float s[128];
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        uint32_t v[32];
-        tmem_ld32(tbase + lane_off + s_col + c * 32, v);
+      const bool got = __all_sync(0xffffffffu, mbar_wait(bar(bl.s_full + (t & 1)), (t >> 1) & 1, status));
+      float s[64];
+      if (got) {
+        tc_fence_after();
+        uint32_t v0[32], v1[32];
+        tmem_ld32(tbase + lane_off + s_col + 64 * kh, v0);
+        tmem_ld32(tbase + lane_off + s_col + 64 * kh + 32, v1);
         tmem_ld_wait();
 #pragma unroll
-        for (int i = 0; i < 32; ++i) s[c * 32 + i] = __uint_as_float(v[i]);
+        for (int i = 0; i < 32; ++i) {
+          s[i] = __uint_as_float(v0[i]);
+          s[32 + i] = __uint_as_float(v1[i]);
+        }
       }
-      const int kv0 = j * kTileRows;
-      const bool masked = (kv0 + kTileRows > p.Nkv) || (p.causal && kv0 + kTileRows - 1 > row);
-      const float c_scale = p.scale_log2;
+      const int kv0 = j * kTileRows + 64 * kh;  // this thread's first key of the tile
+      const bool masked = (kv0 + 64 > p.Nkv) || (p.causal && kv0 + 63 > row);
+      // Scores in the log2 domain: x = s scale log2e (+ bias log2e).  Without a
+      // bias the scale is applied inside the exponent below (it is positive,
+      // so the maximum of s gives the maximum of x).
+      const float c_scale = bias_row ? 1.f : p.scale_log2;
       if (bias_row) {
 #pragma unroll
-        for (int i = 0; i < 128; ++i)
-          s[i] = fmaf(__ldg(bias_row + static_cast<int64_t>(kv0 + min(i, p.Nkv - 1 - kv0)) * p.bias_sk), kLog2e,
-                      s[i] * c_scale);
-      } else {
-#pragma unroll
-        for (int i = 0; i < 128; ++i) s[i] *= c_scale;
+        for (int i = 0; i < 64; ++i)
+          s[i] = fmaf(__ldg(bias_row + static_cast<int64_t>(min(kv0 + i, p.Nkv - 1)) * p.bias_sk), kLog2e,
+                      s[i] * p.scale_log2);
       }
       if (masked) {
 #pragma unroll
-        for (int i = 0; i < 128; ++i) {
+        for (int i = 0; i < 64; ++i) {
           const int kv = kv0 + i;
           if (kv >= p.Nkv || (p.causal && kv > row)) s[i] = -INFINITY;
         }
       }
       float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-      for (int i = 0; i < 128; ++i) mx[i & 3] = fmaxf(mx[i & 3], s[i]);
-      const float m_tile = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+      for (int i = 0; i < 64; ++i) mx[i & 3] = fmaxf(mx[i & 3], s[i]);
+      xmax[128 * kh + r] = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * c_scale;
+      ok = pair_bar_and(nb, got);  // both warps of the quadrant see the same outcome
+      if (!ok) break;
+      const float m_tile = fmaxf(xmax[r], xmax[128 + r]);
       float alpha = 1.f;
       bool rescale = false;
       if (m_used == -INFINITY) {
@@ -335,27 +374,32 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float m_ref = (m_used == -INFINITY) ? 0.f : m_used;
       float ls[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int i = 0; i < 128; ++i) {
-        s[i] = ex2(s[i] - m_ref);  // P, in place
+      for (int i = 0; i < 64; ++i) {
+        s[i] = ex2(fmaf(s[i], c_scale, -m_ref));  // P, in place
         ls[i & 3] += s[i];
       }
-      l_sum = l_sum * alpha + ((ls[0] + ls[1]) + (ls[2] + ls[3]));
+      l_own = l_own * alpha + ((ls[0] + ls[1]) + (ls[2] + ls[3]));
+      xsum[128 * kh + r] = l_own;
+      pair_bar_and(nb, true);
+      l_sum = xsum[r] + xsum[128 + r];
       // the residual term of P on this tile if some row's largest weight
-      // exceeds 1/64 of its running sum (this tile included)
+      // exceeds 1/64 of its running sum (this tile included); the same in both
+      // warps of a quadrant
       const bool warp_lo = __any_sync(0xffffffffu, ex2(m_tile - m_ref) > kLoFrac * l_sum);
       // The correction rewrites O: wait for P_{j-1} V first.  P_{j+1} V cannot
       // have completed yet, so the parity of that phase is unambiguous even
       // when earlier tiles skipped this wait.
-      const bool warp_rescale = __any_sync(0xffffffffu, rescale) && j >= 1;
-      if (warp_rescale) {
-        ok = __all_sync(0xffffffffu, mbar_wait(bar(bl.pv_done + ((t - 1) & 1)), ((t - 1) >> 1) & 1, status));
+      if (__any_sync(0xffffffffu, rescale) && j >= 1) {  // the same in both warps of the quadrant
+        const bool done =
+            __all_sync(0xffffffffu, mbar_wait(bar(bl.pv_done + ((t - 1) & 1)), ((t - 1) >> 1) & 1, status));
+        ok = pair_bar_and(nb, done);
         if (!ok) break;
         tc_fence_after();
-        for (int c = 0; c < 4; ++c) {  // O of this row *= alpha
+        for (int c = 0; c < 2; ++c) {  // this thread's 128 O columns *= alpha
 #pragma unroll
           for (int hh = 0; hh < 2; ++hh) {
             uint32_t v[32];
-            const uint32_t a = tbase + lane_off + c * kChunk + hh * 32;
+            const uint32_t a = tbase + lane_off + (2 * kh + c) * kChunk + hh * 32;
             tmem_ld32(a, v);
             tmem_ld_wait();
 #pragma unroll
@@ -366,10 +410,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       // P_j goes to the buffer S_j arrived in (its previous P V completed before
       // S_j was issued): the rounded value (columns 0..63) and, where needed, its
-      // rounding residual (columns 64..127; zeros from warps that do not need it).
+      // rounding residual (columns 64..127; zeros from warps that do not need
+      // it); this thread's keys are columns 32 kh .. 32 kh + 31 of each.
       if (warp_lo) {
 #pragma unroll
-        for (int g = 0; g < 4; ++g) {
+        for (int g = 0; g < 2; ++g) {
           uint32_t hi[16], lo[16];
 #pragma unroll
           for (int e = 0; e < 16; ++e) {
@@ -378,20 +423,20 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float2 hv = unpack2<BF16>(hi[e]);
             lo[e] = pack2<BF16>(p0 - hv.x, p1 - hv.y);
           }
-          tmem_st16(tbase + lane_off + s_col + 16 * g, hi);
-          tmem_st16(tbase + lane_off + s_col + 64 + 16 * g, lo);
+          tmem_st16(tbase + lane_off + s_col + 32 * kh + 16 * g, hi);
+          tmem_st16(tbase + lane_off + s_col + 64 + 32 * kh + 16 * g, lo);
         }
       } else {
         uint32_t zero[16];
 #pragma unroll
         for (int e = 0; e < 16; ++e) zero[e] = 0u;
 #pragma unroll
-        for (int g = 0; g < 4; ++g) {
+        for (int g = 0; g < 2; ++g) {
           uint32_t hi[16];
 #pragma unroll
           for (int e = 0; e < 16; ++e) hi[e] = pack2<BF16>(s[32 * g + 2 * e], s[32 * g + 2 * e + 1]);
-          tmem_st16(tbase + lane_off + s_col + 16 * g, hi);
-          tmem_st16(tbase + lane_off + s_col + 64 + 16 * g, zero);
+          tmem_st16(tbase + lane_off + s_col + 32 * kh + 16 * g, hi);
+          tmem_st16(tbase + lane_off + s_col + 64 + 32 * kh + 16 * g, zero);
         }
       }
       tmem_st_wait();
@@ -419,7 +464,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float inv_l = l_sum > 0.f ? 1.f / l_sum : 0.f;
         typedef typename std::conditional<BF16, __nv_bfloat16, __half>::type T;
         T* orow = reinterpret_cast<T*>(p.out) + b * p.o_sb + h * p.o_sh + static_cast<int64_t>(row) * p.o_sn;
-        for (int c = 0; c < 4; ++c) {
+        for (int c = 2 * kh; c < 2 * kh + 2; ++c) {
 #pragma unroll
           for (int hh = 0; hh < 2; ++hh) {
             uint32_t v[32];
@@ -439,7 +484,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
         }
-        if (dh == 0 && p.lse && row < p.Nq) {
+        if (dh == 0 && kh == 0 && p.lse && row < p.Nq) {
           constexpr float kLn2 = 0.6931471805599453f;
           p.lse[(static_cast<int64_t>(b) * p.Hq + h) * p.Nq + row] =
               l_sum > 0.f ? (m_used + __log2f(l_sum)) * kLn2 : -INFINITY;

@@ -7,6 +7,13 @@
 
 namespace ffpa {
 
+// Device status word values (written with atomicCAS so the first error wins).
+enum : uint32_t {
+  FFPA_DEV_OK = 0,
+  FFPA_DEV_TIMEOUT = 1,
+  FFPA_DEV_LAYOUT = 2,  // dynamic shared memory not on the boundary a kernel's layout needs
+};
+
 constexpr int kTileRows = 128;  // query/key rows per tile (the MMA M)
 constexpr int kChunk = 64;      // D columns per chunk (one 128-byte swizzled row)
 constexpr int kChunkBytes = kTileRows * kChunk * 2;  // 16 KB

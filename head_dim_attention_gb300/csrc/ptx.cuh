@@ -12,17 +12,14 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
+#include "internal.h"
+
 #ifndef FFPA_WAIT_NS
 #define FFPA_WAIT_NS 250000000ull  // 250 ms per wait
 #endif
 
 namespace ffpa {
 
-// Device status word values (written with atomicCAS so the first error wins).
-enum : uint32_t {
-  FFPA_DEV_OK = 0,
-  FFPA_DEV_TIMEOUT = 1,
-};
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
