@@ -25,20 +25,34 @@
 //                  reduced over the eight 64-column chunks of D
 //   X2 = dP        the same with the second stationary operand (dK, dQ)
 //   dS (or P)      elementwise, rounded to the input type, written to shared
-//                  memory as the K-major A operand (64 rows x 128 columns)
-//   gradient       four quarters of D, M=128, N=128: CTA c supplies the 64
-//                  columns 128 qd + 64 c .. of the column operand (MN-major)
+//                  memory as the K-major A operand (64 rows x 128 columns), in
+//                  two buffers used by alternate column tiles, so the
+//                  elementwise warps write one while the gradient MMAs read
+//                  the other
+//   gradient       dK, dQ: four quarters of D, M=128, N=128: CTA c supplies
+//                  the 64 columns 128 qd + 64 c .. of the column operand
+//                  (MN-major); dV: two halves of D, M=128, N=256: CTA c
+//                  supplies the 128 columns 256 h + 128 c ..
 // Each of these pair MMAs costs the issuing thread more time than the tensor
 // core needs for it, and each barrier wait costs it about as much as four
 // MMAs, so one thread cannot keep the tensor core busy.  Two threads issue:
 //   thread A: X1 and gradient quarters 0, 1;  thread B: X2 and quarters 2, 3
 // (dV: thread A reduces X1 over chunks 0..3 and thread B over chunks 4..7 into
-// two accumulators that the elementwise warps add).  Each issuing thread has
-// its own ring of 16 KB slots with its own TMA producer, so every ring keeps a
-// single producer and a single consumer.
+// two accumulators that the elementwise warps add, and each accumulates one
+// half of dV).  Each issuing thread has its own ring with its own TMA
+// producer, so every ring keeps a single producer and a single consumer.
+// dK and dQ keep two stationary operands resident and fit four 16 KB slots;
+// dV keeps one and uses four 32 KB slots (fewer, larger barrier phases: each
+// of its threads waits twice per column tile instead of four times).
 //
-// TMEM per CTA: gradient quarters [0, 256) (64 columns each), X1 [256, 320),
-// X2 [320, 384).  Warps: 0 producer A, 1 TMEM owner + MMA issuer A (first CTA
+// Signals from the second CTA of the pair to the first: "X consumed" is a
+// relaxed remote arrive (no data changes hands); "dS written" needs a
+// cluster-scope release, which costs the thread that issues it over a
+// thousand cycles, so the elementwise warps arrive on a local barrier and an
+// otherwise idle thread of that CTA (warp 2) forwards each completed phase.
+//
+// TMEM per CTA: gradient [0, 256) (dK, dQ: quarters of 64 columns; dV: halves
+// of 128), X1 [256, 320), X2 [320, 384).  Warps: 0 producer A, 1 TMEM owner + MMA issuer A (first CTA
 // of the pair), 2 MMA issuer B, 3 producer B, 4-7 elementwise + epilogue
 // (thread t = TMEM lane t: stationary row t mod 64, column half t / 64).
 #include <type_traits>
@@ -58,22 +72,24 @@ constexpr int kChunks = 8;                  // D = 512
 constexpr int kHalf = kChunkBytes / 2;      // 64 rows x 64 columns
 constexpr int kResBytes = kChunks * kHalf;  // one stationary operand: 64 rows x 512 columns
 constexpr int kDsBytes = 2 * kHalf;         // dS or P: 64 rows x 128 columns
-constexpr int kSlot = kChunkBytes;          // ring slot: 16 KB
 constexpr float kLog2e = 1.4426950408889634f;
 
-// Ring slots of threads A and B.  dK and dQ keep two operands resident (128 KB)
-// and fit 5 slots; dV keeps one and fits 8.
-__host__ __device__ constexpr int slots_a(int mode) { return mode == kDV ? 4 : 3; }
-__host__ __device__ constexpr int slots_b(int mode) { return mode == kDV ? 4 : 2; }
+// Ring slots of threads A and B: dK and dQ keep two operands resident (128 KB)
+// and fit four 16 KB slots; dV keeps one and uses four of 32 KB.
+__host__ __device__ constexpr int slot_bytes(int mode) { return mode == kDV ? 2 * kChunkBytes : kChunkBytes; }
+__host__ __device__ constexpr int slots_a(int mode) { return 2; }
+__host__ __device__ constexpr int slots_b(int mode) { return 2; }
 __host__ __device__ constexpr int res_bytes(int mode) { return (mode == kDV ? 1 : 2) * kResBytes; }
 __host__ __device__ constexpr int ds_off(int mode) { return res_bytes(mode); }
-__host__ __device__ constexpr int ring_off(int mode) { return ds_off(mode) + kDsBytes; }
-__host__ __device__ constexpr int bar_off(int mode) { return ring_off(mode) + (slots_a(mode) + slots_b(mode)) * kSlot; }
+__host__ __device__ constexpr int ring_off(int mode) { return ds_off(mode) + 2 * kDsBytes; }
+__host__ __device__ constexpr int bar_off(int mode) {
+  return ring_off(mode) + (slots_a(mode) + slots_b(mode)) * slot_bytes(mode);
+}
 __host__ __device__ constexpr int smem_bytes(int mode) { return bar_off(mode) + 512 + 1024; }
 
 struct Bars {
   int full_a, empty_a, full_b, empty_b, res_full, x1_full, x2_full, x1_free, x2_free, p_ready, acc_ready, drain_a,
-      drain_b, count;
+      drain_b, p_local, count;  // p_ready, acc_ready, p_local: one per dS buffer
 };
 __host__ __device__ constexpr Bars bar_layout(int mode) {
   return Bars{0,
@@ -86,10 +102,11 @@ __host__ __device__ constexpr Bars bar_layout(int mode) {
               2 * (slots_a(mode) + slots_b(mode)) + 3,
               2 * (slots_a(mode) + slots_b(mode)) + 4,
               2 * (slots_a(mode) + slots_b(mode)) + 5,
-              2 * (slots_a(mode) + slots_b(mode)) + 6,
               2 * (slots_a(mode) + slots_b(mode)) + 7,
-              2 * (slots_a(mode) + slots_b(mode)) + 8,
-              2 * (slots_a(mode) + slots_b(mode)) + 9};
+              2 * (slots_a(mode) + slots_b(mode)) + 9,
+              2 * (slots_a(mode) + slots_b(mode)) + 10,
+              2 * (slots_a(mode) + slots_b(mode)) + 11,
+              2 * (slots_a(mode) + slots_b(mode)) + 13};
 }
 static_assert(bar_layout(kDV).count * 8 + 16 <= 512, "barrier area");
 
@@ -171,6 +188,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                      const __grid_constant__ BwdParams p) {
   constexpr bool TWO = MODE != kDV;  // a dP product (X2); dV splits X1 over two accumulators instead
   constexpr int SA = slots_a(MODE), SB = slots_b(MODE);
+  constexpr int kSlot = slot_bytes(MODE);
+  constexpr int kHps = kSlot / kHalf;                  // score-operand half-chunks per slot
+  constexpr int kNx = TWO ? 8 : 4;                     // chunks of D in each thread's score product
   constexpr Bars bl = bar_layout(MODE);
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -207,8 +227,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(bar(bl.x2_full), 1);
     mbar_init(bar(bl.x1_free), 8);  // four elementwise warps in each CTA
     mbar_init(bar(bl.x2_free), 8);
-    mbar_init(bar(bl.p_ready), 8);
-    mbar_init(bar(bl.acc_ready), 2);  // gradient commits of threads A and B
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(bar(bl.p_ready + i), 5);  // this CTA's four elementwise warps + the peer's relay
+      mbar_init(bar(bl.p_local + i), 4);  // (second CTA) its four elementwise warps
+      mbar_init(bar(bl.acc_ready + i), 2);  // gradient commits of threads A and B
+    }
     mbar_init(bar(bl.drain_a), 1);
     mbar_init(bar(bl.drain_b), 1);
     fence_mbar_init();
@@ -243,10 +266,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (TWO) tma_load_4d_pair(a2_sm + c * kHalf, mA2, lead(bl.res_full), c * kChunk, g.s_row0, g.s_head, g.b);
       }
     }
-    // Score product: half-chunks [x0, x0 + 8) (dK, dQ) or [x0, x0 + 4) (dV) of B1
-    // or B2, two per slot; gradient quarters q0, q0 + 1: chunk 2 q + rank of B3.
+    // Score product: half-chunks [x0, x0 + kNx) of B1 or B2, kHps per slot.
+    // Gradient: dK, dQ: quarters q0, q0 + 1, one slot each holding chunk
+    // 2 q + rank of B3; dV: half h, one slot holding chunks 4 h + 2 rank + {0, 1}.
     const CUtensorMap* mX = (is_a || !TWO) ? mB1 : mB2;
-    const int x0 = (!TWO && !is_a) ? 4 : 0, nx = TWO ? 8 : 4, q0 = is_a ? 0 : 2;
+    const int x0 = (!TWO && !is_a) ? 4 : 0, q0 = is_a ? 0 : 2;
     bool ok = true;
     uint32_t it = 0;
     auto next_slot = [&](uint32_t* dst, uint32_t* fb) -> bool {
@@ -261,21 +285,30 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto x_loads = [&](int c) {
       int ch, cr0;
       column<MODE>(g, p, c, &ch, &cr0);
-      for (int m = 0; m < nx / 2 && ok; ++m) {
+      for (int m = 0; m < kNx / kHps && ok; ++m) {
         uint32_t dst, fb;
         if (!(ok = next_slot(&dst, &fb))) break;
-        for (int i = 0; i < 2; ++i)
-          tma_load_4d_pair(dst + i * kHalf, mX, fb, (x0 + 2 * m + i) * kChunk, cr0 + 64 * static_cast<int>(rank), ch,
-                           g.b);
+        for (int i = 0; i < kHps; ++i)
+          tma_load_4d_pair(dst + i * kHalf, mX, fb, (x0 + kHps * m + i) * kChunk, cr0 + 64 * static_cast<int>(rank),
+                           ch, g.b);
       }
     };
     auto g_loads = [&](int c) {
       int ch, cr0;
       column<MODE>(g, p, c, &ch, &cr0);
-      for (int qd = q0; qd < q0 + 2 && ok; ++qd) {
+      if constexpr (TWO) {
+        for (int qd = q0; qd < q0 + 2 && ok; ++qd) {
+          uint32_t dst, fb;
+          if (!(ok = next_slot(&dst, &fb))) break;
+          tma_load_4d_pair(dst, mB3, fb, (2 * qd + static_cast<int>(rank)) * kChunk, cr0, ch, g.b);
+        }
+      } else {
         uint32_t dst, fb;
-        if (!(ok = next_slot(&dst, &fb))) break;
-        tma_load_4d_pair(dst, mB3, fb, (2 * qd + static_cast<int>(rank)) * kChunk, cr0, ch, g.b);
+        if (!(ok = next_slot(&dst, &fb))) return;
+        const int hf = is_a ? 0 : 1;
+        for (int i = 0; i < 2; ++i)
+          tma_load_4d_pair(dst + i * kChunkBytes, mB3, fb, (4 * hf + 2 * static_cast<int>(rank) + i) * kChunk, cr0, ch,
+                           g.b);
       }
     };
     if (g.ncols > 0) x_loads(0);
@@ -297,13 +330,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int xfull = is_a ? bl.x1_full : bl.x2_full, xfree = is_a ? bl.x1_free : bl.x2_free;
     const uint32_t x_tm = tbase + (is_a ? kX1 : kX2);
     constexpr uint32_t idesc_x = idesc_f16(BF16, 128, 128, false, false);  // 128 stationary rows x 128 columns
-    constexpr uint32_t idesc_g = idesc_f16(BF16, 128, 128, false, true);   // 128 stationary rows x 128 D columns
+    constexpr uint32_t idesc_g = idesc_f16(BF16, 128, TWO ? 128 : 256, false, true);  // stationary rows x D columns
     // resident stationary operand of this thread's product (dV: K for both halves of D)
     const uint64_t dres = sdesc_sw128((is_a || !TWO) ? a1_sm : a2_sm, 16, 1024);
     const uint64_t dring_k = sdesc_sw128(ring, 16, 1024);     // score operand: K-major half-chunks
-    const uint64_t dring_m = sdesc_sw128(ring, kSlot, 1024);  // gradient operand: one MN-major 64-column atom
+    const uint64_t dring_m = sdesc_sw128(ring, kChunkBytes, 1024);  // gradient operand: MN-major 64-column atoms 16 KB apart
     const uint64_t dds = sdesc_sw128(ds_sm, 16, 1024);
-    const int x0 = (!TWO && !is_a) ? 4 : 0, nx = TWO ? 8 : 4, q0 = is_a ? 0 : 2;
+    const int x0 = (!TWO && !is_a) ? 4 : 0, q0 = is_a ? 0 : 2;
     bool ok = mbar_wait(bar(bl.res_full), 0, status);
     tc_fence_after();
     uint32_t it = 0;
@@ -314,15 +347,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       return s;
     };
-    // X (+)= A B^T over this thread's chunks of D, two chunks per slot
+    // X (+)= A B^T over this thread's chunks of D, kHps chunks per slot
     auto product = [&]() {
-      for (int m = 0; m < nx / 2 && ok; ++m) {
+      for (int m = 0; m < kNx / kHps && ok; ++m) {
         const uint32_t s = wait_slot();
         if (!ok) return;
         const uint64_t bs = sdesc_advance(dring_k, s * kSlot);
 #pragma unroll
-        for (int i = 0; i < 2; ++i) {
-          const uint64_t a = sdesc_advance(dres, (x0 + 2 * m + i) * kHalf);
+        for (int i = 0; i < kHps; ++i) {
+          const uint64_t a = sdesc_advance(dres, (x0 + kHps * m + i) * kHalf);
           const uint64_t bd = sdesc_advance(bs, i * kHalf);
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
@@ -331,17 +364,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         umma_commit_pair(bar(empty0 + s), 3);
       }
     };
-    // gradient quarters q0, q0 + 1 += dS B3: A = dS (K-major, 128 column rows in two
-    // 64-row subtiles), B = this CTA's 64 columns of the quarter (MN-major)
+    // gradient += dS B3: A = dS (K-major, 128 column rows in two 64-row
+    // subtiles), B = this CTA's columns of the quarter (64) or half (128) of D
+    // (MN-major); dK, dQ: quarters q0, q0 + 1, dV: half q0 / 2
     auto grad = [&](int c) {
-      for (int qd = q0; qd < q0 + 2 && ok; ++qd) {
+      const uint64_t da = sdesc_advance(dds, (c & 1) * kDsBytes);
+      for (int qd = q0; qd < q0 + (TWO ? 2 : 1) && ok; ++qd) {
         const uint32_t s = wait_slot();
         if (!ok) return;
         const uint64_t bs = sdesc_advance(dring_m, s * kSlot);
+        const uint32_t acc_tm = tbase + (TWO ? 64 * qd : 64 * q0);
 #pragma unroll
         for (int ks = 0; ks < 8; ++ks)
-          umma_ss_pair(tbase + 64 * qd, sdesc_advance(dds, (ks >> 2) * kHalf + (ks & 3) * 32),
-                       sdesc_advance(bs, ks * 2048), idesc_g, (c > 0 || ks > 0) ? 1u : 0u);
+          umma_ss_pair(acc_tm, sdesc_advance(da, (ks >> 2) * kHalf + (ks & 3) * 32), sdesc_advance(bs, ks * 2048),
+                       idesc_g, (c > 0 || ks > 0) ? 1u : 0u);
         umma_commit_pair(bar(empty0 + s), 3);
       }
     };
@@ -359,16 +395,25 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!ok) break;
         umma_commit_pair(bar(xfull), 3);
       }
-      ok = mbar_wait(bar(bl.p_ready), c & 1, status);
+      ok = mbar_wait(bar(bl.p_ready + (c & 1)), (c >> 1) & 1, status);
       if (!ok) break;
       tc_fence_after();
       grad(c);
       if (!ok) break;
-      umma_commit_pair(bar(bl.acc_ready), 3);
+      umma_commit_pair(bar(bl.acc_ready + (c & 1)), 3);
     }
     const int drain = is_a ? bl.drain_a : bl.drain_b;
     umma_commit_pair(bar(drain), 1);
     mbar_wait(bar(drain), 0, status);
+  } else if (warp == 2 && lane == 0 && rank == 1) {
+    // ------------------------------------------------------------ relay of this CTA's p_ready
+    // The elementwise warps of column c + 2 wait for the gradient MMAs of
+    // column c, which need this relay's arrive: p_local cannot run two phases
+    // ahead of this loop.
+    for (int c = 0; c < g.ncols; ++c) {
+      if (!mbar_wait(bar(bl.p_local + (c & 1)), (c >> 1) & 1, status)) break;
+      mbar_arrive_remote(lead(bl.p_ready + (c & 1)));  // release.cluster: the dS tile is visible first
+    }
   } else if (warp >= 4) {
     // ------------------------------------------------------------ elementwise + epilogue
     typedef typename std::conditional<BF16, __nv_bfloat16, __half>::type T;
@@ -377,7 +422,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int u = t >> 6;     // column half of the column tile
     const int srow = g.s_row0 + r;
     const uint32_t lane_off = static_cast<uint32_t>((warp - 4) * 32) << 16;
-    const uint32_t x1_free_lead = lead(bl.x1_free), x2_free_lead = lead(bl.x2_free), p_ready_lead = lead(bl.p_ready);
+    const uint32_t x1_free_lead = lead(bl.x1_free), x2_free_lead = lead(bl.x2_free);
+    const uint32_t p_ready0 = bar(rank == 0 ? bl.p_ready : bl.p_local);  // local: the first CTA's or the relay's
     float lse2_row = 0.f, delta_row = 0.f;
     if (MODE == kDQ) {
       const int64_t idx = (static_cast<int64_t>(g.b) * p.Hq + g.h) * p.Nq + min(srow, p.Nq - 1);
@@ -385,11 +431,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       delta_row = p.delta[idx];
     }
     bool ok = true;
-    auto arrive_lead = [&](uint32_t a) {
+    auto arrive_free = [&](uint32_t a) {  // "X consumed": no data hand-off
       if (rank == 0)
         mbar_arrive(a);
       else
-        mbar_arrive_remote(a);
+        mbar_arrive_remote_relaxed(a);
     };
     auto load64 = [&](uint32_t col, float (&f)[64]) {
       uint32_t a0[32], a1[32];
@@ -441,15 +487,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_before();
         __syncwarp();
         if (lane == 0) {
-          arrive_lead(x1_free_lead);
-          arrive_lead(x2_free_lead);
+          arrive_free(x1_free_lead);
+          arrive_free(x2_free_lead);
         }
       } else {
         tc_fence_after();
         load64(kX1, pv);
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) arrive_lead(x1_free_lead);
+        if (lane == 0) arrive_free(x1_free_lead);
       }
       // P = 2^(S scale log2e + bias log2e - lse2), 0 where masked
       if (plain) {
@@ -492,7 +538,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         load64(kX2, dp);
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) arrive_lead(x2_free_lead);
+        if (lane == 0) arrive_free(x2_free_lead);
 #pragma unroll
         for (int e = 0; e < 64; ++e) {
           const float dl = (MODE == kDQ) ? delta_row : __shfl_sync(0xffffffffu, dlv[e >> 5], e & 31);
@@ -502,14 +548,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t w[32];
 #pragma unroll
       for (int e = 0; e < 32; ++e) w[e] = pack2<BF16>(pv[2 * e], pv[2 * e + 1]);
-      if (c > 0) {
-        // the previous column's gradient MMAs read the dS tile
-        ok = __all_sync(0xffffffffu, mbar_wait(bar(bl.acc_ready), (c - 1) & 1, status));
+      if (c >= 2) {
+        // the gradient MMAs of column c - 2 read this dS buffer.  Those of
+        // column c cannot have completed yet, so the parity is unambiguous.
+        ok = __all_sync(0xffffffffu, mbar_wait(bar(bl.acc_ready + (c & 1)), ((c - 2) >> 1) & 1, status));
         if (!ok) break;
       }
       {
         // row r of the K-major, 128-byte-swizzled [64 rows x 64 columns] subtile u
-        const uint32_t row = ds_sm + static_cast<uint32_t>(u) * kHalf + static_cast<uint32_t>(r) * 128u;
+        const uint32_t row = ds_sm + static_cast<uint32_t>(c & 1) * kDsBytes + static_cast<uint32_t>(u) * kHalf +
+                             static_cast<uint32_t>(r) * 128u;
 #pragma unroll
         for (int q = 0; q < 8; ++q)
           st_shared_v4(row + ((static_cast<uint32_t>(q) ^ static_cast<uint32_t>(r & 7)) << 4), w[4 * q],
@@ -517,14 +565,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         fence_proxy_async_smem();
       }
       __syncwarp();
-      if (lane == 0) arrive_lead(p_ready_lead);
+      if (lane == 0) mbar_arrive(p_ready0 + 8 * (c & 1));
     }
     if (ok) {
       // ---------------------------------------------------------- epilogue
-      if (g.ncols > 0) {
-        ok = __all_sync(0xffffffffu, mbar_wait(bar(bl.acc_ready), (g.ncols - 1) & 1, status));
-        if (ok) tc_fence_after();
-      }
+      // the last gradient MMAs of each dS buffer (their commits also arrive on the peer)
+      if (g.ncols > 0)
+        ok = __all_sync(0xffffffffu,
+                        mbar_wait(bar(bl.acc_ready + ((g.ncols - 1) & 1)), ((g.ncols - 1) >> 1) & 1, status));
+      if (ok && g.ncols > 1)
+        ok = __all_sync(0xffffffffu, mbar_wait(bar(bl.acc_ready + (g.ncols & 1)), ((g.ncols - 2) >> 1) & 1, status));
+      if (ok && g.ncols > 0) tc_fence_after();
       if (ok) {
         T* dst_base;
         int64_t sb, sh, sn;
@@ -537,20 +588,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         const float mul = (MODE == kDV) ? 1.f : p.scale;
         T* orow = dst_base + g.b * sb + g.s_head * sh + static_cast<int64_t>(srow) * sn;
-        for (int qd = 0; qd < 4; ++qd) {
-#pragma unroll
-          for (int hh = 0; hh < 2; ++hh) {
+        for (int k = 0; k < 8; ++k) {
+          // dK, dQ: TMEM column 64 qd + 32 hh + e of lane 64 u + r is D column
+          // 128 qd + 64 u + 32 hh + e; dV: column 128 h + 32 hh + e is D column
+          // 256 h + 128 u + 32 hh + e
+          const int tcol = 32 * k;
+          const int dcol = TWO ? 128 * (k >> 1) + 64 * u + 32 * (k & 1) : 256 * (k >> 2) + 128 * u + 32 * (k & 3);
+          {
             uint32_t v[32];
             if (g.ncols > 0) {
-              tmem_ld32(tbase + lane_off + 64 * qd + 32 * hh, v);
+              tmem_ld32(tbase + lane_off + tcol, v);
               tmem_ld_wait();
             } else {
 #pragma unroll
               for (int e = 0; e < 32; ++e) v[e] = 0u;
             }
             if (srow < g.s_limit) {
-              // TMEM column 32 hh + e of lane 64 u + r is D column 128 qd + 64 u + 32 hh + e
-              uint4* dst = reinterpret_cast<uint4*>(orow + 128 * qd + 64 * u + 32 * hh);
+              uint4* dst = reinterpret_cast<uint4*>(orow + dcol);
 #pragma unroll
               for (int q4 = 0; q4 < 4; ++q4) {
                 uint4 o;

@@ -49,6 +49,13 @@ __device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
 __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
+// Arrive on another CTA's barrier with relaxed semantics: for signals that
+// hand over no data (e.g. "this CTA has finished reading a TMEM tile", after
+// tcgen05.wait::ld and tcgen05.fence::before_thread_sync).  A cluster-scope
+// release arrive cost the issuing thread over a thousand cycles.
+__device__ __forceinline__ void mbar_arrive_remote_relaxed(uint32_t cluster_bar) {
+  asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar) : "memory");
+}
 // Arrive on a barrier that lives in another CTA of the cluster (address from mapa).
 __device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_bar) {
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar)
