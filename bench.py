@@ -48,6 +48,12 @@ CPU_ROWS = 1024      # cpu_baseline probe: query rows of one head against all ke
 REF_ROWS = 2048      # reference-arm sample per step
 
 
+# NVIDIA's nominal dense BF16/FP16 tensor figure for one GB300 (Blackwell
+# Ultra) GPU: the HGX B300 platform is quoted at 36 PFLOPS FP16/BF16 with 2:4
+# sparsity for eight GPUs, i.e. 4.5 PFLOPS sparse and 2.25 PFLOPS dense per GPU.
+PUBLISHED_BF16_DENSE_TFLOPS = 2250.0
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -254,16 +260,29 @@ def run_ffpa(args, rank, world):
                  "bwd_dk": 6 * B * H * N * N * D, "bwd_dq": 6 * B * H * N * N * D}
     dom = max(kern_ms, key=kern_ms.get)
     achieved = gemm_flop[dom] / (kern_ms[dom] / 1e3) / 1e12
-    peak = peaks["bf16_tflops_sustained"]
+    # The timed region lasts a fraction of a second at the maximum SM clock:
+    # burst conditions, so the burst matmul peak is the denominator; the
+    # sustained (power-capped, seconds-long) figure and NVIDIA's nominal dense
+    # figure are reported beside it.
+    peak = peaks["bf16_tflops"]
+    fwd_tf = FWD_FLOP / (kern_ms["fwd_main"] / 1e3) / 1e12
+    bwd_tf = BWD_FLOP / (sum(kern_ms[n] for n in names[1:]) / 1e3) / 1e12
     roofline = {"bound": "tensor", "kernel": dom, "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                 "frac": achieved / peak, "traffic": TRAFFIC.get(dom),
-                "peak_kind": f"bf16 dense, {peaks['source']} sustained (kernel timed inside a step)",
+                "traffic_from": TRAFFIC_FROM if dom in TRAFFIC else None,
+                "peak_kind": f"bf16 dense, {peaks['source']} burst (timed region well under a second)",
+                "frac_of_sustained": achieved / peaks["bf16_tflops_sustained"],
+                "frac_of_published": achieved / PUBLISHED_BF16_DENSE_TFLOPS,
+                "peaks": {"burst": peaks["bf16_tflops"], "sustained": peaks["bf16_tflops_sustained"],
+                          "published_dense": PUBLISHED_BF16_DENSE_TFLOPS},
                 "kernel_ms": kern_ms,
-                "fwd_tflops": FWD_FLOP / (kern_ms["fwd_main"] / 1e3) / 1e12,
-                "bwd_tflops": BWD_FLOP / (sum(kern_ms[n] for n in names[1:]) / 1e3) / 1e12}
+                "fwd_tflops": fwd_tf, "bwd_tflops": bwd_tf,
+                "fwd_frac": fwd_tf / peak, "bwd_frac": bwd_tf / peak,
+                "algorithmic_flop": {n: gemm_flop[n] for n in names}}
 
     e2e = measure_e2e(inp, scale, world, dev)
     decode = measure_decode(dev, peaks)
+    variants = measure_variants(dev, peaks) if rank == 0 else None
     cpu = None
     if rank == 0 and world == 1:
         secs, flop, heads, rows = oracle_time_bounded()
@@ -281,15 +300,79 @@ def run_ffpa(args, rank, world):
                        "frac_of_peak": {"burst": value / world / peaks["bf16_tflops"],
                                         "sustained": value / world / peaks["bf16_tflops_sustained"]}},
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": 5 * K,
-            "clocks": clocks.summary(), "decode": decode,
+            "clocks": clocks.summary(), "decode": decode, "variants": variants,
         }
         print(json.dumps(line), flush=True)
 
 
-# DRAM bytes (read + write) per launch from the ncu capture summarised in
-# profiles/ncu_full_fwd_bwd_N8192_D512_bf16.md (same workload); only kernels
-# unchanged since that capture are listed.
-TRAFFIC: dict = {"fwd_main": 251212288, "bwd_dv": 253638144, "bwd_dk": 357611520, "bwd_dq": 362597632}
+# DRAM bytes (read + write) per launch, dram__bytes_read.sum +
+# dram__bytes_write.sum from one ncu capture of the same workload; a kernel
+# changed since its capture is left out (its traffic is then reported as null).
+TRAFFIC: dict = {}
+TRAFFIC_FROM = "ncu capture of the same workload (dram__bytes_read.sum + dram__bytes_write.sum per launch)"
+
+
+def measure_variants(dev, peaks, iters=10, warmup=3):
+    """The other configurations of the method at their full sizes, each timed
+    alone: median device time of one library call (CUDA events around it) and
+    the counted TFLOPS (the same rule as the headline).  Inputs are N(0,1)
+    drawn on the device (the values do not change the work)."""
+    import torch
+
+    from head_dim_attention_gb300 import ffpa_bwd, ffpa_fwd
+
+    g = torch.Generator(device=dev)
+    g.manual_seed(11)
+
+    def rnd(*shape, dtype):
+        return torch.randn(*shape, generator=g, device=dev, dtype=torch.float32).to(dtype)
+
+    def median_ms(fn):
+        for _ in range(warmup):
+            fn()
+        times = []
+        for _ in range(iters):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            fn()
+            e1.record()
+            torch.cuda.synchronize()
+            times.append(e0.elapsed_time(e1))
+        return statistics.median(times)
+
+    out_lines = {}
+
+    def case(name, b, hq, hkv, nq, nkv, d, dtype, causal=False, bias=False, backward=False):
+        q = rnd(b, hq, nq, d, dtype=dtype)
+        k, v = rnd(b, hkv, nkv, d, dtype=dtype), rnd(b, hkv, nkv, d, dtype=dtype)
+        bb = rnd(1, 1, 1, nkv, dtype=torch.float32) if bias else None
+        out, lse = torch.empty_like(q), torch.empty(b, hq, nq, dtype=torch.float32, device=dev)
+        sc = d ** -0.5
+        fwd = lambda: ffpa_fwd(q, k, v, bb, int(causal), sc, out, lse)  # noqa: E731
+        ms = median_ms(fwd)
+        rec = {"fwd_ms": ms, "fwd_tflops": attention_flops(nq, nkv, d, b * hq, causal) / (ms / 1e3) / 1e12}
+        if backward:
+            do = rnd(b, hq, nq, d, dtype=dtype)
+            dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+            fwd()
+            bms = median_ms(lambda: ffpa_bwd(q, k, v, bb, int(causal), sc, out, lse, do, dq, dk, dv))
+            rec["bwd_ms"] = bms
+            rec["bwd_tflops"] = attention_flops(nq, nkv, d, b * hq, causal, backward=True) / (bms / 1e3) / 1e12
+        for key in [kk for kk in rec if kk.endswith("tflops")]:
+            rec[key.replace("tflops", "frac")] = rec[key] / peaks["bf16_tflops"]
+        out_lines[name] = rec
+        del q, k, v, out, lse
+
+    bf, fp = torch.bfloat16, torch.float16
+    case("causal_N8192_D512_bf16", 1, 8, 8, 8192, 8192, 512, bf, causal=True, backward=True)
+    case("gqa_Hkv2_N8192_D512_bf16", 1, 8, 2, 8192, 8192, 512, bf, backward=True)
+    case("nonaligned_N8191_D512_bf16", 1, 8, 8, 8191, 8191, 512, bf)
+    case("cross_Nq1024_Nkv8192_bias_D512_bf16", 1, 8, 8, 1024, 8192, 512, bf, bias=True)
+    for d in (320, 384, 448, 512, 576, 640, 768, 1024):
+        case(f"dsweep_N4096_D{d}_fp16", 1, 8, 8, 4096, 4096, d, fp)
+    return {"peak": peaks["bf16_tflops"], "timing": "median of 10 calls after 3 warm-up calls, each timed alone "
+            "with CUDA events; TFLOPS counted by the headline's rule (4 / 10 Nq Nkv D per head, halved "
+            "when causal)", "cases": out_lines}
 
 
 def measure_e2e(inp, scale, world, dev, steps=8):

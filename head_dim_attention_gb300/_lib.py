@@ -17,7 +17,7 @@ FFPA_F16, FFPA_BF16, FFPA_F32 = 0, 1, 2
 STATUS = {0: "FFPA_OK", 1: "FFPA_ERR_INVALID_ARG", 2: "FFPA_ERR_UNSUPPORTED", 3: "FFPA_ERR_ALIGNMENT",
           4: "FFPA_ERR_CUDA", 5: "FFPA_ERR_TIMEOUT", 6: "FFPA_ERR_SCRATCH_LIMIT"}
 EXPORTS = ("ffpa_fwd", "ffpa_bwd", "ffpa_fwd_decode_noalloc", "ffpa_status_string", "ffpa_check_status",
-           "ffpa_set_timing_events", "ffpa_version")
+           "ffpa_set_timing_events", "ffpa_selftest_wait_timeout", "ffpa_version")
 
 
 class FfpaTensor(ctypes.Structure):
@@ -56,6 +56,8 @@ def load(path: str | None = None) -> ctypes.CDLL:
     lib.ffpa_check_status.restype = ctypes.c_int
     lib.ffpa_set_timing_events.argtypes = [ctypes.POINTER(ctypes.c_void_p), ctypes.c_int]
     lib.ffpa_set_timing_events.restype = ctypes.c_int
+    lib.ffpa_selftest_wait_timeout.argtypes = [ctypes.c_void_p]
+    lib.ffpa_selftest_wait_timeout.restype = ctypes.c_int
     lib.ffpa_version.argtypes = []
     lib.ffpa_version.restype = ctypes.c_int
     if path is None:
@@ -89,6 +91,27 @@ def describe(t, as_lse: bool = False):
     return d
 
 
+def check_devices(tensors, current: int) -> None:
+    """All tensors of one call on one CUDA device, and that device the current
+    one: the library encodes its TMA maps, reads its status word and launches
+    on the current device, so a tensor elsewhere would be addressed from the
+    wrong GPU."""
+    devs = {(t.device.type, t.device.index) for t in tensors if t is not None}
+    if len(devs) != 1:
+        raise ValueError(f"ffpa tensors must all be on one CUDA device, got {sorted(map(str, devs))}")
+    kind, index = devs.pop()
+    if kind != "cuda":
+        raise ValueError("ffpa tensors must be CUDA tensors (the library takes device pointers)")
+    if index != current:
+        raise ValueError(f"ffpa tensors are on cuda:{index} but the current device is cuda:{current}; "
+                         f"call torch.cuda.set_device({index}) or use torch.cuda.device({index}) first")
+
+
+def _current_device() -> int:
+    import torch
+    return torch.cuda.current_device()
+
+
 def _ref(d):
     return None if d is None else ctypes.byref(d)
 
@@ -108,6 +131,7 @@ def _raise(code: int):
 def ffpa_fwd(q, k, v, bias, causal, scale, out, lse, stream=None) -> None:
     """Call ffpa_fwd on torch tensors (device memory); raises FfpaError on a non-zero status."""
     lib = load()
+    check_devices((q, k, v, bias, out, lse), _current_device())
     ds = [describe(q), describe(k), describe(v), describe(bias), describe(out), describe(lse, as_lse=True)]
     rc = lib.ffpa_fwd(_ref(ds[0]), _ref(ds[1]), _ref(ds[2]), _ref(ds[3]), int(causal), float(scale),
                       _ref(ds[4]), _ref(ds[5]), _stream(stream))
@@ -117,6 +141,7 @@ def ffpa_fwd(q, k, v, bias, causal, scale, out, lse, stream=None) -> None:
 def ffpa_fwd_decode_noalloc(q, k, v, bias, causal, scale, out, lse, stream=None) -> None:
     """Call ffpa_fwd_decode_noalloc (decode forward, Nq <= 16, no device allocation)."""
     lib = load()
+    check_devices((q, k, v, bias, out, lse), _current_device())
     ds = [describe(q), describe(k), describe(v), describe(bias), describe(out), describe(lse, as_lse=True)]
     rc = lib.ffpa_fwd_decode_noalloc(_ref(ds[0]), _ref(ds[1]), _ref(ds[2]), _ref(ds[3]), int(causal),
                                      float(scale), _ref(ds[4]), _ref(ds[5]), _stream(stream))
@@ -126,6 +151,7 @@ def ffpa_fwd_decode_noalloc(q, k, v, bias, causal, scale, out, lse, stream=None)
 def ffpa_bwd(q, k, v, bias, causal, scale, out, lse, dout, dq, dk, dv, stream=None) -> None:
     """Call ffpa_bwd on torch tensors (device memory); raises FfpaError on a non-zero status."""
     lib = load()
+    check_devices((q, k, v, bias, out, lse, dout, dq, dk, dv), _current_device())
     ds = [describe(x) for x in (q, k, v, bias, out)] + [describe(lse, as_lse=True)] + \
         [describe(x) for x in (dout, dq, dk, dv)]
     rc = lib.ffpa_bwd(*[_ref(x) for x in ds[:4]], int(causal), float(scale), *[_ref(x) for x in ds[4:]],
@@ -148,6 +174,11 @@ def ffpa_set_timing_events(events) -> None:
         raise ValueError("record each torch.cuda.Event once before registering it (torch creates events lazily)")
     arr = (ctypes.c_void_p * max(1, len(handles)))(*handles)
     _raise(load().ffpa_set_timing_events(arr if handles else None, len(handles)))
+
+
+def ffpa_selftest_wait_timeout(stream=None) -> None:
+    """Launch the timeout self-check (a wait that nothing completes); see include/ffpa.h."""
+    _raise(load().ffpa_selftest_wait_timeout(_stream(stream)))
 
 
 def ffpa_version() -> int:

@@ -7,6 +7,7 @@
 
 #include "ffpa.h"
 #include "internal.h"
+#include "ptx.cuh"
 
 namespace ffpa {
 
@@ -380,6 +381,7 @@ extern "C" int ffpa_fwd_decode_noalloc(const ffpa_tensor_t* q, const ffpa_tensor
   p.split_len = decode_split_len(c.B, c.Hq, c.Nkv);
   p.n_splits = (int)((c.Nkv + p.split_len - 1) / p.split_len);
   p.status = device_status_word();  // fetched with cudaGetSymbolAddress, no allocation
+  if (!p.status) return FFPA_ERR_CUDA;
   if (decode_scratch_bytes(p) > decode_noalloc_capacity_bytes()) return FFPA_ERR_SCRATCH_LIMIT;
   timing_begin();
   return cuda_rc(launch_fwd_decode_noalloc(p, dtype_is_bf16(c.dtype), reinterpret_cast<cudaStream_t>(stream)));
@@ -418,6 +420,29 @@ extern "C" int ffpa_set_timing_events(void* const* events, int count) {
   g_hook.n = count;
   g_hook.next = 0;
   return FFPA_OK;
+}
+
+namespace ffpa {
+namespace {
+// One warp waits on an mbarrier that nothing arrives on; the bounded wait
+// records FFPA_DEV_TIMEOUT and returns.
+__global__ void selftest_wait_kernel(uint32_t* status) {
+  __shared__ __align__(8) uint64_t bar;
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&bar), 1);
+    fence_mbar_init();
+  }
+  __syncwarp();
+  if (threadIdx.x == 0) mbar_wait(smem_u32(&bar), 0, status);
+}
+}  // namespace
+}  // namespace ffpa
+
+extern "C" int ffpa_selftest_wait_timeout(ffpa_stream_t stream) {
+  uint32_t* status = device_status_word();
+  if (!status) return FFPA_ERR_CUDA;
+  selftest_wait_kernel<<<1, 32, 0, reinterpret_cast<cudaStream_t>(stream)>>>(status);
+  return cudaGetLastError() == cudaSuccess ? FFPA_OK : FFPA_ERR_CUDA;
 }
 
 extern "C" int ffpa_version(void) { return 100; }

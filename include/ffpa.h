@@ -167,6 +167,20 @@ int ffpa_check_status(ffpa_stream_t stream);
  */
 int ffpa_set_timing_events(void* const* events, int count);
 
+/*
+ * ffpa_selftest_wait_timeout: check of the timeout path (no counterpart on the
+ * pages; every kernel's waits go through the same bounded wait).
+ *
+ * Launches, on `stream`, one warp that initialises an mbarrier nobody arrives
+ * on and waits for it with the library's bounded wait.  After the wait limit
+ * (250 ms) the kernel records a timeout in the device status word and exits;
+ * it issues no TMA copy and no MMA, so nothing is left in flight.  The next
+ * ffpa_check_status on the stream then returns FFPA_ERR_TIMEOUT (and clears
+ * the word), and the context stays usable.  Returns FFPA_ERR_CUDA if the
+ * launch fails, FFPA_OK otherwise.
+ */
+int ffpa_selftest_wait_timeout(ffpa_stream_t stream);
+
 /* Library version: major * 10000 + minor * 100 + patch. */
 int ffpa_version(void);
 

@@ -139,3 +139,19 @@ def test_binding_rejects_host_tensors():
     with pytest.raises(ValueError):
         _lib.describe(torch.zeros(1, 1, 4, 64, dtype=torch.bfloat16))
     assert _lib.describe(None) is None
+
+
+def test_binding_checks_devices():
+    # every tensor of a call on one CUDA device, and that device the current one
+    import types
+
+    import torch
+    on = lambda kind, index=None: types.SimpleNamespace(device=torch.device(kind, index))  # noqa: E731
+    _lib.check_devices((on("cuda", 0), on("cuda", 0), None), 0)
+    _lib.check_devices((on("cuda", 1), on("cuda", 1)), 1)
+    with pytest.raises(ValueError, match="one CUDA device"):
+        _lib.check_devices((on("cuda", 0), on("cuda", 1)), 0)
+    with pytest.raises(ValueError, match="current device"):
+        _lib.check_devices((on("cuda", 1), on("cuda", 1)), 0)
+    with pytest.raises(ValueError, match="CUDA tensors"):
+        _lib.check_devices((on("cpu"),), 0)
