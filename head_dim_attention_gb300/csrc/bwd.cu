@@ -19,8 +19,8 @@
 // columns per pass).  GQA: the dV/dK kernels sweep every query head of the
 // group, so the group's sum forms in TMEM without any atomics or workspace.
 //
-// D = 512 runs the CTA-pair kernels of bwd_pair.cu instead (launch_bwd hands
-// it over after the preprocess).
+// D = 512 runs the full-D CTA-pair kernels of bwd_fulld.cu instead (launch_bwd
+// hands it over after the preprocess).
 //
 // For 320 <= D <= 512 the pair does not exchange: each CTA reduces the score
 // products over the whole of D itself (1.5x to 1.67x the MMA work) and owns

@@ -111,9 +111,6 @@ cudaError_t launch_fwd_decode_noalloc(const DecodeParams& p, bool bf16, cudaStre
 size_t decode_scratch_bytes(const DecodeParams& p);
 size_t decode_noalloc_capacity_bytes();
 cudaError_t launch_bwd(const BwdParams& p, const BwdMaps& m, bool bf16, cudaStream_t s);
-// CTA-pair dV, dK, dQ kernels (bwd_pair.cu): D = 512; the preprocess runs first.
-bool bwd_pair_supported(const BwdParams& p);
-cudaError_t launch_bwd_pair(const BwdParams& p, const BwdMaps& m, bool bf16, cudaStream_t s);
 // Full-D CTA-pair dV, dK, dQ kernels (bwd_fulld.cu): D = 512; the preprocess runs first.
 bool bwd_fulld_supported(const BwdParams& p);
 cudaError_t launch_bwd_fulld(const BwdParams& p, const BwdMaps& m, bool bf16, cudaStream_t s);
