@@ -271,6 +271,8 @@ extern "C" int ffpa_fwd(const ffpa_tensor_t* q, const ffpa_tensor_t* k, const ff
   p.out = out->data;
   p.lse = lse ? static_cast<float*>(lse->data) : nullptr;
   p.bias = bias ? static_cast<const float*>(bias->data) : nullptr;
+  p.q = q->data;
+  p.q_sb = q->stride[0]; p.q_sh = q->stride[1]; p.q_sn = q->stride[2];
   p.o_sb = out->stride[0]; p.o_sh = out->stride[1]; p.o_sn = out->stride[2];
   p.bias_sb = bsb; p.bias_sh = bsh; p.bias_sq = bsq; p.bias_sk = bsk;
   p.B = (int)c.B; p.Hq = (int)c.Hq; p.Hkv = (int)c.Hkv; p.Nq = (int)c.Nq; p.Nkv = (int)c.Nkv; p.D = (int)c.D;
@@ -282,7 +284,7 @@ extern "C" int ffpa_fwd(const ffpa_tensor_t* q, const ffpa_tensor_t* k, const ff
   p.status = status;
   FwdMaps m;
   if ((rc = encode_map(&m.q, q)) || (rc = encode_map(&m.k, k)) || (rc = encode_map(&m.v, v)) ||
-      (rc = encode_map(&m.k_half, k, kTileRows / 2)))
+      (rc = encode_map(&m.k_half, k, kTileRows / 2)) || (rc = encode_map(&m.q_half, q, kTileRows / 2)))
     return rc;
   return cuda_rc(launch_fwd_main(p, m, bf16, st));
 }

@@ -644,7 +644,7 @@ cudaError_t launch_impl(const FwdParams& p_in, const FwdMaps& m, cudaStream_t st
 }  // namespace
 
 cudaError_t launch_fwd_main(const FwdParams& p, const FwdMaps& m, bool bf16, cudaStream_t s) {
-  if (fwd_pair_supported(p)) return launch_fwd_pair(p, m, bf16, s);
+  if (fwd_fulld_supported(p)) return launch_fwd_fulld(p, m, bf16, s);
   if (p.n_chunks <= 4) return bf16 ? launch_impl<kSolo, true>(p, m, s) : launch_impl<kSolo, false>(p, m, s);
   if (p.n_chunks <= 8)
     return bf16 ? launch_impl<kRecompute, true>(p, m, s) : launch_impl<kRecompute, false>(p, m, s);

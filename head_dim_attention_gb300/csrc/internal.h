@@ -23,6 +23,8 @@ struct FwdParams {
   void* out;
   float* lse;         // nullable, contiguous [B, Hq, Nq]
   const float* bias;  // nullable
+  const void* q;      // read directly (not through TMA) by the full-D pair kernel
+  int64_t q_sb, q_sh, q_sn;
   int64_t o_sb, o_sh, o_sn;
   int64_t bias_sb, bias_sh, bias_sq, bias_sk;
   int B, Hq, Hkv, Nq, Nkv, D;
@@ -38,7 +40,8 @@ struct FwdParams {
 
 struct FwdMaps {
   CUtensorMap q, k, v;  // 4-D {D, N, H, B}, box {64, 128, 1, 1}, 128-byte swizzle
-  CUtensorMap k_half;   // K with box {64, 64, 1, 1}: one CTA's half of a key tile in the CTA-pair kernel
+  CUtensorMap k_half;   // K with box {64, 64, 1, 1}: one CTA's half of a key tile in the CTA-pair kernels
+  CUtensorMap q_half;   // Q with box {64, 64, 1, 1}: one CTA's 64 query rows in the full-D pair kernel
 };
 
 // Decode (small Nq) path.
@@ -102,9 +105,12 @@ struct BwdMaps {
 bool dtype_is_bf16(int dtype);
 
 cudaError_t launch_fwd_main(const FwdParams& p, const FwdMaps& m, bool bf16, cudaStream_t s);
-// CTA-pair forward (fwd_pair.cu): D = 512.
+// CTA-pair forward (fwd_pair.cu): D = 512, O's columns split between two pairs.
 bool fwd_pair_supported(const FwdParams& p);
 cudaError_t launch_fwd_pair(const FwdParams& p, const FwdMaps& m, bool bf16, cudaStream_t s);
+// Full-D CTA-pair forward (fwd_fulld.cu): D = 512, one pair holds all of O.
+bool fwd_fulld_supported(const FwdParams& p);
+cudaError_t launch_fwd_fulld(const FwdParams& p, const FwdMaps& m, bool bf16, cudaStream_t s);
 cudaError_t launch_fwd_decode(const DecodeParams& p, bool bf16, cudaStream_t s);
 // Same kernels, partials in the library's fixed device array (no allocation).
 cudaError_t launch_fwd_decode_noalloc(const DecodeParams& p, bool bf16, cudaStream_t s);
