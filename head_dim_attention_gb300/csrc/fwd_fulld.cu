@@ -1,10 +1,10 @@
 // Fused attention forward for D = 512 in which a CTA pair holds ALL of O for
 // one 128-row query tile (tcgen05 cta_group::2 with M = 128).
 //
-// Same computation as fwd_main.cu and fwd_pair.cu: O = softmax(scale Q K^T +
-// bias) V and the row logsumexp, keys in tiles of 128 with an online softmax.
-// fwd_pair.cu splits O's 512 columns between two pairs that each reduce S
-// over the whole of D; here, as in the backward of bwd_fulld.cu, each SM of
+// Same computation as fwd_main.cu: O = softmax(scale Q K^T + bias) V and the
+// row logsumexp, keys in tiles of 128 with an online softmax.  Splitting O's
+// 512 columns between two CTAs (or two pairs) makes each reduce S over the
+// whole of D; here, as in the backward of bwd_fulld.cu, each SM of
 // the pair holds 64 query rows of a 128 x 512 fp32 O across all 128 TMEM
 // lanes (lane r: row r, the first N/2 columns of an accumulator; lane r + 64:
 // the other N/2), so O takes 256 TMEM columns and S is computed once per key

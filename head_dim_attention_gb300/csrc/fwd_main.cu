@@ -35,8 +35,8 @@
 // DSMEM traffic.
 //
 // D = 512 itself does not run here: launch_fwd_main hands it to the CTA-pair
-// kernel of fwd_pair.cu, which pairs two query tiles that own the same half
-// of O so that each SM loads half of every K tile and half of the V columns.
+// kernel of fwd_fulld.cu, in which two SMs hold all 512 columns of O for one
+// 128-row query tile, so S is computed once per key tile.
 //
 // Warp roles (256 threads): warp 0 = TMA producer, warp 1 = TMEM owner and
 // MMA issuer, warps 4-7 = softmax / correction / epilogue (one query row per

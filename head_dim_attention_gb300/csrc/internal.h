@@ -105,9 +105,6 @@ struct BwdMaps {
 bool dtype_is_bf16(int dtype);
 
 cudaError_t launch_fwd_main(const FwdParams& p, const FwdMaps& m, bool bf16, cudaStream_t s);
-// CTA-pair forward (fwd_pair.cu): D = 512, O's columns split between two pairs.
-bool fwd_pair_supported(const FwdParams& p);
-cudaError_t launch_fwd_pair(const FwdParams& p, const FwdMaps& m, bool bf16, cudaStream_t s);
 // Full-D CTA-pair forward (fwd_fulld.cu): D = 512, one pair holds all of O.
 bool fwd_fulld_supported(const FwdParams& p);
 cudaError_t launch_fwd_fulld(const FwdParams& p, const FwdMaps& m, bool bf16, cudaStream_t s);
