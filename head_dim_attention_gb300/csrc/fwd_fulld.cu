@@ -60,19 +60,30 @@ constexpr uint32_t kS0 = 256, kS1 = 320;        // S score buffers (64 columns e
 constexpr uint32_t kQt = 384;                   // Q columns 0..255 as bf16/f16 pairs, 128 TMEM columns
 constexpr float kRescaleLog2 = 8.0f;            // rescale O only when the max grows by > 2^8
 constexpr float kLoFrac = 1.0f / 64.0f;         // residual term of P only where a weight exceeds this share
-constexpr int kChunks = 8;                      // D = 512
 constexpr int kHalfBytes = kChunkBytes / 2;     // 64 rows x 64 columns
-constexpr int kQBytes = 4 * kHalfBytes;         // Q chunks 4..7 in shared memory, 32 KB
 constexpr int kPBytes = 2 * kHalfBytes;         // 64 rows x 128 keys, 16 KB
 constexpr int kPBufBytes = 2 * kPBytes;         // P_hi and P_lo of one key tile
 constexpr int kSlotBytes = 2 * kChunkBytes;     // 32 KB
 constexpr int kKSlots = 2, kVSlots = 2;
-// shared memory: Q | P buffers 0, 1 (P_hi, P_lo) | K ring | V ring | barriers | row-statistics exchange
-constexpr int kPOff = kQBytes, kRingKOff = kPOff + 2 * kPBufBytes;
-constexpr int kRingVOff = kRingKOff + kKSlots * kSlotBytes;
-constexpr int kMiscOff = kRingVOff + kVSlots * kSlotBytes;
-constexpr int kSmemBytes = kMiscOff + 256 + 2 * 128 * 4 + 1024;  // + alignment slack
-static_assert(kSmemBytes <= 232448, "227 KB per CTA");
+
+// Per head dimension D = 64 NC (NC = 5..8).  The P V product runs in two
+// halves: D columns 0..255 (N = 256) and 256..256 + N1 - 1, with N1 = 256 for
+// D > 384 and 128 otherwise; V columns at or past D are zero-filled by TMA and
+// the matching O columns are not stored.
+template <int NC>
+struct Shape {
+  static_assert(NC >= 5 && NC <= 8, "D = 320 .. 512");
+  static constexpr int kQBytes = (NC - 4) * kHalfBytes;  // Q chunks 4..NC-1 in shared memory
+  static constexpr int kN1 = NC >= 7 ? 256 : 128;       // O columns of the second half
+  static constexpr int kOCols = 128 + kN1 / 2;          // TMEM columns of O per lane
+  // shared memory: Q | P buffers 0, 1 (P_hi, P_lo) | K ring | V ring | barriers | row-statistics exchange
+  static constexpr int kPOff = kQBytes, kRingKOff = kPOff + 2 * kPBufBytes;
+  static constexpr int kRingVOff = kRingKOff + kKSlots * kSlotBytes;
+  static constexpr int kMiscOff = kRingVOff + kVSlots * kSlotBytes;
+  static constexpr int kSmemBytes = kMiscOff + 256 + 2 * 128 * 4 + 1024;  // + alignment slack
+  static_assert(kSmemBytes <= 232448, "227 KB per CTA");
+  static_assert(kOCols <= 256, "O below the score buffers");
+};
 
 struct Bars {
   int full_k, empty_k, full_v, empty_v, q_full, s_full, s_free, p_ready, p_local, pv_done, drain_a, drain_b, count;
@@ -128,10 +139,14 @@ __device__ __forceinline__ bool pair_bar_and(uint32_t id, bool v) {
   return r != 0;
 }
 
-template <bool BF16>
+template <int NC, bool BF16>
 __global__ void __launch_bounds__(kThreads, 1)
     fwd_fulld_kernel(const __grid_constant__ CUtensorMap map_qh, const __grid_constant__ CUtensorMap map_kh,
                      const __grid_constant__ CUtensorMap map_v, const __grid_constant__ FwdParams p) {
+  using G = Shape<NC>;
+  constexpr int kQBytes = G::kQBytes, kN1 = G::kN1, kOCols = G::kOCols;
+  constexpr bool kPadded = NC * kChunk < 256 + kN1;  // D = 320, 448: the last O columns are padding
+  constexpr int kPOff = G::kPOff, kRingKOff = G::kRingKOff, kRingVOff = G::kRingVOff, kMiscOff = G::kMiscOff;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   constexpr Bars bl = bar_layout();
@@ -173,7 +188,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(bar(bl.empty_v), 1);
     mbar_init(bar(bl.full_v + 1), 1);
     mbar_init(bar(bl.empty_v + 1), 1);
-    // Q ready: the producer's armed TMA bytes (chunks 4..7) and the eight softmax
+    // Q ready: the producer's armed TMA bytes (chunks 4..NC-1) and the eight softmax
     // warps of the pair that wrote columns 0..255 into TMEM
     mbar_init(bar(bl.q_full), 1 + 8);
     mbar_init(bar(bl.drain_a), 1);
@@ -205,7 +220,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_prefetch_desc(&map_qh);
       tma_prefetch_desc(&map_kh);
       if (rank == 0) mbar_expect_tx(bar(bl.q_full), 2 * kQBytes);
-      for (int c = 4; c < kChunks; ++c)
+      for (int c = 4; c < NC; ++c)
         tma_load_4d_pair(q_sm + (c - 4) * kHalfBytes, &map_qh, lead(bl.q_full), c * kChunk,
                          q0 + 64 * static_cast<int>(rank), h, b);
     } else {
@@ -218,18 +233,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       ++it;
       ok = mbar_wait(bar(empty0 + s), (r & 1) ^ 1, status);
       if (!ok) break;
-      if (rank == 0) mbar_expect_tx(bar(full0 + s), 2 * kSlotBytes);
-      const uint32_t dst = ring + s * kSlotBytes, fb = lead(full0 + s);
       const int j = n >> 1, m = n & 1;
+      // K: chunks 0..3 (m = 0) or 4..NC-1 (m = 1) of this CTA's 64 keys of key
+      // tile j; V: this CTA's share of O half m (one or two 64-column chunks)
+      const int nk = m == 0 ? 4 : NC - 4, nv = (m == 0 || kN1 == 256) ? 2 : 1;
+      if (rank == 0) mbar_expect_tx(bar(full0 + s), is_k ? 2 * nk * kHalfBytes : 2 * nv * kChunkBytes);
+      const uint32_t dst = ring + s * kSlotBytes, fb = lead(full0 + s);
       if (is_k) {
-        // K chunks 4m .. 4m+3 of this CTA's 64 keys of key tile j
-        for (int i = 0; i < 4; ++i)
+        for (int i = 0; i < nk; ++i)
           tma_load_4d_pair(dst + i * kHalfBytes, &map_kh, fb, (4 * m + i) * kChunk,
                            j * kTileRows + 64 * static_cast<int>(rank), kvh, b);
       } else {
-        // this CTA's two V chunks of D half m (columns 256 m + 128 c ..), keys of tile j
-        for (int i = 0; i < 2; ++i)
-          tma_load_4d_pair(dst + i * kChunkBytes, &map_v, fb, (4 * m + 2 * static_cast<int>(rank) + i) * kChunk,
+        for (int i = 0; i < nv; ++i)
+          tma_load_4d_pair(dst + i * kChunkBytes, &map_v, fb, (4 * m + nv * static_cast<int>(rank) + i) * kChunk,
                            j * kTileRows, kvh, b);
       }
     }
@@ -268,9 +284,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int kk = 0; kk < 4; ++kk)
               umma_ts_pair(s_tm, tbase + kQt + 32 * i + 8 * kk, sdesc_advance(bd, kk * 32), idesc_s, (i | kk) != 0);
           }
-        } else {  // Q chunks 4..7 from shared memory
+        } else {  // Q chunks 4..NC-1 from shared memory
 #pragma unroll
-          for (int i = 0; i < 4; ++i) {
+          for (int i = 0; i < NC - 4; ++i) {
             const uint64_t a = sdesc_advance(dq, i * kHalfBytes);
             const uint64_t bd = sdesc_advance(dk, s * kSlotBytes + i * kHalfBytes);
 #pragma unroll
@@ -287,7 +303,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_wait(bar(bl.drain_a), 0, status);
   } else if (warp == 2 && lane == 0 && rank == 0) {
     // ------------------------------------------------------------ MMA issuer B: O += P_j V_j
-    constexpr uint32_t idesc_pv = idesc_f16(BF16, 128, 256, false, true);  // 128 rows x 256 O columns
+    constexpr uint32_t idesc_pv0 = idesc_f16(BF16, 128, 256, false, true);  // 128 rows x 256 O columns
+    constexpr uint32_t idesc_pv1 = idesc_f16(BF16, 128, kN1, false, true);  // 128 rows x N1 O columns
     const uint64_t dv = sdesc_sw128(ring_v, kChunkBytes, 1024);            // V chunk pairs, MN-major
     const uint64_t dp = sdesc_sw128(p_sm, 16, 1024);                       // P (64 rows x 128 keys), K-major
     bool ok = true;
@@ -306,6 +323,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         const uint64_t bd = sdesc_advance(dv, s * kSlotBytes);
         const uint32_t o_tm = tbase + 128 * hf;
+        const uint32_t idesc_pv = hf == 0 ? idesc_pv0 : idesc_pv1;
 #pragma unroll
         for (int ks = 0; ks < 8; ++ks)  // 16-key steps: P subtile ks / 4, V rows 16 ks ..
           umma_ss_pair(o_tm, sdesc_advance(dphi, (ks >> 2) * kHalfBytes + (ks & 3) * 32),
@@ -488,7 +506,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tc_fence_after();
       if (warp_rescale) {
-        for (int c = 0; c < 8; ++c) {  // this lane's 256 O columns *= alpha
+        for (int c = 0; c < kOCols / 32; ++c) {  // this lane's O columns *= alpha
           uint32_t v[32];
           const uint32_t a = tbase + lane_off + c * 32;
           tmem_ld32(a, v);
@@ -523,13 +541,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float inv_l = l_sum > 0.f ? 1.f / l_sum : 0.f;
         typedef typename std::conditional<BF16, __nv_bfloat16, __half>::type T;
         T* orow = reinterpret_cast<T*>(p.out) + b * p.o_sb + h * p.o_sh + static_cast<int64_t>(row) * p.o_sn;
-        for (int c = 0; c < 8; ++c) {
+        for (int c = 0; c < kOCols / 32; ++c) {
           uint32_t v[32];
           tmem_ld32(tbase + lane_off + c * 32, v);
           tmem_ld_wait();
           if (row < p.Nq) {
-            // TMEM column 32 c + i of lane 64 kh + r is D column 256 (c / 4) + 128 kh + 32 (c % 4) + i
-            const int d0 = 256 * (c >> 2) + 128 * kh + 32 * (c & 3);
+            // TMEM column 32 c + i of lane 64 kh + r is D column 128 kh + 32 c + i
+            // (c < 4) or 256 + (N1 / 2) kh + 32 (c - 4) + i (c >= 4)
+            const int d0 = (c < 4 || kN1 == 256) ? 256 * (c >> 2) + 128 * kh + 32 * (c & 3)
+                                                 : 256 + 64 * kh + 32 * (c - 4);
+            if (kPadded && d0 >= NC * kChunk) continue;  // zero-filled V columns past D
             uint4* dst = reinterpret_cast<uint4*>(orow + d0);
 #pragma unroll
             for (int g = 0; g < 4; ++g) {
@@ -560,12 +581,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <bool BF16>
+template <int NC, bool BF16>
 cudaError_t launch_impl(const FwdParams& p_in, const FwdMaps& m, cudaStream_t st) {
+  constexpr int kSmemBytes = Shape<NC>::kSmemBytes;
   FwdParams p = p_in;
   p.stages = kKSlots + kVSlots;
   p.slot_chunks = 2;
-  auto kern = fwd_fulld_kernel<BF16>;
+  auto kern = fwd_fulld_kernel<NC, BF16>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
@@ -588,10 +610,15 @@ cudaError_t launch_impl(const FwdParams& p_in, const FwdMaps& m, cudaStream_t st
 
 }  // namespace
 
-bool fwd_fulld_supported(const FwdParams& p) { return p.n_chunks == kChunks; }
+bool fwd_fulld_supported(const FwdParams& p) { return p.n_chunks >= 5 && p.n_chunks <= 8; }
 
 cudaError_t launch_fwd_fulld(const FwdParams& p, const FwdMaps& m, bool bf16, cudaStream_t s) {
-  return bf16 ? launch_impl<true>(p, m, s) : launch_impl<false>(p, m, s);
+  switch (p.n_chunks) {
+    case 5: return bf16 ? launch_impl<5, true>(p, m, s) : launch_impl<5, false>(p, m, s);
+    case 6: return bf16 ? launch_impl<6, true>(p, m, s) : launch_impl<6, false>(p, m, s);
+    case 7: return bf16 ? launch_impl<7, true>(p, m, s) : launch_impl<7, false>(p, m, s);
+    default: return bf16 ? launch_impl<8, true>(p, m, s) : launch_impl<8, false>(p, m, s);
+  }
 }
 
 }  // namespace ffpa

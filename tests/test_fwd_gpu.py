@@ -40,6 +40,10 @@ def test_config_small_self_attention():
     (1, 2, 1, 200, 200, 512, BF, True, True),
     (1, 2, 2, 200, 200, 512, BF, True, True),
     (1, 4, 2, 333, 333, 512, FP, True, True),
+    # the same at the other full-D pair widths (O's second half N = 128 or 256)
+    (1, 4, 2, 333, 333, 384, BF, True, True),
+    (1, 2, 1, 200, 300, 448, FP, False, True),
+    (2, 2, 2, 190, 190, 320, FP, True, False),
 ])
 def test_fused_small(B, Hq, Hkv, Nq, Nkv, D, dtype, causal, bias):
     check_fwd_full(B, Hq, Hkv, Nq, Nkv, D, dtype, causal=causal, bias=bias)
@@ -52,6 +56,11 @@ def test_sharp_softmax(sharp, dtype):
     # as one 16-bit term and tiles that add its rounding residual mix within a
     # row and within a tile.
     check_fwd_full(1, 2, 2, 700, 1100, 512, dtype, scale=sharp * 512 ** -0.5)
+
+
+@pytest.mark.parametrize("D", [320, 384, 448])
+def test_sharp_softmax_head_dims(D):
+    check_fwd_full(1, 2, 2, 700, 1100, D, BF, scale=2.0 * D ** -0.5)
 
 
 def test_sharp_softmax_8k_bf16():
