@@ -275,6 +275,8 @@ extern "C" int ffpa_fwd(const ffpa_tensor_t* q, const ffpa_tensor_t* k, const ff
   p.q_sb = q->stride[0]; p.q_sh = q->stride[1]; p.q_sn = q->stride[2];
   p.o_sb = out->stride[0]; p.o_sh = out->stride[1]; p.o_sn = out->stride[2];
   p.bias_sb = bsb; p.bias_sh = bsh; p.bias_sq = bsq; p.bias_sk = bsk;
+  p.bias_vec = bias && bsk == 1 && reinterpret_cast<uintptr_t>(bias->data) % 16 == 0 && bsb % 4 == 0 &&
+               bsh % 4 == 0 && bsq % 4 == 0;
   p.B = (int)c.B; p.Hq = (int)c.Hq; p.Hkv = (int)c.Hkv; p.Nq = (int)c.Nq; p.Nkv = (int)c.Nkv; p.D = (int)c.D;
   p.group = (int)(c.Hq / c.Hkv);
   p.causal = causal;

@@ -400,6 +400,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     float m_used = -INFINITY, l_own = 0.f, l_sum = 0.f;  // l_sum: both halves of the row
     for (int j = 0; j < ntiles; ++j) {
       const uint32_t s_col = (j & 1) ? kS1 : kS0;
+      const int kv0 = j * kTileRows + 64 * kh;  // key of s[0]
+      // this tile's bias row segment (256 bytes when contiguous) into L1 ahead of
+      // the wait for S, so that the loads after it do not wait on L2
+      if (bias_row && p.bias_vec) {
+        prefetch_l1(bias_row + min(kv0, p.Nkv - 1));
+        prefetch_l1(bias_row + min(kv0 + 32, p.Nkv - 1));
+        prefetch_l1(bias_row + min(kv0 + 63, p.Nkv - 1));
+      }
       const bool got = __all_sync(0xffffffffu, mbar_wait(bar(bl.s_full + (j & 1)), (j >> 1) & 1, status));
       float s[64];
       if (got) {
@@ -424,7 +432,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_arrive_remote_relaxed(fr);
         }
       }
-      const int kv0 = j * kTileRows + 64 * kh;  // key of s[0]
       const bool masked = (kv0 + 64 > p.Nkv) || (p.causal && kv0 + 63 > row);
       // Scores in the log2 domain: x = s scale log2e (+ bias log2e).  Without a
       // bias the scale is applied inside the exponent below (it is positive,
@@ -432,9 +439,22 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float c_scale = bias_row ? 1.f : p.scale_log2;
       if (bias_row) {
 #pragma unroll
-        for (int i = 0; i < 64; ++i)
-          s[i] = fmaf(__ldg(bias_row + static_cast<int64_t>(min(kv0 + i, p.Nkv - 1)) * p.bias_sk), kLog2e,
-                      s[i] * p.scale_log2);
+        if (p.bias_vec && kv0 + 64 <= p.Nkv) {
+          const float4* src = reinterpret_cast<const float4*>(bias_row + kv0);
+#pragma unroll
+          for (int g = 0; g < 16; ++g) {
+            const float4 x = __ldg(src + g);
+            s[4 * g] = fmaf(x.x, kLog2e, s[4 * g] * p.scale_log2);
+            s[4 * g + 1] = fmaf(x.y, kLog2e, s[4 * g + 1] * p.scale_log2);
+            s[4 * g + 2] = fmaf(x.z, kLog2e, s[4 * g + 2] * p.scale_log2);
+            s[4 * g + 3] = fmaf(x.w, kLog2e, s[4 * g + 3] * p.scale_log2);
+          }
+        } else {
+#pragma unroll
+          for (int i = 0; i < 64; ++i)
+            s[i] = fmaf(__ldg(bias_row + static_cast<int64_t>(min(kv0 + i, p.Nkv - 1)) * p.bias_sk), kLog2e,
+                        s[i] * p.scale_log2);
+        }
       }
       if (masked) {
 #pragma unroll

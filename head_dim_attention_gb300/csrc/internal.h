@@ -27,6 +27,7 @@ struct FwdParams {
   int64_t q_sb, q_sh, q_sn;
   int64_t o_sb, o_sh, o_sn;
   int64_t bias_sb, bias_sh, bias_sq, bias_sk;
+  int bias_vec;       // bias rows contiguous along the keys and 16-byte aligned: 4 keys per load
   int B, Hq, Hkv, Nq, Nkv, D;
   int group;          // Hq / Hkv
   int causal;

@@ -133,6 +133,11 @@ __device__ __forceinline__ float ex2(float x) {
 }
 
 // ---------------------------------------------------------------- TMA
+// Hint: bring the 128-byte line holding p into L1 (no register result, no fault on a valid address).
+__device__ __forceinline__ void prefetch_l1(const void* p) {
+  asm volatile("prefetch.global.L1 [%0];" ::"l"(reinterpret_cast<uint64_t>(p)));
+}
+
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* m) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(m)) : "memory");
 }
