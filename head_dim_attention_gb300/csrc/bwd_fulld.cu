@@ -68,24 +68,32 @@ enum Mode : int { kDV = 0, kDK = 1, kDQ = 2 };
 constexpr int kThreads = 256;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kX1 = 256, kX2 = 320;
-constexpr int kChunks = 8;                  // D = 512
 constexpr int kHalf = kChunkBytes / 2;      // 64 rows x 64 columns
-constexpr int kResBytes = kChunks * kHalf;  // one stationary operand: 64 rows x 512 columns
 constexpr int kDsBytes = 2 * kHalf;         // dS or P: 64 rows x 128 columns
 constexpr float kLog2e = 1.4426950408889634f;
 
-// Ring slots of threads A and B: dK and dQ keep two operands resident (128 KB)
-// and fit four 16 KB slots; dV keeps one and uses four of 32 KB.
+// D = 64 NC with NC = 5..8.  The score products reduce over the NC chunks.
+// The gradient runs in quarters of 128 columns (dK, dQ; ceil(NC / 2) of them)
+// or in two halves (dV: columns 0..255 and 256 .. 256 + N1 - 1, N1 = 256 for
+// D > 384, else 128); gradient operand columns at or past D are zero-filled
+// by TMA and the matching gradient columns are not stored.
+__host__ __device__ constexpr int n_quarters(int nc) { return (nc + 1) / 2; }
+__host__ __device__ constexpr int dv_n1(int nc) { return nc >= 7 ? 256 : 128; }
+// TMEM columns of the gradient per lane
+__host__ __device__ constexpr int grad_cols(int mode, int nc) { return mode == kDV ? 128 + dv_n1(nc) / 2 : 64 * n_quarters(nc); }
+
+// Ring slots of threads A and B: dK and dQ keep two operands resident (up to
+// 128 KB) and use two 16 KB slots each; dV keeps one and uses two of 32 KB.
 __host__ __device__ constexpr int slot_bytes(int mode) { return mode == kDV ? 2 * kChunkBytes : kChunkBytes; }
 __host__ __device__ constexpr int slots_a(int mode) { return 2; }
 __host__ __device__ constexpr int slots_b(int mode) { return 2; }
-__host__ __device__ constexpr int res_bytes(int mode) { return (mode == kDV ? 1 : 2) * kResBytes; }
-__host__ __device__ constexpr int ds_off(int mode) { return res_bytes(mode); }
-__host__ __device__ constexpr int ring_off(int mode) { return ds_off(mode) + 2 * kDsBytes; }
-__host__ __device__ constexpr int bar_off(int mode) {
-  return ring_off(mode) + (slots_a(mode) + slots_b(mode)) * slot_bytes(mode);
+__host__ __device__ constexpr int res_bytes(int mode, int nc) { return (mode == kDV ? 1 : 2) * nc * kHalf; }
+__host__ __device__ constexpr int ds_off(int mode, int nc) { return res_bytes(mode, nc); }
+__host__ __device__ constexpr int ring_off(int mode, int nc) { return ds_off(mode, nc) + 2 * kDsBytes; }
+__host__ __device__ constexpr int bar_off(int mode, int nc) {
+  return ring_off(mode, nc) + (slots_a(mode) + slots_b(mode)) * slot_bytes(mode);
 }
-__host__ __device__ constexpr int smem_bytes(int mode) { return bar_off(mode) + 512 + 1024; }
+__host__ __device__ constexpr int smem_bytes(int mode, int nc) { return bar_off(mode, nc) + 512 + 1024; }
 
 struct Bars {
   int full_a, empty_a, full_b, empty_b, res_full, x1_full, x2_full, x1_free, x2_free, p_ready, acc_ready, drain_a,
@@ -179,7 +187,7 @@ __device__ __forceinline__ void column(const Geo& g, const BwdParams& p, int c, 
   }
 }
 
-template <int MODE, bool BF16>
+template <int MODE, int NC, bool BF16>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_fulld_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
                      const __grid_constant__ CUtensorMap map_v, const __grid_constant__ CUtensorMap map_do,
@@ -190,15 +198,18 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr int SA = slots_a(MODE), SB = slots_b(MODE);
   constexpr int kSlot = slot_bytes(MODE);
   constexpr int kHps = kSlot / kHalf;                  // score-operand half-chunks per slot
-  constexpr int kNx = TWO ? 8 : 4;                     // chunks of D in each thread's score product
+  constexpr int kResBytes = NC * kHalf;                // one stationary operand: 64 rows x D columns
+  constexpr int kNQ = n_quarters(NC), kN1 = dv_n1(NC);
+  constexpr int kGradCols = grad_cols(MODE, NC);
+  constexpr bool kPadded = TWO ? (NC & 1) != 0 : 64 * NC < 256 + kN1;  // gradient columns past D
   constexpr Bars bl = bar_layout(MODE);
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + bar_off(MODE));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + bar_off(MODE, NC));
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + bl.count);
   auto bar = [&](int i) { return smem_u32(&bars[i]); };
-  const uint32_t a1_sm = smem_u32(smem), a2_sm = a1_sm + kResBytes, ds_sm = a1_sm + ds_off(MODE);
-  const uint32_t ring_a = a1_sm + ring_off(MODE), ring_b = ring_a + SA * kSlot;
+  const uint32_t a1_sm = smem_u32(smem), a2_sm = a1_sm + kResBytes, ds_sm = a1_sm + ds_off(MODE, NC);
+  const uint32_t ring_a = a1_sm + ring_off(MODE, NC), ring_b = ring_a + SA * kSlot;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const uint32_t rank = cluster_ctarank();  // 0 issues the pair's MMAs
@@ -260,55 +271,57 @@ __global__ void __launch_bounds__(kThreads, 1)
     tma_prefetch_desc(is_a ? mB1 : (TWO ? mB2 : mB1));
     if (is_a) {
       tma_prefetch_desc(mA1);
-      if (rank == 0) mbar_expect_tx(bar(bl.res_full), 2 * res_bytes(MODE));
-      for (int c = 0; c < kChunks; ++c) {
+      if (rank == 0) mbar_expect_tx(bar(bl.res_full), 2 * res_bytes(MODE, NC));
+      for (int c = 0; c < NC; ++c) {
         tma_load_4d_pair(a1_sm + c * kHalf, mA1, lead(bl.res_full), c * kChunk, g.s_row0, g.s_head, g.b);
         if (TWO) tma_load_4d_pair(a2_sm + c * kHalf, mA2, lead(bl.res_full), c * kChunk, g.s_row0, g.s_head, g.b);
       }
     }
-    // Score product: half-chunks [x0, x0 + kNx) of B1 or B2, kHps per slot.
-    // Gradient: dK, dQ: quarters q0, q0 + 1, one slot each holding chunk
-    // 2 q + rank of B3; dV: half h, one slot holding chunks 4 h + 2 rank + {0, 1}.
+    // Score product: half-chunks [x0, x1) of B1 or B2, kHps per slot (the
+    // last slot may hold fewer).  Gradient: dK, dQ: quarters [q0, q1), one slot
+    // each holding chunk 2 q + rank of B3; dV: half h, one slot holding this
+    // CTA's one or two chunks of it.
     const CUtensorMap* mX = (is_a || !TWO) ? mB1 : mB2;
-    const int x0 = (!TWO && !is_a) ? 4 : 0, q0 = is_a ? 0 : 2;
+    const int x0 = (!TWO && !is_a) ? 4 : 0, x1 = (!TWO && is_a) ? 4 : NC;
+    const int q0 = is_a ? 0 : 2, q1 = is_a ? 2 : kNQ;
     bool ok = true;
     uint32_t it = 0;
-    auto next_slot = [&](uint32_t* dst, uint32_t* fb) -> bool {
+    auto next_slot = [&](uint32_t* dst, uint32_t* fb, int bytes) -> bool {
       const uint32_t s = it % S, r = it / S;
       ++it;
       if (!mbar_wait(bar(empty0 + s), (r & 1) ^ 1, status)) return false;
       *dst = ring + s * kSlot;
       *fb = lead(full0 + s);
-      if (rank == 0) mbar_expect_tx(bar(full0 + s), 2 * kSlot);
+      if (rank == 0) mbar_expect_tx(bar(full0 + s), 2 * bytes);
       return true;
     };
     auto x_loads = [&](int c) {
       int ch, cr0;
       column<MODE>(g, p, c, &ch, &cr0);
-      for (int m = 0; m < kNx / kHps && ok; ++m) {
+      for (int x = x0; x < x1 && ok; x += kHps) {
+        const int n = min(kHps, x1 - x);
         uint32_t dst, fb;
-        if (!(ok = next_slot(&dst, &fb))) break;
-        for (int i = 0; i < kHps; ++i)
-          tma_load_4d_pair(dst + i * kHalf, mX, fb, (x0 + kHps * m + i) * kChunk, cr0 + 64 * static_cast<int>(rank),
-                           ch, g.b);
+        if (!(ok = next_slot(&dst, &fb, n * kHalf))) break;
+        for (int i = 0; i < n; ++i)
+          tma_load_4d_pair(dst + i * kHalf, mX, fb, (x + i) * kChunk, cr0 + 64 * static_cast<int>(rank), ch, g.b);
       }
     };
     auto g_loads = [&](int c) {
       int ch, cr0;
       column<MODE>(g, p, c, &ch, &cr0);
       if constexpr (TWO) {
-        for (int qd = q0; qd < q0 + 2 && ok; ++qd) {
+        for (int qd = q0; qd < q1 && ok; ++qd) {
           uint32_t dst, fb;
-          if (!(ok = next_slot(&dst, &fb))) break;
+          if (!(ok = next_slot(&dst, &fb, kChunkBytes))) break;
           tma_load_4d_pair(dst, mB3, fb, (2 * qd + static_cast<int>(rank)) * kChunk, cr0, ch, g.b);
         }
       } else {
+        const int hf = is_a ? 0 : 1, nv = (hf == 0 || kN1 == 256) ? 2 : 1;
         uint32_t dst, fb;
-        if (!(ok = next_slot(&dst, &fb))) return;
-        const int hf = is_a ? 0 : 1;
-        for (int i = 0; i < 2; ++i)
-          tma_load_4d_pair(dst + i * kChunkBytes, mB3, fb, (4 * hf + 2 * static_cast<int>(rank) + i) * kChunk, cr0, ch,
-                           g.b);
+        if (!(ok = next_slot(&dst, &fb, nv * kChunkBytes))) return;
+        for (int i = 0; i < nv; ++i)
+          tma_load_4d_pair(dst + i * kChunkBytes, mB3, fb, (4 * hf + nv * static_cast<int>(rank) + i) * kChunk, cr0,
+                           ch, g.b);
       }
     };
     if (g.ncols > 0) x_loads(0);
@@ -330,13 +343,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int xfull = is_a ? bl.x1_full : bl.x2_full, xfree = is_a ? bl.x1_free : bl.x2_free;
     const uint32_t x_tm = tbase + (is_a ? kX1 : kX2);
     constexpr uint32_t idesc_x = idesc_f16(BF16, 128, 128, false, false);  // 128 stationary rows x 128 columns
-    constexpr uint32_t idesc_g = idesc_f16(BF16, 128, TWO ? 128 : 256, false, true);  // stationary rows x D columns
+    // stationary rows x gradient columns (dV: half 0, then half 1 of N1 columns)
+    constexpr uint32_t idesc_g = idesc_f16(BF16, 128, TWO ? 128 : 256, false, true);
+    constexpr uint32_t idesc_g1 = idesc_f16(BF16, 128, TWO ? 128 : kN1, false, true);
     // resident stationary operand of this thread's product (dV: K for both halves of D)
     const uint64_t dres = sdesc_sw128((is_a || !TWO) ? a1_sm : a2_sm, 16, 1024);
     const uint64_t dring_k = sdesc_sw128(ring, 16, 1024);     // score operand: K-major half-chunks
     const uint64_t dring_m = sdesc_sw128(ring, kChunkBytes, 1024);  // gradient operand: MN-major 64-column atoms 16 KB apart
     const uint64_t dds = sdesc_sw128(ds_sm, 16, 1024);
-    const int x0 = (!TWO && !is_a) ? 4 : 0, q0 = is_a ? 0 : 2;
+    const int x0 = (!TWO && !is_a) ? 4 : 0, x1 = (!TWO && is_a) ? 4 : NC;
+    const int q0 = is_a ? 0 : 2, q1 = is_a ? 2 : kNQ;
     bool ok = mbar_wait(bar(bl.res_full), 0, status);
     tc_fence_after();
     uint32_t it = 0;
@@ -349,27 +365,30 @@ __global__ void __launch_bounds__(kThreads, 1)
     };
     // X (+)= A B^T over this thread's chunks of D, kHps chunks per slot
     auto product = [&]() {
-      for (int m = 0; m < kNx / kHps && ok; ++m) {
+      for (int x = x0; x < x1 && ok; x += kHps) {
         const uint32_t s = wait_slot();
         if (!ok) return;
         const uint64_t bs = sdesc_advance(dring_k, s * kSlot);
 #pragma unroll
         for (int i = 0; i < kHps; ++i) {
-          const uint64_t a = sdesc_advance(dres, (x0 + kHps * m + i) * kHalf);
+          if (x + i >= x1) break;
+          const uint64_t a = sdesc_advance(dres, (x + i) * kHalf);
           const uint64_t bd = sdesc_advance(bs, i * kHalf);
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
-            umma_ss_pair(x_tm, sdesc_advance(a, kk * 32), sdesc_advance(bd, kk * 32), idesc_x, (m | i | kk) != 0);
+            umma_ss_pair(x_tm, sdesc_advance(a, kk * 32), sdesc_advance(bd, kk * 32), idesc_x,
+                         (x > x0 || i > 0 || kk > 0) ? 1u : 0u);
         }
         umma_commit_pair(bar(empty0 + s), 3);
       }
     };
     // gradient += dS B3: A = dS (K-major, 128 column rows in two 64-row
     // subtiles), B = this CTA's columns of the quarter (64) or half (128) of D
-    // (MN-major); dK, dQ: quarters q0, q0 + 1, dV: half q0 / 2
+    // (MN-major); dK, dQ: quarters [q0, q1), dV: half q0 / 2
     auto grad = [&](int c) {
       const uint64_t da = sdesc_advance(dds, (c & 1) * kDsBytes);
-      for (int qd = q0; qd < q0 + (TWO ? 2 : 1) && ok; ++qd) {
+      const uint32_t idg = (TWO || is_a) ? idesc_g : idesc_g1;
+      for (int qd = q0; qd < (TWO ? q1 : q0 + 1) && ok; ++qd) {
         const uint32_t s = wait_slot();
         if (!ok) return;
         const uint64_t bs = sdesc_advance(dring_m, s * kSlot);
@@ -377,7 +396,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int ks = 0; ks < 8; ++ks)
           umma_ss_pair(acc_tm, sdesc_advance(da, (ks >> 2) * kHalf + (ks & 3) * 32), sdesc_advance(bs, ks * 2048),
-                       idesc_g, (c > 0 || ks > 0) ? 1u : 0u);
+                       idg, (c > 0 || ks > 0) ? 1u : 0u);
         umma_commit_pair(bar(empty0 + s), 3);
       }
     };
@@ -588,12 +607,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         const float mul = (MODE == kDV) ? 1.f : p.scale;
         T* orow = dst_base + g.b * sb + g.s_head * sh + static_cast<int64_t>(srow) * sn;
-        for (int k = 0; k < 8; ++k) {
+        for (int k = 0; k < kGradCols / 32; ++k) {
           // dK, dQ: TMEM column 64 qd + 32 hh + e of lane 64 u + r is D column
           // 128 qd + 64 u + 32 hh + e; dV: column 128 h + 32 hh + e is D column
-          // 256 h + 128 u + 32 hh + e
+          // 256 h + (N_h / 2) u + 32 hh + e (N_0 = 256, N_1 = N1)
           const int tcol = 32 * k;
-          const int dcol = TWO ? 128 * (k >> 1) + 64 * u + 32 * (k & 1) : 256 * (k >> 2) + 128 * u + 32 * (k & 3);
+          const int dcol = TWO ? 128 * (k >> 1) + 64 * u + 32 * (k & 1)
+                               : ((k < 4 || kN1 == 256) ? 256 * (k >> 2) + 128 * u + 32 * (k & 3)
+                                                        : 256 + 64 * u + 32 * (k - 4));
+          if (kPadded && dcol >= 64 * NC) continue;  // zero-filled operand columns past D
           {
             uint32_t v[32];
             if (g.ncols > 0) {
@@ -630,11 +652,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int MODE, bool BF16>
+template <int MODE, int NC, bool BF16>
 cudaError_t launch_mode(const BwdParams& p, const BwdMaps& m, cudaStream_t st) {
-  constexpr int smem = smem_bytes(MODE);
+  constexpr int smem = smem_bytes(MODE, NC);
   static_assert(smem <= 232448, "shared memory per CTA");
-  auto kern = bwd_fulld_kernel<MODE, BF16>;
+  static_assert(grad_cols(MODE, NC) <= 256, "gradient below the score buffers");
+  auto kern = bwd_fulld_kernel<MODE, NC, BF16>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   const int tiles = (MODE == kDQ) ? p.q_tiles : p.kv_tiles;
@@ -655,20 +678,30 @@ cudaError_t launch_mode(const BwdParams& p, const BwdMaps& m, cudaStream_t st) {
   return e;
 }
 
-template <bool BF16>
+template <int NC, bool BF16>
 cudaError_t launch_modes(const BwdParams& p, const BwdMaps& m, cudaStream_t st) {
   cudaError_t e;
-  if ((e = launch_mode<kDV, BF16>(p, m, st)) != cudaSuccess) return e;
-  if ((e = launch_mode<kDK, BF16>(p, m, st)) != cudaSuccess) return e;
-  return launch_mode<kDQ, BF16>(p, m, st);
+  if ((e = launch_mode<kDV, NC, BF16>(p, m, st)) != cudaSuccess) return e;
+  if ((e = launch_mode<kDK, NC, BF16>(p, m, st)) != cudaSuccess) return e;
+  return launch_mode<kDQ, NC, BF16>(p, m, st);
+}
+
+template <bool BF16>
+cudaError_t launch_nc(const BwdParams& p, const BwdMaps& m, cudaStream_t st) {
+  switch (p.n_chunks) {
+    case 5: return launch_modes<5, BF16>(p, m, st);
+    case 6: return launch_modes<6, BF16>(p, m, st);
+    case 7: return launch_modes<7, BF16>(p, m, st);
+    default: return launch_modes<8, BF16>(p, m, st);
+  }
 }
 
 }  // namespace
 
-bool bwd_fulld_supported(const BwdParams& p) { return p.n_chunks == kChunks; }
+bool bwd_fulld_supported(const BwdParams& p) { return p.n_chunks >= 5 && p.n_chunks <= 8; }
 
 cudaError_t launch_bwd_fulld(const BwdParams& p, const BwdMaps& m, bool bf16, cudaStream_t s) {
-  return bf16 ? launch_modes<true>(p, m, s) : launch_modes<false>(p, m, s);
+  return bf16 ? launch_nc<true>(p, m, s) : launch_nc<false>(p, m, s);
 }
 
 }  // namespace ffpa

@@ -35,6 +35,13 @@ BF, FP = torch.bfloat16, torch.float16
     (1, 2, 1, 500, 300, 512, FP, True, False),
     (2, 2, 2, 384, 384, 512, BF, False, False),
     (1, 1, 1, 1, 129, 512, BF, False, False),
+    # the same pair kernels at D = 320 .. 448 (odd chunk counts pad the last
+    # gradient quarter; dV's second half is 128 or 256 columns wide)
+    (1, 4, 2, 300, 500, 384, BF, True, True),
+    (1, 2, 1, 500, 300, 448, FP, True, False),
+    (2, 2, 2, 384, 384, 448, BF, False, False),
+    (1, 2, 2, 200, 333, 320, FP, False, True),
+    (1, 2, 2, 5, 200, 384, BF, False, False),
 ])
 def test_bwd_small(B, Hq, Hkv, Nq, Nkv, D, dtype, causal, bias):
     check_bwd_full(B, Hq, Hkv, Nq, Nkv, D, dtype, causal=causal, bias=bias)
@@ -47,3 +54,8 @@ def test_bwd_query_bias_small():
 @pytest.mark.parametrize("causal", [False, True])
 def test_bwd_8k_bf16(causal):
     check_bwd_sampled(1, 8, 8, 8192, 8192, 512, BF, causal=causal)
+
+
+@pytest.mark.parametrize("D", [320, 384, 448])
+def test_bwd_4k_head_dims(D):
+    check_bwd_sampled(1, 4, 4, 4096, 4096, D, FP, causal=(D == 384))
