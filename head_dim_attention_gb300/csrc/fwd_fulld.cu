@@ -56,8 +56,6 @@ namespace {
 
 constexpr int kThreads = 256;
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kS0 = 256, kS1 = 320;        // S score buffers (64 columns each); O in [0, 256)
-constexpr uint32_t kQt = 384;                   // Q columns 0..255 as bf16/f16 pairs, 128 TMEM columns
 constexpr float kRescaleLog2 = 8.0f;            // rescale O only when the max grows by > 2^8
 constexpr float kLoFrac = 1.0f / 64.0f;         // residual term of P only where a weight exceeds this share
 constexpr int kHalfBytes = kChunkBytes / 2;     // 64 rows x 64 columns
@@ -66,23 +64,42 @@ constexpr int kPBufBytes = 2 * kPBytes;         // P_hi and P_lo of one key tile
 constexpr int kSlotBytes = 2 * kChunkBytes;     // 32 KB
 constexpr int kKSlots = 2, kVSlots = 2;
 
-// Per head dimension D = 64 NC (NC = 5..8).  The P V product runs in two
-// halves: D columns 0..255 (N = 256) and 256..256 + N1 - 1, with N1 = 256 for
-// D > 384 and 128 otherwise; V columns at or past D are zero-filled by TMA and
-// the matching O columns are not stored.
+// Per head dimension D = 64 NC (NC = 5..16).
+//
+// O's columns: for D <= 512 one pair holds all of them; above, kNsplit pairs
+// per query tile each hold a split of at most kOw columns (the last split may
+// be narrower) and each reduces S over the whole of D.  A pair's P V product
+// runs in up to two halves: its columns 0..255 (N = 256, or 128 when the split
+// has at most 128 columns) and 256..256 + N1 - 1 (N1 = 128 or 256); V columns
+// at or past D are zero-filled by TMA and the matching O columns not stored.
+//
+// TMEM (512 columns per SM): O in [0, kOTm) (half 0 from column 0, half 1 from
+// column 128), the two 64-column score buffers, then Q's first kQtc chunks as
+// the TS-form A operand (32 columns per chunk); Q's other chunks sit in shared
+// memory.  Narrower O splits leave room for more of Q in TMEM, which is what
+// lets shared memory hold the rest of Q next to the rings.  P is
+// double-buffered where that shared memory allows (kNpb = 2).
 template <int NC>
 struct Shape {
-  static_assert(NC >= 5 && NC <= 8, "D = 320 .. 512");
-  static constexpr int kQBytes = (NC - 4) * kHalfBytes;  // Q chunks 4..NC-1 in shared memory
-  static constexpr int kN1 = NC >= 7 ? 256 : 128;       // O columns of the second half
-  static constexpr int kOCols = 128 + kN1 / 2;          // TMEM columns of O per lane
-  // shared memory: Q | P buffers 0, 1 (P_hi, P_lo) | K ring | V ring | barriers | row-statistics exchange
-  static constexpr int kPOff = kQBytes, kRingKOff = kPOff + 2 * kPBufBytes;
+  static_assert(NC >= 5 && NC <= 16, "D = 320 .. 1024");
+  static constexpr int kD = 64 * NC;
+  static constexpr int kOw = NC <= 8 ? 512 : (NC <= 14 ? 384 : 256);  // widest O split
+  static constexpr int kNsplit = (kD + kOw - 1) / kOw;
+  static constexpr int kOTm = NC <= 8 ? 256 : kOw / 2;                 // TMEM columns reserved for O
+  // TMEM columns of O that a lane uses at most (rescale loop)
+  static constexpr int kOCols = NC <= 8 ? 128 + (NC >= 7 ? 256 : 128) / 2 : kOTm;
+  static constexpr uint32_t kS0 = kOTm, kS1 = kOTm + 64, kQt = kOTm + 128;
+  static constexpr int kQtc = (512 - static_cast<int>(kQt)) / 32 < NC ? (512 - static_cast<int>(kQt)) / 32 : NC;
+  static constexpr int kQBytes = (NC - kQtc) * kHalfBytes;  // Q chunks kQtc..NC-1 in shared memory
+  static constexpr int kNpb = NC - kQtc <= 4 ? 2 : 1;      // P buffers
+  static constexpr int kKSlotsPerTile = (NC + 3) / 4;      // four K chunks (32 KB) per slot
+  // shared memory: Q | P buffers (P_hi, P_lo) | K ring | V ring | barriers | row-statistics exchange
+  static constexpr int kPOff = kQBytes, kRingKOff = kPOff + kNpb * kPBufBytes;
   static constexpr int kRingVOff = kRingKOff + kKSlots * kSlotBytes;
   static constexpr int kMiscOff = kRingVOff + kVSlots * kSlotBytes;
   static constexpr int kSmemBytes = kMiscOff + 256 + 2 * 128 * 4 + 1024;  // + alignment slack
   static_assert(kSmemBytes <= 232448, "227 KB per CTA");
-  static_assert(kOCols <= 256, "O below the score buffers");
+  static_assert(kOCols <= kOTm && kQtc >= 4, "TMEM layout");
 };
 
 struct Bars {
@@ -144,15 +161,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     fwd_fulld_kernel(const __grid_constant__ CUtensorMap map_qh, const __grid_constant__ CUtensorMap map_kh,
                      const __grid_constant__ CUtensorMap map_v, const __grid_constant__ FwdParams p) {
   using G = Shape<NC>;
-  constexpr int kQBytes = G::kQBytes, kN1 = G::kN1, kOCols = G::kOCols;
-  constexpr bool kPadded = NC * kChunk < 256 + kN1;  // D = 320, 448: the last O columns are padding
+  constexpr int kQBytes = G::kQBytes, kOCols = G::kOCols, kQtc = G::kQtc, kNpb = G::kNpb;
+  constexpr uint32_t kS0 = G::kS0, kS1 = G::kS1, kQt = G::kQt;
   constexpr int kPOff = G::kPOff, kRingKOff = G::kRingKOff, kRingVOff = G::kRingVOff, kMiscOff = G::kMiscOff;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   constexpr Bars bl = bar_layout();
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kMiscOff);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + bl.count);
-  // lo_flag[j & 1] == j + 1: tile j carries the residual term of P.  The first
+  // lo_flag[j % kNpb] == j + 1: tile j carries the residual term of P.  The first
   // CTA's copy is read by thread B; the second CTA's softmax warps set their
   // own copy and its relay thread forwards it.
   volatile uint32_t* lo_flag = tmem_slot + 1;
@@ -165,8 +182,15 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const uint32_t rank = cluster_ctarank();  // 0 issues the pair's MMAs
-  const int qt = p.q_tiles - 1 - (static_cast<int>(blockIdx.x) >> 1);  // heavy causal tiles first
+  const int pair = static_cast<int>(blockIdx.x) >> 1;
+  const int split = pair % G::kNsplit;
+  const int qt = p.q_tiles - 1 - pair / G::kNsplit;  // heavy causal tiles first
   const int q0 = qt * kTileRows;
+  // this pair's O columns [o0, o0 + ow): halves of nv0 and nv1 64-column chunks per CTA
+  const int o0 = split * G::kOw, ow = min(G::kOw, G::kD - o0);
+  const int nv0 = ow >= 256 ? 2 : (ow + 127) / 128;
+  const int nv1 = ow > 256 ? (ow - 256 + 127) / 128 : 0;
+  const int nhalves = nv1 > 0 ? 2 : 1;
   const int h = blockIdx.y, b = blockIdx.z;
   const int kvh = h / p.group;
   const int kv_end = p.causal ? min(p.Nkv, q0 + kTileRows) : p.Nkv;
@@ -220,23 +244,24 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_prefetch_desc(&map_qh);
       tma_prefetch_desc(&map_kh);
       if (rank == 0) mbar_expect_tx(bar(bl.q_full), 2 * kQBytes);
-      for (int c = 4; c < NC; ++c)
-        tma_load_4d_pair(q_sm + (c - 4) * kHalfBytes, &map_qh, lead(bl.q_full), c * kChunk,
+      for (int c = kQtc; c < NC; ++c)
+        tma_load_4d_pair(q_sm + (c - kQtc) * kHalfBytes, &map_qh, lead(bl.q_full), c * kChunk,
                          q0 + 64 * static_cast<int>(rank), h, b);
     } else {
       tma_prefetch_desc(&map_v);
     }
     bool ok = true;
     uint32_t it = 0;
-    for (int n = 0; n < 2 * ntiles && ok; ++n) {
+    const int per_tile = is_k ? G::kKSlotsPerTile : nhalves;
+    for (int n = 0; n < per_tile * ntiles && ok; ++n) {
       const uint32_t s = it % S, r = it / S;
       ++it;
       ok = mbar_wait(bar(empty0 + s), (r & 1) ^ 1, status);
       if (!ok) break;
-      const int j = n >> 1, m = n & 1;
-      // K: chunks 0..3 (m = 0) or 4..NC-1 (m = 1) of this CTA's 64 keys of key
+      const int j = n / per_tile, m = n % per_tile;
+      // K: chunks 4m .. 4m + 3 (at most NC - 1) of this CTA's 64 keys of key
       // tile j; V: this CTA's share of O half m (one or two 64-column chunks)
-      const int nk = m == 0 ? 4 : NC - 4, nv = (m == 0 || kN1 == 256) ? 2 : 1;
+      const int nk = min(4, NC - 4 * m), nv = m == 0 ? nv0 : nv1;
       if (rank == 0) mbar_expect_tx(bar(full0 + s), is_k ? 2 * nk * kHalfBytes : 2 * nv * kChunkBytes);
       const uint32_t dst = ring + s * kSlotBytes, fb = lead(full0 + s);
       if (is_k) {
@@ -245,7 +270,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                            j * kTileRows + 64 * static_cast<int>(rank), kvh, b);
       } else {
         for (int i = 0; i < nv; ++i)
-          tma_load_4d_pair(dst + i * kChunkBytes, &map_v, fb, (4 * m + nv * static_cast<int>(rank) + i) * kChunk,
+          tma_load_4d_pair(dst + i * kChunkBytes, &map_v, fb, o0 + (4 * m + nv * static_cast<int>(rank) + i) * kChunk,
                            j * kTileRows, kvh, b);
       }
     }
@@ -270,25 +295,24 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
       }
       const uint32_t s_tm = tbase + ((j & 1) ? kS1 : kS0);
-      for (int m = 0; m < 2 && ok; ++m) {
+#pragma unroll
+      for (int m = 0; m < G::kKSlotsPerTile; ++m) {
         const uint32_t s = it & 1;
         ok = mbar_wait(bar(bl.full_k + s), (it >> 1) & 1, status);
         ++it;
         if (!ok) break;
         tc_fence_after();
-        if (m == 0) {  // Q chunks 0..3 from TMEM (8 columns per 16-column step)
 #pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const uint64_t bd = sdesc_advance(dk, s * kSlotBytes + i * kHalfBytes);
+        for (int i = 0; i < 4; ++i) {
+          const int x = 4 * m + i;  // chunk of D
+          if (x >= NC) break;
+          const uint64_t bd = sdesc_advance(dk, s * kSlotBytes + i * kHalfBytes);
+          if (x < kQtc) {  // Q from TMEM (8 columns per 16-column step)
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk)
-              umma_ts_pair(s_tm, tbase + kQt + 32 * i + 8 * kk, sdesc_advance(bd, kk * 32), idesc_s, (i | kk) != 0);
-          }
-        } else {  // Q chunks 4..NC-1 from shared memory
-#pragma unroll
-          for (int i = 0; i < NC - 4; ++i) {
-            const uint64_t a = sdesc_advance(dq, i * kHalfBytes);
-            const uint64_t bd = sdesc_advance(dk, s * kSlotBytes + i * kHalfBytes);
+              umma_ts_pair(s_tm, tbase + kQt + 32 * x + 8 * kk, sdesc_advance(bd, kk * 32), idesc_s, (x | kk) != 0);
+          } else {  // Q from shared memory
+            const uint64_t a = sdesc_advance(dq, (x - kQtc) * kHalfBytes);
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk)
               umma_ss_pair(s_tm, sdesc_advance(a, kk * 32), sdesc_advance(bd, kk * 32), idesc_s, 1u);
@@ -303,19 +327,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_wait(bar(bl.drain_a), 0, status);
   } else if (warp == 2 && lane == 0 && rank == 0) {
     // ------------------------------------------------------------ MMA issuer B: O += P_j V_j
-    constexpr uint32_t idesc_pv0 = idesc_f16(BF16, 128, 256, false, true);  // 128 rows x 256 O columns
-    constexpr uint32_t idesc_pv1 = idesc_f16(BF16, 128, kN1, false, true);  // 128 rows x N1 O columns
+    constexpr uint32_t idesc_pv256 = idesc_f16(BF16, 128, 256, false, true);  // 128 rows x 256 O columns
+    constexpr uint32_t idesc_pv128 = idesc_f16(BF16, 128, 128, false, true);  // 128 rows x 128 O columns
     const uint64_t dv = sdesc_sw128(ring_v, kChunkBytes, 1024);            // V chunk pairs, MN-major
     const uint64_t dp = sdesc_sw128(p_sm, 16, 1024);                       // P (64 rows x 128 keys), K-major
     bool ok = true;
     uint32_t it = 0;
     for (int j = 0; j < ntiles && ok; ++j) {
-      ok = mbar_wait(bar(bl.p_ready + (j & 1)), (j >> 1) & 1, status);
+      const int pb = j % kNpb;
+      ok = mbar_wait(bar(bl.p_ready + pb), (j / kNpb) & 1, status);
       if (!ok) break;
       tc_fence_after();
-      const bool use_lo = lo_flag[j & 1] == static_cast<uint32_t>(j + 1);
-      const uint64_t dphi = sdesc_advance(dp, (j & 1) * kPBufBytes), dplo = sdesc_advance(dphi, kPBytes);
-      for (int hf = 0; hf < 2 && ok; ++hf) {
+      const bool use_lo = lo_flag[pb] == static_cast<uint32_t>(j + 1);
+      const uint64_t dphi = sdesc_advance(dp, pb * kPBufBytes), dplo = sdesc_advance(dphi, kPBytes);
+      for (int hf = 0; hf < nhalves && ok; ++hf) {
         const uint32_t s = it & 1;  // two slots: one per half of D
         ok = mbar_wait(bar(bl.full_v + s), (it >> 1) & 1, status);
         ++it;
@@ -323,7 +348,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         const uint64_t bd = sdesc_advance(dv, s * kSlotBytes);
         const uint32_t o_tm = tbase + 128 * hf;
-        const uint32_t idesc_pv = hf == 0 ? idesc_pv0 : idesc_pv1;
+        const uint32_t idesc_pv = (hf == 0 ? nv0 : nv1) == 2 ? idesc_pv256 : idesc_pv128;
 #pragma unroll
         for (int ks = 0; ks < 8; ++ks)  // 16-key steps: P subtile ks / 4, V rows 16 ks ..
           umma_ss_pair(o_tm, sdesc_advance(dphi, (ks >> 2) * kHalfBytes + (ks & 3) * 32),
@@ -337,7 +362,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         umma_commit_pair(bar(bl.empty_v + s), 3);
       }
       if (!ok) break;
-      umma_commit_pair(bar(bl.pv_done + (j & 1)), 3);
+      umma_commit_pair(bar(bl.pv_done + pb), 3);
     }
     umma_commit_pair(bar(bl.drain_b), 1);
     mbar_wait(bar(bl.drain_b), 0, status);
@@ -348,9 +373,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     // run two phases ahead.
     const uint32_t lo_flag_lead = mapa(smem_u32(const_cast<uint32_t*>(lo_flag)), 0);
     for (int j = 0; j < ntiles; ++j) {
-      if (!mbar_wait(bar(bl.p_local + (j & 1)), (j >> 1) & 1, status)) break;
-      if (lo_flag[j & 1] == static_cast<uint32_t>(j + 1)) st_cluster_u32(lo_flag_lead + 4 * (j & 1), j + 1);
-      mbar_arrive_remote(lead(bl.p_ready + (j & 1)));  // release.cluster: P and the flag are visible first
+      const int pb = j % kNpb;
+      if (!mbar_wait(bar(bl.p_local + pb), (j / kNpb) & 1, status)) break;
+      if (lo_flag[pb] == static_cast<uint32_t>(j + 1)) st_cluster_u32(lo_flag_lead + 4 * pb, j + 1);
+      mbar_arrive_remote(lead(bl.p_ready + pb));  // release.cluster: P and the flag are visible first
     }
   } else if (warp >= 4) {
     // ------------------------------------------------------------ softmax / correction / epilogue
@@ -367,14 +393,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t s_free_lead0 = lead(bl.s_free), s_free_lead1 = lead(bl.s_free + 1);
     const uint32_t p_ready_local = bar(rank == 0 ? bl.p_ready : bl.p_local);  // + 8 per P buffer
     {
-      // Q columns 0..255 of this thread's row into its TMEM lane: 128 words of
+      // Q columns 0 .. 64 kQtc - 1 of this thread's row into its TMEM lane: words of
       // two 16-bit values in memory order, the TS form's A layout (the threads of
       // lanes r and r + 64 write the same row)
       typedef typename std::conditional<BF16, __nv_bfloat16, __half>::type T;
       const uint4* qrow = reinterpret_cast<const uint4*>(reinterpret_cast<const T*>(p.q) + b * p.q_sb + h * p.q_sh +
                                                          static_cast<int64_t>(min(row, p.Nq - 1)) * p.q_sn);
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
+      for (int c = 0; c < kQtc; ++c) {
         uint32_t w[32];
 #pragma unroll
         for (int g = 0; g < 8; ++g) {
@@ -506,11 +532,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           lo[e] = 0u;
         }
       }
-      if (j >= 2) {
-        // P_{j-2} V reads the P buffer this tile writes.  P_j V cannot have
+      const int pb = j % kNpb;
+      if (j >= kNpb) {
+        // P_{j-kNpb} V reads the P buffer this tile writes.  P_j V cannot have
         // completed, so the parity of that barrier is unambiguous.
         const bool done =
-            __all_sync(0xffffffffu, mbar_wait(bar(bl.pv_done + (j & 1)), ((j - 2) >> 1) & 1, status));
+            __all_sync(0xffffffffu, mbar_wait(bar(bl.pv_done + pb), ((j - kNpb) / kNpb) & 1, status));
         ok = pair_bar_and(nb, done);
         if (!ok) break;
       }
@@ -520,7 +547,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // completed, so the parity is unambiguous even where earlier tiles
         // skipped this wait)
         const bool done = __all_sync(
-            0xffffffffu, mbar_wait(bar(bl.pv_done + ((j - 1) & 1)), ((j - 1) >> 1) & 1, status));
+            0xffffffffu, mbar_wait(bar(bl.pv_done + (j - 1) % kNpb), ((j - 1) / kNpb) & 1, status));
         ok = pair_bar_and(nb, done);
         if (!ok) break;
       }
@@ -537,24 +564,24 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tmem_st_wait();
       }
-      // P of keys 64 kh .. 64 kh + 63 of row r: K-chunk kh of P buffer j mod 2
-      const uint32_t pb = p_sm + (j & 1) * kPBufBytes;
-      store_row64(pb + kh * kHalfBytes, r, hi);
-      store_row64(pb + kPBytes + kh * kHalfBytes, r, lo);
+      // P of keys 64 kh .. 64 kh + 63 of row r: K-chunk kh of P buffer j mod kNpb
+      const uint32_t pa = p_sm + pb * kPBufBytes;
+      store_row64(pa + kh * kHalfBytes, r, hi);
+      store_row64(pa + kPBytes + kh * kHalfBytes, r, lo);
       fence_proxy_async_smem();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) {
-        if (warp_lo) lo_flag[j & 1] = static_cast<uint32_t>(j + 1);
-        mbar_arrive(p_ready_local + 8 * (j & 1));  // release: P and the flag are visible first
+        if (warp_lo) lo_flag[pb] = static_cast<uint32_t>(j + 1);
+        mbar_arrive(p_ready_local + 8 * pb);  // release: P and the flag are visible first
       }
     }
     if (ok) {
       // ---------------------------------------------------------- epilogue
       // the last P V of each buffer (their commits also arrive on the second CTA)
       ok = __all_sync(0xffffffffu,
-                      mbar_wait(bar(bl.pv_done + ((ntiles - 1) & 1)), ((ntiles - 1) >> 1) & 1, status));
-      if (ok && ntiles >= 2)
+                      mbar_wait(bar(bl.pv_done + (ntiles - 1) % kNpb), ((ntiles - 1) / kNpb) & 1, status));
+      if (ok && kNpb == 2 && ntiles >= 2)
         ok = __all_sync(0xffffffffu, mbar_wait(bar(bl.pv_done + (ntiles & 1)), ((ntiles - 2) >> 1) & 1, status));
       if (ok) {
         tc_fence_after();
@@ -566,11 +593,25 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_ld32(tbase + lane_off + c * 32, v);
           tmem_ld_wait();
           if (row < p.Nq) {
-            // TMEM column 32 c + i of lane 64 kh + r is D column 128 kh + 32 c + i
-            // (c < 4) or 256 + (N1 / 2) kh + 32 (c - 4) + i (c >= 4)
-            const int d0 = (c < 4 || kN1 == 256) ? 256 * (c >> 2) + 128 * kh + 32 * (c & 3)
-                                                 : 256 + 64 * kh + 32 * (c - 4);
-            if (kPadded && d0 >= NC * kChunk) continue;  // zero-filled V columns past D
+            // TMEM column 32 c + i of lane 64 kh + r is O column o0 + (N0 / 2) kh
+            // + 32 c + i (half 0, c < N0 / 64) or o0 + 256 + (N1 / 2) kh + 32 (c - 4)
+            // + i (half 1, c >= 4), with N_h = 128 nv_h
+            int d0;
+            if constexpr (NC <= 8) {
+              constexpr bool kN1Wide = NC >= 7;                 // N1 = 256
+              constexpr bool kPadded = NC == 5 || NC == 7;      // the last O columns are padding
+              d0 = (c < 4 || kN1Wide) ? 256 * (c >> 2) + 128 * kh + 32 * (c & 3) : 256 + 64 * kh + 32 * (c - 4);
+              if (kPadded && d0 >= NC * kChunk) continue;  // zero-filled V columns past D
+            } else {
+              if (c < 4) {
+                if (c >= 2 * nv0) continue;
+                d0 = o0 + 64 * nv0 * kh + 32 * c;
+              } else {
+                if (c - 4 >= 2 * nv1) continue;
+                d0 = o0 + 256 + 64 * nv1 * kh + 32 * (c - 4);
+              }
+              if (d0 >= NC * kChunk) continue;
+            }
             uint4* dst = reinterpret_cast<uint4*>(orow + d0);
 #pragma unroll
             for (int g = 0; g < 4; ++g) {
@@ -583,7 +624,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
         }
-        if (kh == 0 && p.lse && row < p.Nq) {
+        if (kh == 0 && split == 0 && p.lse && row < p.Nq) {
           constexpr float kLn2 = 0.6931471805599453f;
           p.lse[(static_cast<int64_t>(b) * p.Hq + h) * p.Nq + row] =
               l_sum > 0.f ? (m_used + __log2f(l_sum)) * kLn2 : -INFINITY;
@@ -608,10 +649,11 @@ cudaError_t launch_impl(const FwdParams& p_in, const FwdMaps& m, cudaStream_t st
   p.stages = kKSlots + kVSlots;
   p.slot_chunks = 2;
   auto kern = fwd_fulld_kernel<NC, BF16>;
+  constexpr int kNsplit = Shape<NC>::kNsplit;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(2 * p.q_tiles, p.Hq, p.B);  // (pair rank, query tile)
+  cfg.gridDim = dim3(2 * p.q_tiles * kNsplit, p.Hq, p.B);  // (pair rank, O split, query tile)
   cfg.blockDim = dim3(kThreads, 1, 1);
   cfg.dynamicSmemBytes = kSmemBytes;
   cfg.stream = st;
@@ -628,16 +670,29 @@ cudaError_t launch_impl(const FwdParams& p_in, const FwdMaps& m, cudaStream_t st
   return e;
 }
 
+template <int NC>
+cudaError_t launch_nc(const FwdParams& p, const FwdMaps& m, bool bf16, cudaStream_t s) {
+  return bf16 ? launch_impl<NC, true>(p, m, s) : launch_impl<NC, false>(p, m, s);
+}
+
 }  // namespace
 
-bool fwd_fulld_supported(const FwdParams& p) { return p.n_chunks >= 5 && p.n_chunks <= 8; }
+bool fwd_fulld_supported(const FwdParams& p) { return p.n_chunks >= 5 && p.n_chunks <= 16; }
 
 cudaError_t launch_fwd_fulld(const FwdParams& p, const FwdMaps& m, bool bf16, cudaStream_t s) {
   switch (p.n_chunks) {
-    case 5: return bf16 ? launch_impl<5, true>(p, m, s) : launch_impl<5, false>(p, m, s);
-    case 6: return bf16 ? launch_impl<6, true>(p, m, s) : launch_impl<6, false>(p, m, s);
-    case 7: return bf16 ? launch_impl<7, true>(p, m, s) : launch_impl<7, false>(p, m, s);
-    default: return bf16 ? launch_impl<8, true>(p, m, s) : launch_impl<8, false>(p, m, s);
+    case 5: return launch_nc<5>(p, m, bf16, s);
+    case 6: return launch_nc<6>(p, m, bf16, s);
+    case 7: return launch_nc<7>(p, m, bf16, s);
+    case 8: return launch_nc<8>(p, m, bf16, s);
+    case 9: return launch_nc<9>(p, m, bf16, s);
+    case 10: return launch_nc<10>(p, m, bf16, s);
+    case 11: return launch_nc<11>(p, m, bf16, s);
+    case 12: return launch_nc<12>(p, m, bf16, s);
+    case 13: return launch_nc<13>(p, m, bf16, s);
+    case 14: return launch_nc<14>(p, m, bf16, s);
+    case 15: return launch_nc<15>(p, m, bf16, s);
+    default: return launch_nc<16>(p, m, bf16, s);
   }
 }
 

@@ -58,7 +58,7 @@ def test_sharp_softmax(sharp, dtype):
     check_fwd_full(1, 2, 2, 700, 1100, 512, dtype, scale=sharp * 512 ** -0.5)
 
 
-@pytest.mark.parametrize("D", [320, 384, 448])
+@pytest.mark.parametrize("D", [320, 384, 448, 640, 768, 1024])
 def test_sharp_softmax_head_dims(D):
     check_fwd_full(1, 2, 2, 700, 1100, D, BF, scale=2.0 * D ** -0.5)
 
@@ -72,7 +72,7 @@ def test_fused_query_bias_small():
     check_fwd_full(1, 2, 2, 150, 260, 512, torch.bfloat16, bias="query")
 
 
-@pytest.mark.parametrize("D", [320, 384, 448, 512, 576, 640, 768, 1024])
+@pytest.mark.parametrize("D", [320, 384, 448, 512, 576, 640, 704, 768, 832, 896, 960, 1024])
 def test_head_dim_sweep_small(D):
     check_fwd_full(1, 2, 2, 200, 200, D, FP, causal=(D % 128 == 0))
 
