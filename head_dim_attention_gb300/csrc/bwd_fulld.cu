@@ -352,7 +352,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint64_t dring_m = sdesc_sw128(ring, kChunkBytes, 1024);  // gradient operand: MN-major 64-column atoms 16 KB apart
     const uint64_t dds = sdesc_sw128(ds_sm, 16, 1024);
     const int x0 = (!TWO && !is_a) ? 4 : 0, x1 = (!TWO && is_a) ? 4 : NC;
-    const int q0 = is_a ? 0 : 2, q1 = is_a ? 2 : kNQ;
+    const int q0 = is_a ? 0 : 2;
     bool ok = mbar_wait(bar(bl.res_full), 0, status);
     tc_fence_after();
     uint32_t it = 0;
@@ -365,19 +365,22 @@ __global__ void __launch_bounds__(kThreads, 1)
     };
     // X (+)= A B^T over this thread's chunks of D, kHps chunks per slot
     auto product = [&]() {
-      for (int x = x0; x < x1 && ok; x += kHps) {
+      // Straight-line MMAs per slot where every slot is full: a bound check
+      // between the MMAs of the issue loop slowed the kernels by 5%.
+      constexpr int kSlotsX = TWO ? (NC + 1) / 2 : 1;       // slots per product (dV: 4 or NC - 4 chunks)
+      constexpr bool kRagged = TWO ? (NC & 1) != 0 : NC != 8;  // a slot with fewer than kHps chunks
+      for (int m = 0; m < kSlotsX && ok; ++m) {
         const uint32_t s = wait_slot();
         if (!ok) return;
         const uint64_t bs = sdesc_advance(dring_k, s * kSlot);
 #pragma unroll
         for (int i = 0; i < kHps; ++i) {
-          if (x + i >= x1) break;
-          const uint64_t a = sdesc_advance(dres, (x + i) * kHalf);
+          if (kRagged && x0 + kHps * m + i >= x1) break;
+          const uint64_t a = sdesc_advance(dres, (x0 + kHps * m + i) * kHalf);
           const uint64_t bd = sdesc_advance(bs, i * kHalf);
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
-            umma_ss_pair(x_tm, sdesc_advance(a, kk * 32), sdesc_advance(bd, kk * 32), idesc_x,
-                         (x > x0 || i > 0 || kk > 0) ? 1u : 0u);
+            umma_ss_pair(x_tm, sdesc_advance(a, kk * 32), sdesc_advance(bd, kk * 32), idesc_x, (m | i | kk) != 0);
         }
         umma_commit_pair(bar(empty0 + s), 3);
       }
@@ -387,8 +390,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     // (MN-major); dK, dQ: quarters [q0, q1), dV: half q0 / 2
     auto grad = [&](int c) {
       const uint64_t da = sdesc_advance(dds, (c & 1) * kDsBytes);
-      const uint32_t idg = (TWO || is_a) ? idesc_g : idesc_g1;
-      for (int qd = q0; qd < (TWO ? q1 : q0 + 1) && ok; ++qd) {
+      constexpr bool kSameG = idesc_g == idesc_g1;
+      const uint32_t idg = (kSameG || TWO || is_a) ? idesc_g : idesc_g1;
+      const int nq = TWO ? (is_a ? 2 : kNQ - 2) : 1;  // gradient slots of this thread
+      for (int qd = q0; qd < q0 + nq && ok; ++qd) {
         const uint32_t s = wait_slot();
         if (!ok) return;
         const uint64_t bs = sdesc_advance(dring_m, s * kSlot);
