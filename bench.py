@@ -308,7 +308,7 @@ def run_ffpa(args, rank, world):
 # DRAM bytes (read + write) per launch, dram__bytes_read.sum +
 # dram__bytes_write.sum from one ncu capture of the same workload; a kernel
 # changed since its capture is left out (its traffic is then reported as null).
-TRAFFIC: dict = {"fwd_main": 249160960, "bwd_dv": 248239104, "bwd_dk": 323979520, "bwd_dq": 324155648}
+TRAFFIC: dict = {"fwd_main": 248352256, "bwd_dv": 248421120, "bwd_dk": 324214272, "bwd_dq": 324147712}
 TRAFFIC_FROM = "ncu capture of the same workload (dram__bytes_read.sum + dram__bytes_write.sum per launch)"
 
 

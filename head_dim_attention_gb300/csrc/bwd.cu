@@ -19,13 +19,11 @@
 // columns per pass).  GQA: the dV/dK kernels sweep every query head of the
 // group, so the group's sum forms in TMEM without any atomics or workspace.
 //
-// D = 512 runs the full-D CTA-pair kernels of bwd_fulld.cu instead (launch_bwd
-// hands it over after the preprocess).
-//
-// For 320 <= D <= 512 the pair does not exchange: each CTA reduces the score
-// products over the whole of D itself (1.5x to 1.67x the MMA work) and owns
-// half of the gradient's columns.  The exchange's distributed-shared-memory
-// traffic (64 KB per product and tile) costs more time than the extra MMAs.
+// D = 320 .. 512 runs the full-D CTA-pair kernels of bwd_fulld.cu instead
+// (launch_bwd hands it over after the preprocess).  So this file's kernels
+// serve D <= 256 (one CTA holds the whole gradient) and D > 512 (the exchanging
+// pair); the exchange's distributed-shared-memory traffic (64 KB per product
+// and tile) bounds the latter.
 //
 // TMEM (512 columns): gradient accumulator [0, 256), X1 [256, 384) (scores),
 // X2 [384, 512) (dP, then P or dS as the bf16/f16 A operand of the gradient).
@@ -69,9 +67,9 @@ __host__ __device__ inline Bars bar_layout(int stages) {
   return b;
 }
 
-// Kernel flavours: one CTA per stationary tile (D <= 256), a cluster pair that
-// exchanges partial score tiles, or an independent pair that recomputes them.
-enum Flavour : int { kSolo = 0, kExchange = 1, kRecompute = 2 };
+// Kernel flavours: one CTA per stationary tile (D <= 256), or a cluster pair
+// that exchanges partial score tiles (D > 512).
+enum Flavour : int { kSolo = 0, kExchange = 1 };
 
 struct Plan {
   int a_chunks;  // chunks the score products reduce over (per resident operand)
@@ -854,7 +852,6 @@ cudaError_t launch_bwd(const BwdParams& p, const BwdMaps& m, bool bf16, cudaStre
     return e != cudaSuccess ? e : launch_bwd_fulld(p, m, bf16, s);
   }
   if (p.n_chunks <= 4) return bf16 ? launch_all<kSolo, true>(p, m, s) : launch_all<kSolo, false>(p, m, s);
-  if (p.n_chunks <= 8) return bf16 ? launch_all<kRecompute, true>(p, m, s) : launch_all<kRecompute, false>(p, m, s);
   return bf16 ? launch_all<kExchange, true>(p, m, s) : launch_all<kExchange, false>(p, m, s);
 }
 

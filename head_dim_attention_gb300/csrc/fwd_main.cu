@@ -1,4 +1,5 @@
-// Fused attention forward for large head dimensions on sm_103a.
+// Fused attention forward on sm_103a: the one-CTA kernel for D <= 256 and the
+// forward's dispatch.
 //
 // O = softmax(scale * Q K^T + bias) V and lse (natural log), the plain
 // definition in the attention-kernel-profiler design notes (generate_docs.py,
@@ -6,40 +7,16 @@
 // stream in tiles of 128 with an online softmax (running max and sum, lazy
 // rescale of O).
 //
-// Splitting D.  The FFPA pages' idea is to tile finely along the head
-// dimension so on-chip storage per tile stays bounded as D grows (FFPA-Attn
-// Performance Benchmarks page, "Why the Trends Look Like This": shared-memory
-// footprint and register pressure at large D).  On GB300 the binding on-chip
-// store is TMEM (512 fp32 columns x 128 lanes per SM): a 128 x 512 fp32 O
-// accumulator alone fills it.  So a cluster of two CTAs owns one 128-row
-// query tile and splits D in 64-column chunks between them:
-//   * CTA r holds Q[:, own chunks] resident in SMEM and its half of O in TMEM
-//     (<= 256 columns per pass);
-//   * it computes the partial score tile S_r = Q[:, own] K[:, own]^T with
-//     tcgen05.mma into TMEM (double-buffered, 2 x 128 columns);
-//   * the pair swaps the 128 x 128 fp32 partials through distributed shared
-//     memory (st.async with mbarrier complete_tx) and both add them, so both
-//     hold the exact S tile and run the same softmax;
-//   * P (f16/bf16) is written back into the S buffer in TMEM and used as the
-//     A operand of O[:, own] += P V[:, own].
-// With D <= 256 a single CTA holds all of O and no exchange is needed.
-// When a CTA owns more than 4 chunks (D > 512) it sweeps the keys once per
-// 4-chunk slice of its O columns ("passes"), recomputing S each time.
+// This kernel covers D <= 256, where one CTA holds all of O (at most 256 fp32
+// TMEM columns) next to two 128-column score buffers.  Every larger head
+// dimension (320 .. 1024) goes to the CTA-pair kernel of fwd_fulld.cu, which
+// launch_fwd_main below hands it to: there two SMs hold O's columns for one
+// 128-row query tile across all 128 TMEM lanes (the FFPA pages' fine tiling
+// along D, FFPA-Attn Performance Benchmarks page, "Why the Trends Look Like
+// This", applied to TMEM instead of registers and shared memory).
 //
-// Split without exchange (320 <= D <= 768).  The exchange moves 64 KB per key
-// tile and CTA through distributed shared memory, whose bandwidth is far
-// below the tensor pipe's.  So for D <= 512 two CTAs per query tile, and for
-// 576 <= D <= 768 three, each reduce S over the whole of D themselves (Q fully
-// resident, every K chunk streamed) and own at most four 64-column chunks of O:
-// more MMA work than the exchange (1.5x for two CTAs), but no cluster and no
-// DSMEM traffic.
-//
-// D = 512 itself does not run here: launch_fwd_main hands it to the CTA-pair
-// kernel of fwd_fulld.cu, in which two SMs hold all 512 columns of O for one
-// 128-row query tile, so S is computed once per key tile.
-//
-// Warp roles (256 threads): warp 0 = TMA producer, warp 1 = TMEM owner and
-// MMA issuer, warps 4-7 = softmax / correction / epilogue (one query row per
+// Warp roles (256 threads): warps 0, 2 and 3 = TMA producers, warp 1 = TMEM
+// owner and MMA issuer, warps 4-7 = softmax / correction / epilogue (one query row per
 // thread; warp 4+w reads TMEM lanes 32w..32w+31).
 #include <type_traits>
 
@@ -53,16 +30,15 @@ constexpr int kThreads = 256;
 constexpr int kProducers = 3;  // warps 0, 2 and 3
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kS0 = 256, kS1 = 384;  // TMEM columns of the two S/P buffers
-constexpr int kMaxOChunksPerPass = 4;     // O columns per pass: 4 x 64 = 256
+constexpr int kMaxChunks = 4;             // D <= 256: O in TMEM columns [0, 256)
 constexpr float kRescaleLog2 = 8.0f;      // rescale O only when the max grows by > 2^8
 // A key tile feeds P to P V as two 16-bit terms only when some row of it holds
 // a probability above this fraction of the row's running sum (see below).
 constexpr float kLoFrac = 1.0f / 64.0f;
-constexpr int kLandingBytes = kTileRows * kTileRows * 4;  // 64 KB partial-S landing buffer
 
 struct Bars {
   // indices into the barrier array
-  int full, empty, q_full, s_full, p_ready, o_ready, o_free, xfull, xfree, drain, count;
+  int full, empty, q_full, s_full, p_ready, o_ready, drain, count;
 };
 __host__ __device__ inline Bars bar_layout(int stages) {
   Bars b;
@@ -72,33 +48,21 @@ __host__ __device__ inline Bars bar_layout(int stages) {
   b.s_full = b.q_full + 1;   // 2
   b.p_ready = b.s_full + 2;  // 2
   b.o_ready = b.p_ready + 2;
-  b.o_free = b.o_ready + 1;
-  b.xfull = b.o_free + 1;
-  b.xfree = b.xfull + 1;
-  b.drain = b.xfree + 1;
+  b.drain = b.o_ready + 1;
   b.count = b.drain + 1;
   return b;
 }
 
-// Kernel flavours: one CTA per query tile (D <= 256), a cluster pair that
-// exchanges partial scores, or an independent pair that recomputes them.
-enum Flavour : int { kSolo = 0, kExchange = 1, kRecompute = 2, kRecompute3 = 3 };
-
-// CTAs that share one query tile (each owns a slice of O's columns).
-__host__ __device__ constexpr int ctas_per_tile(int fl) { return fl == kSolo ? 1 : (fl == kRecompute3 ? 3 : 2); }
-
+// shared memory: Q (all chunks, resident) | ring | barriers + TMEM slot
 struct SmemPlan {
-  int q_chunks;  // resident Q chunks (the chunks this CTA reduces S over)
-  int q_off, ring_off, land_off, bar_off, total;
+  int q_off, ring_off, bar_off, total;
 };
-__host__ __device__ inline SmemPlan smem_plan(int n_chunks, int fl, int stages, int slot_chunks) {
+__host__ __device__ inline SmemPlan smem_plan(int n_chunks, int stages, int slot_chunks) {
   SmemPlan s;
-  s.q_chunks = (fl == kExchange) ? (n_chunks + 1) / 2 : n_chunks;
   s.q_off = 0;
-  s.ring_off = s.q_chunks * kChunkBytes;
-  s.land_off = s.ring_off + stages * slot_chunks * kChunkBytes;
-  s.bar_off = s.land_off + (fl == kExchange ? kLandingBytes : 0);
-  s.total = s.bar_off + 1024;  // barriers + TMEM slot
+  s.ring_off = n_chunks * kChunkBytes;
+  s.bar_off = s.ring_off + stages * slot_chunks * kChunkBytes;
+  s.total = s.bar_off + 1024;
   return s;
 }
 
@@ -121,7 +85,7 @@ __device__ __forceinline__ uint32_t pack2(float a, float b) {
   }
 }
 
-template <int FL, bool BF16>
+template <bool BF16>
 __global__ void __launch_bounds__(kThreads, 1)
     fwd_main_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
                     const __grid_constant__ CUtensorMap map_v, const __grid_constant__ FwdParams p) {
@@ -130,9 +94,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int stages = p.stages;
   const int G = p.slot_chunks;                  // chunk tiles per ring slot
   const uint32_t slot_bytes = G * kChunkBytes;
-  constexpr int CS = ctas_per_tile(FL);  // CTAs per query tile
-  constexpr bool XCH = (FL == kExchange);
-  const SmemPlan plan = smem_plan(p.n_chunks, FL, stages, G);
+  const SmemPlan plan = smem_plan(p.n_chunks, stages, G);
   const Bars bl = bar_layout(stages);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + plan.bar_off);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + bl.count);
@@ -141,21 +103,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   volatile uint32_t* lo_flag = tmem_slot + 1;
   auto bar = [&](int i) { return smem_u32(&bars[i]); };
   const uint32_t s_base = smem_u32(smem);
-  const uint32_t q_sm = s_base + plan.q_off, ring_sm = s_base + plan.ring_off, land_sm = s_base + plan.land_off;
+  const uint32_t q_sm = s_base + plan.q_off, ring_sm = s_base + plan.ring_off;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const uint32_t rank = XCH ? cluster_ctarank() : static_cast<uint32_t>(blockIdx.x) % CS;  // which half of D
-  const int qt = p.q_tiles - 1 - static_cast<int>(blockIdx.x) / CS;  // heavy causal tiles first
+  const int qt = p.q_tiles - 1 - static_cast<int>(blockIdx.x);  // heavy causal tiles first
   const int h = blockIdx.y, b = blockIdx.z;
   const int kvh = h / p.group;
   const int q0 = qt * kTileRows;
-  const int n = p.n_chunks;
-  const int half = (n + CS - 1) / CS;
-  const int own0 = static_cast<int>(rank) * half;
-  const int own_n = min(half, n - own0);
-  const int s0 = XCH ? own0 : 0;  // chunks S is reduced over (and Q chunks resident)
-  const int s_n = XCH ? own_n : n;
-  const int passes = (half + kMaxOChunksPerPass - 1) / kMaxOChunksPerPass;
+  const int n = p.n_chunks;  // chunks of D: S reduces over them, O holds them
   const int kv_end = p.causal ? min(p.Nkv, q0 + kTileRows) : p.Nkv;
   const int ntiles = (kv_end + kTileRows - 1) / kTileRows;
   uint32_t* status = p.status;
@@ -171,9 +126,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar(bl.p_ready + i), 4);
     }
     mbar_init(bar(bl.o_ready), 1);
-    mbar_init(bar(bl.o_free), 4);
-    mbar_init(bar(bl.xfull), kTileRows);  // one arrive per peer row: "my partial is in your buffer"
-    mbar_init(bar(bl.xfree), kTileRows);  // one arrive per peer row: "your buffer is free again"
     mbar_init(bar(bl.drain), 1);
     lo_flag[0] = 0;
     lo_flag[1] = 0;
@@ -185,7 +137,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   tc_fence_before();
   __syncthreads();
-  if (XCH) cluster_sync();
   tc_fence_after();
   const uint32_t tbase = *tmem_slot;
 
@@ -206,9 +157,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_prefetch_desc(&map_k);
       tma_prefetch_desc(&map_v);
       if (pi == 0) {
-        mbar_expect_tx(bar(bl.q_full), s_n * kChunkBytes);
-        for (int c = 0; c < s_n; ++c)
-          tma_load_4d(q_sm + c * kChunkBytes, &map_q, bar(bl.q_full), (s0 + c) * kChunk, q0, h, b);
+        mbar_expect_tx(bar(bl.q_full), n * kChunkBytes);
+        for (int c = 0; c < n; ++c) tma_load_4d(q_sm + c * kChunkBytes, &map_q, bar(bl.q_full), c * kChunk, q0, h, b);
       }
       bool ok = true;
       uint32_t it = 0;
@@ -229,15 +179,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         ++it;
       };
-      for (int pass = 0; pass < passes && ok; ++pass) {
-        const int oc0 = pass * kMaxOChunksPerPass;
-        const int oc_n = max(0, min(kMaxOChunksPerPass, own_n - oc0));
-        for (int j = 0; j <= ntiles && ok; ++j) {
-          if (j < ntiles)
-            for (int c = 0; c < s_n; c += G) load(&map_k, s0 + c, min(G, s_n - c), j * kTileRows);
-          if (j >= 1)
-            for (int c = 0; c < oc_n; c += G) load(&map_v, own0 + oc0 + c, min(G, oc_n - c), (j - 1) * kTileRows);
-        }
+      // K of tile j, then V of tile j - 1: the order the MMA thread uses them
+      for (int j = 0; j <= ntiles && ok; ++j) {
+        if (j < ntiles)
+          for (int c = 0; c < n; c += G) load(&map_k, c, min(G, n - c), j * kTileRows);
+        if (j >= 1)
+          for (int c = 0; c < n; c += G) load(&map_v, c, min(G, n - c), (j - 1) * kTileRows);
       }
       // Drain: wait for the last release of each ring slot whose last load was
       // ours. The MMA warp's commit arrives on empty[s] only when the MMAs
@@ -264,117 +211,107 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = mbar_wait(bar(bl.q_full), 0, status);
       tc_fence_after();
       uint32_t it = 0;
-      int t0 = 0;  // global tile counter at the start of the pass
-      for (int pass = 0; pass < passes && ok; ++pass) {
-        const int oc0 = pass * kMaxOChunksPerPass;
-        const int oc_n = max(0, min(kMaxOChunksPerPass, own_n - oc0));
-        if (pass > 0) {
-          ok = mbar_wait(bar(bl.o_free), (pass - 1) & 1, status);  // epilogue done reading O
-          tc_fence_after();
-        }
-        for (int j = 0; j <= ntiles && ok; ++j) {
-          if (j < ntiles) {
-            // S_t lands in the buffer that held P_{t-2}, the A operand of the
-            // P_{t-2} V MMA; tcgen05.mma does not order a later MMA's write of D
-            // after an earlier MMA's read of A from TMEM, so S_t is issued once
-            // that MMA has completed.  S is issued whole (N=128): splitting it
-            // into N=64 halves to start earlier measured slower.
-            const int t = t0 + j;
-            const uint32_t s_tm = tbase + ((t & 1) ? kS1 : kS0);
-            if (j >= 2) {
-              ok = mbar_wait(bar(bl.o_ready), (t - 2) & 1, status);
-              if (!ok) break;
-              tc_fence_after();
-            }
-            for (int c = 0; c < s_n && ok; c += G) {
-              const uint32_t s = it % stages;
-              ok = mbar_wait(bar(bl.full + s), (it / stages) & 1, status);
-              if (!ok) break;
-              tc_fence_after();
-              const int cn = min(G, s_n - c);
-              for (int i = 0; i < cn; ++i) {
-                const uint64_t a = sdesc_advance(dq, (c + i) * kChunkBytes);
-                const uint64_t bd = sdesc_advance(dk, s * slot_bytes + i * kChunkBytes);
-#pragma unroll
-                for (int kk = 0; kk < 4; ++kk)
-                  umma_ss(s_tm, sdesc_advance(a, kk * 32), sdesc_advance(bd, kk * 32), idesc_s128,
-                          ((c + i) | kk) != 0);
-              }
-              umma_commit(bar(bl.empty + s));
-              ++it;
-            }
-            if (!ok) break;
-            umma_commit(bar(bl.s_full + (t & 1)));
-          }
-          if (j >= 1 && ok) {
-            const int t = t0 + j - 1;
-            ok = mbar_wait(bar(bl.p_ready + (t & 1)), (t >> 1) & 1, status);
+      for (int j = 0; j <= ntiles && ok; ++j) {
+        if (j < ntiles) {
+          // S_t lands in the buffer that held P_{t-2}, the A operand of the
+          // P_{t-2} V MMA; tcgen05.mma does not order a later MMA's write of D
+          // after an earlier MMA's read of A from TMEM, so S_t is issued once
+          // that MMA has completed.  S is issued whole (N=128): splitting it
+          // into N=64 halves to start earlier measured slower.
+          const int t = j;
+          const uint32_t s_tm = tbase + ((t & 1) ? kS1 : kS0);
+          if (j >= 2) {
+            ok = mbar_wait(bar(bl.o_ready), (t - 2) & 1, status);
             if (!ok) break;
             tc_fence_after();
-            const bool use_lo = lo_flag[t & 1] == static_cast<uint32_t>(t + 1);
-            const uint32_t p_tm = tbase + ((t & 1) ? kS1 : kS0);
-            // O[:, c..] += P V[:, c..]: two chunks per MMA (N=128) when they share
-            // a ring slot, or (one chunk per slot) sit in adjacent slots
-            for (int c = 0; c < oc_n && ok;) {
-              const uint32_t s = it % stages;
-              if (G == 2) {
-                ok = mbar_wait(bar(bl.full + s), (it / stages) & 1, status);
-                if (!ok) break;
-                tc_fence_after();
-                const uint64_t bd = sdesc_advance(dv, s * slot_bytes);
-                const uint32_t acc0 = (j - 1 > 0) ? 1u : 0u;
-                const uint32_t idesc = (c + 1 < oc_n) ? idesc_pv2 : idesc_pv;
+          }
+          for (int c = 0; c < n && ok; c += G) {
+            const uint32_t s = it % stages;
+            ok = mbar_wait(bar(bl.full + s), (it / stages) & 1, status);
+            if (!ok) break;
+            tc_fence_after();
+            const int cn = min(G, n - c);
+            for (int i = 0; i < cn; ++i) {
+              const uint64_t a = sdesc_advance(dq, (c + i) * kChunkBytes);
+              const uint64_t bd = sdesc_advance(dk, s * slot_bytes + i * kChunkBytes);
 #pragma unroll
-                for (int kk = 0; kk < 8; ++kk)
-                  umma_ts(tbase + c * kChunk, p_tm + kk * 8, sdesc_advance(bd, kk * 2048), idesc, acc0 | (kk > 0));
-                if (use_lo) {
-#pragma unroll
-                  for (int kk = 0; kk < 8; ++kk)  // the P_lo term
-                    umma_ts(tbase + c * kChunk, p_tm + 64 + kk * 8, sdesc_advance(bd, kk * 2048), idesc, 1u);
-                }
-                umma_commit(bar(bl.empty + s));
-                it += 1;
-                c += 2;
-                continue;
-              }
-              const bool two = (c + 1 < oc_n) && (s + 1 < static_cast<uint32_t>(stages));
+              for (int kk = 0; kk < 4; ++kk)
+                umma_ss(s_tm, sdesc_advance(a, kk * 32), sdesc_advance(bd, kk * 32), idesc_s128,
+                        ((c + i) | kk) != 0);
+            }
+            umma_commit(bar(bl.empty + s));
+            ++it;
+          }
+          if (!ok) break;
+          umma_commit(bar(bl.s_full + (t & 1)));
+        }
+        if (j >= 1 && ok) {
+          const int t = j - 1;
+          ok = mbar_wait(bar(bl.p_ready + (t & 1)), (t >> 1) & 1, status);
+          if (!ok) break;
+          tc_fence_after();
+          const bool use_lo = lo_flag[t & 1] == static_cast<uint32_t>(t + 1);
+          const uint32_t p_tm = tbase + ((t & 1) ? kS1 : kS0);
+          // O[:, c..] += P V[:, c..]: two chunks per MMA (N=128) when they share
+          // a ring slot, or (one chunk per slot) sit in adjacent slots
+          for (int c = 0; c < n && ok;) {
+            const uint32_t s = it % stages;
+            if (G == 2) {
               ok = mbar_wait(bar(bl.full + s), (it / stages) & 1, status);
-              if (ok && two) ok = mbar_wait(bar(bl.full + s + 1), ((it + 1) / stages) & 1, status);
               if (!ok) break;
               tc_fence_after();
-              const uint64_t bd = sdesc_advance(dv, s * kChunkBytes);
+              const uint64_t bd = sdesc_advance(dv, s * slot_bytes);
               const uint32_t acc0 = (j - 1 > 0) ? 1u : 0u;
-              if (two) {
+              const uint32_t idesc = (c + 1 < n) ? idesc_pv2 : idesc_pv;
 #pragma unroll
-                for (int kk = 0; kk < 8; ++kk)
-                  umma_ts(tbase + c * kChunk, p_tm + kk * 8, sdesc_advance(bd, kk * 2048), idesc_pv2, acc0 | (kk > 0));
-                if (use_lo) {
+              for (int kk = 0; kk < 8; ++kk)
+                umma_ts(tbase + c * kChunk, p_tm + kk * 8, sdesc_advance(bd, kk * 2048), idesc, acc0 | (kk > 0));
+              if (use_lo) {
 #pragma unroll
-                  for (int kk = 0; kk < 8; ++kk)  // the P_lo term
-                    umma_ts(tbase + c * kChunk, p_tm + 64 + kk * 8, sdesc_advance(bd, kk * 2048), idesc_pv2, 1u);
-                }
-                umma_commit(bar(bl.empty + s));
-                umma_commit(bar(bl.empty + s + 1));
-                it += 2;
-                c += 2;
-              } else {
-#pragma unroll
-                for (int kk = 0; kk < 8; ++kk)
-                  umma_ts(tbase + c * kChunk, p_tm + kk * 8, sdesc_advance(bd, kk * 2048), idesc_pv, acc0 | (kk > 0));
-                if (use_lo) {
-#pragma unroll
-                  for (int kk = 0; kk < 8; ++kk)  // the P_lo term
-                    umma_ts(tbase + c * kChunk, p_tm + 64 + kk * 8, sdesc_advance(bd, kk * 2048), idesc_pv, 1u);
-                }
-                umma_commit(bar(bl.empty + s));
-                it += 1;
-                c += 1;
+                for (int kk = 0; kk < 8; ++kk)  // the P_lo term
+                  umma_ts(tbase + c * kChunk, p_tm + 64 + kk * 8, sdesc_advance(bd, kk * 2048), idesc, 1u);
               }
+              umma_commit(bar(bl.empty + s));
+              it += 1;
+              c += 2;
+              continue;
             }
-            umma_commit(bar(bl.o_ready));
+            const bool two = (c + 1 < n) && (s + 1 < static_cast<uint32_t>(stages));
+            ok = mbar_wait(bar(bl.full + s), (it / stages) & 1, status);
+            if (ok && two) ok = mbar_wait(bar(bl.full + s + 1), ((it + 1) / stages) & 1, status);
+            if (!ok) break;
+            tc_fence_after();
+            const uint64_t bd = sdesc_advance(dv, s * kChunkBytes);
+            const uint32_t acc0 = (j - 1 > 0) ? 1u : 0u;
+            if (two) {
+#pragma unroll
+              for (int kk = 0; kk < 8; ++kk)
+                umma_ts(tbase + c * kChunk, p_tm + kk * 8, sdesc_advance(bd, kk * 2048), idesc_pv2, acc0 | (kk > 0));
+              if (use_lo) {
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk)  // the P_lo term
+                  umma_ts(tbase + c * kChunk, p_tm + 64 + kk * 8, sdesc_advance(bd, kk * 2048), idesc_pv2, 1u);
+              }
+              umma_commit(bar(bl.empty + s));
+              umma_commit(bar(bl.empty + s + 1));
+              it += 2;
+              c += 2;
+            } else {
+#pragma unroll
+              for (int kk = 0; kk < 8; ++kk)
+                umma_ts(tbase + c * kChunk, p_tm + kk * 8, sdesc_advance(bd, kk * 2048), idesc_pv, acc0 | (kk > 0));
+              if (use_lo) {
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk)  // the P_lo term
+                  umma_ts(tbase + c * kChunk, p_tm + 64 + kk * 8, sdesc_advance(bd, kk * 2048), idesc_pv, 1u);
+              }
+              umma_commit(bar(bl.empty + s));
+              it += 1;
+              c += 1;
+            }
           }
+          umma_commit(bar(bl.o_ready));
         }
-        t0 += ntiles;
       }
       umma_commit(bar(bl.drain));
       mbar_wait(bar(bl.drain), 0, status);
@@ -384,193 +321,157 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int r = tid - 128;  // query row within the tile == TMEM lane
     const int row = q0 + r;
     const uint32_t lane_off = static_cast<uint32_t>((warp - 4) * 32) << 16;
-    const uint32_t peer = rank ^ 1u;
-    const uint32_t peer_land = XCH ? mapa(land_sm, peer) : 0;
-    const uint32_t peer_xfull = XCH ? mapa(bar(bl.xfull), peer) : 0;
-    const uint32_t peer_xfree = XCH ? mapa(bar(bl.xfree), peer) : 0;
-    const uint32_t swz = static_cast<uint32_t>(r & 7);
     const float* bias_row = nullptr;
     if (p.bias)
       bias_row = p.bias + b * p.bias_sb + h * p.bias_sh + static_cast<int64_t>(min(row, p.Nq - 1)) * p.bias_sq;
     constexpr float kLog2e = 1.4426950408889634f;
     bool ok = true;
-    int t0 = 0;
     float m_used = -INFINITY, l_sum = 0.f;
-    for (int pass = 0; pass < passes && ok; ++pass) {
-      const int oc0 = pass * kMaxOChunksPerPass;
-      const int oc_n = max(0, min(kMaxOChunksPerPass, own_n - oc0));
-      m_used = -INFINITY;
-      l_sum = 0.f;
-      for (int j = 0; j < ntiles; ++j) {
-        const int t = t0 + j;
-        const uint32_t s_col = (t & 1) ? kS1 : kS0;
-        ok = __all_sync(0xffffffffu, mbar_wait(bar(bl.s_full + (t & 1)), (t >> 1) & 1, status));
-        if (!ok) break;
-        tc_fence_after();
-        float s[128];
+    for (int j = 0; j < ntiles; ++j) {
+      const int t = j;
+      const uint32_t s_col = (t & 1) ? kS1 : kS0;
+      ok = __all_sync(0xffffffffu, mbar_wait(bar(bl.s_full + (t & 1)), (t >> 1) & 1, status));
+      if (!ok) break;
+      tc_fence_after();
+      float s[128];
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          uint32_t v[32];
-          tmem_ld32(tbase + lane_off + s_col + c * 32, v);
-          tmem_ld_wait();
+      for (int c = 0; c < 4; ++c) {
+        uint32_t v[32];
+        tmem_ld32(tbase + lane_off + s_col + c * 32, v);
+        tmem_ld_wait();
 #pragma unroll
-          for (int i = 0; i < 32; ++i) s[c * 32 + i] = __uint_as_float(v[i]);
-        }
-        if constexpr (XCH) {
-          // swap partial scores with the peer CTA (it holds the other half of D)
-          if (t >= 1) {
-            ok = __all_sync(0xffffffffu, mbar_wait(bar(bl.xfree), (t - 1) & 1, status));
-            if (!ok) break;
-          }
-          const uint32_t dst = peer_land + r * 512;
+        for (int i = 0; i < 32; ++i) s[c * 32 + i] = __uint_as_float(v[i]);
+      }
+      // scale (log2 domain), bias, masks
+      const int kv0 = j * kTileRows;
+      const bool masked = (kv0 + kTileRows > p.Nkv) || (p.causal && kv0 + kTileRows - 1 > row);
+      const float c_scale = p.scale_log2;
+      if (bias_row) {
 #pragma unroll
-          for (int c = 0; c < 32; ++c)
-            st_cluster_v4(dst + ((c ^ swz) << 4), s[4 * c], s[4 * c + 1], s[4 * c + 2], s[4 * c + 3]);
-          mbar_arrive_remote(peer_xfull);  // release.cluster: the stores above are visible first
-          ok = __all_sync(0xffffffffu, mbar_wait(bar(bl.xfull), t & 1, status));
-          if (!ok) break;
-          const float4* src = reinterpret_cast<const float4*>(smem + plan.land_off + r * 512);
+        for (int i = 0; i < 128; ++i)
+          s[i] = fmaf(__ldg(bias_row + static_cast<int64_t>(kv0 + min(i, p.Nkv - 1 - kv0)) * p.bias_sk), kLog2e,
+                      s[i] * c_scale);
+      } else {
 #pragma unroll
-          for (int c = 0; c < 32; ++c) {
-            const float4 v = src[c ^ swz];
-            s[4 * c] += v.x;
-            s[4 * c + 1] += v.y;
-            s[4 * c + 2] += v.z;
-            s[4 * c + 3] += v.w;
-          }
-          mbar_arrive_remote(peer_xfree);  // my landing buffer is free again
-        }
-        // scale (log2 domain), bias, masks
-        const int kv0 = j * kTileRows;
-        const bool masked = (kv0 + kTileRows > p.Nkv) || (p.causal && kv0 + kTileRows - 1 > row);
-        const float c_scale = p.scale_log2;
-        if (bias_row) {
-#pragma unroll
-          for (int i = 0; i < 128; ++i)
-            s[i] = fmaf(__ldg(bias_row + static_cast<int64_t>(kv0 + min(i, p.Nkv - 1 - kv0)) * p.bias_sk), kLog2e,
-                        s[i] * c_scale);
-        } else {
-#pragma unroll
-          for (int i = 0; i < 128; ++i) s[i] *= c_scale;
-        }
-        if (masked) {
-#pragma unroll
-          for (int i = 0; i < 128; ++i) {
-            const int kv = kv0 + i;
-            if (kv >= p.Nkv || (p.causal && kv > row)) s[i] = -INFINITY;
-          }
-        }
-        float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-#pragma unroll
-        for (int i = 0; i < 128; ++i) mx[i & 3] = fmaxf(mx[i & 3], s[i]);
-        const float m_tile = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
-        float alpha = 1.f;
-        bool rescale = false;
-        if (m_used == -INFINITY) {
-          m_used = m_tile;
-        } else if (m_tile > m_used + kRescaleLog2) {
-          alpha = ex2(m_used - m_tile);
-          m_used = m_tile;
-          rescale = true;
-        }
-        const float m_ref = (m_used == -INFINITY) ? 0.f : m_used;
-        float ls[4] = {0.f, 0.f, 0.f, 0.f};
+        for (int i = 0; i < 128; ++i) s[i] *= c_scale;
+      }
+      if (masked) {
 #pragma unroll
         for (int i = 0; i < 128; ++i) {
-          s[i] = ex2(s[i] - m_ref);  // P, in place
-          ls[i & 3] += s[i];
-        }
-        l_sum = l_sum * alpha + ((ls[0] + ls[1]) + (ls[2] + ls[3]));
-        // Rounding P to 16 bits perturbs each weight by up to 2^-8 of itself
-        // (bf16).  That matters only for rows where a few keys carry much of
-        // the weight (outputs that are sums of a few nearly cancelling V rows);
-        // in a row whose weight is spread, the rounding errors of many small
-        // terms average out far below the tolerance.  So the residual term is
-        // fed only when this tile's largest probability exceeds kLoFrac of the
-        // row's running sum (the final sum is larger still).
-        const bool warp_lo = __any_sync(0xffffffffu, ex2(m_tile - m_ref) > kLoFrac * l_sum);
-        if (j >= 1) {
-          // Wait for the previous P V MMA before touching TMEM again: storing P
-          // while that MMA ran gave wrong O on GB300 (found by testing, single-
-          // CTA configuration), and the O correction below needs it anyway.
-          // The MMA is short, so this wait is normally already satisfied.
-          ok = __all_sync(0xffffffffu, mbar_wait(bar(bl.o_ready), (t - 1) & 1, status));
-          if (!ok) break;
-          tc_fence_after();
-        }
-        if (__any_sync(0xffffffffu, rescale) && j >= 1) {
-          // correction: O of this row *= alpha
-          for (int c = 0; c < oc_n; ++c) {
-#pragma unroll
-            for (int hh = 0; hh < 2; ++hh) {
-              uint32_t v[32];
-              const uint32_t a = tbase + lane_off + c * kChunk + hh * 32;
-              tmem_ld32(a, v);
-              tmem_ld_wait();
-#pragma unroll
-              for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * alpha);
-              tmem_st32(a, v);
-            }
-          }
-        }
-        // P goes to TMEM as two terms of the input type, P = P_hi + P_lo with
-        // P_lo the rounding residual of P_hi (columns 0..63 and 64..127 of the
-        // score buffer); the P V product sums both, so the 16-bit operand costs
-        // about 2^-17 of P instead of 2^-8 (bf16).  A warp whose rows do not
-        // need the residual stores zeros there, in case another warp's rows
-        // make the MMA thread issue the residual product for the whole tile.
-        if (warp_lo) {
-#pragma unroll
-          for (int g = 0; g < 4; ++g) {
-            uint32_t hi[16], lo[16];
-#pragma unroll
-            for (int e = 0; e < 16; ++e) {
-              const float p0 = s[32 * g + 2 * e], p1 = s[32 * g + 2 * e + 1];
-              hi[e] = pack2<BF16>(p0, p1);
-              const float2 h = unpack2<BF16>(hi[e]);
-              lo[e] = pack2<BF16>(p0 - h.x, p1 - h.y);
-            }
-            tmem_st16(tbase + lane_off + s_col + 16 * g, hi);
-            tmem_st16(tbase + lane_off + s_col + 64 + 16 * g, lo);
-          }
-        } else {
-          uint32_t zero[16];
-#pragma unroll
-          for (int e = 0; e < 16; ++e) zero[e] = 0u;
-#pragma unroll
-          for (int g = 0; g < 4; ++g) {
-            uint32_t hi[16];
-#pragma unroll
-            for (int e = 0; e < 16; ++e) hi[e] = pack2<BF16>(s[32 * g + 2 * e], s[32 * g + 2 * e + 1]);
-            tmem_st16(tbase + lane_off + s_col + 16 * g, hi);
-            tmem_st16(tbase + lane_off + s_col + 64 + 16 * g, zero);
-          }
-        }
-        tmem_st_wait();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) {
-          if (warp_lo) lo_flag[t & 1] = static_cast<uint32_t>(t + 1);
-          mbar_arrive(bar(bl.p_ready + (t & 1)));  // release: the flag store is visible first
+          const int kv = kv0 + i;
+          if (kv >= p.Nkv || (p.causal && kv > row)) s[i] = -INFINITY;
         }
       }
-      if (!ok) break;
-      // ---------------------------------------------------------- epilogue
-      const int t_last = t0 + ntiles - 1;
-      ok = __all_sync(0xffffffffu, mbar_wait(bar(bl.o_ready), t_last & 1, status));
-      if (!ok) break;
+      float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+      for (int i = 0; i < 128; ++i) mx[i & 3] = fmaxf(mx[i & 3], s[i]);
+      const float m_tile = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+      float alpha = 1.f;
+      bool rescale = false;
+      if (m_used == -INFINITY) {
+        m_used = m_tile;
+      } else if (m_tile > m_used + kRescaleLog2) {
+        alpha = ex2(m_used - m_tile);
+        m_used = m_tile;
+        rescale = true;
+      }
+      const float m_ref = (m_used == -INFINITY) ? 0.f : m_used;
+      float ls[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int i = 0; i < 128; ++i) {
+        s[i] = ex2(s[i] - m_ref);  // P, in place
+        ls[i & 3] += s[i];
+      }
+      l_sum = l_sum * alpha + ((ls[0] + ls[1]) + (ls[2] + ls[3]));
+      // Rounding P to 16 bits perturbs each weight by up to 2^-8 of itself
+      // (bf16).  That matters only for rows where a few keys carry much of
+      // the weight (outputs that are sums of a few nearly cancelling V rows);
+      // in a row whose weight is spread, the rounding errors of many small
+      // terms average out far below the tolerance.  So the residual term is
+      // fed only when this tile's largest probability exceeds kLoFrac of the
+      // row's running sum (the final sum is larger still).
+      const bool warp_lo = __any_sync(0xffffffffu, ex2(m_tile - m_ref) > kLoFrac * l_sum);
+      if (j >= 1) {
+        // Wait for the previous P V MMA before touching TMEM again: storing P
+        // while that MMA ran gave wrong O on GB300 (found by testing, single-
+        // CTA configuration), and the O correction below needs it anyway.
+        // The MMA is short, so this wait is normally already satisfied.
+        ok = __all_sync(0xffffffffu, mbar_wait(bar(bl.o_ready), (t - 1) & 1, status));
+        if (!ok) break;
+        tc_fence_after();
+      }
+      if (__any_sync(0xffffffffu, rescale) && j >= 1) {
+        // correction: O of this row *= alpha
+        for (int c = 0; c < n; ++c) {
+#pragma unroll
+          for (int hh = 0; hh < 2; ++hh) {
+            uint32_t v[32];
+            const uint32_t a = tbase + lane_off + c * kChunk + hh * 32;
+            tmem_ld32(a, v);
+            tmem_ld_wait();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * alpha);
+            tmem_st32(a, v);
+          }
+        }
+      }
+      // P goes to TMEM as two terms of the input type, P = P_hi + P_lo with
+      // P_lo the rounding residual of P_hi (columns 0..63 and 64..127 of the
+      // score buffer); the P V product sums both, so the 16-bit operand costs
+      // about 2^-17 of P instead of 2^-8 (bf16).  A warp whose rows do not
+      // need the residual stores zeros there, in case another warp's rows
+      // make the MMA thread issue the residual product for the whole tile.
+      if (warp_lo) {
+#pragma unroll
+        for (int g = 0; g < 4; ++g) {
+          uint32_t hi[16], lo[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            const float p0 = s[32 * g + 2 * e], p1 = s[32 * g + 2 * e + 1];
+            hi[e] = pack2<BF16>(p0, p1);
+            const float2 h = unpack2<BF16>(hi[e]);
+            lo[e] = pack2<BF16>(p0 - h.x, p1 - h.y);
+          }
+          tmem_st16(tbase + lane_off + s_col + 16 * g, hi);
+          tmem_st16(tbase + lane_off + s_col + 64 + 16 * g, lo);
+        }
+      } else {
+        uint32_t zero[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) zero[e] = 0u;
+#pragma unroll
+        for (int g = 0; g < 4; ++g) {
+          uint32_t hi[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e) hi[e] = pack2<BF16>(s[32 * g + 2 * e], s[32 * g + 2 * e + 1]);
+          tmem_st16(tbase + lane_off + s_col + 16 * g, hi);
+          tmem_st16(tbase + lane_off + s_col + 64 + 16 * g, zero);
+        }
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        if (warp_lo) lo_flag[t & 1] = static_cast<uint32_t>(t + 1);
+        mbar_arrive(bar(bl.p_ready + (t & 1)));  // release: the flag store is visible first
+      }
+    }
+    // ---------------------------------------------------------- epilogue
+    const int t_last = ntiles - 1;
+    if (ok) ok = __all_sync(0xffffffffu, mbar_wait(bar(bl.o_ready), t_last & 1, status));
+    if (ok) {
       tc_fence_after();
       const float inv_l = l_sum > 0.f ? 1.f / l_sum : 0.f;
       typedef typename std::conditional<BF16, __nv_bfloat16, __half>::type T;
       T* orow = reinterpret_cast<T*>(p.out) + b * p.o_sb + h * p.o_sh + static_cast<int64_t>(row) * p.o_sn;
-      for (int c = 0; c < oc_n; ++c) {
+      for (int c = 0; c < n; ++c) {
 #pragma unroll
         for (int hh = 0; hh < 2; ++hh) {
           uint32_t v[32];
           tmem_ld32(tbase + lane_off + c * kChunk + hh * 32, v);
           tmem_ld_wait();
           if (row < p.Nq) {
-            uint4* dst = reinterpret_cast<uint4*>(orow + (own0 + oc0 + c) * kChunk + hh * 32);
+            uint4* dst = reinterpret_cast<uint4*>(orow + c * kChunk + hh * 32);
 #pragma unroll
             for (int g = 0; g < 4; ++g) {
               uint4 w;
@@ -583,33 +484,27 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
-      if (pass == 0 && rank == 0 && p.lse && row < p.Nq) {
+      if (p.lse && row < p.Nq) {
         constexpr float kLn2 = 0.6931471805599453f;
         p.lse[(static_cast<int64_t>(b) * p.Hq + h) * p.Nq + row] =
             l_sum > 0.f ? (m_used + __log2f(l_sum)) * kLn2 : -INFINITY;
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar(bl.o_free));
-      t0 += ntiles;
     }
   }
 
   tc_fence_before();
   __syncthreads();
-  if (XCH) cluster_sync();
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tbase, kTmemCols);
   }
 }
 
-template <int FL, bool BF16>
+template <bool BF16>
 cudaError_t launch_impl(const FwdParams& p_in, const FwdMaps& m, cudaStream_t st) {
   FwdParams p = p_in;
-  constexpr int CS = ctas_per_tile(FL);
   constexpr int kMaxSmem = 232448;  // 227 KB opt-in per block
-  const SmemPlan base = smem_plan(p.n_chunks, FL, 0, 1);
+  const SmemPlan base = smem_plan(p.n_chunks, 0, 1);
   const int room = kMaxSmem - 1024 - base.total;
   // Two chunk tiles per ring slot when at least two such slots fit, else one.
   int G = (room / (2 * kChunkBytes) >= 2) ? 2 : 1;
@@ -618,23 +513,16 @@ cudaError_t launch_impl(const FwdParams& p_in, const FwdMaps& m, cudaStream_t st
   if (stages < 2) return cudaErrorInvalidConfiguration;
   p.stages = stages;
   p.slot_chunks = G;
-  const SmemPlan plan = smem_plan(p.n_chunks, FL, stages, G);
+  const SmemPlan plan = smem_plan(p.n_chunks, stages, G);
   const int smem = plan.total + 1024;  // + alignment slack
-  auto kern = fwd_main_kernel<FL, BF16>;
+  auto kern = fwd_main_kernel<BF16>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(CS * p.q_tiles, p.Hq, p.B);
+  cfg.gridDim = dim3(p.q_tiles, p.Hq, p.B);
   cfg.blockDim = dim3(kThreads, 1, 1);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = st;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = CS;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = (FL == kExchange) ? 1 : 0;  // only the exchanging pair is a cluster
   timing_mark(st);
   e = cudaLaunchKernelEx(&cfg, kern, m.q, m.k, m.v, p);
   timing_mark(st);
@@ -644,13 +532,9 @@ cudaError_t launch_impl(const FwdParams& p_in, const FwdMaps& m, cudaStream_t st
 }  // namespace
 
 cudaError_t launch_fwd_main(const FwdParams& p, const FwdMaps& m, bool bf16, cudaStream_t s) {
-  if (fwd_fulld_supported(p)) return launch_fwd_fulld(p, m, bf16, s);
-  if (p.n_chunks <= 4) return bf16 ? launch_impl<kSolo, true>(p, m, s) : launch_impl<kSolo, false>(p, m, s);
-  if (p.n_chunks <= 8)
-    return bf16 ? launch_impl<kRecompute, true>(p, m, s) : launch_impl<kRecompute, false>(p, m, s);
-  if (p.n_chunks <= 12)
-    return bf16 ? launch_impl<kRecompute3, true>(p, m, s) : launch_impl<kRecompute3, false>(p, m, s);
-  return bf16 ? launch_impl<kExchange, true>(p, m, s) : launch_impl<kExchange, false>(p, m, s);
+  if (fwd_fulld_supported(p)) return launch_fwd_fulld(p, m, bf16, s);  // D = 320 .. 1024
+  if (p.n_chunks > kMaxChunks) return cudaErrorInvalidValue;
+  return bf16 ? launch_impl<true>(p, m, s) : launch_impl<false>(p, m, s);
 }
 
 }  // namespace ffpa
