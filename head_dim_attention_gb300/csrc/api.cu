@@ -319,6 +319,10 @@ extern "C" int ffpa_bwd(const ffpa_tensor_t* q, const ffpa_tensor_t* k, const ff
   p.dq = dq->data;
   p.dk = dk->data;
   p.dv = dv->data;
+  p.k = k->data;
+  p.v = v->data;
+  p.k_sb = k->stride[0]; p.k_sh = k->stride[1]; p.k_sn = k->stride[2];
+  p.v_sb = v->stride[0]; p.v_sh = v->stride[1]; p.v_sn = v->stride[2];
   p.o_sb = out->stride[0]; p.o_sh = out->stride[1]; p.o_sn = out->stride[2];
   p.do_sb = dout->stride[0]; p.do_sh = dout->stride[1]; p.do_sn = dout->stride[2];
   p.dq_sb = dq->stride[0]; p.dq_sh = dq->stride[1]; p.dq_sn = dq->stride[2];

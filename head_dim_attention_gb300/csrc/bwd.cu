@@ -847,9 +847,11 @@ cudaError_t launch_all(const BwdParams& p, const BwdMaps& m, cudaStream_t st) {
 }  // namespace
 
 cudaError_t launch_bwd(const BwdParams& p, const BwdMaps& m, bool bf16, cudaStream_t s) {
-  if (bwd_fulld_supported(p)) {
+  if (bwd_fulld_supported(p) && bwd_dkv_supported(p)) {
+    // preprocess, fused dK/dV (two CTA pairs per key tile), then dQ
     cudaError_t e = bf16 ? launch_preprocess<true>(p, s) : launch_preprocess<false>(p, s);
-    return e != cudaSuccess ? e : launch_bwd_fulld(p, m, bf16, s);
+    if (e == cudaSuccess) e = launch_bwd_dkv(p, m, bf16, s);
+    return e != cudaSuccess ? e : launch_bwd_fulld_dq(p, m, bf16, s);
   }
   if (p.n_chunks <= 4) return bf16 ? launch_all<kSolo, true>(p, m, s) : launch_all<kSolo, false>(p, m, s);
   return bf16 ? launch_all<kExchange, true>(p, m, s) : launch_all<kExchange, false>(p, m, s);

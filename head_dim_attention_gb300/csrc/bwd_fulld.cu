@@ -683,21 +683,13 @@ cudaError_t launch_mode(const BwdParams& p, const BwdMaps& m, cudaStream_t st) {
   return e;
 }
 
-template <int NC, bool BF16>
-cudaError_t launch_modes(const BwdParams& p, const BwdMaps& m, cudaStream_t st) {
-  cudaError_t e;
-  if ((e = launch_mode<kDV, NC, BF16>(p, m, st)) != cudaSuccess) return e;
-  if ((e = launch_mode<kDK, NC, BF16>(p, m, st)) != cudaSuccess) return e;
-  return launch_mode<kDQ, NC, BF16>(p, m, st);
-}
-
 template <bool BF16>
-cudaError_t launch_nc(const BwdParams& p, const BwdMaps& m, cudaStream_t st) {
+cudaError_t launch_dq(const BwdParams& p, const BwdMaps& m, cudaStream_t st) {
   switch (p.n_chunks) {
-    case 5: return launch_modes<5, BF16>(p, m, st);
-    case 6: return launch_modes<6, BF16>(p, m, st);
-    case 7: return launch_modes<7, BF16>(p, m, st);
-    default: return launch_modes<8, BF16>(p, m, st);
+    case 5: return launch_mode<kDQ, 5, BF16>(p, m, st);
+    case 6: return launch_mode<kDQ, 6, BF16>(p, m, st);
+    case 7: return launch_mode<kDQ, 7, BF16>(p, m, st);
+    default: return launch_mode<kDQ, 8, BF16>(p, m, st);
   }
 }
 
@@ -705,8 +697,8 @@ cudaError_t launch_nc(const BwdParams& p, const BwdMaps& m, cudaStream_t st) {
 
 bool bwd_fulld_supported(const BwdParams& p) { return p.n_chunks >= 5 && p.n_chunks <= 8; }
 
-cudaError_t launch_bwd_fulld(const BwdParams& p, const BwdMaps& m, bool bf16, cudaStream_t s) {
-  return bf16 ? launch_nc<true>(p, m, s) : launch_nc<false>(p, m, s);
+cudaError_t launch_bwd_fulld_dq(const BwdParams& p, const BwdMaps& m, bool bf16, cudaStream_t s) {
+  return bf16 ? launch_dq<true>(p, m, s) : launch_dq<false>(p, m, s);
 }
 
 }  // namespace ffpa
