@@ -210,14 +210,14 @@ def run_ffpa(args, rank, world):
     out = torch.empty_like(q)
     lse = torch.empty(B, H, N, dtype=torch.float32, device=dev)
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
-    names = ["fwd_main", "bwd_preprocess", "bwd_dv", "bwd_dk", "bwd_dq"]
+    names = ["fwd_main", "bwd_preprocess", "bwd_dkv", "bwd_dq"]
 
     def step(evs=None):
         if evs:
             ffpa_set_timing_events(evs[0:2])
         ffpa_fwd(q, k, v, None, 0, scale, out, lse)
         if evs:
-            ffpa_set_timing_events(evs[2:7])
+            ffpa_set_timing_events(evs[2:6])
         ffpa_bwd(q, k, v, None, 0, scale, out, lse, do, dq, dk, dv)
         if evs:
             ffpa_set_timing_events(None)
@@ -229,7 +229,7 @@ def run_ffpa(args, rank, world):
         raise RuntimeError("a kernel reported a timeout during warm-up")
 
     K = args.steps
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(7)] for _ in range(K)]
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(K)]
     for row in evs:
         for e in row:
             e.record()  # torch creates the CUDA event on first record
@@ -248,7 +248,7 @@ def run_ffpa(args, rank, world):
     if ffpa_check_status() != 0:
         raise RuntimeError("a kernel reported a timeout in the timed region")
     ms = t0.elapsed_time(t1)
-    spans = [(0, 1), (2, 3), (3, 4), (4, 5), (5, 6)]
+    spans = [(0, 1), (2, 3), (3, 4), (4, 5)]
     kern_ms = {n: statistics.mean(evs[i][a].elapsed_time(evs[i][b]) for i in range(K))
                for n, (a, b) in zip(names, spans)}
     ms = max_over_ranks(ms, dev)  # the slowest rank sets the job's time
@@ -256,8 +256,9 @@ def run_ffpa(args, rank, world):
     value = world * step_flop * K / (ms / 1e3) / 1e12
 
     # dominant kernel: the largest share of the step; its own GEMMs as algorithmic work
-    gemm_flop = {"fwd_main": FWD_FLOP, "bwd_preprocess": 0, "bwd_dv": 4 * B * H * N * N * D,
-                 "bwd_dk": 6 * B * H * N * N * D, "bwd_dq": 6 * B * H * N * N * D}
+    # fused dK/dV: S^T, dP^T, dK and dV products (4 x 2 N^2 D per head); dQ: S, dP, dQ
+    gemm_flop = {"fwd_main": FWD_FLOP, "bwd_preprocess": 0, "bwd_dkv": 8 * B * H * N * N * D,
+                 "bwd_dq": 6 * B * H * N * N * D}
     dom = max(kern_ms, key=kern_ms.get)
     achieved = gemm_flop[dom] / (kern_ms[dom] / 1e3) / 1e12
     # The timed region lasts a fraction of a second at the maximum SM clock:
@@ -299,7 +300,7 @@ def run_ffpa(args, rank, world):
                        "l2": "no flush: each step reads Q/K/V/O/dO and writes O/dQ/dK/dV, 512 MiB > 129 MB L2",
                        "frac_of_peak": {"burst": value / world / peaks["bf16_tflops"],
                                         "sustained": value / world / peaks["bf16_tflops_sustained"]}},
-            "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": 5 * K,
+            "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": len(names) * K,
             "clocks": clocks.summary(), "decode": decode, "variants": variants,
         }
         print(json.dumps(line), flush=True)
@@ -308,7 +309,7 @@ def run_ffpa(args, rank, world):
 # DRAM bytes (read + write) per launch, dram__bytes_read.sum +
 # dram__bytes_write.sum from one ncu capture of the same workload; a kernel
 # changed since its capture is left out (its traffic is then reported as null).
-TRAFFIC: dict = {"fwd_main": 248352256, "bwd_dv": 248421120, "bwd_dk": 324214272, "bwd_dq": 324147712}
+TRAFFIC: dict = {"fwd_main": 248352256}
 TRAFFIC_FROM = "ncu capture of the same workload (dram__bytes_read.sum + dram__bytes_write.sum per launch)"
 
 
