@@ -319,8 +319,10 @@ extern "C" int ffpa_bwd(const ffpa_tensor_t* q, const ffpa_tensor_t* k, const ff
   p.dq = dq->data;
   p.dk = dk->data;
   p.dv = dv->data;
+  p.q = q->data;
   p.k = k->data;
   p.v = v->data;
+  p.q_sb = q->stride[0]; p.q_sh = q->stride[1]; p.q_sn = q->stride[2];
   p.k_sb = k->stride[0]; p.k_sh = k->stride[1]; p.k_sn = k->stride[2];
   p.v_sb = v->stride[0]; p.v_sh = v->stride[1]; p.v_sn = v->stride[2];
   p.o_sb = out->stride[0]; p.o_sh = out->stride[1]; p.o_sn = out->stride[2];

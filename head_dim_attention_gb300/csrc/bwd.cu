@@ -19,7 +19,7 @@
 // columns per pass).  GQA: the dV/dK kernels sweep every query head of the
 // group, so the group's sum forms in TMEM without any atomics or workspace.
 //
-// D = 320 .. 512 runs the full-D CTA-pair kernels of bwd_fulld.cu instead
+// D = 320 .. 512 runs the CTA-pair kernels of bwd_dkv.cu and bwd_dq.cu instead
 // (launch_bwd hands it over after the preprocess).  So this file's kernels
 // serve D <= 256 (one CTA holds the whole gradient) and D > 512 (the exchanging
 // pair); the exchange's distributed-shared-memory traffic (64 KB per product
@@ -847,11 +847,11 @@ cudaError_t launch_all(const BwdParams& p, const BwdMaps& m, cudaStream_t st) {
 }  // namespace
 
 cudaError_t launch_bwd(const BwdParams& p, const BwdMaps& m, bool bf16, cudaStream_t s) {
-  if (bwd_fulld_supported(p) && bwd_dkv_supported(p)) {
-    // preprocess, fused dK/dV (two CTA pairs per key tile), then dQ
+  if (bwd_dq_supported(p) && bwd_dkv_supported(p)) {
+    // preprocess, fused dK/dV (two CTA pairs per key tile), then dQ (one pair per query tile)
     cudaError_t e = bf16 ? launch_preprocess<true>(p, s) : launch_preprocess<false>(p, s);
     if (e == cudaSuccess) e = launch_bwd_dkv(p, m, bf16, s);
-    return e != cudaSuccess ? e : launch_bwd_fulld_dq(p, m, bf16, s);
+    return e != cudaSuccess ? e : launch_bwd_dq(p, m, bf16, s);
   }
   if (p.n_chunks <= 4) return bf16 ? launch_all<kSolo, true>(p, m, s) : launch_all<kSolo, false>(p, m, s);
   return bf16 ? launch_all<kExchange, true>(p, m, s) : launch_all<kExchange, false>(p, m, s);

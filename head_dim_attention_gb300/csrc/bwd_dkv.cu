@@ -1,8 +1,8 @@
 // Fused dK/dV backward for D = 320..512: one cluster of four CTAs (two CTA
 // pairs) per 128-row key tile.
 //
-// The separate dV and dK kernels of bwd_fulld.cu both rebuild S^T = K Q^T for
-// every (key tile, query tile) and execute 4 + 6 = 10 Nq Nkv D per head.  A
+// Separate dV and dK kernels would both rebuild S^T = K Q^T for every (key
+// tile, query tile) and execute 4 + 6 = 10 Nq Nkv D per head.  A
 // single pair cannot hold both gradients (128 x 512 fp32 each fills half of
 // an SM's TMEM in the M = 128 pair layout, and the score tiles need room too),
 // so the two gradients go to two pairs of one cluster that share the work of
@@ -17,7 +17,7 @@
 // Each pair executes one score product and one gradient product per column
 // tile: 8 Nq Nkv D per head for dK and dV together, split evenly.
 //
-// Within a pair the layout is bwd_fulld.cu's: CTA c (c = rank & 1) holds
+// Within a pair the layout is that of bwd_dq.cu: CTA c (c = rank & 1) holds
 // stationary rows 64c .. 64c + 63 across all 128 TMEM lanes (lane r: row r,
 // the first half of an accumulator's columns; lane r + 64: the second half).
 // CTA r of pair A and CTA r + 2 of pair B hold the same 64 key rows, so each

@@ -80,8 +80,10 @@ struct BwdParams {
   void* dq;
   void* dk;
   void* dv;
-  const void* k;      // read directly (not through TMA) by the fused dK/dV kernel
+  const void* q;      // read directly (not through TMA) by the dQ and fused dK/dV kernels
+  const void* k;
   const void* v;
+  int64_t q_sb, q_sh, q_sn;
   int64_t k_sb, k_sh, k_sn;
   int64_t v_sb, v_sh, v_sn;
   int64_t o_sb, o_sh, o_sn;
@@ -119,10 +121,9 @@ cudaError_t launch_fwd_decode_noalloc(const DecodeParams& p, bool bf16, cudaStre
 size_t decode_scratch_bytes(const DecodeParams& p);
 size_t decode_noalloc_capacity_bytes();
 cudaError_t launch_bwd(const BwdParams& p, const BwdMaps& m, bool bf16, cudaStream_t s);
-// Full-D CTA-pair dQ (and separate dV, dK) kernels (bwd_fulld.cu): D = 320 .. 512;
-// the preprocess runs first.
-bool bwd_fulld_supported(const BwdParams& p);
-cudaError_t launch_bwd_fulld_dq(const BwdParams& p, const BwdMaps& m, bool bf16, cudaStream_t s);
+// Full-D CTA-pair dQ kernel (bwd_dq.cu): D = 320 .. 512; the preprocess runs first.
+bool bwd_dq_supported(const BwdParams& p);
+cudaError_t launch_bwd_dq(const BwdParams& p, const BwdMaps& m, bool bf16, cudaStream_t s);
 // Fused dK/dV kernel, a cluster of two CTA pairs per key tile (bwd_dkv.cu): D = 320 .. 512.
 bool bwd_dkv_supported(const BwdParams& p);
 cudaError_t launch_bwd_dkv(const BwdParams& p, const BwdMaps& m, bool bf16, cudaStream_t s);
