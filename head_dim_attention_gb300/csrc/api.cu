@@ -180,8 +180,9 @@ int cuda_rc(cudaError_t e) { return e == cudaSuccess ? FFPA_OK : FFPA_ERR_CUDA; 
 constexpr int kDecodeMaxRows = 16;
 
 // Keys per decode slice: the multiple of 16 in [128, 256] for which the
-// decode CTAs (one per batch, query head and slice; two fit on an SM) fill
-// their last wave best on the current device.  Ties go to the longer slice.
+// decode CTAs (one per batch, group of query heads sharing a kv head, and
+// slice; two fit on an SM) fill their last wave best on the current device;
+// `Hq` counts those groups.  Ties go to the longer slice.
 // Slices of at least 128 keys keep a call's partials within what 128-key
 // slices would take (the no-allocation entry point's capacity check).
 int decode_split_len(int64_t B, int64_t Hq, int64_t Nkv) {
@@ -253,7 +254,8 @@ extern "C" int ffpa_fwd(const ffpa_tensor_t* q, const ffpa_tensor_t* k, const ff
     p.group = (int)(c.Hq / c.Hkv);
     p.causal = causal;
     p.scale_log2 = scale * kLog2e;
-    p.split_len = decode_split_len(c.B, c.Hq, c.Nkv);
+    p.heads_per_cta = decode_heads_per_cta(p.group, p.Nq, p.D);
+    p.split_len = decode_split_len(c.B, c.Hq / p.heads_per_cta, c.Nkv);
     p.n_splits = (int)((c.Nkv + p.split_len - 1) / p.split_len);
     p.status = status;
     const size_t n_rows = (size_t)c.B * c.Hq * c.Nq * p.n_splits;
@@ -388,7 +390,8 @@ extern "C" int ffpa_fwd_decode_noalloc(const ffpa_tensor_t* q, const ffpa_tensor
   p.group = (int)(c.Hq / c.Hkv);
   p.causal = causal;
   p.scale_log2 = scale * kLog2e;
-  p.split_len = decode_split_len(c.B, c.Hq, c.Nkv);
+  p.heads_per_cta = decode_heads_per_cta(p.group, p.Nq, p.D);
+  p.split_len = decode_split_len(c.B, c.Hq / p.heads_per_cta, c.Nkv);
   p.n_splits = (int)((c.Nkv + p.split_len - 1) / p.split_len);
   p.status = device_status_word();  // fetched with cudaGetSymbolAddress, no allocation
   if (!p.status) return FFPA_ERR_CUDA;

@@ -211,8 +211,11 @@ __global__ void __launch_bounds__(kDecThreads) decode_split_kernel(const __grid_
 template <int R, int G, int U, bool BF16>
 __global__ void __launch_bounds__(kDecThreads) decode_stream_kernel(const __grid_constant__ DecodeParams p) {
   extern __shared__ __align__(16) float wsm[];  // [8 warps][R][D] partial O, then [8][R] m and l
-  const int split = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
-  const int g = h / p.group;
+  const int split = blockIdx.x, b = blockIdx.z;
+  // query heads h0 .. h0 + heads_per_cta - 1 share kv head g: row r of this
+  // CTA is query row r % Nq of head h0 + r / Nq
+  const int h0 = blockIdx.y * p.heads_per_cta, g = h0 / p.group;
+  const int nrows = p.heads_per_cta * p.Nq;
   const int D = p.D, Nq = p.Nq, L = p.split_len;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int groups = D / 8;
@@ -230,9 +233,9 @@ __global__ void __launch_bounds__(kDecThreads) decode_stream_kernel(const __grid
 #pragma unroll
     for (int k = 0; k < G; ++k) {
       const int c = lane + 32 * k;
-      if (r < Nq && c < groups)
-        Vec8<BF16>::load(reinterpret_cast<const T*>(p.q) + b * p.q_sb + h * p.q_sh + static_cast<int64_t>(r) * p.q_sn +
-                             c * 8,
+      if (r < nrows && c < groups)
+        Vec8<BF16>::load(reinterpret_cast<const T*>(p.q) + b * p.q_sb + (h0 + r / Nq) * p.q_sh +
+                             static_cast<int64_t>(r % Nq) * p.q_sn + c * 8,
                          qf[r][k]);
       else
 #pragma unroll
@@ -296,10 +299,10 @@ __global__ void __launch_bounds__(kDecThreads) decode_stream_kernel(const __grid
         const int kv = kv_begin + j0 + u;
         float x = s[u][r] * p.scale_log2;
         if (p.bias)
-          x = fmaf(__ldg(p.bias + b * p.bias_sb + h * p.bias_sh + static_cast<int64_t>(r) * p.bias_sq +
+          x = fmaf(__ldg(p.bias + b * p.bias_sb + (h0 + r / Nq) * p.bias_sh + static_cast<int64_t>(r % Nq) * p.bias_sq +
                          static_cast<int64_t>(min(kv, p.Nkv - 1)) * p.bias_sk),
                    kLog2e, x);
-        const bool valid = (j0 + u < j_end) && r < Nq && !(p.causal && kv > r);
+        const bool valid = (j0 + u < j_end) && r < nrows && !(p.causal && kv > r % Nq);
         s[u][r] = valid ? x : -INFINITY;
       }
     }
@@ -361,7 +364,7 @@ __global__ void __launch_bounds__(kDecThreads) decode_stream_kernel(const __grid
     }
   }
   __syncthreads();
-  for (int r = 0; r < Nq; ++r) {
+  for (int r = 0; r < nrows; ++r) {
     float M = -INFINITY;
 #pragma unroll
     for (int w = 0; w < 8; ++w) M = fmaxf(M, sm[w * R + r]);
@@ -373,7 +376,7 @@ __global__ void __launch_bounds__(kDecThreads) decode_stream_kernel(const __grid
       wgt[w] = ex2(sm[w * R + r] - Mref);  // -inf (empty warp) gives 0
       Ls += wgt[w] * sl[w * R + r];
     }
-    float* dst = p.part_o + ((((static_cast<int64_t>(b) * p.Hq + h) * Nq + r) * p.n_splits + split) * D);
+    float* dst = p.part_o + ((((static_cast<int64_t>(b) * p.Hq + h0 + r / Nq) * Nq + r % Nq) * p.n_splits + split) * D);
     for (int d = threadIdx.x * 4; d < D; d += kDecThreads * 4) {
       float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
@@ -387,7 +390,7 @@ __global__ void __launch_bounds__(kDecThreads) decode_stream_kernel(const __grid
       *reinterpret_cast<float4*>(dst + d) = acc;
     }
     if (threadIdx.x == 0) {
-      float* ml = p.part_ml + (((static_cast<int64_t>(b) * p.Hq + h) * Nq + r) * p.n_splits + split) * 2;
+      float* ml = p.part_ml + (((static_cast<int64_t>(b) * p.Hq + h0 + r / Nq) * Nq + r % Nq) * p.n_splits + split) * 2;
       ml[0] = M;
       ml[1] = Ls;
     }
@@ -415,8 +418,11 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
 template <int R, int G, bool BF16>
 __global__ void __launch_bounds__(kDecThreads) decode_bulk_kernel(const __grid_constant__ DecodeParams p) {
   extern __shared__ __align__(128) uint8_t bsm[];
-  const int split = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
-  const int g = h / p.group;
+  const int split = blockIdx.x, b = blockIdx.z;
+  // query heads h0 .. h0 + heads_per_cta - 1 share kv head g: row r of this
+  // CTA is query row r % Nq of head h0 + r / Nq
+  const int h0 = blockIdx.y * p.heads_per_cta, g = h0 / p.group;
+  const int nrows = p.heads_per_cta * p.Nq;
   const int D = p.D, Nq = p.Nq, L = p.split_len;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int groups = D / 8;
@@ -461,9 +467,9 @@ __global__ void __launch_bounds__(kDecThreads) decode_bulk_kernel(const __grid_c
 #pragma unroll
     for (int k = 0; k < G; ++k) {
       const int c = lane + 32 * k;
-      if (r < Nq && c < groups)
-        Vec8<BF16>::load(reinterpret_cast<const T*>(p.q) + b * p.q_sb + h * p.q_sh + static_cast<int64_t>(r) * p.q_sn +
-                             c * 8,
+      if (r < nrows && c < groups)
+        Vec8<BF16>::load(reinterpret_cast<const T*>(p.q) + b * p.q_sb + (h0 + r / Nq) * p.q_sh +
+                             static_cast<int64_t>(r % Nq) * p.q_sn + c * 8,
                          qf[r][k]);
       else
 #pragma unroll
@@ -526,10 +532,10 @@ __global__ void __launch_bounds__(kDecThreads) decode_bulk_kernel(const __grid_c
         const int kv = kv_begin + i * kBulkKeys + kk;
         float x = sc[u][r] * p.scale_log2;
         if (p.bias)
-          x = fmaf(__ldg(p.bias + b * p.bias_sb + h * p.bias_sh + static_cast<int64_t>(r) * p.bias_sq +
+          x = fmaf(__ldg(p.bias + b * p.bias_sb + (h0 + r / Nq) * p.bias_sh + static_cast<int64_t>(r % Nq) * p.bias_sq +
                          static_cast<int64_t>(min(kv, p.Nkv - 1)) * p.bias_sk),
                    kLog2e, x);
-        const bool valid = kk < n && r < Nq && !(p.causal && kv > r);
+        const bool valid = kk < n && r < nrows && !(p.causal && kv > r % Nq);
         sc[u][r] = valid ? x : -INFINITY;
       }
     }
@@ -595,7 +601,7 @@ __global__ void __launch_bounds__(kDecThreads) decode_bulk_kernel(const __grid_c
     }
   }
   __syncthreads();
-  for (int r = 0; r < Nq; ++r) {
+  for (int r = 0; r < nrows; ++r) {
     float M = -INFINITY;
 #pragma unroll
     for (int w = 0; w < 8; ++w) M = fmaxf(M, sm[w * R + r]);
@@ -607,7 +613,7 @@ __global__ void __launch_bounds__(kDecThreads) decode_bulk_kernel(const __grid_c
       wgt[w] = ex2(sm[w * R + r] - Mref);
       Ls += wgt[w] * sl[w * R + r];
     }
-    float* dst = p.part_o + ((((static_cast<int64_t>(b) * p.Hq + h) * Nq + r) * p.n_splits + split) * D);
+    float* dst = p.part_o + ((((static_cast<int64_t>(b) * p.Hq + h0 + r / Nq) * Nq + r % Nq) * p.n_splits + split) * D);
     for (int d = threadIdx.x * 4; d < D; d += kDecThreads * 4) {
       float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
@@ -621,7 +627,7 @@ __global__ void __launch_bounds__(kDecThreads) decode_bulk_kernel(const __grid_c
       *reinterpret_cast<float4*>(dst + d) = acc;
     }
     if (threadIdx.x == 0) {
-      float* ml = p.part_ml + (((static_cast<int64_t>(b) * p.Hq + h) * Nq + r) * p.n_splits + split) * 2;
+      float* ml = p.part_ml + (((static_cast<int64_t>(b) * p.Hq + h0 + r / Nq) * Nq + r % Nq) * p.n_splits + split) * 2;
       ml[0] = M;
       ml[1] = Ls;
     }
@@ -719,7 +725,7 @@ cudaError_t launch_stream(const DecodeParams& p, cudaStream_t st) {
   auto k1 = decode_stream_kernel<R, G, U, BF16>;
   cudaError_t e = cudaFuncSetAttribute(k1, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return e;
-  k1<<<dim3(p.n_splits, p.Hq, p.B), kDecThreads, smem, st>>>(p);
+  k1<<<dim3(p.n_splits, p.Hq / p.heads_per_cta, p.B), kDecThreads, smem, st>>>(p);
   return cudaSuccess;
 }
 
@@ -731,7 +737,7 @@ cudaError_t launch_bulk(const DecodeParams& p, cudaStream_t st) {
   auto k1 = decode_bulk_kernel<R, G, BF16>;
   cudaError_t e = cudaFuncSetAttribute(k1, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return e;
-  k1<<<dim3(p.n_splits, p.Hq, p.B), kDecThreads, smem, st>>>(p);
+  k1<<<dim3(p.n_splits, p.Hq / p.heads_per_cta, p.B), kDecThreads, smem, st>>>(p);
   return cudaSuccess;
 }
 
@@ -740,15 +746,22 @@ cudaError_t launch_decode_impl(const DecodeParams& p, cudaStream_t st) {
   cudaError_t e = cudaSuccess;
   timing_mark(st);
   // rows of K and V contiguous (row stride D): the slice streams through
-  // shared memory with bulk copies
+  // shared memory with bulk copies.  A CTA takes heads_per_cta query heads of
+  // one kv head (decode_heads_per_cta), so its rows are their query rows.
   const bool rows_contiguous = p.k_sn == p.D && p.v_sn == p.D;
-  if (p.Nq <= 2 && p.D <= 512 && rows_contiguous && p.split_len % kBulkKeys == 0) {
-    e = p.Nq == 1 ? launch_bulk<1, 2, BF16>(p, st) : launch_bulk<2, 2, BF16>(p, st);
-  } else if (p.Nq <= 2 && p.D <= 512) {
-    e = p.Nq == 1 ? launch_stream<1, 2, 4, BF16>(p, st) : launch_stream<2, 2, 4, BF16>(p, st);
-  } else if (p.Nq <= 2) {
-    e = p.Nq == 1 ? launch_stream<1, 4, 2, BF16>(p, st) : launch_stream<2, 4, 2, BF16>(p, st);
+  const int nrows = p.heads_per_cta * p.Nq;
+  if (nrows <= 4 && p.D <= 512 && rows_contiguous && p.split_len % kBulkKeys == 0) {
+    e = nrows == 1   ? launch_bulk<1, 2, BF16>(p, st)
+        : nrows == 2 ? launch_bulk<2, 2, BF16>(p, st)
+                     : launch_bulk<4, 2, BF16>(p, st);
+  } else if (nrows <= 4 && p.D <= 512) {
+    e = nrows == 1   ? launch_stream<1, 2, 4, BF16>(p, st)
+        : nrows == 2 ? launch_stream<2, 2, 4, BF16>(p, st)
+                     : launch_stream<4, 2, 2, BF16>(p, st);
+  } else if (nrows <= 2) {
+    e = nrows == 1 ? launch_stream<1, 4, 2, BF16>(p, st) : launch_stream<2, 4, 2, BF16>(p, st);
   } else {
+    if (p.heads_per_cta != 1) return cudaErrorInvalidValue;
     const size_t smem = (static_cast<size_t>(p.Nq) * p.D + static_cast<size_t>(p.Nq) * p.split_len + 2 * p.Nq) * 4;
     auto k1 = decode_split_kernel<BF16>;
     e = cudaFuncSetAttribute(k1, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
@@ -780,6 +793,14 @@ cudaError_t launch_decode_impl(const DecodeParams& p, cudaStream_t st) {
 
 cudaError_t launch_fwd_decode(const DecodeParams& p, bool bf16, cudaStream_t s) {
   return bf16 ? launch_decode_impl<true>(p, s) : launch_decode_impl<false>(p, s);
+}
+
+// Query heads one decode CTA takes: the whole GQA group when its rows (group
+// x Nq) fit the register-fed kernels (K and V are then read once per group
+// instead of once per query head), else one.
+int decode_heads_per_cta(int group, int Nq, int D) {
+  const int rows = group * Nq;
+  return (rows <= 4 && D <= 512) || rows <= 2 ? group : 1;
 }
 
 }  // namespace ffpa

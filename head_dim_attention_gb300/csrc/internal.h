@@ -62,6 +62,7 @@ struct DecodeParams {
   int group;
   int causal;
   float scale_log2;
+  int heads_per_cta;  // query heads (of one kv head) per split CTA: 1 or the GQA group
   int split_len;      // keys per split
   int n_splits;
   float* part_o;      // [B, Hq, Nq, n_splits, D] fp32 scratch
@@ -116,6 +117,7 @@ cudaError_t launch_fwd_main(const FwdParams& p, const FwdMaps& m, bool bf16, cud
 bool fwd_fulld_supported(const FwdParams& p);
 cudaError_t launch_fwd_fulld(const FwdParams& p, const FwdMaps& m, bool bf16, cudaStream_t s);
 cudaError_t launch_fwd_decode(const DecodeParams& p, bool bf16, cudaStream_t s);
+int decode_heads_per_cta(int group, int Nq, int D);
 // Same kernels, partials in the library's fixed device array (no allocation).
 cudaError_t launch_fwd_decode_noalloc(const DecodeParams& p, bool bf16, cudaStream_t s);
 size_t decode_scratch_bytes(const DecodeParams& p);

@@ -63,9 +63,20 @@ def tile_errors(gpu, want, what, tile=128):
     return errs
 
 
-def gpu_fwd(inp, causal, scale):
+def _row_padded(t, pad, dev):
+    """The same values in a buffer whose rows are `pad` elements longer (a
+    non-contiguous row stride, as a slice of a wider tensor would have)."""
+    if not pad:
+        return t.to(dev)
+    wide = torch.zeros(*t.shape[:-1], t.shape[-1] + pad, dtype=t.dtype, device=dev)
+    wide[..., : t.shape[-1]] = t.to(dev)
+    return wide[..., : t.shape[-1]]
+
+
+def gpu_fwd(inp, causal, scale, kv_row_pad=0):
     dev = torch.device("cuda")
-    q, k, v = inp.q.to(dev), inp.k.to(dev), inp.v.to(dev)
+    q = inp.q.to(dev)
+    k, v = _row_padded(inp.k, kv_row_pad, dev), _row_padded(inp.v, kv_row_pad, dev)
     bias = None if inp.bias is None else inp.bias.to(dev)
     out, lse = attention_fwd(q, k, v, bias=bias, causal=causal, scale=scale)
     torch.cuda.synchronize()
@@ -73,10 +84,10 @@ def gpu_fwd(inp, causal, scale):
     return out, lse
 
 
-def check_fwd_full(B, Hq, Hkv, Nq, Nkv, D, dtype, causal=False, bias=False, seed=0, scale=None):
+def check_fwd_full(B, Hq, Hkv, Nq, Nkv, D, dtype, causal=False, bias=False, seed=0, scale=None, kv_row_pad=0):
     inp = make_inputs(B, Hq, Hkv, Nq, Nkv, D, dtype, bias=bias, seed=seed)
     scale = D ** -0.5 if scale is None else scale
-    out, lse = gpu_fwd(inp, causal, scale)
+    out, lse = gpu_fwd(inp, causal, scale, kv_row_pad)
     o_ref, lse_ref = ref.attn_fwd(f64(inp.q), f64(inp.k), f64(inp.v), bias=f64(inp.bias), causal=causal,
                                   scale=scale)
     atol, rtol = TOL[dtype]

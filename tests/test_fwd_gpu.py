@@ -90,6 +90,13 @@ def test_head_dim_sweep_small(D):
     (2, 3, 3, 1, 777, 320, FP, False, True),
     (1, 2, 1, 2, 8191, 448, BF, False, False),
     (1, 1, 1, 1, 17, 512, FP, True, False),
+    # a CTA takes the whole GQA group when group x Nq <= 4 (D <= 512) or <= 2:
+    # groups of 4 and 3, D > 512 with a group of 2, and a group of 4 that
+    # does not fit at D > 512
+    (1, 8, 2, 1, 1500, 512, BF, False, True),
+    (1, 6, 2, 1, 333, 320, FP, True, True),
+    (1, 4, 2, 1, 500, 1024, FP, True, False),
+    (2, 4, 1, 1, 700, 768, BF, False, True),
 ])
 def test_decode_small(B, Hq, Hkv, Nq, Nkv, D, dtype, causal, bias):
     check_fwd_full(B, Hq, Hkv, Nq, Nkv, D, dtype, causal=causal, bias=bias)
@@ -123,3 +130,15 @@ def test_cross_attention_bias():
 
 def test_decode_8k():
     check_fwd_full(1, 8, 8, 1, 8192, 512, BF)
+
+
+def test_decode_gqa_8k():
+    # Hq = 8 on Hkv = 2: one CTA per (slice, kv head) scores all four query heads
+    check_fwd_full(1, 8, 2, 1, 8192, 512, BF)
+
+
+@pytest.mark.parametrize("Hq,Hkv,Nq,D", [(8, 2, 1, 512), (4, 2, 2, 448), (2, 2, 2, 768), (4, 4, 3, 512)])
+def test_decode_strided_kv_rows(Hq, Hkv, Nq, D):
+    # K and V rows D + 64 elements apart: the register-fed kernel instead of
+    # the shared-memory one, with and without a shared GQA group
+    check_fwd_full(1, Hq, Hkv, Nq, 900, D, BF, causal=True, bias=True, kv_row_pad=64)
