@@ -369,6 +369,7 @@ def measure_variants(dev, peaks, iters=10, warmup=3):
     case("gqa_Hkv2_N8192_D512_bf16", 1, 8, 2, 8192, 8192, 512, bf, backward=True)
     case("nonaligned_N8191_D512_bf16", 1, 8, 8, 8191, 8191, 512, bf)
     case("cross_Nq1024_Nkv8192_bias_D512_bf16", 1, 8, 8, 1024, 8192, 512, bf, bias=True)
+    case("short_Nq64_Nkv8192_D512_bf16", 1, 8, 8, 64, 8192, 512, bf)
     for d in (320, 384, 448, 512, 576, 640, 768, 1024):
         case(f"dsweep_N4096_D{d}_fp16", 1, 8, 8, 4096, 4096, d, fp)
     return {"peak": peaks["bf16_tflops"], "timing": "median of 10 calls after 3 warm-up calls, each timed alone "

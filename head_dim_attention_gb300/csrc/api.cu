@@ -185,7 +185,40 @@ constexpr int kDecodeMaxRows = 16;
 // `Hq` counts those groups.  Ties go to the longer slice.
 // Slices of at least 128 keys keep a call's partials within what 128-key
 // slices would take (the no-allocation entry point's capacity check).
-int decode_split_len(int64_t B, int64_t Hq, int64_t Nkv) {
+// Stream-ordered scratch (backward Delta and lse2, decode and key-split
+// partials) comes from a memory pool the library creates per device and whose
+// release threshold keeps freed blocks reserved: after the first call of a
+// size, an allocation reuses them instead of mapping new memory, which with a
+// default pool (threshold 0) happened on every call and left the GPU idle for
+// tens of microseconds while the host mapped it.
+cudaError_t scratch_alloc(void** ptr, size_t bytes, cudaStream_t st) {
+  static std::mutex mu;
+  static cudaMemPool_t pools[64] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  cudaMemPool_t pool;
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    if (!pools[dev]) {
+      cudaMemPoolProps props = {};
+      props.allocType = cudaMemAllocationTypePinned;
+      props.location.type = cudaMemLocationTypeDevice;
+      props.location.id = dev;
+      cudaMemPool_t created;
+      if ((e = cudaMemPoolCreate(&created, &props)) != cudaSuccess) return e;
+      uint64_t keep = UINT64_MAX;
+      if ((e = cudaMemPoolSetAttribute(created, cudaMemPoolAttrReleaseThreshold, &keep)) != cudaSuccess) return e;
+      pools[dev] = created;
+    }
+    pool = pools[dev];
+  }
+  return cudaMallocFromPoolAsync(ptr, bytes, pool, st);
+}
+
+// SMs of the current device (cached per device; 0 if unknown).
+int device_sm_count() {
   static std::mutex mu;
   static int sms_cache[64] = {};
   int dev = 0, sms = 0;
@@ -197,6 +230,11 @@ int decode_split_len(int64_t B, int64_t Hq, int64_t Nkv) {
     }
     sms = sms_cache[dev];
   }
+  return sms;
+}
+
+int decode_split_len(int64_t B, int64_t Hq, int64_t Nkv) {
+  const int sms = device_sm_count();
   if (sms <= 0) return 128;
   const int64_t slots = 2 * static_cast<int64_t>(sms);
   int best = 128;
@@ -261,7 +299,7 @@ extern "C" int ffpa_fwd(const ffpa_tensor_t* q, const ffpa_tensor_t* k, const ff
     const size_t n_rows = (size_t)c.B * c.Hq * c.Nq * p.n_splits;
     void* scratch = nullptr;
     const size_t o_bytes = n_rows * c.D * sizeof(float), ml_bytes = n_rows * 2 * sizeof(float);
-    if (cudaMallocAsync(&scratch, o_bytes + ml_bytes, st) != cudaSuccess) return FFPA_ERR_CUDA;
+    if (scratch_alloc(&scratch, o_bytes + ml_bytes, st) != cudaSuccess) return FFPA_ERR_CUDA;
     p.part_o = static_cast<float*>(scratch);
     p.part_ml = reinterpret_cast<float*>(static_cast<char*>(scratch) + o_bytes);
     cudaError_t e = launch_fwd_decode(p, bf16, st);
@@ -290,6 +328,34 @@ extern "C" int ffpa_fwd(const ffpa_tensor_t* q, const ffpa_tensor_t* k, const ff
   if ((rc = encode_map(&m.q, q)) || (rc = encode_map(&m.k, k)) || (rc = encode_map(&m.v, v)) ||
       (rc = encode_map(&m.k_half, k, kTileRows / 2)) || (rc = encode_map(&m.q_half, q, kTileRows / 2)))
     return rc;
+  int per = 0;
+  const int splits = fwd_fulld_supported(p) ? fwd_fulld_kv_splits(p, device_sm_count(), &per) : 1;
+  if (splits > 1) {
+    // a short query set: the key splits write partials, the combine merges them
+    const size_t n_rows = (size_t)c.B * c.Hq * c.Nq * splits;
+    const size_t o_bytes = n_rows * c.D * sizeof(float), ml_bytes = n_rows * 2 * sizeof(float);
+    void* scratch = nullptr;
+    if (scratch_alloc(&scratch, o_bytes + ml_bytes, st) != cudaSuccess) return FFPA_ERR_CUDA;
+    p.kv_splits = splits;
+    p.kv_split_tiles = per;
+    p.part_o = static_cast<float*>(scratch);
+    p.part_ml = reinterpret_cast<float*>(static_cast<char*>(scratch) + o_bytes);
+    cudaError_t e = launch_fwd_main(p, m, bf16, st);
+    if (e == cudaSuccess) {
+      DecodeParams dp = {};
+      dp.out = out->data;
+      dp.lse = p.lse;
+      dp.o_sb = p.o_sb; dp.o_sh = p.o_sh; dp.o_sn = p.o_sn;
+      dp.B = p.B; dp.Hq = p.Hq; dp.Hkv = p.Hkv; dp.Nq = p.Nq; dp.Nkv = p.Nkv; dp.D = p.D;
+      dp.n_splits = splits;
+      dp.part_o = p.part_o;
+      dp.part_ml = p.part_ml;
+      dp.status = status;
+      e = launch_decode_combine(dp, bf16, st);
+    }
+    cudaError_t e2 = cudaFreeAsync(scratch, st);
+    return cuda_rc(e != cudaSuccess ? e : e2);
+  }
   return cuda_rc(launch_fwd_main(p, m, bf16, st));
 }
 
@@ -351,7 +417,7 @@ extern "C" int ffpa_bwd(const ffpa_tensor_t* q, const ffpa_tensor_t* k, const ff
   const size_t rows = (size_t)c.B * c.Hq * c.Nq;
   timing_begin();
   void* scratch = nullptr;
-  if (cudaMallocAsync(&scratch, rows * 2 * sizeof(float), st) != cudaSuccess) return FFPA_ERR_CUDA;
+  if (scratch_alloc(&scratch, rows * 2 * sizeof(float), st) != cudaSuccess) return FFPA_ERR_CUDA;
   p.delta = static_cast<float*>(scratch);
   p.lse2 = p.delta + rows;
   cudaError_t e = launch_bwd(p, m, dtype_is_bf16(c.dtype), st);

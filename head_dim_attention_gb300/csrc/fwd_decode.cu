@@ -742,6 +742,9 @@ cudaError_t launch_bulk(const DecodeParams& p, cudaStream_t st) {
 }
 
 template <bool BF16>
+cudaError_t launch_combine(const DecodeParams& p, cudaStream_t st);
+
+template <bool BF16>
 cudaError_t launch_decode_impl(const DecodeParams& p, cudaStream_t st) {
   cudaError_t e = cudaSuccess;
   timing_mark(st);
@@ -772,6 +775,11 @@ cudaError_t launch_decode_impl(const DecodeParams& p, cudaStream_t st) {
   timing_mark(st);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
+  return launch_combine<BF16>(p, st);
+}
+
+template <bool BF16>
+cudaError_t launch_combine(const DecodeParams& p, cudaStream_t st) {
   // programmatic dependent launch: the combine grid's launch overlaps the end
   // of the split grid (it waits for the split grid's results in the kernel)
   cudaLaunchConfig_t cfg = {};
@@ -784,7 +792,7 @@ cudaError_t launch_decode_impl(const DecodeParams& p, cudaStream_t st) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  e = cudaLaunchKernelEx(&cfg, decode_combine_kernel<BF16>, p);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, decode_combine_kernel<BF16>, p);
   timing_mark(st);
   return e != cudaSuccess ? e : cudaGetLastError();
 }
@@ -793,6 +801,10 @@ cudaError_t launch_decode_impl(const DecodeParams& p, cudaStream_t st) {
 
 cudaError_t launch_fwd_decode(const DecodeParams& p, bool bf16, cudaStream_t s) {
   return bf16 ? launch_decode_impl<true>(p, s) : launch_decode_impl<false>(p, s);
+}
+
+cudaError_t launch_decode_combine(const DecodeParams& p, bool bf16, cudaStream_t s) {
+  return bf16 ? launch_combine<true>(p, s) : launch_combine<false>(p, s);
 }
 
 // Query heads one decode CTA takes: the whole GQA group when its rows (group

@@ -46,6 +46,7 @@
 // Warps: 0 K producer (and Q), 1 TMEM owner + MMA issuer A (first CTA), 2 MMA
 // issuer B (first CTA) or the relay (second CTA), 3 V producer, 4-7 softmax /
 // correction / epilogue.  Every wait is bounded (ptx.cuh).
+#include <algorithm>
 #include <type_traits>
 
 #include "internal.h"
@@ -156,7 +157,7 @@ __device__ __forceinline__ bool pair_bar_and(uint32_t id, bool v) {
   return r != 0;
 }
 
-template <int NC, bool BF16>
+template <int NC, bool BF16, bool KSPLIT>
 __global__ void __launch_bounds__(kThreads, 1)
     fwd_fulld_kernel(const __grid_constant__ CUtensorMap map_qh, const __grid_constant__ CUtensorMap map_kh,
                      const __grid_constant__ CUtensorMap map_v, const __grid_constant__ FwdParams p) {
@@ -182,7 +183,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const uint32_t rank = cluster_ctarank();  // 0 issues the pair's MMAs
-  const int pair = static_cast<int>(blockIdx.x) >> 1;
+  const int pair0 = static_cast<int>(blockIdx.x) >> 1;
+  const int kvs = KSPLIT ? pair0 % p.kv_splits : 0;  // key split of this pair (KSPLIT: short query sets)
+  const int pair = KSPLIT ? pair0 / p.kv_splits : pair0;
   const int split = pair % G::kNsplit;
   const int qt = p.q_tiles - 1 - pair / G::kNsplit;  // heavy causal tiles first
   const int q0 = qt * kTileRows;
@@ -194,7 +197,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int h = blockIdx.y, b = blockIdx.z;
   const int kvh = h / p.group;
   const int kv_end = p.causal ? min(p.Nkv, q0 + kTileRows) : p.Nkv;
-  const int ntiles = (kv_end + kTileRows - 1) / kTileRows;
+  // key tiles t0 .. t0 + ntiles - 1 (all of them without a key split)
+  const int t0 = KSPLIT ? kvs * p.kv_split_tiles : 0;
+  const int ntiles = KSPLIT ? max(0, min((kv_end + kTileRows - 1) / kTileRows - t0, p.kv_split_tiles))
+                            : (kv_end + kTileRows - 1) / kTileRows;
   uint32_t* status = p.status;
   auto lead = [&](int i) { return rank == 0 ? bar(i) : mapa(bar(i), 0); };
 
@@ -267,11 +273,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (is_k) {
         for (int i = 0; i < nk; ++i)
           tma_load_4d_pair(dst + i * kHalfBytes, &map_kh, fb, (4 * m + i) * kChunk,
-                           j * kTileRows + 64 * static_cast<int>(rank), kvh, b);
+                           (t0 + j) * kTileRows + 64 * static_cast<int>(rank), kvh, b);
       } else {
         for (int i = 0; i < nv; ++i)
           tma_load_4d_pair(dst + i * kChunkBytes, &map_v, fb, o0 + (4 * m + nv * static_cast<int>(rank) + i) * kChunk,
-                           j * kTileRows, kvh, b);
+                           (t0 + j) * kTileRows, kvh, b);
       }
     }
     // the ring's last commits (they arrive on both CTAs) complete before exit
@@ -426,7 +432,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     float m_used = -INFINITY, l_own = 0.f, l_sum = 0.f;  // l_sum: both halves of the row
     for (int j = 0; j < ntiles; ++j) {
       const uint32_t s_col = (j & 1) ? kS1 : kS0;
-      const int kv0 = j * kTileRows + 64 * kh;  // key of s[0]
+      const int kv0 = (t0 + j) * kTileRows + 64 * kh;  // key of s[0]
       // this tile's bias row segment (256 bytes when contiguous) into L1 ahead of
       // the wait for S, so that the loads after it do not wait on L2
       if (bias_row && p.bias_vec) {
@@ -578,11 +584,53 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (ok) {
       // ---------------------------------------------------------- epilogue
-      // the last P V of each buffer (their commits also arrive on the second CTA)
-      ok = __all_sync(0xffffffffu,
-                      mbar_wait(bar(bl.pv_done + (ntiles - 1) % kNpb), ((ntiles - 1) / kNpb) & 1, status));
+      // the last P V of each buffer (their commits also arrive on the second
+      // CTA); a key split may have no key tile at all
+      if (!KSPLIT || ntiles > 0)
+        ok = __all_sync(0xffffffffu,
+                        mbar_wait(bar(bl.pv_done + (ntiles - 1) % kNpb), ((ntiles - 1) / kNpb) & 1, status));
       if (ok && kNpb == 2 && ntiles >= 2)
         ok = __all_sync(0xffffffffu, mbar_wait(bar(bl.pv_done + (ntiles & 1)), ((ntiles - 2) >> 1) & 1, status));
+      if constexpr (KSPLIT) {
+      if (ok) {
+        // key split: the unnormalised partial O (fp32) and this split's (max,
+        // sum) in the log2 domain, merged by the decode path's combine kernel
+        tc_fence_after();
+        const int prow_i = min(row, p.Nq - 1);
+        float* prow = p.part_o + (((static_cast<int64_t>(b) * p.Hq + h) * p.Nq + prow_i) * p.kv_splits + kvs) * p.D;
+        for (int c = 0; c < kOCols / 32; ++c) {
+          uint32_t v[32];
+          if (ntiles > 0) {
+            tmem_ld32(tbase + lane_off + c * 32, v);
+            tmem_ld_wait();
+          } else {
+#pragma unroll
+            for (int e = 0; e < 32; ++e) v[e] = 0u;
+          }
+          // the O column of TMEM column 32 c of this lane, as in the epilogue below
+          int d0;
+          if (NC <= 8) {
+            d0 = (c < 4 || NC >= 7) ? 256 * (c >> 2) + 128 * kh + 32 * (c & 3) : 256 + 64 * kh + 32 * (c - 4);
+          } else if (c < 4) {
+            d0 = c < 2 * nv0 ? o0 + 64 * nv0 * kh + 32 * c : NC * kChunk;
+          } else {
+            d0 = c - 4 < 2 * nv1 ? o0 + 256 + 64 * nv1 * kh + 32 * (c - 4) : NC * kChunk;
+          }
+          if (row < p.Nq && d0 < NC * kChunk) {
+            float4* dst = reinterpret_cast<float4*>(prow + d0);
+#pragma unroll
+            for (int g = 0; g < 8; ++g)
+              dst[g] = make_float4(__uint_as_float(v[4 * g]), __uint_as_float(v[4 * g + 1]),
+                                   __uint_as_float(v[4 * g + 2]), __uint_as_float(v[4 * g + 3]));
+          }
+        }
+        if (kh == 0 && split == 0 && row < p.Nq) {
+          float* ml = p.part_ml + (((static_cast<int64_t>(b) * p.Hq + h) * p.Nq + row) * p.kv_splits + kvs) * 2;
+          ml[0] = ntiles > 0 ? m_used : -INFINITY;
+          ml[1] = l_sum;
+        }
+      }
+      } else {
       if (ok) {
         tc_fence_after();
         const float inv_l = l_sum > 0.f ? 1.f / l_sum : 0.f;
@@ -630,6 +678,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               l_sum > 0.f ? (m_used + __log2f(l_sum)) * kLn2 : -INFINITY;
         }
       }
+      }
     }
   }
 
@@ -648,12 +697,12 @@ cudaError_t launch_impl(const FwdParams& p_in, const FwdMaps& m, cudaStream_t st
   FwdParams p = p_in;
   p.stages = kKSlots + kVSlots;
   p.slot_chunks = 2;
-  auto kern = fwd_fulld_kernel<NC, BF16>;
+  auto kern = p.part_o ? fwd_fulld_kernel<NC, BF16, true> : fwd_fulld_kernel<NC, BF16, false>;
   constexpr int kNsplit = Shape<NC>::kNsplit;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(2 * p.q_tiles * kNsplit, p.Hq, p.B);  // (pair rank, O split, query tile)
+  cfg.gridDim = dim3(2 * p.q_tiles * kNsplit * (p.part_o ? p.kv_splits : 1), p.Hq, p.B);  // (pair rank, key split, O split, query tile)
   cfg.blockDim = dim3(kThreads, 1, 1);
   cfg.dynamicSmemBytes = kSmemBytes;
   cfg.stream = st;
@@ -678,6 +727,35 @@ cudaError_t launch_nc(const FwdParams& p, const FwdMaps& m, bool bf16, cudaStrea
 }  // namespace
 
 bool fwd_fulld_supported(const FwdParams& p) { return p.n_chunks >= 5 && p.n_chunks <= 16; }
+
+// Key splits for short query sets: when the pairs of a launch would not fill
+// one wave of pair slots, split the keys so that about one wave runs, each
+// split at least two key tiles long.  Returns the split count (1: none) and
+// the key tiles per split.
+int fwd_fulld_kv_splits(const FwdParams& p, int sms, int* tiles_per_split) {
+  int nsplit = 1;
+  switch (p.n_chunks) {
+    case 9: nsplit = Shape<9>::kNsplit; break;
+    case 10: nsplit = Shape<10>::kNsplit; break;
+    case 11: nsplit = Shape<11>::kNsplit; break;
+    case 12: nsplit = Shape<12>::kNsplit; break;
+    case 13: nsplit = Shape<13>::kNsplit; break;
+    case 14: nsplit = Shape<14>::kNsplit; break;
+    case 15: nsplit = Shape<15>::kNsplit; break;
+    case 16: nsplit = Shape<16>::kNsplit; break;
+    default: nsplit = 1;
+  }
+  const int64_t pairs = static_cast<int64_t>(p.q_tiles) * nsplit * p.Hq * p.B;
+  const int kv_tiles = (p.Nkv + kTileRows - 1) / kTileRows;
+  const int64_t slots = sms / 2;
+  *tiles_per_split = kv_tiles;
+  if (pairs * 2 > slots || kv_tiles < 4) return 1;  // half a wave or more: no split
+  const int want = static_cast<int>(std::min<int64_t>(slots / pairs, kv_tiles / 2));
+  if (want < 2) return 1;
+  const int per = (kv_tiles + want - 1) / want;
+  *tiles_per_split = per;
+  return (kv_tiles + per - 1) / per;
+}
 
 cudaError_t launch_fwd_fulld(const FwdParams& p, const FwdMaps& m, bool bf16, cudaStream_t s) {
   switch (p.n_chunks) {

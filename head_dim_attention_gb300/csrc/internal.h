@@ -37,6 +37,12 @@ struct FwdParams {
   int slot_chunks;    // 64-column chunk tiles per ring slot (1 or 2), loaded under one barrier phase
   int q_tiles;        // ceil(Nq / 128)
   uint32_t* status;   // device status word
+  // split over the keys (short query sets): each CTA pair takes kv_split_tiles
+  // key tiles and writes an unnormalised partial O and its (max, sum) for the
+  // decode path's combine kernel; part_o == nullptr: no split
+  int kv_splits, kv_split_tiles;
+  float* part_o;      // [B, Hq, Nq, kv_splits, D] fp32
+  float* part_ml;     // [B, Hq, Nq, kv_splits, 2] fp32 (max, sum), log2 domain
 };
 
 struct FwdMaps {
@@ -115,8 +121,13 @@ bool dtype_is_bf16(int dtype);
 cudaError_t launch_fwd_main(const FwdParams& p, const FwdMaps& m, bool bf16, cudaStream_t s);
 // Full-D CTA-pair forward (fwd_fulld.cu): D = 512, one pair holds all of O.
 bool fwd_fulld_supported(const FwdParams& p);
+// Key splits (1: none) for a short query set on `sms` SMs, and key tiles per split.
+int fwd_fulld_kv_splits(const FwdParams& p, int sms, int* tiles_per_split);
 cudaError_t launch_fwd_fulld(const FwdParams& p, const FwdMaps& m, bool bf16, cudaStream_t s);
 cudaError_t launch_fwd_decode(const DecodeParams& p, bool bf16, cudaStream_t s);
+// The decode path's merge of per-split partials (part_o, part_ml) into out and
+// lse; also merges the key splits of the full-D forward for short query sets.
+cudaError_t launch_decode_combine(const DecodeParams& p, bool bf16, cudaStream_t s);
 int decode_heads_per_cta(int group, int Nq, int D);
 // Same kernels, partials in the library's fixed device array (no allocation).
 cudaError_t launch_fwd_decode_noalloc(const DecodeParams& p, bool bf16, cudaStream_t s);

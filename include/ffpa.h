@@ -83,8 +83,11 @@ typedef struct ffpa_tensor {
  *        O row is then 0).
  *
  * Nq <= 16 takes a split-KV decode path (CUDA-core dot products over slices
- * of the keys, then an lse-weighted merge); it uses stream-ordered scratch
- * from cudaMallocAsync on `stream`.  Otherwise one fused tcgen05 kernel runs.
+ * of the keys, then an lse-weighted merge).  Otherwise one fused tcgen05
+ * kernel runs; when its CTA pairs would fill less than half of the GPU (short
+ * query sets) the keys are split between pairs and the same merge follows.
+ * The partials live in stream-ordered scratch on `stream` from a memory pool
+ * the library keeps per device (its blocks stay reserved for later calls).
  * Returns FFPA_OK or an ffpa_status code (see above).
  */
 int ffpa_fwd(const ffpa_tensor_t* q, const ffpa_tensor_t* k, const ffpa_tensor_t* v,
@@ -103,8 +106,8 @@ int ffpa_fwd(const ffpa_tensor_t* q, const ffpa_tensor_t* k, const ffpa_tensor_t
  *   dk, dv [B, Hkv, Nkv, D] written (summed over the query heads of a group)
  *
  * No gradient is produced for the bias.  Delta and lse in log2 units (f32
- * [B, Hq, Nq] each) live in stream-ordered scratch from cudaMallocAsync on
- * `stream`.
+ * [B, Hq, Nq] each) live in stream-ordered scratch on `stream` from the
+ * library's per-device memory pool.
  */
 int ffpa_bwd(const ffpa_tensor_t* q, const ffpa_tensor_t* k, const ffpa_tensor_t* v,
              const ffpa_tensor_t* bias, int causal, float scale, const ffpa_tensor_t* out,
@@ -117,7 +120,7 @@ int ffpa_bwd(const ffpa_tensor_t* q, const ffpa_tensor_t* k, const ffpa_tensor_t
  * device memory during the call: code running under another framework's
  * memory pool or a serving loop that must not enter the CUDA
  * allocator on its hot path.  ffpa_fwd's decode path takes its slice
- * partials from cudaMallocAsync; this entry point keeps them in a fixed
+ * partials from the library's memory pool; this entry point keeps them in a fixed
  * 8 MiB device array inside the library (held by every GPU that loads the
  * library until the process exits) and calls no allocating routine.
  *

@@ -128,6 +128,18 @@ def test_cross_attention_bias():
     check_fwd_sampled(1, 8, 8, 1024, 8192, 512, BF, bias=True)
 
 
+@pytest.mark.parametrize("B,Hq,Hkv,Nq,Nkv,D,dtype,causal,bias", [
+    (1, 8, 2, 64, 8192, 512, BF, False, True),
+    (1, 4, 4, 17, 3000, 384, FP, True, False),   # causal: the later key splits see no key
+    (2, 2, 1, 40, 5000, 1024, BF, False, False),  # O split over pairs and keys split
+    (1, 1, 1, 130, 2048, 576, FP, True, True),
+])
+def test_short_query_key_splits(B, Hq, Hkv, Nq, Nkv, D, dtype, causal, bias):
+    # 17..130 query rows fill a fraction of a wave of CTA pairs: the keys are
+    # split between pairs and the partials merged by the decode combine
+    check_fwd_full(B, Hq, Hkv, Nq, Nkv, D, dtype, causal=causal, bias=bias)
+
+
 def test_decode_8k():
     check_fwd_full(1, 8, 8, 1, 8192, 512, BF)
 
