@@ -63,7 +63,7 @@ constexpr int kHalfBytes = kChunkBytes / 2;     // 64 rows x 64 columns
 constexpr int kPBytes = 2 * kHalfBytes;         // 64 rows x 128 keys, 16 KB
 constexpr int kPBufBytes = 2 * kPBytes;         // P_hi and P_lo of one key tile
 constexpr int kSlotBytes = 2 * kChunkBytes;     // 32 KB
-constexpr int kKSlots = 2, kVSlots = 2;
+constexpr int kKSlots = 2;
 
 // Per head dimension D = 64 NC (NC = 5..16).
 //
@@ -79,21 +79,26 @@ constexpr int kKSlots = 2, kVSlots = 2;
 // the TS-form A operand (32 columns per chunk); Q's other chunks sit in shared
 // memory.  Narrower O splits leave room for more of Q in TMEM, which is what
 // lets shared memory hold the rest of Q next to the rings.  P is
-// double-buffered where that shared memory allows (kNpb = 2).
+// double-buffered where that shared memory allows (kNpb = 2).  Above D = 768
+// the splits are 512 columns wide again (two pairs: S is computed twice, not
+// three or four times) and the V ring has a single slot: the S product of
+// such a key tile takes longer than the wait for V's second half.
 template <int NC>
 struct Shape {
   static_assert(NC >= 5 && NC <= 16, "D = 320 .. 1024");
   static constexpr int kD = 64 * NC;
-  static constexpr int kOw = NC <= 8 ? 512 : (NC <= 14 ? 384 : 256);  // widest O split
+  static constexpr int kOw = (NC <= 8 || NC >= 13) ? 512 : 384;  // widest O split
   static constexpr int kNsplit = (kD + kOw - 1) / kOw;
-  static constexpr int kOTm = NC <= 8 ? 256 : kOw / 2;                 // TMEM columns reserved for O
+  static constexpr int kOTm = kOw / 2;                          // TMEM columns reserved for O
   // TMEM columns of O that a lane uses at most (rescale loop)
   static constexpr int kOCols = NC <= 8 ? 128 + (NC >= 7 ? 256 : 128) / 2 : kOTm;
+  static_assert(kOTm <= 256, "O below the score buffers");
   static constexpr uint32_t kS0 = kOTm, kS1 = kOTm + 64, kQt = kOTm + 128;
   static constexpr int kQtc = (512 - static_cast<int>(kQt)) / 32 < NC ? (512 - static_cast<int>(kQt)) / 32 : NC;
   static constexpr int kQBytes = (NC - kQtc) * kHalfBytes;  // Q chunks kQtc..NC-1 in shared memory
   static constexpr int kNpb = NC - kQtc <= 4 ? 2 : 1;      // P buffers
   static constexpr int kKSlotsPerTile = (NC + 3) / 4;      // four K chunks (32 KB) per slot
+  static constexpr int kVSlots = NC >= 13 ? 1 : 2;         // V ring slots (32 KB)
   // shared memory: Q | P buffers (P_hi, P_lo) | K ring | V ring | barriers | row-statistics exchange
   static constexpr int kPOff = kQBytes, kRingKOff = kPOff + kNpb * kPBufBytes;
   static constexpr int kRingVOff = kRingKOff + kKSlots * kSlotBytes;
@@ -245,7 +250,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool is_k = warp == 0;
     const int full0 = is_k ? bl.full_k : bl.full_v, empty0 = is_k ? bl.empty_k : bl.empty_v;
     const uint32_t ring = is_k ? ring_k : ring_v;
-    const uint32_t S = is_k ? kKSlots : kVSlots;
+    const uint32_t S = is_k ? kKSlots : G::kVSlots;
     if (is_k) {
       tma_prefetch_desc(&map_qh);
       tma_prefetch_desc(&map_kh);
@@ -347,8 +352,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool use_lo = lo_flag[pb] == static_cast<uint32_t>(j + 1);
       const uint64_t dphi = sdesc_advance(dp, pb * kPBufBytes), dplo = sdesc_advance(dphi, kPBytes);
       for (int hf = 0; hf < nhalves && ok; ++hf) {
-        const uint32_t s = it & 1;  // two slots: one per half of D
-        ok = mbar_wait(bar(bl.full_v + s), (it >> 1) & 1, status);
+        const uint32_t s = it % G::kVSlots;  // two slots (one per half of D), or one
+        ok = mbar_wait(bar(bl.full_v + s), (it / G::kVSlots) & 1, status);
         ++it;
         if (!ok) break;
         tc_fence_after();
@@ -695,7 +700,7 @@ template <int NC, bool BF16>
 cudaError_t launch_impl(const FwdParams& p_in, const FwdMaps& m, cudaStream_t st) {
   constexpr int kSmemBytes = Shape<NC>::kSmemBytes;
   FwdParams p = p_in;
-  p.stages = kKSlots + kVSlots;
+  p.stages = kKSlots + Shape<NC>::kVSlots;
   p.slot_chunks = 2;
   auto kern = p.part_o ? fwd_fulld_kernel<NC, BF16, true> : fwd_fulld_kernel<NC, BF16, false>;
   constexpr int kNsplit = Shape<NC>::kNsplit;
