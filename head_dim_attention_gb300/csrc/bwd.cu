@@ -853,6 +853,12 @@ cudaError_t launch_bwd(const BwdParams& p, const BwdMaps& m, bool bf16, cudaStre
     if (e == cudaSuccess) e = launch_bwd_dkv(p, m, bf16, s);
     return e != cudaSuccess ? e : launch_bwd_dq(p, m, bf16, s);
   }
+  if (bwd_xch_supported(p)) {
+    // preprocess, then the exchange kernel's dK/dV mode (two clusters per key
+    // tile, one per range of gradient columns) and its dQ mode
+    cudaError_t e = bf16 ? launch_preprocess<true>(p, s) : launch_preprocess<false>(p, s);
+    return e != cudaSuccess ? e : launch_bwd_xch(p, m, bf16, s);
+  }
   if (p.n_chunks <= 4) return bf16 ? launch_all<kSolo, true>(p, m, s) : launch_all<kSolo, false>(p, m, s);
   return bf16 ? launch_all<kExchange, true>(p, m, s) : launch_all<kExchange, false>(p, m, s);
 }

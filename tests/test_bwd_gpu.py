@@ -42,6 +42,14 @@ BF, FP = torch.bfloat16, torch.float16
     (2, 2, 2, 384, 384, 448, BF, False, False),
     (1, 2, 2, 200, 333, 320, FP, False, True),
     (1, 2, 2, 5, 200, 384, BF, False, False),
+    # D = 576 .. 1024: the exchange kernel's two modes (two ranges of gradient
+    # columns; a range that is not a multiple of 128 pads with zero-filled
+    # operand columns), with tails, GQA, bias and causal
+    (1, 4, 2, 300, 500, 832, BF, True, True),
+    (1, 2, 1, 260, 130, 960, FP, False, False),
+    (2, 2, 2, 256, 256, 704, BF, True, False),
+    (1, 2, 2, 5, 200, 896, BF, False, True),
+    (1, 2, 1, 129, 383, 1024, BF, False, True),
 ])
 def test_bwd_small(B, Hq, Hkv, Nq, Nkv, D, dtype, causal, bias):
     check_bwd_full(B, Hq, Hkv, Nq, Nkv, D, dtype, causal=causal, bias=bias)
@@ -56,6 +64,6 @@ def test_bwd_8k_bf16(causal):
     check_bwd_sampled(1, 8, 8, 8192, 8192, 512, BF, causal=causal)
 
 
-@pytest.mark.parametrize("D", [320, 384, 448])
+@pytest.mark.parametrize("D", [320, 384, 448, 640, 832, 1024])
 def test_bwd_4k_head_dims(D):
-    check_bwd_sampled(1, 4, 4, 4096, 4096, D, FP, causal=(D == 384))
+    check_bwd_sampled(1, 4, 4, 4096, 4096, D, FP, causal=(D in (384, 832)))
