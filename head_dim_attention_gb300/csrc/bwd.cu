@@ -11,19 +11,15 @@
 // P is rebuilt exactly from the forward's lse, so no online softmax is needed.
 //
 // Each kernel keeps one 128-row tile "stationary" (key rows for dV/dK, query
-// rows for dQ) and sweeps the other side in 128-row "column" tiles.  As in
-// the forward, a cluster of two CTAs splits D in 64-column chunks: each CTA
-// computes partial score tiles over its own chunks with tcgen05.mma into TMEM,
-// the pair swaps the fp32 partials through distributed shared memory and adds
-// them, and each CTA accumulates the gradient for its own chunks (<= 256 TMEM
-// columns per pass).  GQA: the dV/dK kernels sweep every query head of the
-// group, so the group's sum forms in TMEM without any atomics or workspace.
+// rows for dQ) and sweeps the other side in 128-row "column" tiles; one CTA
+// computes the score tiles over all of D with tcgen05.mma into TMEM and
+// accumulates the whole gradient (<= 256 TMEM columns).  GQA: the dV/dK
+// kernels sweep every query head of the group, so the group's sum forms in
+// TMEM without any atomics or workspace.
 //
-// D = 320 .. 512 runs the CTA-pair kernels of bwd_dkv.cu and bwd_dq.cu instead
-// (launch_bwd hands it over after the preprocess).  So this file's kernels
-// serve D <= 256 (one CTA holds the whole gradient) and D > 512 (the exchanging
-// pair); the exchange's distributed-shared-memory traffic (64 KB per product
-// and tile) bounds the latter.
+// These kernels serve D <= 256.  launch_bwd hands larger head dimensions,
+// after the preprocess, to the cluster kernels of bwd_dkv.cu and bwd_dq.cu
+// (D = 320 .. 512) and of bwd_xch.cu (D = 576 .. 1024).
 //
 // TMEM (512 columns): gradient accumulator [0, 256), X1 [256, 384) (scores),
 // X2 [384, 512) (dP, then P or dS as the bf16/f16 A operand of the gradient).
@@ -44,11 +40,10 @@ constexpr int kProducers = 3;  // warps 0, 2 and 3
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kX1 = 256, kX2 = 384;
 constexpr int kMaxAccChunks = 4;
-constexpr int kLandingBytes = kTileRows * kTileRows * 4;
 constexpr float kLog2e = 1.4426950408889634f;
 
 struct Bars {
-  int full, empty, a_full, x_full, x1_free, p_ready, acc_ready, acc_free, xfull, xfree, drain, count;
+  int full, empty, a_full, x_full, x1_free, p_ready, acc_ready, acc_free, drain, count;
 };
 __host__ __device__ inline Bars bar_layout(int stages) {
   Bars b;
@@ -60,30 +55,23 @@ __host__ __device__ inline Bars bar_layout(int stages) {
   b.p_ready = b.x1_free + 1;
   b.acc_ready = b.p_ready + 1;
   b.acc_free = b.acc_ready + 1;
-  b.xfull = b.acc_free + 1;
-  b.xfree = b.xfull + 1;
-  b.drain = b.xfree + 1;
+  b.drain = b.acc_free + 1;
   b.count = b.drain + 1;
   return b;
 }
 
-// Kernel flavours: one CTA per stationary tile (D <= 256), or a cluster pair
-// that exchanges partial score tiles (D > 512).
-enum Flavour : int { kSolo = 0, kExchange = 1 };
-
 struct Plan {
   int a_chunks;  // chunks the score products reduce over (per resident operand)
   int n_a;       // resident stationary operands (A1, then A2); the rest stream through the ring
-  int a_off, ring_off, land_off, bar_off, total;
+  int a_off, ring_off, bar_off, total;
 };
-__host__ __device__ inline Plan make_plan(int n_chunks, int fl, int stages, int n_res, int slot_chunks) {
+__host__ __device__ inline Plan make_plan(int n_chunks, int stages, int n_res, int slot_chunks) {
   Plan s;
-  s.a_chunks = (fl == kExchange) ? (n_chunks + 1) / 2 : n_chunks;
+  s.a_chunks = n_chunks;
   s.n_a = n_res;
   s.a_off = 0;
   s.ring_off = s.n_a * s.a_chunks * kChunkBytes;
-  s.land_off = s.ring_off + stages * slot_chunks * kChunkBytes;
-  s.bar_off = s.land_off + (fl == kExchange ? kLandingBytes : 0);
+  s.bar_off = s.ring_off + stages * slot_chunks * kChunkBytes;
   s.total = s.bar_off + 1024;
   return s;
 }
@@ -150,11 +138,11 @@ struct Geo {
 };
 
 template <int MODE>
-__device__ __forceinline__ Geo make_geo(const BwdParams& p, int cs) {
+__device__ __forceinline__ Geo make_geo(const BwdParams& p) {
   Geo g;
   g.b = blockIdx.z;
   if (MODE == kDQ) {
-    const int qt = p.q_tiles - 1 - static_cast<int>(blockIdx.x) / cs;  // heavy causal tiles first
+    const int qt = p.q_tiles - 1 - static_cast<int>(blockIdx.x);  // heavy causal tiles first
     g.h = blockIdx.y;
     g.kvh = g.h / p.group;
     g.s_head = g.h;
@@ -166,7 +154,7 @@ __device__ __forceinline__ Geo make_geo(const BwdParams& p, int cs) {
     g.nq_h = 0;
     g.rot = g.ncols > 0 ? qt % g.ncols : 0;
   } else {
-    const int kvt = static_cast<int>(blockIdx.x) / cs;
+    const int kvt = static_cast<int>(blockIdx.x);
     g.kvh = blockIdx.y;
     g.h = g.kvh * p.group;
     g.s_head = g.kvh;
@@ -197,36 +185,31 @@ __device__ __forceinline__ void column(const Geo& g, const BwdParams& p, int c, 
   }
 }
 
-template <int MODE, int FL, bool BF16>
+template <int MODE, bool BF16>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_main_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
                     const __grid_constant__ CUtensorMap map_v, const __grid_constant__ CUtensorMap map_do,
                     const __grid_constant__ BwdParams p, const int n_res) {
-  constexpr int CS = (FL == kSolo) ? 1 : 2;  // CTAs per stationary tile
-  constexpr bool XCH = (FL == kExchange);
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int stages = p.stages;
   const int G = p.slot_chunks;  // 16 KB tiles per ring slot
   const uint32_t slot_bytes = G * kChunkBytes;
-  const Plan plan = make_plan(p.n_chunks, FL, stages, n_res, G);
+  const Plan plan = make_plan(p.n_chunks, stages, n_res, G);
   const Bars bl = bar_layout(stages);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + plan.bar_off);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + bl.count);
   auto bar = [&](int i) { return smem_u32(&bars[i]); };
   const uint32_t s_base = smem_u32(smem);
-  const uint32_t a_sm = s_base + plan.a_off, ring_sm = s_base + plan.ring_off, land_sm = s_base + plan.land_off;
+  const uint32_t a_sm = s_base + plan.a_off, ring_sm = s_base + plan.ring_off;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const uint32_t rank = XCH ? cluster_ctarank() : static_cast<uint32_t>(blockIdx.x) % CS;  // which half of D
-  const Geo g = make_geo<MODE>(p, CS);
+  const Geo g = make_geo<MODE>(p);
   const int n = p.n_chunks;
-  const int half = (n + CS - 1) / CS;
-  const int own0 = static_cast<int>(rank) * half;
-  const int own_n = min(half, n - own0);
-  const int s0 = XCH ? own0 : 0;  // chunks the score products reduce over
-  const int s_n = XCH ? own_n : n;
-  const int passes = (half + kMaxAccChunks - 1) / kMaxAccChunks;
+  // the score products reduce over chunks s0 .. s0 + s_n - 1 and the gradient
+  // covers chunks own0 .. own0 + own_n - 1: all of D
+  const int s0 = 0, s_n = n, own0 = 0, own_n = n;
+  const int passes = (n + kMaxAccChunks - 1) / kMaxAccChunks;
   const bool two = (MODE != kDV);  // a second score-like product (dP)
   uint32_t* status = p.status;
 
@@ -247,8 +230,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(bar(bl.p_ready), 4);
     mbar_init(bar(bl.acc_ready), 1);
     mbar_init(bar(bl.acc_free), 4);
-    mbar_init(bar(bl.xfull), kTileRows);  // one arrive per peer row: "my partial is in your buffer"
-    mbar_init(bar(bl.xfree), kTileRows);  // one arrive per peer row: "your buffer is free again"
     mbar_init(bar(bl.drain), 1);
     fence_mbar_init();
   }
@@ -258,7 +239,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   tc_fence_before();
   __syncthreads();
-  if (XCH) cluster_sync();
   tc_fence_after();
   const uint32_t tbase = *tmem_slot;
 
@@ -536,12 +516,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int r = tid - 128;
     const int srow = g.s_row0 + r;
     const uint32_t lane_off = static_cast<uint32_t>((warp - 4) * 32) << 16;
-    const uint32_t peer = rank ^ 1u;
-    const uint32_t peer_land = XCH ? mapa(land_sm, peer) : 0;
-    const uint32_t peer_xfull = XCH ? mapa(bar(bl.xfull), peer) : 0;
-    const uint32_t peer_xfree = XCH ? mapa(bar(bl.xfree), peer) : 0;
-    const uint32_t swz = static_cast<uint32_t>(r & 7);
-    const float4* land = reinterpret_cast<const float4*>(smem + plan.land_off + r * 512);
     float lse2_row = 0.f, delta_row = 0.f;
     if (MODE == kDQ) {
       const int64_t idx = (static_cast<int64_t>(g.b) * p.Hq + g.h) * p.Nq + min(srow, p.Nq - 1);
@@ -550,48 +524,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     bool ok = true;
     int t0 = 0;
-    uint32_t x = 0;  // exchanges done so far
-    // Send this CTA's partial tile at TMEM column `col` to the peer, then wait for the peer's.
-    auto send = [&](uint32_t col) {
-      if (x >= 1) {
-        ok = __all_sync(0xffffffffu, mbar_wait(bar(bl.xfree), (x - 1) & 1, status));
-        if (!ok) return;
-      }
-      const uint32_t dst = peer_land + r * 512;
-#pragma unroll
-      for (int c4 = 0; c4 < 4; ++c4) {
-        uint32_t v[32];
-        tmem_ld32(tbase + lane_off + col + c4 * 32, v);
-        tmem_ld_wait();
-#pragma unroll
-        for (int c8 = 0; c8 < 8; ++c8)
-          st_cluster_v4(dst + (((c4 * 8 + c8) ^ swz) << 4), __uint_as_float(v[4 * c8]), __uint_as_float(v[4 * c8 + 1]),
-                        __uint_as_float(v[4 * c8 + 2]), __uint_as_float(v[4 * c8 + 3]));
-      }
-      mbar_arrive_remote(peer_xfull);  // release.cluster: the stores above are visible first
-      ok = __all_sync(0xffffffffu, mbar_wait(bar(bl.xfull), x & 1, status));
-    };
-    auto release = [&]() {
-      mbar_arrive_remote(peer_xfree);
-      ++x;
-    };
-    // 32 columns of the full tile: own partial (TMEM) + the peer's (landing buffer)
+    // 32 columns of a score tile
     auto chunk = [&](uint32_t col, int c4, float (&f)[32]) {
       uint32_t v[32];
       tmem_ld32(tbase + lane_off + col + c4 * 32, v);
       tmem_ld_wait();
 #pragma unroll
       for (int i = 0; i < 32; ++i) f[i] = __uint_as_float(v[i]);
-      if constexpr (XCH) {
-#pragma unroll
-        for (int c8 = 0; c8 < 8; ++c8) {
-          const float4 w = land[(c4 * 8 + c8) ^ swz];
-          f[4 * c8] += w.x;
-          f[4 * c8 + 1] += w.y;
-          f[4 * c8 + 2] += w.z;
-          f[4 * c8 + 3] += w.w;
-        }
-      }
     };
     for (int pass = 0; pass < passes && ok; ++pass) {
       const int oc0 = pass * kMaxAccChunks;
@@ -618,10 +557,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!ok) break;
         tc_fence_after();
         float pv[128];
-        if constexpr (XCH) {
-          send(kX1);
-          if (!ok) break;
-        }
         // A tile with no masked score and no bias (every tile but the diagonal
         // and the ragged edges) skips the per-score checks.
         bool plain;
@@ -674,16 +609,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         }
-        if constexpr (XCH) release();
         // The scores have been read: X1 may take the next column's.
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(bl.x1_free));
         if (two) {
-          if constexpr (XCH) {
-            send(kX2);
-            if (!ok) break;
-          }
 #pragma unroll
           for (int c4 = 0; c4 < 4; ++c4) {
             float f[32];
@@ -699,7 +629,6 @@ __global__ void __launch_bounds__(kThreads, 1)
               pv[ci] = pv[ci] * (f[e] - dl);
             }
           }
-          if constexpr (XCH) release();
         }
         {
           uint32_t lo[32], hi[32];
@@ -775,24 +704,22 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   tc_fence_before();
   __syncthreads();
-  if (XCH) cluster_sync();
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tbase, kTmemCols);
   }
 }
 
-template <int MODE, int FL, bool BF16>
+template <int MODE, bool BF16>
 cudaError_t launch_mode(const BwdParams& p_in, const BwdMaps& m, cudaStream_t st) {
   BwdParams p = p_in;
-  constexpr int CS = (FL == kSolo) ? 1 : 2;
   constexpr int kMaxSmem = 232448;
   // Keep as many stationary operands resident as leave a ring of >= 3 stages
   // (>= 2 when nothing is resident).
   int n_res = (MODE == kDV) ? 1 : 2;
   int room = 0;
   for (; n_res >= 0; --n_res) {
-    const Plan base = make_plan(p.n_chunks, FL, 0, n_res, 1);
+    const Plan base = make_plan(p.n_chunks, 0, n_res, 1);
     room = kMaxSmem - 1024 - base.total;
     if (room / kChunkBytes >= 3) break;
   }
@@ -804,23 +731,16 @@ cudaError_t launch_mode(const BwdParams& p_in, const BwdMaps& m, cudaStream_t st
   if (stages < 2) return cudaErrorInvalidConfiguration;
   p.stages = stages;
   p.slot_chunks = G;
-  const Plan plan = make_plan(p.n_chunks, FL, stages, n_res, G);
+  const Plan plan = make_plan(p.n_chunks, stages, n_res, G);
   const int smem = plan.total + 1024;
-  auto kern = bwd_main_kernel<MODE, FL, BF16>;
+  auto kern = bwd_main_kernel<MODE, BF16>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = (MODE == kDQ) ? dim3(CS * p.q_tiles, p.Hq, p.B) : dim3(CS * p.kv_tiles, p.Hkv, p.B);
+  cfg.gridDim = (MODE == kDQ) ? dim3(p.q_tiles, p.Hq, p.B) : dim3(p.kv_tiles, p.Hkv, p.B);
   cfg.blockDim = dim3(kThreads, 1, 1);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = st;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = CS;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = (FL == kExchange) ? 1 : 0;  // only the exchanging pair is a cluster
   e = cudaLaunchKernelEx(&cfg, kern, m.q, m.k, m.v, m.dout, p, n_res);
   timing_mark(st);
   return e;
@@ -835,13 +755,13 @@ cudaError_t launch_preprocess(const BwdParams& p, cudaStream_t st) {
   return cudaGetLastError();
 }
 
-template <int FL, bool BF16>
+template <bool BF16>
 cudaError_t launch_all(const BwdParams& p, const BwdMaps& m, cudaStream_t st) {
   cudaError_t e = launch_preprocess<BF16>(p, st);
   if (e != cudaSuccess) return e;
-  if ((e = launch_mode<kDV, FL, BF16>(p, m, st)) != cudaSuccess) return e;
-  if ((e = launch_mode<kDK, FL, BF16>(p, m, st)) != cudaSuccess) return e;
-  return launch_mode<kDQ, FL, BF16>(p, m, st);
+  if ((e = launch_mode<kDV, BF16>(p, m, st)) != cudaSuccess) return e;
+  if ((e = launch_mode<kDK, BF16>(p, m, st)) != cudaSuccess) return e;
+  return launch_mode<kDQ, BF16>(p, m, st);
 }
 
 }  // namespace
@@ -859,8 +779,8 @@ cudaError_t launch_bwd(const BwdParams& p, const BwdMaps& m, bool bf16, cudaStre
     cudaError_t e = bf16 ? launch_preprocess<true>(p, s) : launch_preprocess<false>(p, s);
     return e != cudaSuccess ? e : launch_bwd_xch(p, m, bf16, s);
   }
-  if (p.n_chunks <= 4) return bf16 ? launch_all<kSolo, true>(p, m, s) : launch_all<kSolo, false>(p, m, s);
-  return bf16 ? launch_all<kExchange, true>(p, m, s) : launch_all<kExchange, false>(p, m, s);
+  if (p.n_chunks <= 4) return bf16 ? launch_all<true>(p, m, s) : launch_all<false>(p, m, s);
+  return cudaErrorInvalidValue;
 }
 
 }  // namespace ffpa

@@ -96,7 +96,9 @@ int ffpa_fwd(const ffpa_tensor_t* q, const ffpa_tensor_t* k, const ffpa_tensor_t
 
 /*
  * ffpa_bwd: attention backward (FFPA Attention Benchmark page, "More
- * Benchmark": preprocess, then dV, dK, dQ).
+ * Benchmark": a preprocess, then the key-side gradients dK and dV, then dQ).
+ * D <= 256 runs preprocess, dV, dK and dQ as four kernels; D = 320 .. 1024
+ * runs preprocess, one fused dK/dV kernel and a dQ kernel.
  *
  *   q, k, v, bias, causal, scale   exactly as passed to ffpa_fwd
  *   out   [B, Hq, Nq, D]  the forward's O
@@ -163,8 +165,8 @@ int ffpa_check_status(ffpa_stream_t stream);
  * While set (per calling host thread), every later ffpa_fwd / ffpa_bwd call on
  * this thread records events[0] on its stream before its first kernel launch
  * and events[i] right after its i-th launch, for as many events as given
- * (ffpa_fwd launches 1 kernel on the fused path and 2 on the decode path;
- * ffpa_bwd launches 4: preprocess, dV, dK, dQ).  The caller keeps ownership of
+ * (ffpa_fwd launches 1 kernel on the fused path and 2 on the decode and
+ * key-split paths; ffpa_bwd launches 4 for D <= 256 and 3 above).  The caller keeps ownership of
  * the events.  Returns FFPA_ERR_INVALID_ARG if count < 0, count > 8, or
  * events (or one of its first `count` handles) is NULL with count > 0.
  */
