@@ -309,7 +309,7 @@ def run_ffpa(args, rank, world):
 # DRAM bytes (read + write) per launch, dram__bytes_read.sum +
 # dram__bytes_write.sum from one ncu capture of the same workload; a kernel
 # changed since its capture is left out (its traffic is then reported as null).
-TRAFFIC: dict = {"fwd_main": 248862464, "bwd_dkv": 372845824, "bwd_dq": 322821376}
+TRAFFIC: dict = {"fwd_main": 248862464, "bwd_dq": 322821376}
 TRAFFIC_FROM = "ncu capture of the same workload (dram__bytes_read.sum + dram__bytes_write.sum per launch)"
 
 

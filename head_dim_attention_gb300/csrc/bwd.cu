@@ -18,8 +18,9 @@
 // TMEM without any atomics or workspace.
 //
 // These kernels serve D <= 256.  launch_bwd hands larger head dimensions,
-// after the preprocess, to the cluster kernels of bwd_dkv.cu and bwd_dq.cu
-// (D = 320 .. 512) and of bwd_xch.cu (D = 576 .. 1024).
+// after the preprocess, to the fused dK/dV cluster kernel of bwd_xch.cu and
+// then to the dQ kernel of bwd_dq.cu (D = 320 .. 512) or bwd_xch.cu's dQ mode
+// (D = 576 .. 1024).
 //
 // TMEM (512 columns): gradient accumulator [0, 256), X1 [256, 384) (scores),
 // X2 [384, 512) (dP, then P or dS as the bf16/f16 A operand of the gradient).
@@ -767,17 +768,14 @@ cudaError_t launch_all(const BwdParams& p, const BwdMaps& m, cudaStream_t st) {
 }  // namespace
 
 cudaError_t launch_bwd(const BwdParams& p, const BwdMaps& m, bool bf16, cudaStream_t s) {
-  if (bwd_dq_supported(p) && bwd_dkv_supported(p)) {
-    // preprocess, fused dK/dV (two CTA pairs per key tile), then dQ (one pair per query tile)
+  if (bwd_xch_dkv_supported(p) && (bwd_dq_supported(p) || bwd_xch_dq_supported(p))) {
+    // preprocess, the fused dK/dV kernel (two CTA pairs per key tile, or two
+    // such clusters above D = 512), then dQ: one CTA pair per query tile up to
+    // D = 512, two exchanging pairs above
     cudaError_t e = bf16 ? launch_preprocess<true>(p, s) : launch_preprocess<false>(p, s);
-    if (e == cudaSuccess) e = launch_bwd_dkv(p, m, bf16, s);
-    return e != cudaSuccess ? e : launch_bwd_dq(p, m, bf16, s);
-  }
-  if (bwd_xch_supported(p)) {
-    // preprocess, then the exchange kernel's dK/dV mode (two clusters per key
-    // tile, one per range of gradient columns) and its dQ mode
-    cudaError_t e = bf16 ? launch_preprocess<true>(p, s) : launch_preprocess<false>(p, s);
-    return e != cudaSuccess ? e : launch_bwd_xch(p, m, bf16, s);
+    if (e == cudaSuccess) e = launch_bwd_xch_dkv(p, m, bf16, s);
+    if (e != cudaSuccess) return e;
+    return bwd_dq_supported(p) ? launch_bwd_dq(p, m, bf16, s) : launch_bwd_xch_dq(p, m, bf16, s);
   }
   if (p.n_chunks <= 4) return bf16 ? launch_all<true>(p, m, s) : launch_all<false>(p, m, s);
   return cudaErrorInvalidValue;

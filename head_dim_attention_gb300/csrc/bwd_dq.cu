@@ -1,5 +1,5 @@
 // Attention backward dQ for D = 320..512, the third launch after the
-// preprocess and the fused dK/dV kernel of bwd_dkv.cu (FFPA Attention
+// preprocess and the fused dK/dV kernel of bwd_xch.cu (FFPA Attention
 // Benchmark page, "More Benchmark": the SM100 backward's separate dQ pass).
 // P is rebuilt from the forward's lse; per 128-row query tile, over the key
 // tiles (to the diagonal when causal):

@@ -1,26 +1,29 @@
-// Attention backward for D = 576..1024 on clusters of four CTAs (two CTA
-// pairs) that exchange the probability tiles and their gradients, so that no
-// CTA has to keep two 64 x D operands resident (at D = 1024 one of them alone
-// is 128 KB of shared memory).  Two modes of one kernel, after the preprocess
-// (FFPA Attention Benchmark page, "More Benchmark": the SM100 backward's fused
-// dK/dV pass, then dQ; the fused dK/dV kernel of bwd_dkv.cu is this file's
-// dK/dV mode for D <= 512, where one cluster holds all of the gradient):
+// Attention backward for D = 320..1024 on clusters of four CTAs (two CTA
+// pairs) that exchange the probability tiles and their gradients (FFPA
+// Attention Benchmark page, "More Benchmark": the SM100 backward's fused
+// dK/dV pass, then dQ).  Two modes of one kernel, after the preprocess:
 //
-//   dK/dV mode, per 128-row key tile and sweeping the query tiles of every
-//   query head of the GQA group:
+//   dK/dV mode (every D), per 128-row key tile, sweeping the query tiles of
+//   every query head of the GQA group:
 //     pair A: K resident;  X = S^T = K Q^T;  P^T  -> pair B;  dK += dS^T Q
 //     pair B: V resident;  X = dP^T = V dO^T; dS^T = P^T (dP^T - Delta) -> A;
-//             dV += P^T dO
-//     The gradients' columns are split over two clusters per key tile (each
-//     at most 512 columns wide); each cluster computes S^T and dP^T over all
-//     of D.
-//   dQ mode, per 128-row query tile and sweeping the key tiles:
+//             dV += P^T dO  with P^T straight from the received buffer
+//     Separate dV and dK kernels would both rebuild S^T and execute 4 + 6 =
+//     10 Nq Nkv D per head; here each pair executes one score product and one
+//     gradient product per column tile, 8 Nq Nkv D in all.  A pair cannot hold
+//     both gradients (128 x 512 fp32 each takes half of an SM's TMEM in the
+//     M = 128 pair layout, and the score tiles need room too), hence the two
+//     pairs.  Up to D = 512 one cluster holds all of a gradient's columns;
+//     above, two clusters per key tile take one range of columns each (at
+//     most 512 wide) and each computes S^T and dP^T over all of D.
+//   dQ mode (D = 576..1024, where one pair cannot keep Q and dO resident and
+//   hold dQ), per 128-row query tile, sweeping the key tiles:
 //     pair A: Q resident;  X = S = Q K^T;  P  -> pair B;
 //             dQ[:, columns of A] += dS K  with dS received from B
 //     pair B: dO resident; X = dP = dO V^T;  dS = P (dP - Delta) -> A;
 //             dQ[:, columns of B] += dS K  with its own dS
-//     Each score product is computed once; each pair accumulates half of
-//     dQ's columns.
+//     Each score product is computed once; each pair accumulates one range
+//     of dQ's columns.
 //
 // Layout within a pair (tcgen05 cta_group::2, M = 128): CTA c (c = rank & 1)
 // holds stationary rows 64c .. 64c + 63 across all 128 TMEM lanes (lane r:
@@ -32,6 +35,8 @@
 // bulk copy into the other CTA, whose barrier counts the bytes.  A received
 // tile is the receiving pair's A operand as it lies (dK/dV mode: both pairs;
 // dQ mode: pair A).  In dQ mode pair B's A operand is its own staging tile.
+// Two or three receive buffers per direction cover the round trip (P out, dS
+// back) while the score products of the next tiles run.
 //
 // Signals that cross the two pairs:
 //   pt_full[b] / ds_full[b]  bulk-copy bytes, armed by a thread of the
@@ -46,11 +51,13 @@
 // and free once the pair's dQ MMAs and the bulk copy have read it (st_free).
 //
 // TMEM per CTA: gradient [0, 256), score tiles [256, 384), the stationary
-// tile's chunks 0..3 as the TS-form operand [384, 512).  Warps: 0 producer of
-// the score-operand ring (and the stationary tile), 1 TMEM owner + MMA issuer
-// X (first CTA of a pair), 2 MMA issuer G (first CTA) or relay (second CTA),
-// 3 producer of the gradient-operand ring, 4-7 elementwise, exchange and
-// epilogue.  Every wait is bounded (ptx.cuh).
+// tile's chunks 0..3 as the TS-form operand [384, 512) (the score MMAs' operand
+// reads from shared memory alone would need the SM's full shared-memory
+// bandwidth at M = 128, N = 128).  Warps: 0 producer of the score-operand
+// ring (and the stationary tile), 1 TMEM owner + MMA issuer X (first CTA of a
+// pair), 2 MMA issuer G (first CTA) or relay (second CTA), 3 producer of the
+// gradient-operand ring, 4-7 elementwise, exchange and epilogue.  Every wait
+// is bounded (ptx.cuh).
 #include <type_traits>
 
 #include "internal.h"
@@ -68,17 +75,22 @@ constexpr uint32_t kSt = 384;               // the stationary tile's chunks 0..3
 constexpr int kHalf = kChunkBytes / 2;      // 64 rows x 64 columns, 8 KB
 constexpr int kTileX = 2 * kHalf;           // one CTA's exchanged tile: 64 rows x 128 columns, 16 KB
 constexpr int kSlice = kTileX / 4;          // one elementwise warp's rows of it, 4 KB
-constexpr int kNrecv = 2;                   // receive buffers per direction
 constexpr int kNstage = 2;                  // staging tiles
 constexpr int kSlot = 2 * kHalf;            // ring slots of 16 KB
 constexpr float kLog2e = 1.4426950408889634f;
 
 template <int NC>
 struct Shape {
-  static_assert(NC >= 9 && NC <= 16, "D = 576 .. 1024");
+  static_assert(NC >= 5 && NC <= 16, "D = 320 .. 1024");
   static constexpr int kD = 64 * NC;
-  // gradient columns: [0, kGa) and [kGa, D), each at most 512 wide
-  static constexpr int kGa = ((kD / 2 + 127) / 128) * 128 < 512 ? ((kD / 2 + 127) / 128) * 128 : 512;
+  static constexpr int kHalfD = ((kD / 2 + 127) / 128) * 128 < 512 ? ((kD / 2 + 127) / 128) * 128 : 512;
+  // dK/dV mode: up to D = 512 one cluster per key tile holds all of a
+  // gradient's columns; above, two clusters take [0, kGaKV) and [kGaKV, D)
+  static constexpr int kSplitKV = NC <= 8 ? 1 : 2;
+  static constexpr int kGaKV = NC <= 8 ? kD : kHalfD;
+  // dQ mode: pair A accumulates dQ's columns [0, kGaQ), pair B [kGaQ, D)
+  static constexpr int kGaQ = kHalfD;
+  static constexpr int kNrecv = NC <= 8 ? 3 : 2;  // receive buffers per direction
   static constexpr int kRes = (NC - 4) * kHalf;  // the stationary tile's chunks 4..NC-1 in shared memory
   static constexpr int kSlots = NC <= 12 ? 3 : 2;  // per ring, as many as fit
   // shared memory: resident | receive buffers | staging | score ring | gradient ring | barriers
@@ -89,7 +101,7 @@ struct Shape {
   static constexpr int kMiscOff = kRingGOff + kSlots * kSlot;
   static constexpr int kSmemBytes = kMiscOff + 512 + 1024;  // + alignment slack
   static_assert(kSmemBytes <= 232448, "227 KB per CTA");
-  static_assert(kD - kGa <= 512, "two gradient ranges");
+  static_assert(kGaKV <= 512 && kD - kGaKV <= 512 && kD - kGaQ <= 512, "ranges of at most 512 columns");
 };
 
 struct Bars {
@@ -97,9 +109,9 @@ struct Bars {
       ds_free, st_ready, st_local, st_free, drain_x, drain_g, g_done, count;
 };
 // rings: up to three slots; x_full, x_free, st_*: one per TMEM score buffer or
-// staging tile; pt_*, ds_*: one per receive buffer
+// staging tile; pt_*, ds_*: one per receive buffer (up to three)
 __host__ __device__ constexpr Bars bar_layout() {
-  return Bars{0, 3, 6, 9, 12, 13, 15, 17, 19, 21, 23, 25, 27, 29, 31, 33, 35, 36, 37, 38};
+  return Bars{0, 3, 6, 9, 12, 13, 15, 17, 20, 23, 26, 29, 32, 35, 37, 39, 41, 42, 43, 44};
 }
 static_assert(bar_layout().count * 8 + 16 <= 512, "barrier area");
 
@@ -156,8 +168,8 @@ __device__ __forceinline__ Geo make_geo(const BwdParams& p, int pr, bool is_b) {
   const int cl = static_cast<int>(blockIdx.x) >> 2;
   int gsel;
   if (MODE == kDKV) {
-    gsel = cl & 1;  // two clusters per key tile split the gradient's columns
-    g.st = cl >> 1;
+    gsel = G::kSplitKV == 2 ? (cl & 1) : 0;  // above D = 512 two clusters per key tile
+    g.st = cl / G::kSplitKV;
     g.kvh = blockIdx.y;
     g.hs = g.kvh;
     g.s_limit = p.Nkv;
@@ -175,8 +187,9 @@ __device__ __forceinline__ Geo make_geo(const BwdParams& p, int pr, bool is_b) {
     g.qt_begin = 0;
     g.nq_h = 0;
   }
-  g.g0 = gsel ? G::kGa : 0;
-  g.gw = gsel ? G::kD - G::kGa : G::kGa;
+  const int ga = MODE == kDKV ? G::kGaKV : G::kGaQ;
+  g.g0 = gsel ? ga : 0;
+  g.gw = gsel ? G::kD - ga : ga;
   g.nv0 = g.gw >= 256 ? 2 : (g.gw + 127) / 128;
   g.nv1 = g.gw > 256 ? (g.gw - 256 + 127) / 128 : 0;
   g.s_row0 = g.st * kTileRows + 64 * pr;
@@ -204,7 +217,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                    const __grid_constant__ CUtensorMap map_vh, const __grid_constant__ CUtensorMap map_doh,
                    const __grid_constant__ BwdParams p) {
   using G = Shape<NC>;
-  constexpr int kSlots = G::kSlots;
+  constexpr int kSlots = G::kSlots, kNrecv = G::kNrecv;
   constexpr bool DQ = MODE == kDQ;
   constexpr Bars bl = bar_layout();
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -726,8 +739,8 @@ cudaError_t launch_impl(const BwdParams& p, const BwdMaps& m, cudaStream_t st) {
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
-  // dK/dV: two clusters per key tile (one per range of gradient columns); dQ: one per query tile
-  cfg.gridDim = MODE == kDKV ? dim3(8 * p.kv_tiles, p.Hkv, p.B) : dim3(4 * p.q_tiles, p.Hq, p.B);
+  // dK/dV: one or two clusters per key tile (one per range of gradient columns); dQ: one per query tile
+  cfg.gridDim = MODE == kDKV ? dim3(4 * Shape<NC>::kSplitKV * p.kv_tiles, p.Hkv, p.B) : dim3(4 * p.q_tiles, p.Hq, p.B);
   cfg.blockDim = dim3(kThreads, 1, 1);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = st;
@@ -743,32 +756,40 @@ cudaError_t launch_impl(const BwdParams& p, const BwdMaps& m, cudaStream_t st) {
   return e;
 }
 
-template <int NC, bool BF16>
-cudaError_t launch_both(const BwdParams& p, const BwdMaps& m, cudaStream_t st) {
-  cudaError_t e = launch_impl<kDKV, NC, BF16>(p, m, st);
-  return e != cudaSuccess ? e : launch_impl<kDQ, NC, BF16>(p, m, st);
-}
-
-template <bool BF16>
+template <int MODE, bool BF16>
 cudaError_t launch_nc(const BwdParams& p, const BwdMaps& m, cudaStream_t st) {
+  if constexpr (MODE == kDKV) {
+    switch (p.n_chunks) {
+      case 5: return launch_impl<MODE, 5, BF16>(p, m, st);
+      case 6: return launch_impl<MODE, 6, BF16>(p, m, st);
+      case 7: return launch_impl<MODE, 7, BF16>(p, m, st);
+      case 8: return launch_impl<MODE, 8, BF16>(p, m, st);
+      default: break;
+    }
+  }
   switch (p.n_chunks) {
-    case 9: return launch_both<9, BF16>(p, m, st);
-    case 10: return launch_both<10, BF16>(p, m, st);
-    case 11: return launch_both<11, BF16>(p, m, st);
-    case 12: return launch_both<12, BF16>(p, m, st);
-    case 13: return launch_both<13, BF16>(p, m, st);
-    case 14: return launch_both<14, BF16>(p, m, st);
-    case 15: return launch_both<15, BF16>(p, m, st);
-    default: return launch_both<16, BF16>(p, m, st);
+    case 9: return launch_impl<MODE, 9, BF16>(p, m, st);
+    case 10: return launch_impl<MODE, 10, BF16>(p, m, st);
+    case 11: return launch_impl<MODE, 11, BF16>(p, m, st);
+    case 12: return launch_impl<MODE, 12, BF16>(p, m, st);
+    case 13: return launch_impl<MODE, 13, BF16>(p, m, st);
+    case 14: return launch_impl<MODE, 14, BF16>(p, m, st);
+    case 15: return launch_impl<MODE, 15, BF16>(p, m, st);
+    case 16: return launch_impl<MODE, 16, BF16>(p, m, st);
+    default: return cudaErrorInvalidValue;
   }
 }
 
 }  // namespace
 
-bool bwd_xch_supported(const BwdParams& p) { return p.n_chunks >= 9 && p.n_chunks <= 16; }
+bool bwd_xch_dkv_supported(const BwdParams& p) { return p.n_chunks >= 5 && p.n_chunks <= 16; }
+bool bwd_xch_dq_supported(const BwdParams& p) { return p.n_chunks >= 9 && p.n_chunks <= 16; }
 
-cudaError_t launch_bwd_xch(const BwdParams& p, const BwdMaps& m, bool bf16, cudaStream_t s) {
-  return bf16 ? launch_nc<true>(p, m, s) : launch_nc<false>(p, m, s);
+cudaError_t launch_bwd_xch_dkv(const BwdParams& p, const BwdMaps& m, bool bf16, cudaStream_t s) {
+  return bf16 ? launch_nc<kDKV, true>(p, m, s) : launch_nc<kDKV, false>(p, m, s);
+}
+cudaError_t launch_bwd_xch_dq(const BwdParams& p, const BwdMaps& m, bool bf16, cudaStream_t s) {
+  return bf16 ? launch_nc<kDQ, true>(p, m, s) : launch_nc<kDQ, false>(p, m, s);
 }
 
 }  // namespace ffpa

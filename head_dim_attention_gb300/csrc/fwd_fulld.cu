@@ -4,7 +4,7 @@
 // Same computation as fwd_main.cu: O = softmax(scale Q K^T + bias) V and the
 // row logsumexp, keys in tiles of 128 with an online softmax.  Splitting O's
 // 512 columns between two CTAs (or two pairs) makes each reduce S over the
-// whole of D; here, as in the backward kernels (bwd_dkv.cu, bwd_dq.cu), each SM of
+// whole of D; here, as in the backward kernels (bwd_xch.cu, bwd_dq.cu), each SM of
 // the pair holds 64 query rows of a 128 x 512 fp32 O across all 128 TMEM
 // lanes (lane r: row r, the first N/2 columns of an accumulator; lane r + 64:
 // the other N/2), so O takes 256 TMEM columns and S is computed once per key

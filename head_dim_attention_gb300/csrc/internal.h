@@ -137,13 +137,12 @@ cudaError_t launch_bwd(const BwdParams& p, const BwdMaps& m, bool bf16, cudaStre
 // Full-D CTA-pair dQ kernel (bwd_dq.cu): D = 320 .. 512; the preprocess runs first.
 bool bwd_dq_supported(const BwdParams& p);
 cudaError_t launch_bwd_dq(const BwdParams& p, const BwdMaps& m, bool bf16, cudaStream_t s);
-// Fused dK/dV kernel, a cluster of two CTA pairs per key tile (bwd_dkv.cu): D = 320 .. 512.
-bool bwd_dkv_supported(const BwdParams& p);
-cudaError_t launch_bwd_dkv(const BwdParams& p, const BwdMaps& m, bool bf16, cudaStream_t s);
-// Exchange kernel for D = 576 .. 1024 (bwd_xch.cu): its dK/dV mode, then its
-// dQ mode, clusters of two CTA pairs; the preprocess runs first.
-bool bwd_xch_supported(const BwdParams& p);
-cudaError_t launch_bwd_xch(const BwdParams& p, const BwdMaps& m, bool bf16, cudaStream_t s);
+// Exchange kernel on clusters of two CTA pairs (bwd_xch.cu): its fused dK/dV
+// mode (D = 320 .. 1024) and its dQ mode (D = 576 .. 1024), after the preprocess.
+bool bwd_xch_dkv_supported(const BwdParams& p);
+bool bwd_xch_dq_supported(const BwdParams& p);
+cudaError_t launch_bwd_xch_dkv(const BwdParams& p, const BwdMaps& m, bool bf16, cudaStream_t s);
+cudaError_t launch_bwd_xch_dq(const BwdParams& p, const BwdMaps& m, bool bf16, cudaStream_t s);
 
 uint32_t* device_status_word();  // per current device
 
