@@ -8,8 +8,11 @@ from .attn_ref import (  # noqa: F401
     attn_bwd_sampled,
     attn_fwd,
     attn_fwd_rows,
+    dropout_keep,
+    dropout_threshold,
     kv_head_of,
     probs_head,
     sample_rows,
     scores_head,
 )
+from .philox import philox4x32_10  # noqa: F401

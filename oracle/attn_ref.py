@@ -29,6 +29,20 @@ Benchmark page ("More Benchmark") splits the same backward into a
 preprocess (Delta) and dV, dK, dQ launches; the oracle computes each gradient
 directly from its definition instead.
 
+Dropout (the "dropout" rows of the FFPA Attention Benchmark page's "More
+Benchmark" tables) drops entries of P after the softmax and scales the kept
+ones by 1 / (1 - p), so O = (P * Z) V with Z = keep / (1 - p) and lse that of
+the undropped scores.  The backward is the gradient of the same function for
+a fixed keep mask:
+    dV = (P * Z)^T dO,  dP = (dO V^T) * Z,  Delta_i = sum_d dO_id O_id,
+    dS = P * (dP - Delta),  dQ, dK as above.
+The pages name no generator, so the keep mask follows a contract written
+here (``dropout_keep``): Philox4x32-10 (``oracle.philox``) with key = the
+64-bit seed and counter (j // 8, i, b * Hq + h, offset) for query row i and
+key j of query head h in batch b; score (i, j) takes the 16-bit field
+(j mod 2) of output word (j mod 8) // 2 and is kept when that value is at
+least t = min(65535, floor(p * 65536 + 1/2)).
+
 Readings where the pages are silent (each also listed in the design notes):
   * lse is the natural log of the scaled and biased scores.
   * causal with Nq != Nkv is top-left (query i sees keys j <= i).
@@ -44,7 +58,11 @@ import math
 
 import numpy as np
 
+from .philox import philox4x32_10
+
 __all__ = [
+    "dropout_threshold",
+    "dropout_keep",
     "kv_head_of",
     "scores_head",
     "probs_head",
@@ -74,6 +92,35 @@ def _bias_rows(bias, b: int, h: int, rows: np.ndarray, nkv: int) -> np.ndarray |
     if bb.shape[0] == 1:
         return np.broadcast_to(bb[0], (len(rows), nkv))
     return bb[rows]
+
+
+def dropout_threshold(p: float) -> int:
+    """16-bit threshold of drop probability p: a score is kept when its value >= t."""
+    p = float(p)
+    if not 0.0 <= p < 1.0:
+        raise ValueError("dropout probability must be in [0, 1)")
+    return min(65535, int(math.floor(p * 65536.0 + 0.5)))
+
+
+def dropout_keep(b: int, h: int, hq: int, rows, cols, p: float, seed: int, offset: int) -> np.ndarray:
+    """Keep mask [len(rows), len(cols)] of query head h of batch b under the contract above."""
+    t = dropout_threshold(p)
+    i = np.asarray(rows, dtype=np.uint64)[:, None]
+    j = np.asarray(cols, dtype=np.uint64)[None, :]
+    seed = int(seed) & 0xFFFFFFFFFFFFFFFF
+    x = philox4x32_10((j >> np.uint64(3), i, b * hq + h, int(offset)), (seed & 0xFFFFFFFF, seed >> 32))
+    jm = (j & np.uint64(7)) + np.zeros_like(i)
+    word = np.choose((jm >> np.uint64(1)).astype(np.int64), x)
+    u = (word >> (np.uint64(16) * (jm & np.uint64(1)))) & np.uint64(0xFFFF)
+    return u >= np.uint64(t)
+
+
+def _dropout_z(dropout, b, h, hq, rows, cols):
+    """Z = keep / (1 - p) on [rows, cols], or 1.0 without dropout."""
+    if dropout is None:
+        return 1.0
+    p, seed, offset = dropout
+    return dropout_keep(b, h, hq, rows, cols, p, seed, offset) / (1.0 - float(p))
 
 
 def scores_head(q, k, bias, b, h, hkv_idx, scale, causal, rows=None, cols=None) -> np.ndarray:
@@ -124,8 +171,11 @@ def _scale(scale, d):
     return 1.0 / math.sqrt(d) if scale is None else float(scale)
 
 
-def attn_fwd(q, k, v, bias=None, causal=False, scale=None):
-    """Full forward: O [B,Hq,Nq,D] and lse [B,Hq,Nq] (fp64)."""
+def attn_fwd(q, k, v, bias=None, causal=False, scale=None, dropout=None):
+    """Full forward: O [B,Hq,Nq,D] and lse [B,Hq,Nq] (fp64).
+
+    dropout: None or (p, seed, offset) under the contract above.
+    """
     q, k, v = (np.asarray(x, dtype=np.float64) for x in (q, k, v))
     _check(q, k, v)
     bsz, hq, nq, d = q.shape
@@ -137,21 +187,23 @@ def attn_fwd(q, k, v, bias=None, causal=False, scale=None):
         for h in range(hq):
             g = kv_head_of(h, hq, hkv)
             p, lse[b, h] = probs_head(scores_head(q, k, bias, b, h, g, scale, causal))
-            o[b, h] = p @ v[b, g]
+            z = _dropout_z(dropout, b, h, hq, np.arange(nq), np.arange(k.shape[2]))
+            o[b, h] = (p * z) @ v[b, g]
     return o, lse
 
 
-def attn_fwd_rows(q, k, v, b, h, rows, bias=None, causal=False, scale=None):
+def attn_fwd_rows(q, k, v, b, h, rows, bias=None, causal=False, scale=None, dropout=None):
     """Forward for selected query rows of one (batch, head): O[rows] and lse[rows]."""
     q, k, v = (np.asarray(x, dtype=np.float64) for x in (q, k, v))
     _check(q, k, v)
     scale = _scale(scale, q.shape[3])
     g = kv_head_of(h, q.shape[1], k.shape[1])
     p, lse = probs_head(scores_head(q, k, bias, b, h, g, scale, causal, rows=rows))
-    return p @ v[b, g], lse
+    z = _dropout_z(dropout, b, h, q.shape[1], rows, np.arange(k.shape[2]))
+    return (p * z) @ v[b, g], lse
 
 
-def attn_bwd(q, k, v, do, bias=None, causal=False, scale=None):
+def attn_bwd(q, k, v, do, bias=None, causal=False, scale=None, dropout=None):
     """Full analytic backward: (dQ, dK, dV), fp64, dK/dV summed over each GQA group."""
     q, k, v, do = (np.asarray(x, dtype=np.float64) for x in (q, k, v, do))
     _check(q, k, v)
@@ -165,9 +217,10 @@ def attn_bwd(q, k, v, do, bias=None, causal=False, scale=None):
         for h in range(hq):
             g = kv_head_of(h, hq, hkv)
             p, _ = probs_head(scores_head(q, k, bias, b, h, g, scale, causal))
-            o = p @ v[b, g]
-            dv[b, g] += p.T @ do[b, h]
-            dp = do[b, h] @ v[b, g].T
+            z = _dropout_z(dropout, b, h, hq, np.arange(q.shape[2]), np.arange(k.shape[2]))
+            o = (p * z) @ v[b, g]
+            dv[b, g] += (p * z).T @ do[b, h]
+            dp = (do[b, h] @ v[b, g].T) * z
             delta = np.sum(do[b, h] * o, axis=1)
             ds = p * (dp - delta[:, None])
             dq[b, h] = scale * (ds @ k[b, g])
@@ -176,7 +229,7 @@ def attn_bwd(q, k, v, do, bias=None, causal=False, scale=None):
 
 
 def attn_bwd_sampled(q, k, v, do, b, h_kv, q_rows, kv_rows, bias=None, causal=False, scale=None,
-                     block=1024):
+                     block=1024, dropout=None):
     """Exact gradients at selected rows, for shapes too large for the full backward.
 
     For kv head ``h_kv`` of batch ``b``: returns
@@ -203,11 +256,13 @@ def attn_bwd_sampled(q, k, v, do, b, h_kv, q_rows, kv_rows, bias=None, causal=Fa
         for r0 in range(0, nq, block):
             rows = np.arange(r0, min(nq, r0 + block))
             p, lse[rows] = probs_head(scores_head(q, k, bias, b, h, h_kv, scale, causal, rows=rows))
-            delta[rows] = np.sum(do[b, h][rows] * (p @ v[b, h_kv]), axis=1)
+            z = _dropout_z(dropout, b, h, hq, rows, np.arange(k.shape[2]))
+            delta[rows] = np.sum(do[b, h][rows] * ((p * z) @ v[b, h_kv]), axis=1)
         # dQ at the sampled query rows (needs those rows of P and dP over all keys)
         rows_h = np.asarray(q_rows[h] if isinstance(q_rows, dict) else q_rows)
         p, _ = probs_head(scores_head(q, k, bias, b, h, h_kv, scale, causal, rows=rows_h))
-        dp = do[b, h][rows_h] @ v[b, h_kv].T
+        z = _dropout_z(dropout, b, h, hq, rows_h, np.arange(k.shape[2]))
+        dp = (do[b, h][rows_h] @ v[b, h_kv].T) * z
         ds = p * (dp - delta[rows_h][:, None])
         dq_out[h] = scale * (ds @ k[b, h_kv])
         # dK/dV at the sampled key rows (needs those columns of P over all queries)
@@ -215,8 +270,9 @@ def attn_bwd_sampled(q, k, v, do, b, h_kv, q_rows, kv_rows, bias=None, causal=Fa
         with np.errstate(invalid="ignore"):
             p_cols = np.where(np.isfinite(lse)[:, None], np.exp(s_cols - np.where(
                 np.isfinite(lse), lse, 0.0)[:, None]), 0.0)
-        dv += p_cols.T @ do[b, h]
-        dp_cols = do[b, h] @ v[b, h_kv][kv_rows].T
+        z = _dropout_z(dropout, b, h, hq, np.arange(nq), kv_rows)
+        dv += (p_cols * z).T @ do[b, h]
+        dp_cols = (do[b, h] @ v[b, h_kv][kv_rows].T) * z
         ds_cols = p_cols * (dp_cols - delta[:, None])
         dk += scale * (ds_cols.T @ q[b, h])
     return dq_out, dk, dv

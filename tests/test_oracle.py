@@ -7,6 +7,7 @@ plausible mistakes in copies of the oracle and checks that some pin fails for
 each, so the pins are known to bite.
 """
 import math
+import os
 
 import numpy as np
 import pytest
@@ -259,9 +260,111 @@ def pin_torch_bias_broadcast(m=ref):
                     assert np.allclose(sdv, dv[bi, g, kr], atol=1e-12), (shape, causal, bi, g)
 
 
+def pin_philox_known_answers(m=ref):
+    # the generator against the published known-answer vectors
+    path = os.path.join(os.path.dirname(__file__), "golden", "philox4x32_10_kat.txt")
+    rows = [ln.split() for ln in open(path) if ln.strip() and not ln.startswith("#")]
+    assert len(rows) == 3
+    for r in rows:
+        w = [int(x, 16) for x in r]
+        out = m.philox4x32_10(w[0:4], w[4:6])
+        assert [int(x) for x in out] == w[6:10], r
+
+
+def pin_dropout_layout(m=ref):
+    # the keep mask's layout, element by element: score (i, j) of query head h in
+    # batch b reads 16-bit field j % 2 of word (j % 8) // 2 of the generator's
+    # output at counter (j // 8, i, b * Hq + h, offset), key = (seed lo, seed hi)
+    p, seed, offset, hq = 0.37, 0x0123456789ABCDEF, 5, 3
+    t = m.dropout_threshold(p)
+    assert t == 24248                                    # floor(0.37 * 65536 + 1/2)
+    rows, cols = np.array([0, 1, 7, 130, 8191]), np.array([0, 1, 2, 7, 8, 9, 63, 100, 8190])
+    for b, h in ((0, 0), (1, 2)):
+        keep = m.dropout_keep(b, h, hq, rows, cols, p, seed, offset)
+        for a, i in enumerate(rows):
+            for c, j in enumerate(cols):
+                x = m.philox4x32_10((int(j) // 8, int(i), b * hq + h, offset),
+                                    (seed & 0xFFFFFFFF, seed >> 32))
+                u = (int(x[(int(j) % 8) // 2]) >> (16 * (int(j) % 2))) & 0xFFFF
+                assert bool(keep[a, c]) == (u >= t), (b, h, i, j)
+
+
+def pin_dropout_rate(m=ref):
+    # the kept fraction is 1 - t / 65536 within 6 sigma; p = 0 keeps every score;
+    # other heads, batches and offsets draw other masks
+    n_r, n_c = 128, 2048
+    for p in (0.1, 0.5, 0.9):
+        keep = m.dropout_keep(0, 1, 4, np.arange(n_r), np.arange(n_c), p, 99, 0)
+        q = 1.0 - m.dropout_threshold(p) / 65536.0
+        sigma = math.sqrt(q * (1 - q) / keep.size)
+        assert abs(keep.mean() - q) < 6 * sigma, (p, keep.mean(), q)
+        for other in (m.dropout_keep(0, 2, 4, np.arange(n_r), np.arange(n_c), p, 99, 0),
+                      m.dropout_keep(1, 1, 4, np.arange(n_r), np.arange(n_c), p, 99, 0),
+                      m.dropout_keep(0, 1, 4, np.arange(n_r), np.arange(n_c), p, 99, 1),
+                      m.dropout_keep(0, 1, 4, np.arange(n_r), np.arange(n_c), p, 98, 0)):
+            # two independent masks differ at a fraction 2 q (1 - q) of the scores
+            diff = float(np.mean(keep != other))
+            assert abs(diff - 2 * q * (1 - q)) < 0.02, (p, diff)
+    assert m.dropout_keep(0, 0, 1, np.arange(64), np.arange(64), 0.0, 5, 0).all()
+
+
+def _torch_dropout_attention(q, k, v, bias, causal, scale, z):
+    # fp64 autograd through softmax, a fixed multiplier Z on P, and P V
+    tq, tk, tv = (torch.from_numpy(x.copy()).requires_grad_(True) for x in (q, k, v))
+    hq, hkv, nq, nkv = q.shape[1], k.shape[1], q.shape[2], k.shape[2]
+    kk = tk.repeat_interleave(hq // hkv, dim=1)
+    vv = tv.repeat_interleave(hq // hkv, dim=1)
+    s = tq @ kk.transpose(-1, -2) * scale
+    if bias is not None:
+        s = s + torch.from_numpy(bias)
+    if causal:
+        s = s.masked_fill(~torch.ones(nq, nkv, dtype=torch.bool).tril(), float("-inf"))
+    pz = torch.softmax(s, dim=-1) * torch.from_numpy(z)
+    return tq, tk, tv, pz @ vv, torch.logsumexp(s, dim=-1)
+
+
+def pin_dropout_torch_autograd(m=ref):
+    # forward and gradients with dropout against PyTorch autograd in fp64, the
+    # multiplier Z = keep / (1 - p) taken from the layout-pinned keep mask; the
+    # row-sampled forms against the full ones
+    for (bsz, hq, hkv, nq, nkv, d, causal, use_bias) in [
+            (1, 2, 1, 7, 19, 8, False, True), (2, 2, 2, 9, 9, 4, True, False), (1, 4, 2, 6, 17, 8, True, True)]:
+        q, k, v, do = rand(bsz, hq, nq, d), rand(bsz, hkv, nkv, d), rand(bsz, hkv, nkv, d), rand(bsz, hq, nq, d)
+        bias = rand(1, 1, 1, nkv) if use_bias else None
+        drop = (0.3, 0xDEADBEEF12345678, 3)
+        z = np.zeros((bsz, hq, nq, nkv))
+        for b in range(bsz):
+            for h in range(hq):
+                z[b, h] = m.dropout_keep(b, h, hq, np.arange(nq), np.arange(nkv), *drop) / 0.7
+        assert 0 < np.count_nonzero(z) < z.size
+        scale = 1.0 / math.sqrt(d)
+        tq, tk, tv, out, lse_t = _torch_dropout_attention(q, k, v, bias, causal, scale, z)
+        o, lse = m.attn_fwd(q, k, v, bias=bias, causal=causal, dropout=drop)
+        assert np.allclose(o, out.detach().numpy(), atol=1e-12), (nq, nkv, causal)
+        assert np.allclose(lse, lse_t.detach().numpy(), atol=1e-12)
+        out.backward(torch.from_numpy(do))
+        dq, dk, dv = m.attn_bwd(q, k, v, do, bias=bias, causal=causal, dropout=drop)
+        for mine, theirs in ((dq, tq), (dk, tk), (dv, tv)):
+            assert np.allclose(mine, theirs.grad.numpy(), atol=1e-11), (nq, nkv, causal)
+        rows, kr = np.array([nq - 1, 0, 2]), np.array([nkv - 1, 1, 4])
+        orow, lrow = m.attn_fwd_rows(q, k, v, bsz - 1, hq - 1, rows, bias=bias, causal=causal, dropout=drop)
+        assert np.allclose(orow, o[bsz - 1, hq - 1, rows], atol=1e-12)
+        for g in range(hkv):
+            sdq, sdk, sdv = m.attn_bwd_sampled(q, k, v, do, bsz - 1, g, rows, kr, bias=bias, causal=causal,
+                                               block=4, dropout=drop)
+            for h, val in sdq.items():
+                assert np.allclose(val, dq[bsz - 1, h, rows], atol=1e-12)
+            assert np.allclose(sdk, dk[bsz - 1, g, kr], atol=1e-12)
+            assert np.allclose(sdv, dv[bsz - 1, g, kr], atol=1e-12)
+        # p = 0 is the plain attention
+        o0, _ = m.attn_fwd(q, k, v, bias=bias, causal=causal, dropout=(0.0, 1, 0))
+        assert np.allclose(o0, m.attn_fwd(q, k, v, bias=bias, causal=causal)[0], atol=1e-14)
+
+
 PINS = [pin_rows_sum_to_one, pin_constant_v, pin_zero_q, pin_causal_row0, pin_single_key, pin_bias_shift,
         pin_permutation, pin_gqa_repeat_interleave, pin_torch_sdpa, pin_torch_autograd, pin_finite_differences,
-        pin_bwd_sums, pin_sampled_bwd, pin_query_bias, pin_torch_bias_broadcast]
+        pin_bwd_sums, pin_sampled_bwd, pin_query_bias, pin_torch_bias_broadcast, pin_philox_known_answers,
+        pin_dropout_layout, pin_dropout_rate, pin_dropout_torch_autograd]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=[p.__name__ for p in PINS])
@@ -294,7 +397,8 @@ def test_lse_magnitude():
 # ---------------------------------------------------------------- the pins bite
 def _mutant_module(**over):
     import importlib.util
-    spec = importlib.util.spec_from_file_location("attn_ref_mutant", ref.__file__)
+    # a fresh copy of the oracle module inside the oracle package (its relative imports resolve)
+    spec = importlib.util.spec_from_file_location("oracle.attn_ref_mutant", ref.__file__)
     mod = importlib.util.module_from_spec(spec)
     spec.loader.exec_module(mod)
     for name, fn in over.items():
@@ -435,6 +539,65 @@ def _mut_bias_batch_ignored(mod):
     return lambda bias, b, h, rows, nkv: orig(bias, 0, h, rows, nkv)
 
 
+def _mut_philox_nine_rounds(mod):
+    def f(counter, key):
+        c = [np.asarray(x, dtype=np.uint64) & np.uint64(0xFFFFFFFF) for x in counter]
+        c = list(np.broadcast_arrays(*c))
+        k0, k1 = int(key[0]) & 0xFFFFFFFF, int(key[1]) & 0xFFFFFFFF
+        for r in range(9):                                # one round short
+            if r:
+                k0, k1 = (k0 + 0x9E3779B9) & 0xFFFFFFFF, (k1 + 0xBB67AE85) & 0xFFFFFFFF
+            p0, p1 = np.uint64(0xD2511F53) * c[0], np.uint64(0xCD9E8D57) * c[2]
+            c = [(p1 >> np.uint64(32)) ^ c[1] ^ np.uint64(k0), p1 & np.uint64(0xFFFFFFFF),
+                 (p0 >> np.uint64(32)) ^ c[3] ^ np.uint64(k1), p0 & np.uint64(0xFFFFFFFF)]
+        return c
+    return f
+
+
+def _mut_dropout_field(mod):
+    # the 16-bit field picked as word j % 4, half (j // 4) % 2
+    def f(b, h, hq, rows, cols, p, seed, offset):
+        t = mod.dropout_threshold(p)
+        i = np.asarray(rows, dtype=np.uint64)[:, None]
+        j = np.asarray(cols, dtype=np.uint64)[None, :]
+        x = mod.philox4x32_10((j >> np.uint64(3), i, b * hq + h, offset), (seed & 0xFFFFFFFF, seed >> 32))
+        jm = (j & np.uint64(7)) + np.zeros_like(i)
+        word = np.choose((jm & np.uint64(3)).astype(np.int64), x)
+        return ((word >> (np.uint64(16) * (jm >> np.uint64(2)))) & np.uint64(0xFFFF)) >= np.uint64(t)
+    return f
+
+
+def _mut_dropout_head_ignored(mod):
+    orig = mod.dropout_keep
+    return lambda b, h, hq, rows, cols, p, seed, offset: orig(b, 0, hq, rows, cols, p, seed, offset)
+
+
+def _mut_dropout_dp_unmasked(mod):
+    orig = mod.attn_bwd
+
+    def f(q, k, v, do, bias=None, causal=False, scale=None, dropout=None):
+        if dropout is None:
+            return orig(q, k, v, do, bias, causal, scale)
+        q, k, v, do = (np.asarray(x, dtype=np.float64) for x in (q, k, v, do))
+        scale = 1.0 / math.sqrt(q.shape[3]) if scale is None else scale
+        hq = q.shape[1]
+        dq, dk, dv = np.zeros(q.shape), np.zeros(k.shape), np.zeros(v.shape)
+        for b in range(q.shape[0]):
+            for h in range(hq):
+                g = mod.kv_head_of(h, hq, k.shape[1])
+                p, _ = mod.probs_head(mod.scores_head(q, k, bias, b, h, g, scale, causal))
+                z = mod.dropout_keep(b, h, hq, np.arange(q.shape[2]), np.arange(k.shape[2]), *dropout) / (
+                    1.0 - dropout[0])
+                o = (p * z) @ v[b, g]
+                dv[b, g] += (p * z).T @ do[b, h]
+                dp = do[b, h] @ v[b, g].T                 # Z left out of dP
+                ds = p * (dp - np.sum(do[b, h] * o, axis=1)[:, None])
+                dq[b, h] = scale * (ds @ k[b, g])
+                dk[b, g] += scale * (ds.T @ q[b, h])
+        return dq, dk, dv
+    return f
+
+
 MUTANTS = {
     "no_scale": {"scores_head": _mut_no_scale},
     "causal_flipped": {"scores_head": _mut_causal_flipped},
@@ -450,6 +613,10 @@ MUTANTS = {
     "bias_row_shifted": {"_bias_rows": _mut_bias_row_shifted},
     "bias_head_ignored": {"_bias_rows": _mut_bias_head_ignored},
     "bias_batch_ignored": {"_bias_rows": _mut_bias_batch_ignored},
+    "philox_nine_rounds": {"philox4x32_10": _mut_philox_nine_rounds},
+    "dropout_field": {"dropout_keep": _mut_dropout_field},
+    "dropout_head_ignored": {"dropout_keep": _mut_dropout_head_ignored},
+    "dropout_dp_unmasked": {"attn_bwd": _mut_dropout_dp_unmasked},
 }
 
 
