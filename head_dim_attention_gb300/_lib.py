@@ -16,7 +16,7 @@ from . import build as _build
 FFPA_F16, FFPA_BF16, FFPA_F32 = 0, 1, 2
 STATUS = {0: "FFPA_OK", 1: "FFPA_ERR_INVALID_ARG", 2: "FFPA_ERR_UNSUPPORTED", 3: "FFPA_ERR_ALIGNMENT",
           4: "FFPA_ERR_CUDA", 5: "FFPA_ERR_TIMEOUT", 6: "FFPA_ERR_SCRATCH_LIMIT"}
-EXPORTS = ("ffpa_fwd", "ffpa_bwd", "ffpa_fwd_decode_noalloc", "ffpa_status_string", "ffpa_check_status",
+EXPORTS = ("ffpa_fwd", "ffpa_bwd", "ffpa_fwd_dropout", "ffpa_bwd_dropout", "ffpa_fwd_decode_noalloc", "ffpa_status_string", "ffpa_check_status",
            "ffpa_set_timing_events", "ffpa_selftest_wait_timeout", "ffpa_version")
 
 
@@ -48,6 +48,12 @@ def load(path: str | None = None) -> ctypes.CDLL:
     lib.ffpa_fwd.restype = ctypes.c_int
     lib.ffpa_bwd.argtypes = [P, P, P, P, ctypes.c_int, ctypes.c_float, P, P, P, P, P, P, ctypes.c_void_p]
     lib.ffpa_bwd.restype = ctypes.c_int
+    D, U64, U32 = ctypes.c_double, ctypes.c_uint64, ctypes.c_uint32
+    lib.ffpa_fwd_dropout.argtypes = [P, P, P, P, ctypes.c_int, ctypes.c_float, D, U64, U32, P, P, ctypes.c_void_p]
+    lib.ffpa_fwd_dropout.restype = ctypes.c_int
+    lib.ffpa_bwd_dropout.argtypes = [P, P, P, P, ctypes.c_int, ctypes.c_float, D, U64, U32, P, P, P, P, P, P,
+                                     ctypes.c_void_p]
+    lib.ffpa_bwd_dropout.restype = ctypes.c_int
     lib.ffpa_fwd_decode_noalloc.argtypes = [P, P, P, P, ctypes.c_int, ctypes.c_float, P, P, ctypes.c_void_p]
     lib.ffpa_fwd_decode_noalloc.restype = ctypes.c_int
     lib.ffpa_status_string.argtypes = [ctypes.c_int]
@@ -135,6 +141,28 @@ def ffpa_fwd(q, k, v, bias, causal, scale, out, lse, stream=None) -> None:
     ds = [describe(q), describe(k), describe(v), describe(bias), describe(out), describe(lse, as_lse=True)]
     rc = lib.ffpa_fwd(_ref(ds[0]), _ref(ds[1]), _ref(ds[2]), _ref(ds[3]), int(causal), float(scale),
                       _ref(ds[4]), _ref(ds[5]), _stream(stream))
+    _raise(rc)
+
+
+def ffpa_fwd_dropout(q, k, v, bias, causal, scale, dropout_p, seed, offset, out, lse, stream=None) -> None:
+    """Call ffpa_fwd_dropout (the forward with dropout on P); raises FfpaError on a non-zero status."""
+    lib = load()
+    check_devices((q, k, v, bias, out, lse), _current_device())
+    ds = [describe(q), describe(k), describe(v), describe(bias), describe(out), describe(lse, as_lse=True)]
+    rc = lib.ffpa_fwd_dropout(_ref(ds[0]), _ref(ds[1]), _ref(ds[2]), _ref(ds[3]), int(causal), float(scale),
+                              float(dropout_p), int(seed), int(offset), _ref(ds[4]), _ref(ds[5]), _stream(stream))
+    _raise(rc)
+
+
+def ffpa_bwd_dropout(q, k, v, bias, causal, scale, dropout_p, seed, offset, out, lse, dout, dq, dk, dv,
+                     stream=None) -> None:
+    """Call ffpa_bwd_dropout (the backward of ffpa_fwd_dropout with the same p, seed and offset)."""
+    lib = load()
+    check_devices((q, k, v, bias, out, lse, dout, dq, dk, dv), _current_device())
+    ds = [describe(x) for x in (q, k, v, bias, out)] + [describe(lse, as_lse=True)] + \
+        [describe(x) for x in (dout, dq, dk, dv)]
+    rc = lib.ffpa_bwd_dropout(*[_ref(x) for x in ds[:4]], int(causal), float(scale), float(dropout_p), int(seed),
+                              int(offset), *[_ref(x) for x in ds[4:]], _stream(stream))
     _raise(rc)
 
 

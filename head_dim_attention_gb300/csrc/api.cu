@@ -1,6 +1,7 @@
 // C ABI: argument validation, TMA descriptor encoding and dispatch.
 // Every check runs on the host before anything is enqueued; on failure the
 // call returns a status and launches nothing.
+#include <algorithm>
 #include <cmath>
 #include <cstring>
 #include <mutex>
@@ -257,13 +258,47 @@ constexpr float kLog2e = 1.4426950408889634f;
 
 using namespace ffpa;
 
-extern "C" int ffpa_fwd(const ffpa_tensor_t* q, const ffpa_tensor_t* k, const ffpa_tensor_t* v,
-                        const ffpa_tensor_t* bias, int causal, float scale, const ffpa_tensor_t* out,
-                        const ffpa_tensor_t* lse, ffpa_stream_t stream) {
+namespace {
+
+// Dropout arguments as the entry points take them; p == 0 is no dropout.
+struct DropArgs {
+  double p;
+  uint64_t seed;
+  uint32_t offset;
+};
+
+// Checks p (0 <= p < 1) and derives the kernels' parameters: the 16-bit keep
+// threshold round(p * 65536) (at most 65535) and the multiplier 1 / (1 - p).
+int drop_params(const DropArgs* d, int* on, uint32_t* t, uint32_t* seed_lo, uint32_t* seed_hi, uint32_t* off,
+                float* scale) {
+  *on = 0;
+  *t = 0;
+  *seed_lo = *seed_hi = *off = 0;
+  *scale = 1.f;
+  if (!d) return FFPA_OK;
+  if (!(d->p >= 0.0 && d->p < 1.0)) return FFPA_ERR_INVALID_ARG;
+  if (d->p == 0.0) return FFPA_OK;
+  *on = 1;
+  *t = static_cast<uint32_t>(std::min(65535.0, std::floor(d->p * 65536.0 + 0.5)));
+  *seed_lo = static_cast<uint32_t>(d->seed);
+  *seed_hi = static_cast<uint32_t>(d->seed >> 32);
+  *off = d->offset;
+  *scale = static_cast<float>(1.0 / (1.0 - d->p));
+  return FFPA_OK;
+}
+
+int fwd_impl(const ffpa_tensor_t* q, const ffpa_tensor_t* k, const ffpa_tensor_t* v, const ffpa_tensor_t* bias,
+             int causal, float scale, const DropArgs* drop, const ffpa_tensor_t* out, const ffpa_tensor_t* lse,
+             ffpa_stream_t stream) {
   Common c;
   int rc = check_common(q, k, v, bias, scale, &c);
   if (rc) return rc;
   if (causal != 0 && causal != 1) return FFPA_ERR_INVALID_ARG;
+  int dropout;
+  uint32_t drop_t, seed_lo, seed_hi, drop_off;
+  float drop_scale;
+  if ((rc = drop_params(drop, &dropout, &drop_t, &seed_lo, &seed_hi, &drop_off, &drop_scale))) return rc;
+  if (dropout && c.D < 320) return FFPA_ERR_UNSUPPORTED;  // dropout: the D = 320 .. 1024 kernels
   rc = check_bhnd(out, c.dtype, {c.B, c.Hq, c.Nq, c.D});
   if (rc) return rc;
   if (lse && (rc = check_lse(lse, c))) return rc;
@@ -275,7 +310,7 @@ extern "C" int ffpa_fwd(const ffpa_tensor_t* q, const ffpa_tensor_t* k, const ff
   bias_strides(bias, &bsb, &bsh, &bsq, &bsk);
   timing_begin();
 
-  if (c.Nq <= kDecodeMaxRows) {
+  if (c.Nq <= kDecodeMaxRows && !dropout) {
     DecodeParams p = {};
     p.q = q->data;
     p.k = k->data;
@@ -324,6 +359,9 @@ extern "C" int ffpa_fwd(const ffpa_tensor_t* q, const ffpa_tensor_t* k, const ff
   p.n_chunks = (int)(c.D / kChunk);
   p.q_tiles = (int)((c.Nq + kTileRows - 1) / kTileRows);
   p.status = status;
+  p.dropout = dropout;
+  p.drop_t = drop_t; p.drop_seed_lo = seed_lo; p.drop_seed_hi = seed_hi; p.drop_off = drop_off;
+  p.drop_scale = drop_scale;
   FwdMaps m;
   if ((rc = encode_map(&m.q, q)) || (rc = encode_map(&m.k, k)) || (rc = encode_map(&m.v, v)) ||
       (rc = encode_map(&m.k_half, k, kTileRows / 2)) || (rc = encode_map(&m.q_half, q, kTileRows / 2)))
@@ -359,14 +397,19 @@ extern "C" int ffpa_fwd(const ffpa_tensor_t* q, const ffpa_tensor_t* k, const ff
   return cuda_rc(launch_fwd_main(p, m, bf16, st));
 }
 
-extern "C" int ffpa_bwd(const ffpa_tensor_t* q, const ffpa_tensor_t* k, const ffpa_tensor_t* v,
-                        const ffpa_tensor_t* bias, int causal, float scale, const ffpa_tensor_t* out,
-                        const ffpa_tensor_t* lse, const ffpa_tensor_t* dout, const ffpa_tensor_t* dq,
-                        const ffpa_tensor_t* dk, const ffpa_tensor_t* dv, ffpa_stream_t stream) {
+int bwd_impl(const ffpa_tensor_t* q, const ffpa_tensor_t* k, const ffpa_tensor_t* v, const ffpa_tensor_t* bias,
+             int causal, float scale, const DropArgs* drop, const ffpa_tensor_t* out, const ffpa_tensor_t* lse,
+             const ffpa_tensor_t* dout, const ffpa_tensor_t* dq, const ffpa_tensor_t* dk, const ffpa_tensor_t* dv,
+             ffpa_stream_t stream) {
   Common c;
   int rc = check_common(q, k, v, bias, scale, &c);
   if (rc) return rc;
   if (causal != 0 && causal != 1) return FFPA_ERR_INVALID_ARG;
+  int dropout;
+  uint32_t drop_t, seed_lo, seed_hi, drop_off;
+  float drop_scale;
+  if ((rc = drop_params(drop, &dropout, &drop_t, &seed_lo, &seed_hi, &drop_off, &drop_scale))) return rc;
+  if (dropout && c.D < 320) return FFPA_ERR_UNSUPPORTED;
   if ((rc = check_bhnd(out, c.dtype, {c.B, c.Hq, c.Nq, c.D}))) return rc;
   if ((rc = check_bhnd(dout, c.dtype, {c.B, c.Hq, c.Nq, c.D}))) return rc;
   if ((rc = check_bhnd(dq, c.dtype, {c.B, c.Hq, c.Nq, c.D}))) return rc;
@@ -408,6 +451,9 @@ extern "C" int ffpa_bwd(const ffpa_tensor_t* q, const ffpa_tensor_t* k, const ff
   p.q_tiles = (int)((c.Nq + kTileRows - 1) / kTileRows);
   p.kv_tiles = (int)((c.Nkv + kTileRows - 1) / kTileRows);
   p.status = status;
+  p.dropout = dropout;
+  p.drop_t = drop_t; p.drop_seed_lo = seed_lo; p.drop_seed_hi = seed_hi; p.drop_off = drop_off;
+  p.drop_scale = drop_scale;
   BwdMaps m;
   if ((rc = encode_map(&m.q, q)) || (rc = encode_map(&m.k, k)) || (rc = encode_map(&m.v, v)) ||
       (rc = encode_map(&m.dout, dout)) || (rc = encode_map(&m.q_half, q, kTileRows / 2)) ||
@@ -423,6 +469,38 @@ extern "C" int ffpa_bwd(const ffpa_tensor_t* q, const ffpa_tensor_t* k, const ff
   cudaError_t e = launch_bwd(p, m, dtype_is_bf16(c.dtype), st);
   cudaError_t e2 = cudaFreeAsync(scratch, st);
   return cuda_rc(e != cudaSuccess ? e : e2);
+}
+
+}  // namespace
+
+extern "C" int ffpa_fwd(const ffpa_tensor_t* q, const ffpa_tensor_t* k, const ffpa_tensor_t* v,
+                        const ffpa_tensor_t* bias, int causal, float scale, const ffpa_tensor_t* out,
+                        const ffpa_tensor_t* lse, ffpa_stream_t stream) {
+  return fwd_impl(q, k, v, bias, causal, scale, nullptr, out, lse, stream);
+}
+
+extern "C" int ffpa_fwd_dropout(const ffpa_tensor_t* q, const ffpa_tensor_t* k, const ffpa_tensor_t* v,
+                                const ffpa_tensor_t* bias, int causal, float scale, double dropout_p,
+                                uint64_t seed, uint32_t offset, const ffpa_tensor_t* out, const ffpa_tensor_t* lse,
+                                ffpa_stream_t stream) {
+  const DropArgs d = {dropout_p, seed, offset};
+  return fwd_impl(q, k, v, bias, causal, scale, &d, out, lse, stream);
+}
+
+extern "C" int ffpa_bwd(const ffpa_tensor_t* q, const ffpa_tensor_t* k, const ffpa_tensor_t* v,
+                        const ffpa_tensor_t* bias, int causal, float scale, const ffpa_tensor_t* out,
+                        const ffpa_tensor_t* lse, const ffpa_tensor_t* dout, const ffpa_tensor_t* dq,
+                        const ffpa_tensor_t* dk, const ffpa_tensor_t* dv, ffpa_stream_t stream) {
+  return bwd_impl(q, k, v, bias, causal, scale, nullptr, out, lse, dout, dq, dk, dv, stream);
+}
+
+extern "C" int ffpa_bwd_dropout(const ffpa_tensor_t* q, const ffpa_tensor_t* k, const ffpa_tensor_t* v,
+                                const ffpa_tensor_t* bias, int causal, float scale, double dropout_p,
+                                uint64_t seed, uint32_t offset, const ffpa_tensor_t* out, const ffpa_tensor_t* lse,
+                                const ffpa_tensor_t* dout, const ffpa_tensor_t* dq, const ffpa_tensor_t* dk,
+                                const ffpa_tensor_t* dv, ffpa_stream_t stream) {
+  const DropArgs d = {dropout_p, seed, offset};
+  return bwd_impl(q, k, v, bias, causal, scale, &d, out, lse, dout, dq, dk, dv, stream);
 }
 
 // Decode without allocation: validation and parameters as ffpa_fwd's decode

@@ -49,6 +49,7 @@
 #include <type_traits>
 
 #include "internal.h"
+#include "philox.cuh"
 #include "ptx.cuh"
 
 namespace ffpa {
@@ -131,7 +132,7 @@ __device__ __forceinline__ int column(const Geo& g, int c) {
   return c * kTileRows;
 }
 
-template <int NC, bool BF16>
+template <int NC, bool BF16, bool DROP>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_dq_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant__ CUtensorMap map_qh,
                   const __grid_constant__ CUtensorMap map_kh, const __grid_constant__ CUtensorMap map_vh,
@@ -379,6 +380,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       lse2_row = p.lse2[idx];
       delta_row = p.delta[idx];
     }
+    const DropKey dkey = {p.drop_seed_lo, p.drop_seed_hi, static_cast<uint32_t>(g.b * p.Hq + g.h), p.drop_off,
+                          p.drop_t};
     bool ok = true;
     auto arrive_free = [&](uint32_t a) {  // "X consumed": no data hand-off
       if (rank == 0)
@@ -401,6 +404,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int cbase = column(g, c) + 64 * u;  // first key of this thread's half
       bool plain = srow < p.Nq && cbase + 64 <= p.Nkv && (!p.causal || cbase + 63 <= srow) && lse2_row > -INFINITY;
       plain = __all_sync(0xffffffffu, plain) && p.bias == nullptr;
+      // dropout: the keep bits of this thread's 64 keys, drawn while S is computed
+      uint32_t keep_lo = 0, keep_hi = 0;
+      if constexpr (DROP) keep64_row(dkey, cbase, srow, keep_lo, keep_hi);
 
       ok = __all_sync(0xffffffffu, mbar_wait(bar(bl.x1_full), c & 1, status));
       if (!ok) break;
@@ -438,8 +444,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_before();
         __syncwarp();
         if (lane == 0) arrive_free(x2_free_lead);
+        if constexpr (DROP) {
+          // dP of the dropped output: dO V^T times keep / (1 - p)
 #pragma unroll
-        for (int e = 0; e < 64; ++e) pv[e] *= dp[e] - delta_row;
+          for (int e = 0; e < 64; ++e) {
+            const bool kept = (((e < 32 ? keep_lo : keep_hi) >> (e & 31)) & 1u) != 0;
+            pv[e] *= (kept ? dp[e] * p.drop_scale : 0.f) - delta_row;
+          }
+        } else {
+#pragma unroll
+          for (int e = 0; e < 64; ++e) pv[e] *= dp[e] - delta_row;
+        }
       }
       uint32_t w[32];
 #pragma unroll
@@ -524,7 +539,7 @@ cudaError_t launch_impl(const BwdParams& p, const BwdMaps& m, cudaStream_t st) {
   constexpr int smem = smem_bytes(NC);
   static_assert(smem <= 232448, "shared memory per CTA");
   static_assert(grad_cols(NC) <= 256, "dQ below the score buffers");
-  auto kern = bwd_dq_kernel<NC, BF16>;
+  auto kern = p.dropout ? bwd_dq_kernel<NC, BF16, true> : bwd_dq_kernel<NC, BF16, false>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};

@@ -61,6 +61,7 @@
 #include <type_traits>
 
 #include "internal.h"
+#include "philox.cuh"
 #include "ptx.cuh"
 
 namespace ffpa {
@@ -106,12 +107,12 @@ struct Shape {
 
 struct Bars {
   int full_x, empty_x, full_g, empty_g, res_full, x_full, x_free, pt_full, pt_peer, pt_free, ds_full, ds_peer,
-      ds_free, st_ready, st_local, st_free, drain_x, drain_g, g_done, count;
+      ds_free, st_ready, st_local, st_free, pm_ready, pm_local, drain_x, drain_g, g_done, count;
 };
 // rings: up to three slots; x_full, x_free, st_*: one per TMEM score buffer or
-// staging tile; pt_*, ds_*: one per receive buffer (up to three)
+// staging tile; pt_*, ds_*, pm_*: one per receive buffer (up to three)
 __host__ __device__ constexpr Bars bar_layout() {
-  return Bars{0, 3, 6, 9, 12, 13, 15, 17, 20, 23, 26, 29, 32, 35, 37, 39, 41, 42, 43, 44};
+  return Bars{0, 3, 6, 9, 12, 13, 15, 17, 20, 23, 26, 29, 32, 35, 37, 39, 41, 44, 47, 48, 49, 50};
 }
 static_assert(bar_layout().count * 8 + 16 <= 512, "barrier area");
 
@@ -211,7 +212,7 @@ __device__ __forceinline__ void column(const Geo& g, const BwdParams& p, int c, 
   }
 }
 
-template <int MODE, int NC, bool BF16>
+template <int MODE, int NC, bool BF16, bool DROP>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_xch_kernel(const __grid_constant__ CUtensorMap map_qh, const __grid_constant__ CUtensorMap map_kh,
                    const __grid_constant__ CUtensorMap map_vh, const __grid_constant__ CUtensorMap map_doh,
@@ -269,6 +270,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar(bl.ds_full + i), 1);
       mbar_init(bar(bl.ds_peer + i), 1);
       mbar_init(bar(bl.ds_free + i), 1);  // pair A's gradient commit
+      mbar_init(bar(bl.pm_ready + i), 5);  // dropout, dK/dV mode, pair B: four local warps + the relay
+      mbar_init(bar(bl.pm_local + i), 4);  // (second CTA) its four elementwise warps
     }
     mbar_init(bar(bl.drain_x), 1);
     mbar_init(bar(bl.drain_g), 1);
@@ -425,6 +428,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (c + kNrecv < ncols) mbar_expect_tx(bar(rfull + rb), kTileX);  // the buffer's next use
         ok = mbar_wait(bar(rpeer + rb), use & 1, status);
         if (!ok) break;
+        if (DROP && !DQ && is_b) {
+          // dropout: both CTAs' elementwise warps have zeroed the dropped P^T entries in place
+          ok = mbar_wait(bar(bl.pm_ready + rb), use & 1, status);
+          if (!ok) break;
+        }
         da = sdesc_advance(drecv, rb * kTileX);
       }
       tc_fence_after();
@@ -469,6 +477,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!mbar_wait(bar(rfull + rb), use & 1, status)) break;
         if (c + kNrecv < ncols) mbar_expect_tx(bar(rfull + rb), kTileX);
         mbar_arrive_remote(lead(rpeer + rb));  // release.cluster: the tile is visible to the first CTA's MMAs
+        if (DROP && !DQ && is_b) {  // and, with dropout, once this CTA's warps have masked it
+          if (!mbar_wait(bar(bl.pm_local + rb), use & 1, status)) break;
+          mbar_arrive_remote(lead(bl.pm_ready + rb));
+        }
       }
     }
   } else if (warp >= 4) {
@@ -546,6 +558,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       // statistic of column e of this thread's half (per query row: the column
       // in dK/dV mode, this thread's row in dQ mode)
       auto stat = [&](int e) { return DQ ? row_stat : __shfl_sync(0xffffffffu, cs[e >> 5], e & 31); };
+      // dropout, pair A: the keep bits of this thread's 64 scores (query head
+      // hs in dQ mode, the column's query head in dK/dV mode), drawn while the
+      // score product runs; bit e for column e
+      uint32_t keep_lo = 0, keep_hi = 0;
+      if constexpr (DROP) {
+        if (!is_b) {
+          DropKey dk = {p.drop_seed_lo, p.drop_seed_hi, static_cast<uint32_t>(g.b * p.Hq + (DQ ? g.hs : ch)),
+                        p.drop_off, p.drop_t};
+          if (DQ)
+            keep64_row(dk, cbase, srow, keep_lo, keep_hi);
+          else
+            keep64_col(dk, g.s_row0 + 32 * (w & 1), cbase, lane, keep_lo, keep_hi);
+        }
+      }
       ok = __all_sync(0xffffffffu, mbar_wait(bar(bl.x_full + (c & 1)), (c >> 1) & 1, status));
       if (!ok) break;
       tc_fence_after();
@@ -598,6 +624,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             xv[e] = valid ? ex2(xx) : 0.f;
           }
         }
+        if constexpr (DROP) {
+          // a dropped probability travels with its sign bit set
+#pragma unroll
+          for (int e = 0; e < 64; ++e)
+            if (!(((e < 32 ? keep_lo : keep_hi) >> (e & 31)) & 1u)) xv[e] = -xv[e];
+        }
 #pragma unroll
         for (int e = 0; e < 32; ++e) wds[e] = pack2<BF16>(xv[2 * e], xv[2 * e + 1]);
       } else {
@@ -611,12 +643,32 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int gq = 0; gq < 8; ++gq) {
           const uint4 v = ld_shared_v4(swz(pt, r, gq));
           const uint32_t pw[4] = {v.x, v.y, v.z, v.w};
+          uint32_t pm[4];
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
             const int e = 8 * gq + 2 * q;
-            const float2 pp = unpack2<BF16>(pw[q]);
-            wds[4 * gq + q] = pack2<BF16>(pp.x * (xv[e] - stat(e)), pp.y * (xv[e + 1] - stat(e + 1)));
+            if constexpr (DROP) {
+              // dropout: the sign bit marks a dropped probability; dP of the
+              // dropped output is dO V^T times keep / (1 - p)
+              const uint32_t wq = pw[q];
+              const float2 pp = unpack2<BF16>(wq & 0x7FFF7FFFu);
+              const float d0 = (wq & 0x8000u) ? 0.f : xv[e] * p.drop_scale;
+              const float d1 = (wq & 0x80000000u) ? 0.f : xv[e + 1] * p.drop_scale;
+              wds[4 * gq + q] = pack2<BF16>(pp.x * (d0 - stat(e)), pp.y * (d1 - stat(e + 1)));
+              pm[q] = wq & ~(((wq >> 15) & 0x00010001u) * 0xFFFFu);  // dropped entries -> +0
+            } else {
+              const float2 pp = unpack2<BF16>(pw[q]);
+              wds[4 * gq + q] = pack2<BF16>(pp.x * (xv[e] - stat(e)), pp.y * (xv[e + 1] - stat(e + 1)));
+              pm[q] = 0u;
+            }
           }
+          // dK/dV mode with dropout: dV's MMAs read P^T with the dropped entries zeroed
+          if (DROP && !DQ) st_shared_v4(swz(pt, r, gq), pm[0], pm[1], pm[2], pm[3]);
+        }
+        if (DROP && !DQ) {
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar((pr == 0 ? bl.pm_ready : bl.pm_local) + rb));
         }
         __syncwarp();
         // P has been read into registers: pair A may refill this buffer once
@@ -687,7 +739,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         } else {
           dst_base = reinterpret_cast<T*>(p.dk); sb = p.dk_sb; sh = p.dk_sh; sn = p.dk_sn;
         }
-        const float mul = (!DQ && is_b) ? 1.f : p.scale;
+        const float mul = (!DQ && is_b) ? (DROP ? p.drop_scale : 1.f) : p.scale;  // dV: kept P carries 1 / (1 - p)
         T* orow = dst_base + g.b * sb + g.hs * sh + static_cast<int64_t>(srow) * sn;
         const int gcols = 128 + 64 * g.nv1;  // TMEM columns of the gradient per lane
         for (int k = 0; k < gcols / 32; ++k) {
@@ -735,7 +787,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 template <int MODE, int NC, bool BF16>
 cudaError_t launch_impl(const BwdParams& p, const BwdMaps& m, cudaStream_t st) {
   constexpr int smem = Shape<NC>::kSmemBytes;
-  auto kern = bwd_xch_kernel<MODE, NC, BF16>;
+  auto kern = p.dropout ? bwd_xch_kernel<MODE, NC, BF16, true> : bwd_xch_kernel<MODE, NC, BF16, false>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};

@@ -50,6 +50,7 @@
 #include <type_traits>
 
 #include "internal.h"
+#include "philox.cuh"
 #include "ptx.cuh"
 
 namespace ffpa {
@@ -162,7 +163,7 @@ __device__ __forceinline__ bool pair_bar_and(uint32_t id, bool v) {
   return r != 0;
 }
 
-template <int NC, bool BF16, bool KSPLIT>
+template <int NC, bool BF16, bool KSPLIT, bool DROP>
 __global__ void __launch_bounds__(kThreads, 1)
     fwd_fulld_kernel(const __grid_constant__ CUtensorMap map_qh, const __grid_constant__ CUtensorMap map_kh,
                      const __grid_constant__ CUtensorMap map_v, const __grid_constant__ FwdParams p) {
@@ -398,6 +399,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_off = static_cast<uint32_t>((warp - 4) * 32) << 16;
     const uint32_t nb = 1 + ((warp - 4) & 1);  // named barrier of warps w and w ^ 2 (lanes t and t ^ 64)
     const float* bias_row = nullptr;
+    const DropKey dkey = {p.drop_seed_lo, p.drop_seed_hi, static_cast<uint32_t>(b * p.Hq + h), p.drop_off,
+                          p.drop_t};
     if (p.bias)
       bias_row = p.bias + b * p.bias_sb + h * p.bias_sh + static_cast<int64_t>(min(row, p.Nq - 1)) * p.bias_sq;
     constexpr float kLog2e = 1.4426950408889634f;
@@ -445,6 +448,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         prefetch_l1(bias_row + min(kv0 + 32, p.Nkv - 1));
         prefetch_l1(bias_row + min(kv0 + 63, p.Nkv - 1));
       }
+      // dropout: the keep bits of this thread's 64 keys, drawn while S is computed
+      uint32_t keep_lo = 0, keep_hi = 0;
+      if constexpr (DROP) keep64_row(dkey, kv0, row, keep_lo, keep_hi);
       const bool got = __all_sync(0xffffffffu, mbar_wait(bar(bl.s_full + (j & 1)), (j >> 1) & 1, status));
       float s[64];
       if (got) {
@@ -534,7 +540,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t hi[32], lo[32];
 #pragma unroll
       for (int e = 0; e < 32; ++e) {
-        const float p0 = s[2 * e], p1 = s[2 * e + 1];
+        float p0 = s[2 * e], p1 = s[2 * e + 1];
+        if constexpr (DROP) {  // dropped probabilities leave P V (the row sum above keeps them)
+          const uint32_t kb = (e < 16 ? keep_lo : keep_hi) >> ((2 * e) & 31);
+          p0 = (kb & 1u) ? p0 : 0.f;
+          p1 = (kb & 2u) ? p1 : 0.f;
+        }
         hi[e] = pack2<BF16>(p0, p1);
         if (warp_lo) {
           const float2 hv = unpack2<BF16>(hi[e]);
@@ -638,7 +649,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       } else {
       if (ok) {
         tc_fence_after();
-        const float inv_l = l_sum > 0.f ? 1.f / l_sum : 0.f;
+        // dropout: kept probabilities carry 1 / (1 - p)
+        const float inv_l = l_sum > 0.f ? (DROP ? p.drop_scale : 1.f) / l_sum : 0.f;
         typedef typename std::conditional<BF16, __nv_bfloat16, __half>::type T;
         T* orow = reinterpret_cast<T*>(p.out) + b * p.o_sb + h * p.o_sh + static_cast<int64_t>(row) * p.o_sn;
         for (int c = 0; c < kOCols / 32; ++c) {
@@ -702,7 +714,9 @@ cudaError_t launch_impl(const FwdParams& p_in, const FwdMaps& m, cudaStream_t st
   FwdParams p = p_in;
   p.stages = kKSlots + Shape<NC>::kVSlots;
   p.slot_chunks = 2;
-  auto kern = p.part_o ? fwd_fulld_kernel<NC, BF16, true> : fwd_fulld_kernel<NC, BF16, false>;
+  // key splits and dropout are not combined (the host takes no key split with dropout)
+  auto kern = p.part_o ? fwd_fulld_kernel<NC, BF16, true, false>
+                       : (p.dropout ? fwd_fulld_kernel<NC, BF16, false, true> : fwd_fulld_kernel<NC, BF16, false, false>);
   constexpr int kNsplit = Shape<NC>::kNsplit;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   if (e != cudaSuccess) return e;
@@ -738,6 +752,10 @@ bool fwd_fulld_supported(const FwdParams& p) { return p.n_chunks >= 5 && p.n_chu
 // split at least two key tiles long.  Returns the split count (1: none) and
 // the key tiles per split.
 int fwd_fulld_kv_splits(const FwdParams& p, int sms, int* tiles_per_split) {
+  if (p.dropout) {  // no key-split form of the dropout kernel
+    *tiles_per_split = (p.Nkv + kTileRows - 1) / kTileRows;
+    return 1;
+  }
   int nsplit = 1;
   switch (p.n_chunks) {
     case 9: nsplit = Shape<9>::kNsplit; break;

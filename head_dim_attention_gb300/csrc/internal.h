@@ -43,6 +43,11 @@ struct FwdParams {
   int kv_splits, kv_split_tiles;
   float* part_o;      // [B, Hq, Nq, kv_splits, D] fp32
   float* part_ml;     // [B, Hq, Nq, kv_splits, 2] fp32 (max, sum), log2 domain
+  // dropout (philox.cuh): on when `dropout` is set; keep threshold, seed words,
+  // stream offset and the multiplier 1 / (1 - p) of kept probabilities
+  int dropout;
+  uint32_t drop_t, drop_seed_lo, drop_seed_hi, drop_off;
+  float drop_scale;
 };
 
 struct FwdMaps {
@@ -109,6 +114,10 @@ struct BwdParams {
   int slot_chunks;    // 16 KB tiles per ring slot (1 or 2), loaded under one barrier phase
   int q_tiles, kv_tiles;
   uint32_t* status;
+  // dropout, as in FwdParams
+  int dropout;
+  uint32_t drop_t, drop_seed_lo, drop_seed_hi, drop_off;
+  float drop_scale;
 };
 
 struct BwdMaps {

@@ -117,6 +117,37 @@ int ffpa_bwd(const ffpa_tensor_t* q, const ffpa_tensor_t* k, const ffpa_tensor_t
              const ffpa_tensor_t* dk, const ffpa_tensor_t* dv, ffpa_stream_t stream);
 
 /*
+ * ffpa_fwd_dropout / ffpa_bwd_dropout: ffpa_fwd and ffpa_bwd with dropout on
+ * the attention probabilities (the "dropout" rows of the FFPA Attention
+ * Benchmark page's "More Benchmark" tables).  Arguments as in ffpa_fwd /
+ * ffpa_bwd, plus:
+ *   dropout_p  drop probability, 0 <= p < 1 (else FFPA_ERR_INVALID_ARG);
+ *              p == 0 is the call without dropout
+ *   seed       64-bit generator key
+ *   offset     32-bit stream index (e.g. a step counter)
+ * The forward computes O = (P * Z) V with Z = keep / (1 - p) and the lse of
+ * the undropped scores; the backward, given the same (p, seed, offset),
+ * returns the gradients of that function for the same keep mask.  Keep mask:
+ * for query row i and key j of query head h in batch b, Philox4x32-10 (ten
+ * rounds of four 32-bit words, Salmon et al., SC 2011) runs on counter
+ * (j / 8, i, b * Hq + h, offset) with key (seed & 0xffffffff, seed >> 32);
+ * score (i, j) reads 16-bit field j % 2 of output word (j % 8) / 2 and is kept
+ * when that value is at least t = min(65535, floor(p * 65536 + 1/2)).
+ * The pages give no generator; this contract is the library's.  Dropout runs
+ * on the D = 320 .. 1024 kernels only (FFPA_ERR_UNSUPPORTED for D <= 256),
+ * with neither the decode path nor key splits (every Nq takes the fused
+ * kernel).
+ */
+int ffpa_fwd_dropout(const ffpa_tensor_t* q, const ffpa_tensor_t* k, const ffpa_tensor_t* v,
+                     const ffpa_tensor_t* bias, int causal, float scale, double dropout_p, uint64_t seed,
+                     uint32_t offset, const ffpa_tensor_t* out, const ffpa_tensor_t* lse, ffpa_stream_t stream);
+int ffpa_bwd_dropout(const ffpa_tensor_t* q, const ffpa_tensor_t* k, const ffpa_tensor_t* v,
+                     const ffpa_tensor_t* bias, int causal, float scale, double dropout_p, uint64_t seed,
+                     uint32_t offset, const ffpa_tensor_t* out, const ffpa_tensor_t* lse,
+                     const ffpa_tensor_t* dout, const ffpa_tensor_t* dq, const ffpa_tensor_t* dk,
+                     const ffpa_tensor_t* dv, ffpa_stream_t stream);
+
+/*
  * ffpa_fwd_decode_noalloc: the decode forward (Nq <= 16) without allocating.
  * The pages have no counterpart; it exists for callers that cannot allocate
  * device memory during the call: code running under another framework's

@@ -9,6 +9,8 @@ Tolerances are the ones the task fixes for this method:
             causal diagonal block) cannot hide under the whole tensor's norm;
             a tile whose exact gradient is zero (keys no query sees) must come
             back zero
+With dropout (``dropout=(p, seed, offset)``) both sides draw the keep mask
+from the same Philox contract; the same tolerances apply.
 """
 from __future__ import annotations
 
@@ -73,33 +75,42 @@ def _row_padded(t, pad, dev):
     return wide[..., : t.shape[-1]]
 
 
-def gpu_fwd(inp, causal, scale, kv_row_pad=0):
+def _drop_kw(dropout):
+    if dropout is None:
+        return {}
+    p, seed, offset = dropout
+    return {"dropout_p": p, "seed": seed, "offset": offset}
+
+
+def gpu_fwd(inp, causal, scale, kv_row_pad=0, dropout=None):
     dev = torch.device("cuda")
     q = inp.q.to(dev)
     k, v = _row_padded(inp.k, kv_row_pad, dev), _row_padded(inp.v, kv_row_pad, dev)
     bias = None if inp.bias is None else inp.bias.to(dev)
-    out, lse = attention_fwd(q, k, v, bias=bias, causal=causal, scale=scale)
+    out, lse = attention_fwd(q, k, v, bias=bias, causal=causal, scale=scale, **_drop_kw(dropout))
     torch.cuda.synchronize()
     assert ffpa_check_status() == 0
     return out, lse
 
 
-def check_fwd_full(B, Hq, Hkv, Nq, Nkv, D, dtype, causal=False, bias=False, seed=0, scale=None, kv_row_pad=0):
+def check_fwd_full(B, Hq, Hkv, Nq, Nkv, D, dtype, causal=False, bias=False, seed=0, scale=None, kv_row_pad=0,
+                   dropout=None):
     inp = make_inputs(B, Hq, Hkv, Nq, Nkv, D, dtype, bias=bias, seed=seed)
     scale = D ** -0.5 if scale is None else scale
-    out, lse = gpu_fwd(inp, causal, scale, kv_row_pad)
+    out, lse = gpu_fwd(inp, causal, scale, kv_row_pad, dropout=dropout)
     o_ref, lse_ref = ref.attn_fwd(f64(inp.q), f64(inp.k), f64(inp.v), bias=f64(inp.bias), causal=causal,
-                                  scale=scale)
+                                  scale=scale, dropout=dropout)
     atol, rtol = TOL[dtype]
     assert_close(out.float().cpu().numpy(), o_ref, atol, rtol, "O")
     assert_close(lse.cpu().numpy(), lse_ref, LSE_ATOL, 0.0, "lse")
 
 
-def check_fwd_sampled(B, Hq, Hkv, Nq, Nkv, D, dtype, causal=False, bias=False, rows=64, seed=0, scale=None):
+def check_fwd_sampled(B, Hq, Hkv, Nq, Nkv, D, dtype, causal=False, bias=False, rows=64, seed=0, scale=None,
+                      dropout=None):
     """Large shapes: the oracle computes `rows` seeded query rows per head, one by one."""
     inp = make_inputs(B, Hq, Hkv, Nq, Nkv, D, dtype, bias=bias, seed=seed)
     scale = D ** -0.5 if scale is None else scale
-    out, lse = gpu_fwd(inp, causal, scale)
+    out, lse = gpu_fwd(inp, causal, scale, dropout=dropout)
     out = out.float().cpu().numpy()
     lse = lse.cpu().numpy()
     q, k, v, bb = f64(inp.q), f64(inp.k), f64(inp.v), f64(inp.bias)
@@ -107,29 +118,30 @@ def check_fwd_sampled(B, Hq, Hkv, Nq, Nkv, D, dtype, causal=False, bias=False, r
     for b in range(B):
         for h in range(Hq):
             r = ref.sample_rows(Nq, rows, 1000 + h)
-            o_ref, lse_ref = ref.attn_fwd_rows(q, k, v, b, h, r, bias=bb, causal=causal, scale=scale)
+            o_ref, lse_ref = ref.attn_fwd_rows(q, k, v, b, h, r, bias=bb, causal=causal, scale=scale,
+                                               dropout=dropout)
             assert_close(out[b, h, r], o_ref, atol, rtol, f"O[b={b},h={h}]")
             assert_close(lse[b, h, r], lse_ref, LSE_ATOL, 0.0, f"lse[b={b},h={h}]")
     return out, lse
 
 
-def gpu_fwd_bwd(inp, causal, scale):
+def gpu_fwd_bwd(inp, causal, scale, dropout=None):
     dev = torch.device("cuda")
     q, k, v, do = inp.q.to(dev), inp.k.to(dev), inp.v.to(dev), inp.do.to(dev)
     bias = None if inp.bias is None else inp.bias.to(dev)
-    out, lse = attention_fwd(q, k, v, bias=bias, causal=causal, scale=scale)
-    dq, dk, dv = attention_bwd(q, k, v, out, lse, do, bias=bias, causal=causal, scale=scale)
+    out, lse = attention_fwd(q, k, v, bias=bias, causal=causal, scale=scale, **_drop_kw(dropout))
+    dq, dk, dv = attention_bwd(q, k, v, out, lse, do, bias=bias, causal=causal, scale=scale, **_drop_kw(dropout))
     torch.cuda.synchronize()
     assert ffpa_check_status() == 0
     return out, lse, dq, dk, dv
 
 
-def check_bwd_full(B, Hq, Hkv, Nq, Nkv, D, dtype, causal=False, bias=False, seed=0):
+def check_bwd_full(B, Hq, Hkv, Nq, Nkv, D, dtype, causal=False, bias=False, seed=0, dropout=None):
     inp = make_inputs(B, Hq, Hkv, Nq, Nkv, D, dtype, bias=bias, grad=True, seed=seed)
     scale = D ** -0.5
-    _, _, dq, dk, dv = gpu_fwd_bwd(inp, causal, scale)
+    _, _, dq, dk, dv = gpu_fwd_bwd(inp, causal, scale, dropout=dropout)
     gq, gk, gv = ref.attn_bwd(f64(inp.q), f64(inp.k), f64(inp.v), f64(inp.do), bias=f64(inp.bias),
-                              causal=causal, scale=scale)
+                              causal=causal, scale=scale, dropout=dropout)
     errs, tiles = {}, {}
     for name, gpu, want in (("dQ", dq, gq), ("dK", dk, gk), ("dV", dv, gv)):
         g = gpu.float().cpu().numpy()
@@ -142,10 +154,10 @@ def check_bwd_full(B, Hq, Hkv, Nq, Nkv, D, dtype, causal=False, bias=False, seed
     return errs
 
 
-def check_bwd_sampled(B, Hq, Hkv, Nq, Nkv, D, dtype, causal=False, bias=False, rows=64, seed=0):
+def check_bwd_sampled(B, Hq, Hkv, Nq, Nkv, D, dtype, causal=False, bias=False, rows=64, seed=0, dropout=None):
     inp = make_inputs(B, Hq, Hkv, Nq, Nkv, D, dtype, bias=bias, grad=True, seed=seed)
     scale = D ** -0.5
-    _, _, dq, dk, dv = gpu_fwd_bwd(inp, causal, scale)
+    _, _, dq, dk, dv = gpu_fwd_bwd(inp, causal, scale, dropout=dropout)
     dq, dk, dv = (x.float().cpu().numpy() for x in (dq, dk, dv))
     q, k, v, do, bb = f64(inp.q), f64(inp.k), f64(inp.v), f64(inp.do), f64(inp.bias)
     errs = {}
@@ -154,7 +166,8 @@ def check_bwd_sampled(B, Hq, Hkv, Nq, Nkv, D, dtype, causal=False, bias=False, r
             kr = ref.sample_rows(Nkv, rows, 2000 + g)
             group = Hq // Hkv
             qrows = {h: ref.sample_rows(Nq, rows, 1000 + h) for h in range(g * group, (g + 1) * group)}
-            sdq, sdk, sdv = ref.attn_bwd_sampled(q, k, v, do, b, g, qrows, kr, bias=bb, causal=causal, scale=scale)
+            sdq, sdk, sdv = ref.attn_bwd_sampled(q, k, v, do, b, g, qrows, kr, bias=bb, causal=causal, scale=scale,
+                                                 dropout=dropout)
             for h in qrows:
                 errs[f"dQ[{b},{h}]"] = rel_fro(dq[b, h, qrows[h]], sdq[h])
             errs[f"dK[{b},{g}]"] = rel_fro(dk[b, g, kr], sdk)
