@@ -309,7 +309,7 @@ def run_ffpa(args, rank, world):
 # DRAM bytes (read + write) per launch, dram__bytes_read.sum +
 # dram__bytes_write.sum from one ncu capture of the same workload; a kernel
 # changed since its capture is left out (its traffic is then reported as null).
-TRAFFIC: dict = {"fwd_main": 248862464, "bwd_dq": 322821376}
+TRAFFIC: dict = {"fwd_main": 246767104, "bwd_dkv": 372583808, "bwd_dq": 322819328}
 TRAFFIC_FROM = "ncu capture of the same workload (dram__bytes_read.sum + dram__bytes_write.sum per launch)"
 
 
@@ -320,7 +320,7 @@ def measure_variants(dev, peaks, iters=10, warmup=3):
     drawn on the device (the values do not change the work)."""
     import torch
 
-    from head_dim_attention_gb300 import ffpa_bwd, ffpa_fwd
+    from head_dim_attention_gb300 import ffpa_bwd, ffpa_bwd_dropout, ffpa_fwd, ffpa_fwd_dropout
 
     g = torch.Generator(device=dev)
     g.manual_seed(11)
@@ -343,20 +343,27 @@ def measure_variants(dev, peaks, iters=10, warmup=3):
 
     out_lines = {}
 
-    def case(name, b, hq, hkv, nq, nkv, d, dtype, causal=False, bias=False, backward=False):
+    def case(name, b, hq, hkv, nq, nkv, d, dtype, causal=False, bias=False, backward=False, dropout=0.0):
         q = rnd(b, hq, nq, d, dtype=dtype)
         k, v = rnd(b, hkv, nkv, d, dtype=dtype), rnd(b, hkv, nkv, d, dtype=dtype)
         bb = rnd(1, 1, 1, nkv, dtype=torch.float32) if bias else None
         out, lse = torch.empty_like(q), torch.empty(b, hq, nq, dtype=torch.float32, device=dev)
         sc = d ** -0.5
-        fwd = lambda: ffpa_fwd(q, k, v, bb, int(causal), sc, out, lse)  # noqa: E731
+        if dropout:
+            fwd = lambda: ffpa_fwd_dropout(q, k, v, bb, int(causal), sc, dropout, 7, 0, out, lse)  # noqa: E731
+        else:
+            fwd = lambda: ffpa_fwd(q, k, v, bb, int(causal), sc, out, lse)  # noqa: E731
         ms = median_ms(fwd)
         rec = {"fwd_ms": ms, "fwd_tflops": attention_flops(nq, nkv, d, b * hq, causal) / (ms / 1e3) / 1e12}
         if backward:
             do = rnd(b, hq, nq, d, dtype=dtype)
             dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
             fwd()
-            bms = median_ms(lambda: ffpa_bwd(q, k, v, bb, int(causal), sc, out, lse, do, dq, dk, dv))
+            if dropout:
+                bms = median_ms(lambda: ffpa_bwd_dropout(q, k, v, bb, int(causal), sc, dropout, 7, 0, out, lse, do,
+                                                         dq, dk, dv))
+            else:
+                bms = median_ms(lambda: ffpa_bwd(q, k, v, bb, int(causal), sc, out, lse, do, dq, dk, dv))
             rec["bwd_ms"] = bms
             rec["bwd_tflops"] = attention_flops(nq, nkv, d, b * hq, causal, backward=True) / (bms / 1e3) / 1e12
         for key in [kk for kk in rec if kk.endswith("tflops")]:
@@ -370,8 +377,9 @@ def measure_variants(dev, peaks, iters=10, warmup=3):
     case("nonaligned_N8191_D512_bf16", 1, 8, 8, 8191, 8191, 512, bf)
     case("cross_Nq1024_Nkv8192_bias_D512_bf16", 1, 8, 8, 1024, 8192, 512, bf, bias=True)
     case("short_Nq64_Nkv8192_D512_bf16", 1, 8, 8, 64, 8192, 512, bf)
+    case("dropout_p0.1_N8192_D512_bf16", 1, 8, 8, 8192, 8192, 512, bf, backward=True, dropout=0.1)
     for d in (320, 384, 448, 512, 576, 640, 768, 1024):
-        case(f"dsweep_N4096_D{d}_fp16", 1, 8, 8, 4096, 4096, d, fp)
+        case(f"dsweep_N4096_D{d}_fp16", 1, 8, 8, 4096, 4096, d, fp, backward=True)
     return {"peak": peaks["bf16_tflops"], "timing": "median of 10 calls after 3 warm-up calls, each timed alone "
             "with CUDA events; TFLOPS counted by the headline's rule (4 / 10 Nq Nkv D per head, halved "
             "when causal)", "cases": out_lines}

@@ -399,8 +399,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_off = static_cast<uint32_t>((warp - 4) * 32) << 16;
     const uint32_t nb = 1 + ((warp - 4) & 1);  // named barrier of warps w and w ^ 2 (lanes t and t ^ 64)
     const float* bias_row = nullptr;
-    const DropKey dkey = {p.drop_seed_lo, p.drop_seed_hi, static_cast<uint32_t>(b * p.Hq + h), p.drop_off,
-                          p.drop_t};
     if (p.bias)
       bias_row = p.bias + b * p.bias_sb + h * p.bias_sh + static_cast<int64_t>(min(row, p.Nq - 1)) * p.bias_sq;
     constexpr float kLog2e = 1.4426950408889634f;
@@ -450,7 +448,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       // dropout: the keep bits of this thread's 64 keys, drawn while S is computed
       uint32_t keep_lo = 0, keep_hi = 0;
-      if constexpr (DROP) keep64_row(dkey, kv0, row, keep_lo, keep_hi);
+      if constexpr (DROP) {
+        const DropKey dkey = {p.drop_seed_lo, p.drop_seed_hi, static_cast<uint32_t>(b * p.Hq + h), p.drop_off,
+                              p.drop_t};
+        keep64_row(dkey, kv0, row, keep_lo, keep_hi);
+      }
       const bool got = __all_sync(0xffffffffu, mbar_wait(bar(bl.s_full + (j & 1)), (j >> 1) & 1, status));
       float s[64];
       if (got) {

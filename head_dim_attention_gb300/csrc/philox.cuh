@@ -59,15 +59,16 @@ __device__ __forceinline__ uint32_t keep8(const DropKey& dk, uint32_t jb, uint32
 }
 
 // Keep bits of keys j0 .. j0 + 63 of query row i (j0 a multiple of 8): bit e
-// of lo (e < 32) or hi (e >= 32) for key j0 + e.
+// of lo (e < 32) or hi (e >= 32) for key j0 + e.  The eight generator calls
+// run in a loop that is not unrolled: eight inlined copies of the ten rounds
+// overflowed the instruction cache of the kernels that call this.
 __device__ __forceinline__ void keep64_row(const DropKey& dk, int j0, int i, uint32_t& lo, uint32_t& hi) {
-  lo = 0;
-  hi = 0;
-#pragma unroll
-  for (int g = 0; g < 4; ++g) {
-    lo |= keep8(dk, static_cast<uint32_t>(j0 / 8 + g), static_cast<uint32_t>(i)) << (8 * g);
-    hi |= keep8(dk, static_cast<uint32_t>(j0 / 8 + 4 + g), static_cast<uint32_t>(i)) << (8 * g);
-  }
+  uint64_t bits = 0;
+#pragma unroll 1
+  for (int g = 0; g < 8; ++g)
+    bits |= static_cast<uint64_t>(keep8(dk, static_cast<uint32_t>(j0 / 8 + g), static_cast<uint32_t>(i))) << (8 * g);
+  lo = static_cast<uint32_t>(bits);
+  hi = static_cast<uint32_t>(bits >> 32);
 }
 
 // The transposed layout: lane l of a warp holds key j0 + l (j0 a multiple of
@@ -79,13 +80,14 @@ __device__ __forceinline__ void keep64_row(const DropKey& dk, int j0, int i, uin
 // must call it together.
 __device__ __forceinline__ void keep64_col(const DropKey& dk, int j0, int i0, int lane, uint32_t& lo,
                                            uint32_t& hi) {
-  uint32_t m_lo = 0, m_hi = 0;  // byte g: the bits of this lane's generator call for group g
+  // byte g of m: the bits of this lane's generator call for group g (a loop
+  // that is not unrolled, as in keep64_row)
+  uint64_t m = 0;
   const uint32_t jb = static_cast<uint32_t>(j0 / 8 + (lane >> 3));
-#pragma unroll
-  for (int g = 0; g < 4; ++g) {
-    m_lo |= keep8(dk, jb, static_cast<uint32_t>(i0 + 8 * g + (lane & 7))) << (8 * g);
-    m_hi |= keep8(dk, jb, static_cast<uint32_t>(i0 + 32 + 8 * g + (lane & 7))) << (8 * g);
-  }
+#pragma unroll 1
+  for (int g = 0; g < 8; ++g)
+    m |= static_cast<uint64_t>(keep8(dk, jb, static_cast<uint32_t>(i0 + 8 * g + (lane & 7)))) << (8 * g);
+  const uint32_t m_lo = static_cast<uint32_t>(m), m_hi = static_cast<uint32_t>(m >> 32);
   lo = 0;
   hi = 0;
   const int sh = lane & 7;
