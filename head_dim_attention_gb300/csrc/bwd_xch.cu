@@ -539,22 +539,27 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int64_t idx = (static_cast<int64_t>(g.b) * p.Hq + g.hs) * p.Nq + min(srow, p.Nq - 1);
       row_stat = is_b ? p.delta[idx] : p.lse2[idx];
     }
+    // dK/dV mode: column statistics of a column tile; lane l holds those of
+    // query rows cbase + l and cbase + 32 + l.  They are loaded one column tile
+    // ahead, so that the loads are in flight during the score product.
+    const float* stat_vec = is_b ? p.delta : p.lse2;
+    auto load_stats = [&](int c, float (&dst)[2]) {
+      int ch, cr0;
+      column<MODE>(g, p, c, &ch, &cr0);
+      const int64_t sbase = (static_cast<int64_t>(g.b) * p.Hq + ch) * p.Nq;
+#pragma unroll
+      for (int k2 = 0; k2 < 2; ++k2) dst[k2] = stat_vec[sbase + min(cr0 + 64 * u + 32 * k2 + lane, p.Nq - 1)];
+    };
+    float cs_next[2] = {0.f, 0.f};
+    if (!DQ && ncols > 0) load_stats(0, cs_next);
     bool ok = true;
     for (int c = 0; c < ncols; ++c) {
       int ch, cr0;
       column<MODE>(g, p, c, &ch, &cr0);
       const int cbase = cr0 + 64 * u;  // first column row of this thread's half
       const int rb = c % kNrecv, use = c / kNrecv;
-      // dK/dV mode: column statistics; lane l holds those of query rows cbase + l and cbase + 32 + l
-      float cs[2] = {0.f, 0.f};
-      if (!DQ) {
-        const int64_t sbase = (static_cast<int64_t>(g.b) * p.Hq + ch) * p.Nq;
-#pragma unroll
-        for (int k2 = 0; k2 < 2; ++k2) {
-          const int64_t i = sbase + min(cbase + 32 * k2 + lane, p.Nq - 1);
-          cs[k2] = is_b ? p.delta[i] : p.lse2[i];
-        }
-      }
+      float cs[2] = {cs_next[0], cs_next[1]};
+      if (!DQ && c + 1 < ncols) load_stats(c + 1, cs_next);
       // statistic of column e of this thread's half (per query row: the column
       // in dK/dV mode, this thread's row in dQ mode)
       auto stat = [&](int e) { return DQ ? row_stat : __shfl_sync(0xffffffffu, cs[e >> 5], e & 31); };
