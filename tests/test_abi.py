@@ -133,6 +133,19 @@ def test_bwd_rejects(lib):
     assert call(q=t4([1, 4, 100, 320])) == INVALID
 
 
+@pytest.mark.parametrize("p,D,expect", [(1.0, 512, INVALID), (-0.1, 512, INVALID), (float("nan"), 512, INVALID),
+                                         (1.5, 512, INVALID), (0.1, 256, UNSUPPORTED), (0.1, 64, UNSUPPORTED)])
+def test_dropout_rejects(lib, p, D, expect):
+    # dropout: 0 <= p < 1, and only the D = 320 .. 1024 kernels draw keep masks
+    q, k, v, out = good(D=D)
+    lse = t4([1, 4, 100, 1], dtype=_lib.FFPA_F32)
+    r = ctypes.byref
+    assert lib.ffpa_fwd_dropout(r(q), r(k), r(v), None, 0, 0.05, p, 7, 0, r(out), r(lse), None) == expect
+    dout, dq, dk, dv = t4([1, 4, 100, D]), t4([1, 4, 100, D]), t4([1, 2, 200, D]), t4([1, 2, 200, D])
+    assert lib.ffpa_bwd_dropout(r(q), r(k), r(v), None, 0, 0.05, p, 7, 0, r(out), r(lse), r(dout), r(dq), r(dk),
+                                r(dv), None) == expect
+
+
 def test_binding_rejects_host_tensors():
     # the binding passes data pointers as device addresses: host tensors never reach the library
     import torch
