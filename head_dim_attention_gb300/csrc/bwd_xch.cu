@@ -50,6 +50,15 @@
 // (st_ready: the second CTA's warps arrive locally and its relay forwards),
 // and free once the pair's dQ MMAs and the bulk copy have read it (st_free).
 //
+// Dropout (philox.cuh; the DROP instantiations): pair A draws the keep bits
+// of its scores (in the dK/dV mode with one generator call per lane per eight
+// query rows and warp shuffles, since its threads hold key rows) and sends P
+// (or P^T) with the sign bit set on dropped entries.  Pair B reads the sign as
+// the keep bit and forms dS = P (keep dP / (1 - p) - Delta); in the dK/dV mode
+// it then clears the dropped entries of the received tile in place before its
+// dV MMAs read it (pm_ready / pm_local, relayed like st_ready), and dV carries
+// 1 / (1 - p) in the epilogue.
+//
 // TMEM per CTA: gradient [0, 256), score tiles [256, 384), the stationary
 // tile's chunks 0..3 as the TS-form operand [384, 512) (the score MMAs' operand
 // reads from shared memory alone would need the SM's full shared-memory
