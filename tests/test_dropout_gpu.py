@@ -64,6 +64,8 @@ def test_keep_mask_bit_exact(D, Nkv, Nq, p):
     (1, 4, 2, 17, 260, 640, BF, False, False),
     (1, 2, 1, 256, 300, 1024, FP, True, True),
     (1, 1, 1, 5, 200, 832, BF, False, False),
+    (1, 4, 2, 200, 300, 768, BF, True, True),
+    (2, 4, 1, 130, 260, 448, FP, True, False),
 ])
 def test_dropout_fwd_bwd_small(B, Hq, Hkv, Nq, Nkv, D, dtype, causal, bias):
     drop = (0.2, 0xC0FFEE, 3)
