@@ -19,7 +19,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(BUILD, "libffpa.so")
-SOURCES = ["api.cu", "fwd_main.cu", "fwd_fulld.cu", "fwd_decode.cu", "bwd.cu", "bwd_dq.cu", "bwd_xch.cu"]
+SOURCES = ["api.cu", "fwd_main.cu", "fwd_fulld.cu", "fwd_xch.cu", "fwd_decode.cu", "bwd.cu", "bwd_dq.cu", "bwd_xch.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
          "-I" + INCLUDE, "-I" + CSRC]

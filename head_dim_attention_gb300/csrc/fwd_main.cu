@@ -532,6 +532,7 @@ cudaError_t launch_impl(const FwdParams& p_in, const FwdMaps& m, cudaStream_t st
 }  // namespace
 
 cudaError_t launch_fwd_main(const FwdParams& p, const FwdMaps& m, bool bf16, cudaStream_t s) {
+  if (fwd_xch_supported(p)) return launch_fwd_xch(p, m, bf16, s);      // D = 704 .. 1024
   if (fwd_fulld_supported(p)) return launch_fwd_fulld(p, m, bf16, s);  // D = 320 .. 1024
   if (p.n_chunks > kMaxChunks) return cudaErrorInvalidValue;
   return bf16 ? launch_impl<true>(p, m, s) : launch_impl<false>(p, m, s);

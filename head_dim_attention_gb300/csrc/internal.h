@@ -133,6 +133,10 @@ bool fwd_fulld_supported(const FwdParams& p);
 // Key splits (1: none) for a short query set on `sms` SMs, and key tiles per split.
 int fwd_fulld_kv_splits(const FwdParams& p, int sms, int* tiles_per_split);
 cudaError_t launch_fwd_fulld(const FwdParams& p, const FwdMaps& m, bool bf16, cudaStream_t s);
+// Forward for D = 704 .. 1024 on clusters of two CTA pairs (fwd_xch.cu): one
+// pair computes S and P, the other holds all of O; no dropout, no key split.
+bool fwd_xch_supported(const FwdParams& p);
+cudaError_t launch_fwd_xch(const FwdParams& p, const FwdMaps& m, bool bf16, cudaStream_t s);
 cudaError_t launch_fwd_decode(const DecodeParams& p, bool bf16, cudaStream_t s);
 // The decode path's merge of per-split partials (part_o, part_ml) into out and
 // lse; also merges the key splits of the full-D forward for short query sets.
