@@ -483,7 +483,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       // so the maximum of s gives the maximum of x).
       const float c_scale = bias_row ? 1.f : p.scale_log2;
       if (bias_row) {
-#pragma unroll
         if (p.bias_vec && kv0 + 64 <= p.Nkv) {
           const float4* src = reinterpret_cast<const float4*>(bias_row + kv0);
 #pragma unroll
