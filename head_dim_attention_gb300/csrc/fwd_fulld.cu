@@ -268,7 +268,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int n = 0; n < per_tile * ntiles && ok; ++n) {
       const uint32_t s = it % S, r = it / S;
       ++it;
-      ok = mbar_wait(bar(empty0 + s), (r & 1) ^ 1, status);
+      ok = mbar_wait<false>(bar(empty0 + s), (r & 1) ^ 1, status);
       if (!ok) break;
       const int j = n / per_tile, m = n % per_tile;
       // K: chunks 4m .. 4m + 3 (at most NC - 1) of this CTA's 64 keys of key
@@ -289,20 +289,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     // the ring's last commits (they arrive on both CTAs) complete before exit
     for (uint32_t s = 0; s < S && s < it && ok; ++s) {
       const uint32_t last = s + ((it - 1 - s) / S) * S;
-      mbar_wait(bar(empty0 + s), (last / S) & 1, status);
+      mbar_wait<false>(bar(empty0 + s), (last / S) & 1, status);
     }
   } else if (warp == 1 && lane == 0 && rank == 0) {
     // ------------------------------------------------------------ MMA issuer A: S_j = Q K_j^T
     constexpr uint32_t idesc_s = idesc_f16(BF16, 128, 128, false, false);  // 128 rows x 128 keys
     const uint64_t dq = sdesc_sw128(q_sm, 16, 1024);                        // Q chunks (64 rows), K-major
     const uint64_t dk = sdesc_sw128(ring_k, 16, 1024);                      // K chunks (64 keys), K-major
-    bool ok = mbar_wait(bar(bl.q_full), 0, status);
+    bool ok = mbar_wait<false>(bar(bl.q_full), 0, status);
     tc_fence_after();
     uint32_t it = 0;
     for (int j = 0; j < ntiles && ok; ++j) {
       if (j >= 2) {
         // S_j goes to the buffer S_{j-2} used: the softmax warps have copied it out
-        ok = mbar_wait(bar(bl.s_free + (j & 1)), ((j - 2) >> 1) & 1, status);
+        ok = mbar_wait<false>(bar(bl.s_free + (j & 1)), ((j - 2) >> 1) & 1, status);
         if (!ok) break;
         tc_fence_after();
       }
@@ -310,7 +310,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int m = 0; m < G::kKSlotsPerTile; ++m) {
         const uint32_t s = it & 1;
-        ok = mbar_wait(bar(bl.full_k + s), (it >> 1) & 1, status);
+        ok = mbar_wait<false>(bar(bl.full_k + s), (it >> 1) & 1, status);
         ++it;
         if (!ok) break;
         tc_fence_after();
@@ -336,7 +336,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       umma_commit_pair(bar(bl.s_full + (j & 1)), 3);
     }
     umma_commit_pair(bar(bl.drain_a), 1);
-    mbar_wait(bar(bl.drain_a), 0, status);
+    mbar_wait<false>(bar(bl.drain_a), 0, status);
   } else if (warp == 2 && lane == 0 && rank == 0) {
     // ------------------------------------------------------------ MMA issuer B: O += P_j V_j
     constexpr uint32_t idesc_pv256 = idesc_f16(BF16, 128, 256, false, true);  // 128 rows x 256 O columns
@@ -347,14 +347,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t it = 0;
     for (int j = 0; j < ntiles && ok; ++j) {
       const int pb = j % kNpb;
-      ok = mbar_wait(bar(bl.p_ready + pb), (j / kNpb) & 1, status);
+      ok = mbar_wait<false>(bar(bl.p_ready + pb), (j / kNpb) & 1, status);
       if (!ok) break;
       tc_fence_after();
       const bool use_lo = lo_flag[pb] == static_cast<uint32_t>(j + 1);
       const uint64_t dphi = sdesc_advance(dp, pb * kPBufBytes), dplo = sdesc_advance(dphi, kPBytes);
       for (int hf = 0; hf < nhalves && ok; ++hf) {
         const uint32_t s = it % G::kVSlots;  // two slots (one per half of D), or one
-        ok = mbar_wait(bar(bl.full_v + s), (it / G::kVSlots) & 1, status);
+        ok = mbar_wait<false>(bar(bl.full_v + s), (it / G::kVSlots) & 1, status);
         ++it;
         if (!ok) break;
         tc_fence_after();
@@ -377,7 +377,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       umma_commit_pair(bar(bl.pv_done + pb), 3);
     }
     umma_commit_pair(bar(bl.drain_b), 1);
-    mbar_wait(bar(bl.drain_b), 0, status);
+    mbar_wait<false>(bar(bl.drain_b), 0, status);
   } else if (warp == 2 && lane == 0 && rank == 1) {
     // ------------------------------------------------------------ relay of this CTA's p_ready
     // The softmax warps of tile j + 2 wait for P_j V (pv_done of buffer j mod
@@ -386,7 +386,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lo_flag_lead = mapa(smem_u32(const_cast<uint32_t*>(lo_flag)), 0);
     for (int j = 0; j < ntiles; ++j) {
       const int pb = j % kNpb;
-      if (!mbar_wait(bar(bl.p_local + pb), (j / kNpb) & 1, status)) break;
+      if (!mbar_wait<false>(bar(bl.p_local + pb), (j / kNpb) & 1, status)) break;
       if (lo_flag[pb] == static_cast<uint32_t>(j + 1)) st_cluster_u32(lo_flag_lead + 4 * pb, j + 1);
       mbar_arrive_remote(lead(bl.p_ready + pb));  // release.cluster: P and the flag are visible first
     }
@@ -453,7 +453,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                               p.drop_t};
         keep64_row(dkey, kv0, row, keep_lo, keep_hi);
       }
-      const bool got = __all_sync(0xffffffffu, mbar_wait(bar(bl.s_full + (j & 1)), (j >> 1) & 1, status));
+      const bool got = __all_sync(0xffffffffu, mbar_wait<false>(bar(bl.s_full + (j & 1)), (j >> 1) & 1, status));
       float s[64];
       if (got) {
         tc_fence_after();
@@ -560,7 +560,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // P_{j-kNpb} V reads the P buffer this tile writes.  P_j V cannot have
         // completed, so the parity of that barrier is unambiguous.
         const bool done =
-            __all_sync(0xffffffffu, mbar_wait(bar(bl.pv_done + pb), ((j - kNpb) / kNpb) & 1, status));
+            __all_sync(0xffffffffu, mbar_wait<false>(bar(bl.pv_done + pb), ((j - kNpb) / kNpb) & 1, status));
         ok = pair_bar_and(nb, done);
         if (!ok) break;
       }
@@ -570,7 +570,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // completed, so the parity is unambiguous even where earlier tiles
         // skipped this wait)
         const bool done = __all_sync(
-            0xffffffffu, mbar_wait(bar(bl.pv_done + (j - 1) % kNpb), ((j - 1) / kNpb) & 1, status));
+            0xffffffffu, mbar_wait<false>(bar(bl.pv_done + (j - 1) % kNpb), ((j - 1) / kNpb) & 1, status));
         ok = pair_bar_and(nb, done);
         if (!ok) break;
       }
@@ -605,9 +605,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       // CTA); a key split may have no key tile at all
       if (!KSPLIT || ntiles > 0)
         ok = __all_sync(0xffffffffu,
-                        mbar_wait(bar(bl.pv_done + (ntiles - 1) % kNpb), ((ntiles - 1) / kNpb) & 1, status));
+                        mbar_wait<false>(bar(bl.pv_done + (ntiles - 1) % kNpb), ((ntiles - 1) / kNpb) & 1, status));
       if (ok && kNpb == 2 && ntiles >= 2)
-        ok = __all_sync(0xffffffffu, mbar_wait(bar(bl.pv_done + (ntiles & 1)), ((ntiles - 2) >> 1) & 1, status));
+        ok = __all_sync(0xffffffffu, mbar_wait<false>(bar(bl.pv_done + (ntiles & 1)), ((ntiles - 2) >> 1) & 1, status));
       if constexpr (KSPLIT) {
       if (ok) {
         // key split: the unnormalised partial O (fp32) and this split's (max,

@@ -236,7 +236,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int n = 0; n < G::kKSlotsPerTile * ntiles && ok; ++n) {
       const uint32_t s = it % kSlots, rr = it / kSlots;
       ++it;
-      ok = mbar_wait(bar(bl.empty_r + s), (rr & 1) ^ 1, status);
+      ok = mbar_wait<false>(bar(bl.empty_r + s), (rr & 1) ^ 1, status);
       if (!ok) break;
       const int j = n / G::kKSlotsPerTile, m = n % G::kKSlotsPerTile;
       const int nk = min(4, NC - 4 * m);  // K chunks 4m .. 4m + nk - 1 of this CTA's 64 keys of key tile j
@@ -248,7 +248,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (uint32_t s = 0; s < static_cast<uint32_t>(kSlots) && s < it && ok; ++s) {
       const uint32_t last = s + ((it - 1 - s) / kSlots) * kSlots;
-      mbar_wait(bar(bl.empty_r + s), (last / kSlots) & 1, status);
+      mbar_wait<false>(bar(bl.empty_r + s), (last / kSlots) & 1, status);
     }
   } else if (is_b && warp == 3 && lane == 0) {
     // ------------------------------------------------------------ pair B: the V ring
@@ -260,7 +260,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int n = 0; n < kNblk * ntiles && ok; ++n) {
       const uint32_t s = it % kSlotsB, rr = it / kSlotsB;
       ++it;
-      ok = mbar_wait(bar(bl.empty_r + s), (rr & 1) ^ 1, status);
+      ok = mbar_wait<false>(bar(bl.empty_r + s), (rr & 1) ^ 1, status);
       if (!ok) break;
       const int j = n / kNblk, nb = n % kNblk;
       const int w = min(256, G::kD - 256 * nb);
@@ -273,20 +273,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (uint32_t s = 0; s < static_cast<uint32_t>(kSlotsB) && s < it && ok; ++s) {
       const uint32_t last = s + ((it - 1 - s) / kSlotsB) * kSlotsB;
-      mbar_wait(bar(bl.empty_r + s), (last / kSlotsB) & 1, status);
+      mbar_wait<false>(bar(bl.empty_r + s), (last / kSlotsB) & 1, status);
     }
   } else if (!is_b && warp == 1 && lane == 0 && pr == 0) {
     // ------------------------------------------------------------ pair A's MMA issuer: S_j = Q K_j^T
     constexpr uint32_t idesc_s = idesc_f16(BF16, 128, 128, false, false);  // 128 rows x 128 keys
     const uint64_t dq = sdesc_sw128(q_sm, 16, 1024);                        // Q chunks (64 rows), K-major
     const uint64_t dk = sdesc_sw128(ring, 16, 1024);                        // K chunks (64 keys), K-major
-    bool ok = mbar_wait(bar(bl.q_full), 0, status);
+    bool ok = mbar_wait<false>(bar(bl.q_full), 0, status);
     tc_fence_after();
     uint32_t it = 0;
     for (int j = 0; j < ntiles && ok; ++j) {
       if (j >= 2) {
         // S_j goes to the buffer S_{j-2} used: the softmax warps have copied it out
-        ok = mbar_wait(bar(bl.s_free + (j & 1)), ((j - 2) >> 1) & 1, status);
+        ok = mbar_wait<false>(bar(bl.s_free + (j & 1)), ((j - 2) >> 1) & 1, status);
         if (!ok) break;
         tc_fence_after();
       }
@@ -294,7 +294,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int m = 0; m < G::kKSlotsPerTile; ++m) {
         const uint32_t s = it % kSlots;
-        ok = mbar_wait(bar(bl.full_r + s), (it / kSlots) & 1, status);
+        ok = mbar_wait<false>(bar(bl.full_r + s), (it / kSlots) & 1, status);
         ++it;
         if (!ok) break;
         tc_fence_after();
@@ -321,7 +321,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       umma_commit_pair(bar(bl.s_full + (j & 1)), pair_mask);
     }
     umma_commit_pair(bar(bl.drain), static_cast<uint16_t>(1u << rank));
-    mbar_wait(bar(bl.drain), 0, status);
+    mbar_wait<false>(bar(bl.drain), 0, status);
   } else if (is_b && warp == 1 && lane == 0 && pr == 0) {
     // ------------------------------------------------------------ pair B's MMA issuer: O += P_j V_j (+ P_lo V_j)
     constexpr uint32_t idesc_256 = idesc_f16(BF16, 128, 256, false, true);  // 128 rows x 256 O columns
@@ -333,7 +333,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int j = 0; j < ntiles && ok; ++j) {
       const int rb = j % kNbuf;
       // both CTAs' warps have read the message and rescaled O where it asked
-      ok = mbar_wait(bar(bl.ready + rb), (j / kNbuf) & 1, status);
+      ok = mbar_wait<false>(bar(bl.ready + rb), (j / kNbuf) & 1, status);
       if (!ok) break;
       tc_fence_after();
       // the residual term: this CTA's message flags or the second CTA's (forwarded)
@@ -344,7 +344,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t dphi = sdesc_advance(dp, rb * kMsgStride), dplo = sdesc_advance(dphi, kPBytes);
       for (int nb = 0; nb < kNblk && ok; ++nb) {
         const uint32_t s = it % kSlotsB;
-        ok = mbar_wait(bar(bl.full_r + s), (it / kSlotsB) & 1, status);
+        ok = mbar_wait<false>(bar(bl.full_r + s), (it / kSlotsB) & 1, status);
         ++it;
         if (!ok) break;
         tc_fence_after();
@@ -368,13 +368,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       umma_commit_pair(bar(bl.rfree + rb), other_mask);   // pair A may refill buffer rb
     }
     umma_commit_pair(bar(bl.drain), static_cast<uint16_t>(1u << rank));
-    mbar_wait(bar(bl.drain), 0, status);
+    mbar_wait<false>(bar(bl.drain), 0, status);
   } else if (is_b && warp == 2 && lane == 0 && pr == 1) {
     // ------------------------------------------------------------ pair B's relay for its first CTA
     const uint32_t lo_lead = mapa(smem_u32(const_cast<uint32_t*>(lo_peer)), lead_rank);
     for (int j = 0; j < ntiles; ++j) {
       const int rb = j % kNbuf;
-      if (!mbar_wait(bar(bl.ready_local + rb), (j / kNbuf) & 1, status)) break;
+      if (!mbar_wait<false>(bar(bl.ready_local + rb), (j / kNbuf) & 1, status)) break;
       const uint32_t fl = buf_sm + rb * kMsgStride + kFlagOff;
       if ((ld_shared_u32(fl) | ld_shared_u32(fl + 16) | ld_shared_u32(fl + 32) | ld_shared_u32(fl + 48)) != 0)
         st_cluster_u32(lo_lead + 4 * rb, j + 1);
@@ -443,7 +443,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         prefetch_l1(bias_row + min(kv0 + 32, p.Nkv - 1));
         prefetch_l1(bias_row + min(kv0 + 63, p.Nkv - 1));
       }
-      const bool got = __all_sync(0xffffffffu, mbar_wait(bar(bl.s_full + (j & 1)), (j >> 1) & 1, status));
+      const bool got = __all_sync(0xffffffffu, mbar_wait<false>(bar(bl.s_full + (j & 1)), (j >> 1) & 1, status));
       float s[64];
       if (got) {
         tc_fence_after();
@@ -549,7 +549,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) {
         // pair B's buffer rb is free once its P V products of tile j - 2 are done
         bool fr = true;
-        if (j >= kNbuf) fr = mbar_wait(bar(bl.rfree + rb), ((j - kNbuf) / kNbuf) & 1, status);
+        if (j >= kNbuf) fr = mbar_wait<false>(bar(bl.rfree + rb), ((j - kNbuf) / kNbuf) & 1, status);
         if (fr) {
           // pair B's receive buffer rb (its buffers start at offset 0 of its shared memory)
           const uint32_t dst = mapa(base + rb * kMsgStride, other), fb = mapa(bar(bl.rfull + rb), other);
@@ -571,7 +571,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (ok && lane == 0) {
       for (int rb = 0; rb < kNbuf && rb < ntiles && ok; ++rb) {
         const int last = (ntiles - 1 - rb) / kNbuf;
-        ok = mbar_wait(bar(bl.rfree + rb), last & 1, status);
+        ok = mbar_wait<false>(bar(bl.rfree + rb), last & 1, status);
       }
     }
     if (kh == 0 && p.lse && row < p.Nq) {
@@ -593,7 +593,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     float l_last = 0.f;
     for (int j = 0; j < ntiles; ++j) {
       const int rb = j % kNbuf, use = j / kNbuf;
-      ok = __all_sync(0xffffffffu, mbar_wait(bar(bl.rfull + rb), use & 1, status));
+      ok = __all_sync(0xffffffffu, mbar_wait<false>(bar(bl.rfull + rb), use & 1, status));
       if (!ok) break;
       // no MMA thread waits on this buffer's bytes: warp 0 arms its next use
       if (w == 0 && lane == 0 && j + kNbuf < ntiles) mbar_expect_tx(bar(bl.rfull + rb), kMsgBytes);
@@ -603,7 +603,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // O *= alpha for this warp's rows, after P_{j-1} V_{j-1} (P_{j+1} V cannot
         // have completed, so the parity is unambiguous)
         ok = __all_sync(0xffffffffu,
-                        mbar_wait(bar(bl.pv_done + (j - 1) % kNbuf), ((j - 1) / kNbuf) & 1, status));
+                        mbar_wait<false>(bar(bl.pv_done + (j - 1) % kNbuf), ((j - 1) / kNbuf) & 1, status));
         if (!ok) break;
         tc_fence_after();
 #pragma unroll 1
@@ -626,10 +626,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       // ---------------------------------------------------------- epilogue
       // the last P V of each buffer (their commits also arrive on the second CTA)
       ok = __all_sync(0xffffffffu,
-                      mbar_wait(bar(bl.pv_done + (ntiles - 1) % kNbuf), ((ntiles - 1) / kNbuf) & 1, status));
+                      mbar_wait<false>(bar(bl.pv_done + (ntiles - 1) % kNbuf), ((ntiles - 1) / kNbuf) & 1, status));
       if (ok && ntiles >= 2)
         ok = __all_sync(0xffffffffu,
-                        mbar_wait(bar(bl.pv_done + (ntiles - 2) % kNbuf), ((ntiles - 2) / kNbuf) & 1, status));
+                        mbar_wait<false>(bar(bl.pv_done + (ntiles - 2) % kNbuf), ((ntiles - 2) / kNbuf) & 1, status));
       if (ok) {
         tc_fence_after();
         const float inv_l = l_last > 0.f ? 1.f / l_last : 0.f;
