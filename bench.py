@@ -309,7 +309,7 @@ def run_ffpa(args, rank, world):
 # DRAM bytes (read + write) per launch, dram__bytes_read.sum +
 # dram__bytes_write.sum from one ncu capture of the same workload; a kernel
 # changed since its capture is left out (its traffic is then reported as null).
-TRAFFIC: dict = {"bwd_dkv": 372583808, "bwd_dq": 322819328}
+TRAFFIC: dict = {"fwd_main": 249217920, "bwd_dkv": 373564672, "bwd_dq": 323346560}
 TRAFFIC_FROM = "ncu capture of the same workload (dram__bytes_read.sum + dram__bytes_write.sum per launch)"
 
 
