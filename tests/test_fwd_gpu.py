@@ -2,10 +2,11 @@
 
 Small shapes are compared element by element over the whole output; they span
 several 128-row tiles, ragged tails, both dtypes, every head-dimension regime
-of the fused kernel (one CTA for D <= 256, two or three CTAs splitting D up to
-D = 768, an exchanging pair above) and the decode path (Nq <= 16).  The workload-sized
-cases compare 64 seeded query rows per head, which the oracle computes one by
-one.
+of the fused kernels (one CTA for D <= 256; a CTA pair holding all of O for
+D = 320..512; two pairs splitting O along D at D = 576 and 640 and with
+dropout or key splits above; a score pair and an O pair for D = 704..1024)
+and the decode path (Nq <= 16).  The workload-sized cases compare 64 seeded
+query rows per head, which the oracle computes one by one.
 """
 import pytest
 import torch
