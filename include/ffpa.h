@@ -133,6 +133,10 @@ int ffpa_bwd(const ffpa_tensor_t* q, const ffpa_tensor_t* k, const ffpa_tensor_t
  * (j / 8, i, b * Hq + h, offset) with key (seed & 0xffffffff, seed >> 32);
  * score (i, j) reads 16-bit field j % 2 of output word (j % 8) / 2 and is kept
  * when that value is at least t = min(65535, floor(p * 65536 + 1/2)).
+ * b and h index the tensors of this call: a caller that splits a problem's
+ * batches or heads over several calls (or GPUs) and wants the masks of the
+ * unsplit call must pass views whose indices match, or tell the pieces apart
+ * with distinct seeds or offsets.
  * The pages give no generator; this contract is the library's.  Dropout runs
  * on the D = 320 .. 1024 kernels only (FFPA_ERR_UNSUPPORTED for D <= 256),
  * with neither the decode path nor key splits (every Nq takes the fused
