@@ -45,6 +45,10 @@ def test_config_small_self_attention():
     (1, 4, 2, 333, 333, 384, BF, True, True),
     (1, 2, 1, 200, 300, 448, FP, False, True),
     (2, 2, 2, 190, 190, 320, FP, True, False),
+    # the score pair + O pair kernel (D >= 704) with GQA, two batches, causal
+    # with Nq != Nkv and a key bias
+    (2, 4, 2, 200, 300, 1024, BF, True, True),
+    (1, 4, 1, 300, 200, 832, FP, False, False),
 ])
 def test_fused_small(B, Hq, Hkv, Nq, Nkv, D, dtype, causal, bias):
     check_fwd_full(B, Hq, Hkv, Nq, Nkv, D, dtype, causal=causal, bias=bias)
